@@ -1,0 +1,198 @@
+"""ctypes front end of the CPU oracle (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU leg may
+import this module.  It compiles ``smla_oracle.c`` with gcc on first use (or
+through :func:`build`) and exposes the two oracle modes over numpy arrays:
+
+* :func:`fp64` -- the plain definition of sparse MLA decode (DeepSeek-V4.1
+  ``sparse_mla_cute`` page, module docstring, "What this module computes").
+* :func:`emulate` -- the Kimi K3.1 ``attn_sparse`` datapath (module docstring,
+  the per-chunk softmax with E4M3 P at 448 of the running max, and
+  ``SparseDcpDecode.merge``) replayed on a given (splits, chunk) partition.
+
+It shares no code with the CUDA path and never imports it.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "smla_oracle.c")
+LIBRARY = os.path.join(HERE, "_build", "libsmla_oracle.so")
+
+NO_P_ROUNDING = 1
+EXACT = 2
+LATENT = 512
+
+_lock = threading.Lock()
+_lib = None
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int32),
+        ("heads", ctypes.c_int32),
+        ("width", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("num_pools", ctypes.c_int32),
+        ("pool_split", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("q_stride_token", ctypes.c_int64),
+        ("q_stride_head", ctypes.c_int64),
+        ("pool", ctypes.c_void_p * 2),
+        ("pool_rows", ctypes.c_int64 * 2),
+        ("indices", ctypes.c_void_p),
+        ("idx_stride_token", ctypes.c_int64),
+        ("lens", ctypes.c_void_p),
+        ("sinks", ctypes.c_void_p),
+        ("bmm1_scale", ctypes.c_double),
+        ("bmm2_scale", ctypes.c_double),
+        ("k_scale", ctypes.c_double),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build`` (gcc, OpenMP, no FP contraction)."""
+    if not force and os.path.exists(LIBRARY) and os.path.getmtime(LIBRARY) >= max(
+        os.path.getmtime(SOURCE), os.path.getmtime(os.path.join(HERE, "smla_oracle.h"))
+    ):
+        return LIBRARY
+    os.makedirs(os.path.dirname(LIBRARY), exist_ok=True)
+    tmp = LIBRARY + f".{os.getpid()}.tmp"
+    cmd = [
+        "gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+        "-ffp-contract=off", "-fno-fast-math", "-Wall",
+        "-o", tmp, SOURCE, "-lm",
+    ]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIBRARY)
+    return LIBRARY
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.POINTER(_Problem)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+            lib.smla_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.smla_oracle_e4m3_to_double.restype = ctypes.c_double
+            lib.smla_oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.smla_oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.smla_oracle_bf16_from_float.argtypes = [ctypes.c_float]
+            lib.smla_oracle_bf16_from_float.restype = ctypes.c_uint16
+            lib.smla_oracle_fp64_pairs.argtypes = [P, vp, vp, i32, vp, vp, i32]
+            lib.smla_oracle_emulate_pairs.argtypes = [P, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
+            lib.smla_oracle_max_threads.restype = i32
+            del i64
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().smla_oracle_max_threads())
+
+
+def e4m3_to_double(byte: int) -> float:
+    return float(_load().smla_oracle_e4m3_to_double(int(byte)))
+
+
+def e4m3_from_float(value: float) -> int:
+    return int(_load().smla_oracle_e4m3_from_float(float(value)))
+
+
+def bf16_from_float(value: float) -> int:
+    return int(_load().smla_oracle_bf16_from_float(float(value)))
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class Problem:
+    """Host copy of one decode problem, held alive for the C structure.
+
+    ``q`` uint8 [T, H, D]; ``pools`` list of uint8 [rows, D]; ``indices`` int32
+    [T, W]; ``lens`` int32 [T]; ``sinks`` float32 [H] or None."""
+
+    def __init__(self, q, pools, indices, lens, sinks, bmm1_scale, bmm2_scale, k_scale,
+                 pool_split=0):
+        self.q = _c(q, np.uint8)
+        self.pools = [_c(p, np.uint8) for p in pools]
+        self.indices = _c(indices, np.int32)
+        self.lens = _c(lens, np.int32)
+        self.sinks = None if sinks is None else _c(sinks, np.float32)
+        T, H, D = self.q.shape
+        W = self.indices.shape[1]
+        s = _Problem()
+        s.tokens, s.heads, s.width, s.head_dim = T, H, W, D
+        s.num_pools = len(self.pools)
+        s.pool_split = int(pool_split)
+        s.q = self.q.ctypes.data
+        s.q_stride_token, s.q_stride_head = H * D, D
+        for i, p in enumerate(self.pools):
+            assert p.ndim == 2 and p.shape[1] == D
+            s.pool[i] = p.ctypes.data
+            s.pool_rows[i] = p.shape[0]
+        if len(self.pools) == 1:
+            s.pool[1] = self.pools[0].ctypes.data
+            s.pool_rows[1] = self.pools[0].shape[0]
+        s.indices = self.indices.ctypes.data
+        s.idx_stride_token = W
+        s.lens = self.lens.ctypes.data
+        s.sinks = None if self.sinks is None else self.sinks.ctypes.data
+        s.bmm1_scale, s.bmm2_scale, s.k_scale = float(bmm1_scale), float(bmm2_scale), float(k_scale)
+        self.struct = s
+        self.tokens, self.heads = T, H
+
+    @classmethod
+    def from_workload(cls, w):
+        return cls(w["q"], w["pools"], w["indices"], w["lens"], w["sinks"], w["bmm1_scale"],
+                   w["bmm2_scale"], w["k_scale"], w.get("pool_split", 0))
+
+
+def _pairs(problem, pairs):
+    if pairs is None:
+        t, h = np.meshgrid(np.arange(problem.tokens), np.arange(problem.heads), indexing="ij")
+        return _c(t.ravel(), np.int32), _c(h.ravel(), np.int32)
+    pairs = np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
+    return _c(pairs[:, 0], np.int32), _c(pairs[:, 1], np.int32)
+
+
+def fp64(problem: Problem, pairs=None, threads: int = 0):
+    """FP64 definition. Returns (out [n, 512] float64, lse2 [n] float64) for the
+    (token, head) ``pairs`` (all pairs in row-major order when None)."""
+    lib = _load()
+    tok, head = _pairs(problem, pairs)
+    n = tok.size
+    out = np.zeros((n, LATENT), np.float64)
+    lse = np.zeros(n, np.float64)
+    lib.smla_oracle_fp64_pairs(ctypes.byref(problem.struct), tok.ctypes.data, head.ctypes.data,
+                               n, out.ctypes.data, lse.ctypes.data, threads)
+    return out, lse
+
+
+def emulate(problem: Problem, splits: int, chunk: int, pairs=None, flags: int = 0,
+            threads: int = 0):
+    """E4M3-P datapath on the given partition. Returns (value [n, 512] float64 --
+    the pre-BF16 result, bf16 [n, 512] uint16 bits, lse2 [n] float64)."""
+    lib = _load()
+    tok, head = _pairs(problem, pairs)
+    n = tok.size
+    value = np.zeros((n, LATENT), np.float64)
+    bits = np.zeros((n, LATENT), np.uint16)
+    lse = np.zeros(n, np.float64)
+    rc = lib.smla_oracle_emulate_pairs(ctypes.byref(problem.struct), tok.ctypes.data,
+                                       head.ctypes.data, n, int(splits), int(chunk), int(flags),
+                                       value.ctypes.data, bits.ctypes.data, lse.ctypes.data,
+                                       threads)
+    if rc != 0:
+        raise ValueError("oracle emulate: bad partition")
+    return value, bits, lse

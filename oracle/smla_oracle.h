@@ -1,0 +1,66 @@
+/*
+ * smla_oracle.h -- the CPU oracle's own interface (test infrastructure).
+ * Nothing outside tests/, __graft_entry__.smoke() and bench.py's CPU leg uses
+ * it; the CUDA library has its own, unrelated, header.
+ */
+#ifndef SMLA_ORACLE_H
+#define SMLA_ORACLE_H
+
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* One decode problem, all arrays in host memory.
+ * q:       E4M3 bytes, element (t, h, d) at t*q_stride_token + h*q_stride_head + d.
+ * pool[i]: pool_rows[i] rows of head_dim E4M3 bytes each, rows contiguous.
+ * indices: int32 (t, c) at t*idx_stride_token + c; -1 marks a hole.
+ * lens:    int32 [tokens], active count per token (clamped to [0, width]).
+ * sinks:   float [heads] or NULL. */
+typedef struct smla_oracle_problem {
+    int32_t tokens, heads, width, head_dim, num_pools, pool_split;
+    const uint8_t* q;
+    int64_t q_stride_token, q_stride_head;
+    const uint8_t* pool[2];
+    int64_t pool_rows[2];
+    const int32_t* indices;
+    int64_t idx_stride_token;
+    const int32_t* lens;
+    const float* sinks;
+    double bmm1_scale, bmm2_scale, k_scale;
+} smla_oracle_problem;
+
+enum {
+    SMLA_ORACLE_NO_P_ROUNDING = 1, /* keep P unrounded (no E4M3 step) */
+    SMLA_ORACLE_EXACT = 2          /* no FP32 roundings anywhere */
+};
+
+double smla_oracle_e4m3_to_double(uint8_t byte);
+uint8_t smla_oracle_e4m3_from_float(float value);
+uint16_t smla_oracle_bf16_from_float(float value);
+float smla_oracle_bf16_to_float(uint16_t bits);
+
+/* The plain definition: out[512] (double) and the base-2 LSE of (t, h). */
+int smla_oracle_fp64(const smla_oracle_problem* p, int t, int h, double* out, double* lse2);
+
+/* The E4M3-P datapath on `splits` splits of `chunk`-column chunks: out_value
+ * (pre-BF16 value, double), out_bf16 (bits) and the base-2 LSE; any may be NULL. */
+int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, int chunk,
+                        int flags, double* out_value, uint16_t* out_bf16, double* lse2_out);
+
+int smla_oracle_fp64_all(const smla_oracle_problem* p, double* out, double* lse2, int threads);
+int smla_oracle_fp64_pairs(const smla_oracle_problem* p, const int32_t* tokens,
+                           const int32_t* heads, int n, double* out, double* lse2, int threads);
+int smla_oracle_emulate_pairs(const smla_oracle_problem* p, const int32_t* tokens,
+                              const int32_t* heads, int n, int splits, int chunk, int flags,
+                              double* out_value, uint16_t* out_bf16, double* lse2, int threads);
+int smla_oracle_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,298 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each test checks one part of ``oracle/`` against something it does not share
+code with: torch's E4M3 / BF16 codecs (library routines), torch's
+scaled-dot-product attention in float64 (the special case of the decode with
+every gathered row active), closed forms, and invariants of the definition
+(DeepSeek-V4.1 ``sparse_mla_cute`` page, "What this module computes"; Kimi K3.1
+``attn_sparse`` page, module docstring and ``SparseDcpDecode.merge``).  A
+plausible slip in the oracle -- a dropped term, a wrong sign or index, a
+transposed operand, the P anchor at the wrong maximum -- fails one of them.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from sparse_mla_decode_gb300 import workloads
+
+LOG2E = 1.0 / math.log(2.0)
+
+
+def dec(b):
+    """E4M3 bytes -> float64 through torch (the library decoder)."""
+    t = torch.from_numpy(np.ascontiguousarray(b, np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+# ----------------------------------------------------------------- codecs
+
+
+def test_e4m3_decode_every_byte_matches_torch():
+    ref = dec(np.arange(256, dtype=np.uint8))
+    got = np.array([oracle.e4m3_to_double(b) for b in range(256)])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+    assert np.array_equal(np.signbit(ref[ok]), np.signbit(got[ok]))
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def _e4m3_grid():
+    finite = dec(np.arange(0, 0x7F, dtype=np.uint8))  # 0 .. 448
+    mids = (finite[1:] + finite[:-1]) / 2
+    pts = np.concatenate([finite, mids])
+    f32 = pts.astype(np.float32)
+    up = np.nextafter(f32, np.float32(np.inf))
+    dn = np.nextafter(f32, np.float32(-np.inf))
+    rng = np.random.default_rng(7)
+    rand = rng.uniform(0, 470, 20000).astype(np.float32)
+    tiny = rng.uniform(0, 2 ** -5, 5000).astype(np.float32)
+    g = np.concatenate([f32, up, dn, rand, tiny])
+    return np.concatenate([g, -g])
+
+
+def test_e4m3_encode_rn_matches_torch_in_range():
+    g = _e4m3_grid()
+    g = g[np.abs(g) < 464.0]  # torch's cast is RN without saturation; equal below 464
+    ref = torch.from_numpy(g).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_float(x) for x in g], np.uint8)
+    bad = np.nonzero(ref != got)[0]
+    assert bad.size == 0, [(float(g[i]), int(ref[i]), int(got[i])) for i in bad[:5]]
+
+
+def test_e4m3_encode_saturates_and_nan():
+    # satfinite: anything at or beyond the largest finite value maps to +-448
+    for x in [448.0, 449.0, 464.0, 500.0, 1e30, float("inf")]:
+        assert oracle.e4m3_from_float(x) == 0x7E
+        assert oracle.e4m3_from_float(-x) == 0xFE
+    assert oracle.e4m3_from_float(float("nan")) & 0x7F == 0x7F
+    assert oracle.e4m3_from_float(2.0 ** -10) == 0x00  # tie to even (0)
+    assert oracle.e4m3_from_float(3 * 2.0 ** -10) == 0x02  # tie to even (2)
+
+
+def test_bf16_rn_matches_torch():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([
+        rng.standard_normal(50000).astype(np.float32) * 10.0 ** rng.integers(-30, 30, 50000),
+        np.array([0.0, -0.0, 1.0, 3.4e38, -3.4e38, 1e-40], np.float32),
+    ]).astype(np.float32)
+    # exact ties: a BF16 value plus half an ULP
+    base = (rng.integers(0, 1 << 16, 2000).astype(np.uint32) << 16) | 0x8000
+    x = np.concatenate([x, base.view(np.float32)])
+    x = x[np.isfinite(x)]
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_from_float(v) for v in x], np.uint16)
+    assert np.array_equal(ref, got)
+
+
+# ------------------------------------------------------- the definition
+
+
+def _sdpa_reference(w, t, h):
+    """Library evaluation of one (token, head): torch SDPA in float64 over the
+    gathered active rows (numpy indexing), the sink as an extra key whose bias
+    equals the sink and whose value row is zero."""
+    D = w["q"].shape[2]
+    W = w["indices"].shape[1]
+    n = max(0, min(int(w["lens"][t]), W))
+    rows = []
+    for c in range(n):
+        r = int(w["indices"][t, c])
+        pool = 1 if (len(w["pools"]) == 2 and c >= w["pool_split"]) else 0
+        if r < 0 or r >= w["pools"][pool].shape[0]:
+            continue
+        rows.append(w["pools"][pool][r])
+    if not rows:
+        return np.zeros(512), -np.inf
+    kv = torch.from_numpy(dec(np.stack(rows)))  # [n, D]
+    q = torch.from_numpy(dec(w["q"][t, h]))[None, None, None, :]  # [1,1,1,D]
+    k = kv[None, None]  # [1,1,n,D]
+    v = kv[None, None, :, :512]
+    bias = torch.zeros(1, 1, 1, kv.shape[0], dtype=torch.float64)
+    if w["sinks"] is not None:
+        k = torch.cat([k, torch.zeros(1, 1, 1, D, dtype=torch.float64)], dim=2)
+        v = torch.cat([v, torch.zeros(1, 1, 1, 512, dtype=torch.float64)], dim=2)
+        bias = torch.cat([bias, torch.full((1, 1, 1, 1), float(w["sinks"][h]), dtype=torch.float64)], -1)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q, k, v, attn_mask=bias, scale=float(w["bmm1_scale"]))
+    logits = (q[0, 0] @ k[0, 0].T)[0] * w["bmm1_scale"] + bias[0, 0, 0]
+    lse = torch.logsumexp(logits, dim=0).item()
+    return out[0, 0, 0].numpy() * w["bmm2_scale"] * w["k_scale"], lse * LOG2E
+
+
+CASES = [
+    dict(name="dense", seed=11, tokens=2, heads=16, width=40, head_dim=576),
+    dict(name="holes_lens", seed=12, tokens=3, heads=16, width=50, head_dim=576, holes=0.3,
+         lens=[50, 17, 33]),
+    dict(name="sinks_512", seed=13, tokens=2, heads=16, width=30, head_dim=512, sinks=True,
+         k_scale=0.05, bmm2_scale=0.5),
+    dict(name="two_pools", seed=14, tokens=2, heads=16, width=37, head_dim=512, two_pools=True,
+         pool_split=13, holes=0.1, sinks=True),
+    dict(name="duplicates", seed=15, tokens=1, heads=16, width=64, head_dim=576,
+         pool_rows=20, duplicates=True),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c["name"] for c in CASES])
+def test_fp64_matches_library_attention(case):
+    w = workloads.small(**case)
+    prob = oracle.Problem.from_workload(w)
+    out, lse = oracle.fp64(prob)
+    T, H = w["q"].shape[:2]
+    for t in range(T):
+        for h in range(H):
+            ref_out, ref_lse = _sdpa_reference(w, t, h)
+            i = t * H + h
+            scale = max(1e-300, np.abs(ref_out).max())
+            assert np.abs(out[i] - ref_out).max() <= 1e-12 * scale
+            assert abs(lse[i] - ref_lse) <= 1e-12 * max(1.0, abs(ref_lse))
+
+
+def test_single_active_key_returns_the_row():
+    w = workloads.small("one", seed=21, tokens=1, heads=16, width=8, head_dim=576, lens=[8])
+    w["indices"][0, :] = -1
+    w["indices"][0, 5] = 77
+    w["k_scale"], w["bmm2_scale"] = 0.25, 0.5
+    prob = oracle.Problem.from_workload(w)
+    out, lse = oracle.fp64(prob)
+    v = dec(w["pools"][0][77, :512]) * 0.125
+    s = dec(w["q"][0]) @ dec(w["pools"][0][77]) * w["bmm1_scale"]
+    assert np.array_equal(out, np.broadcast_to(v, out.shape))
+    assert np.allclose(lse, s * LOG2E, rtol=0, atol=1e-12)
+    # emulating mode: P = 448 exactly, l = 448, so out = BF16(V * scale)
+    val, bits, lse_e = oracle.emulate(prob, splits=3, chunk=2)
+    ref_bits = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(bits.view(np.int16), np.broadcast_to(ref_bits, bits.shape))
+    assert np.allclose(lse_e, s * LOG2E, atol=1e-5)
+
+
+def test_equal_scores_give_the_mean_row():
+    w = workloads.small("eq", seed=22, tokens=1, heads=16, width=100, head_dim=576, holes=0.2)
+    w["q"][:] = 0  # every score 0
+    prob = oracle.Problem.from_workload(w)
+    out, lse = oracle.fp64(prob)
+    act = w["indices"][0][w["indices"][0] >= 0]
+    mean = dec(w["pools"][0][act, :512]).mean(axis=0)
+    assert np.allclose(out, mean[None], rtol=0, atol=1e-14)
+    assert np.allclose(lse, math.log2(act.size), atol=1e-13)
+    val, bits, lse_e = oracle.emulate(prob, splits=2, chunk=32)
+    assert np.allclose(val, mean[None], rtol=0, atol=2e-6 * np.abs(mean).max())
+    assert np.allclose(lse_e, math.log2(act.size), atol=1e-6)
+
+
+def test_permuting_columns_changes_nothing():
+    w = workloads.small("perm", seed=23, tokens=2, heads=16, width=90, head_dim=576, holes=0.15,
+                        sinks=True)
+    prob = oracle.Problem.from_workload(w)
+    out, lse = oracle.fp64(prob)
+    rng = np.random.default_rng(5)
+    for t in range(2):
+        w["indices"][t] = w["indices"][t][rng.permutation(90)]
+    out2, lse2 = oracle.fp64(oracle.Problem.from_workload(w))
+    assert np.allclose(out, out2, rtol=0, atol=1e-12 * np.abs(out).max())
+    assert np.allclose(lse, lse2, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("sinks", [False, True])
+def test_empty_tokens_give_zeros_and_minus_inf(sinks):
+    w = workloads.small("empty", seed=24, tokens=4, heads=16, width=20, head_dim=576,
+                        lens=[0, 20, -5, 7], sinks=sinks)
+    w["indices"][1, :] = -1  # all holes
+    w["indices"][3, :7] = -1  # holes inside the count, active ones past it
+    prob = oracle.Problem.from_workload(w)
+    out, lse = oracle.fp64(prob)
+    val, bits, lse_e = oracle.emulate(prob, splits=2, chunk=8)
+    assert np.all(out == 0) and not np.any(np.signbit(out))
+    assert np.all(np.isneginf(lse))
+    assert np.all(bits == 0)
+    assert np.all(np.isneginf(lse_e))
+
+
+def test_sink_removes_weight_in_closed_form():
+    base = workloads.small("sink", seed=25, tokens=2, heads=16, width=60, head_dim=576,
+                           holes=0.1, sinks=True)
+    with_sink = oracle.fp64(oracle.Problem.from_workload(base))
+    no = dict(base)
+    no["sinks"] = None
+    out0, lse0 = oracle.fp64(oracle.Problem.from_workload(no))
+    sinks = np.tile(base["sinks"].astype(np.float64), 2)
+    # exp(lse) is the denominator; a sink adds exp(sink) to it and nothing to the sum
+    den0 = lse0 / LOG2E
+    frac = 1.0 / (1.0 + np.exp(sinks - den0))
+    assert np.allclose(with_sink[0], out0 * frac[:, None], rtol=1e-12, atol=1e-15)
+    assert np.allclose(with_sink[1], np.logaddexp(den0, sinks) * LOG2E, atol=1e-12)
+
+
+# ---------------------------------------------------- the emulated datapath
+
+
+@pytest.mark.parametrize("splits,chunk", [(1, 128), (2, 16), (3, 7), (4, 1), (7, 5)])
+def test_online_softmax_and_merge_equal_the_definition(splits, chunk):
+    """With P unrounded and no FP32 steps, any partition into chunks and splits
+    must reproduce the plain definition (the running-max rescale and the merge
+    weights cancel exactly)."""
+    w = workloads.small("merge", seed=31, tokens=3, heads=16, width=70, head_dim=576, holes=0.2,
+                        lens=[70, 3, 41], sinks=True)
+    prob = oracle.Problem.from_workload(w)
+    out, lse = oracle.fp64(prob)
+    val, _, lse_e = oracle.emulate(prob, splits, chunk, flags=oracle.EXACT | oracle.NO_P_ROUNDING)
+    assert np.abs(val - out).max() <= 1e-12 * np.abs(out).max()
+    assert np.abs(lse_e - lse).max() <= 1e-12 * np.abs(lse).max()
+
+
+def test_p_anchors_at_the_running_max():
+    """Two active keys in two one-key chunks, the second scoring far higher.
+    Against the running max both P are exactly 448, so the result is the exact
+    softmax; anchored at the final maximum, the first P would be rounded."""
+    w = workloads.small("anchor", seed=32, tokens=1, heads=16, width=2, head_dim=576)
+    w["q"][:] = 0
+    q = np.zeros(576, np.float32)
+    q[0] = 1.0
+    w["q"][0, :] = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    pool = w["pools"][0]
+    pool[:2, 0] = torch.tensor([1.0, 1.5]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    w["indices"][0] = [0, 1]
+    w["bmm1_scale"] = 1.0
+    prob = oracle.Problem.from_workload(w)
+    v0, v1 = dec(pool[0, :512]), dec(pool[1, :512])
+    s0, s1 = 1.0 * LOG2E, 1.5 * LOG2E
+    alpha = 2.0 ** (np.float32(s0) - np.float32(s1))
+    exact = (alpha * v0 + v1) / (alpha + 1)
+    val, _, _ = oracle.emulate(prob, splits=1, chunk=1)
+    assert np.allclose(val[0], exact, rtol=0, atol=1e-5 * np.abs(exact).max())
+    # one chunk: the first P is rounded to E4M3 (torch's codec) before PV
+    p0 = float(torch.tensor([448.0 * alpha], dtype=torch.float32).to(torch.float8_e4m3fn).float())
+    assert p0 != np.float32(448.0 * alpha)  # the test is only meaningful if rounding bites
+    quantised = (p0 * v0 + 448.0 * v1) / (448.0 * alpha + 448.0)
+    val1, _, _ = oracle.emulate(prob, splits=1, chunk=2)
+    assert np.allclose(val1[0], quantised, rtol=0, atol=1e-5 * np.abs(quantised).max())
+    assert np.abs(val1[0] - exact).max() > 1e-3 * np.abs(exact).max()
+
+
+def test_one_chunk_matches_a_float32_library_evaluation():
+    """One split, one chunk: the datapath is P = E4M3(2^(s2 - m + log2 448))
+    with FP32 logits, sums of the unrounded P, FP32 PV, one BF16 rounding --
+    evaluated here with torch float32 ops and torch's E4M3 cast."""
+    w = workloads.small("chunk", seed=33, tokens=2, heads=16, width=100, head_dim=576, holes=0.1)
+    prob = oracle.Problem.from_workload(w)
+    val, bits, lse = oracle.emulate(prob, splits=1, chunk=128)
+    for t in range(2):
+        act = w["indices"][t][w["indices"][t] >= 0]
+        kv = torch.from_numpy(dec(w["pools"][0][act]))
+        q = torch.from_numpy(dec(w["q"][t]))
+        logits = (q @ kv.T).to(torch.float32)  # exact sums rounded once
+        s2 = logits * torch.tensor(w["bmm1_scale"] * LOG2E, dtype=torch.float32)
+        m = s2.max(dim=1, keepdim=True).values
+        p = torch.exp2(s2 - (m - torch.tensor(math.log2(448.0), dtype=torch.float32)))
+        l = p.sum(dim=1, keepdim=True)
+        p8 = p.to(torch.float8_e4m3fn).to(torch.float64)
+        acc = (p8 @ kv[:, :512]).to(torch.float32)
+        ref = (acc * (1.0 / l)).to(torch.float64).numpy()
+        got = val[t * 16:(t + 1) * 16]
+        assert np.abs(got - ref).max() <= 2e-6 * np.abs(ref).max()
+        ref_lse = (m[:, 0] - math.log2(448.0) + torch.log2(l[:, 0])).numpy()
+        assert np.abs(lse[t * 16:(t + 1) * 16] - ref_lse).max() <= 1e-5
