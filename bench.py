@@ -1,0 +1,531 @@
+#!/usr/bin/env python
+"""Benchmark: sparse MLA decode on GB300 (µs per call, achieved HBM GB/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config batch|tiny|verify|two_pool]
+
+A step is one smla_decode call over one batch of seeded synthetic inputs. The
+default workload is the bandwidth-bound batch: 64 tokens x 128 heads x 2048
+top-k keys of 576-byte E4M3 rows from a 1,048,576-row pool, half of each
+token's rows drawn from a shared 20k-row hot set. Inputs are resident in HBM
+before timing; consecutive steps rotate over input sets whose distinct rows
+sum to more than twice the L2, so each step streams its KV rows from HBM.
+
+One JSON line on rank 0:
+  value       algorithmic bytes (unique gathered KV rows + Q + out) / time, GB/s
+  ms_per_step device time per call (CUDA events, max over ranks)
+  roofline    achieved GB/s of the decode kernel vs the measured HBM copy peak
+  e2e         the same metric with host buffers: per step the H2D copy of q,
+              indices and lens from pinned memory, the call, and the D2H copy
+              of out and lse, all inside the timed region
+  cpu_baseline the CPU oracle (fp64 definition) on a bounded sample, all cores
+With --impl reference the same line is produced by the CPU oracle alone.
+Under torchrun (--gpus N > 1) every rank runs an independent replica on its
+own GPU (the path has no exchange step); value sums the ranks' bytes.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s (% of 8 TB/s) for sparse MLA decode"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool"], default="batch")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work of the oracle baseline sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ inputs
+
+
+def make_sets(config: str, rank: int, sets: int):
+    from sparse_mla_decode_gb300 import workloads
+
+    if config == "batch":
+        rng = np.random.default_rng(5000 + rank)
+        pool = workloads.e4m3_normal(rng, (1 << 20, 576))
+        return [workloads.bandwidth_batch(seed=1003 + 101 * rank + r, pool=pool) for r in range(sets)]
+    make = {"tiny": workloads.tiny, "verify": workloads.verify_rows,
+            "two_pool": workloads.two_pool_sinks}[config]
+    base = {"tiny": 1000, "verify": 1001, "two_pool": 1002}[config]
+    return [make(seed=base + 101 * rank + r) for r in range(sets)]
+
+
+def bytes_alg(w) -> int:
+    """Unique gathered KV rows x row bytes + Q + BF16 out (per call)."""
+    from sparse_mla_decode_gb300 import workloads
+
+    T, H, D = w["q"].shape
+    return workloads.unique_active_rows(w) * D + T * H * D + T * H * 512 * 2
+
+
+def flops_alg(w) -> int:
+    T, H, D = w["q"].shape
+    active = 0
+    for t in range(T):
+        n = max(0, min(int(w["lens"][t]), w["indices"].shape[1]))
+        active += int(np.count_nonzero(w["indices"][t, :n] >= 0))
+    return active * H * (2 * D + 2 * 512)
+
+
+def workload_name(config: str, w) -> str:
+    T, H, D = w["q"].shape
+    W = w["indices"].shape[1]
+    desc = {
+        "batch": f"{T} tokens x {H} heads x {W} top-k keys, {D}-byte E4M3 rows, 1,048,576-row pool, "
+                 "~50% of rows shared via a 20k-row hot set",
+        "tiny": f"{T} token x {H} heads x {W} keys, {D}-byte rows, 4096-row pool",
+        "verify": f"{T} verify rows x {H} heads x <= {W} keys, {D}-byte rows, k_scale 0.05, one empty row",
+        "two_pool": f"{T} tokens x {H} heads, width {W} over two pools (128 window + top-k), "
+                    f"{D}-byte rows, sinks",
+    }[config]
+    return f"{w['name']}: {desc}"
+
+
+# -------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9 or not (t0 - 0.15 <= ts <= t1 + 0.15):
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, name in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(name)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = data.get(config)
+    if not entry or entry.get("kernel_sha") != kernel_sha():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def cpu_oracle_rate(sets, seconds: float):
+    """Times the fp64 oracle on a bounded sample of (token, head) pairs of the
+    first input set, on all host cores. Returns (GB/s-equivalent, seconds per
+    full call, cores, sample description)."""
+    from oracle import oracle
+
+    w = sets[0]
+    T, H = w["q"].shape[:2]
+    prob = oracle.Problem.from_workload(w)
+    cores = oracle.max_threads()
+    rng = np.random.default_rng(11)
+    n = min(T * H, max(cores, 16))
+    pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
+    t0 = time.perf_counter()
+    oracle.fp64(prob, pairs, threads=cores)
+    per_pair = (time.perf_counter() - t0) / n
+    n = int(min(T * H, max(n, seconds / max(per_pair, 1e-9))))
+    pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
+    t0 = time.perf_counter()
+    oracle.fp64(prob, pairs, threads=cores)
+    elapsed = time.perf_counter() - t0
+    per_call = elapsed / n * T * H
+    rate = bytes_alg(w) / per_call / 1e9
+    return rate, per_call, cores, f"{n} of {T * H} (token, head) pairs of one call, {elapsed:.1f} s"
+
+
+# --------------------------------------------------------------- our arm
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+    from sparse_mla_decode_gb300 import smla
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    sets_n = 6 if args.config == "batch" else 8
+    sets = make_sets(args.config, rank, sets_n)
+    pools_dev = {}
+    dsets = []
+    for w in sets:
+        key = id(w["pools"][0])
+        if key not in pools_dev:
+            pools_dev[key] = [torch.from_numpy(p).to(dev) for p in w["pools"]]
+        T, H, _ = w["q"].shape
+        dsets.append({
+            "q": torch.from_numpy(w["q"]).to(dev),
+            "pools": pools_dev[key],
+            "indices": torch.from_numpy(w["indices"]).to(dev),
+            "lens": torch.from_numpy(w["lens"]).to(dev),
+            "sinks": None if w["sinks"] is None else torch.from_numpy(w["sinks"]).to(dev),
+            "out": torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((T, H), dtype=torch.float32, device=dev),
+        })
+    byts = [bytes_alg(w) for w in sets]
+    flops = [flops_alg(w) for w in sets]
+    T, H, D = sets[0]["q"].shape
+    shape = smla.make_shape(T, H, sets[0]["indices"].shape[1], D, len(sets[0]["pools"]),
+                            sets[0].get("pool_split", 0))
+    plan = smla.smla_plan_for(shape)
+    stream = torch.cuda.current_stream(dev)
+    flush = None if args.config == "batch" else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def call(i):
+        w, d = sets[i % len(sets)], dsets[i % len(sets)]
+        smla.smla_decode(d["q"], d["pools"], d["indices"], d["lens"], d["sinks"], w["bmm1_scale"],
+                         w["bmm2_scale"], w["k_scale"], d["out"], d["lse"], stream=stream,
+                         pool_split=w.get("pool_split", 0))
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(max(3, args.warmup)):
+        call(i)
+    barrier()
+    if smla.smla_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    t_wall0 = time.time()
+    if flush is None:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            call(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = start.elapsed_time(end)
+    else:  # latency workloads: L2 flushed before every timed call
+        elapsed_ms = 0.0
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            call(i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in evs)
+    t_wall1 = time.time()
+    # keep the GPU under the same load for the clock sampler when the timed
+    # region was shorter than a few samples
+    soak_until = t_wall1 + max(0.0, 0.6 - (t_wall1 - t_wall0))
+    i = 0
+    while time.time() < soak_until:
+        for _ in range(200):
+            call(i)
+            i += 1
+        torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, max(t_wall1, soak_until))
+    if smla.smla_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    step_bytes = float(np.mean([byts[i % len(byts)] for i in range(args.steps)]))
+    step_flops = float(np.mean([flops[i % len(flops)] for i in range(args.steps)]))
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        b = torch.tensor([step_bytes], dtype=torch.float64, device=dev)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+        total_bytes = float(b.item())
+    else:
+        total_bytes = step_bytes
+    ms = elapsed_ms / args.steps
+    value = total_bytes / (ms * 1e-3) / 1e9
+
+    # end to end through the public API, host buffers in pinned memory
+    e2e = None
+    if not args.no_e2e:
+        hq = [torch.from_numpy(w["q"]).pin_memory() for w in sets]
+        hi = [torch.from_numpy(w["indices"]).pin_memory() for w in sets]
+        hl = [torch.from_numpy(w["lens"]).pin_memory() for w in sets]
+        ho = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+        hlse = torch.empty((T, H), dtype=torch.float32).pin_memory()
+        h2d = hq[0].numel() + hi[0].numel() * 4 + hl[0].numel() * 4
+        d2h = ho.numel() * 2 + hlse.numel() * 4
+
+        def e2e_step(i):
+            k = i % len(sets)
+            d = dsets[k]
+            d["q"].copy_(hq[k], non_blocking=True)
+            d["indices"].copy_(hi[k], non_blocking=True)
+            d["lens"].copy_(hl[k], non_blocking=True)
+            call(k)
+            ho.copy_(d["out"], non_blocking=True)
+            hlse.copy_(d["lse"], non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        barrier()
+        steps = min(args.steps, 500)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(steps):
+            e2e_step(i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1) / steps
+        if dist is not None:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        return
+    peak, peak_src = measured_hbm_peak()
+    achieved = step_bytes / (ms * 1e-3) / 1e9  # this rank's kernel
+    traffic = ncu_traffic(args.config)
+    cpu = None
+    if not args.no_cpu:
+        rate, per_call, cores, sample = cpu_oracle_rate(sets, args.cpu_seconds)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": sample, "us_per_call": round(per_call * 1e6, 1)}
+    fp8_peak_tflops = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            fp8_peak_tflops = 2.0 * float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        fp8_peak_tflops = 2.0 * 1900.0
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 6),
+        "us_per_call": round(ms * 1e3, 3),
+        "pct_of_8tbs": round(100.0 * achieved / NOMINAL_HBM_GBS, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {
+            "workload": workload_name(args.config, sets[0]),
+            "tokens": int(T), "heads": int(H), "width": int(sets[0]["indices"].shape[1]),
+            "head_dim": int(D), "input_sets": len(sets),
+            "l2": ("rotating %d input sets (distinct rows per set ~%.0f MB) between back-to-back calls"
+                   % (len(sets), np.mean(byts) / 1e6)) if flush is None else
+                  "L2 flushed (256 MB write) before every timed call",
+            "plan": plan,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": peak_src,
+            "traffic": traffic, "bytes_alg_per_launch": int(step_bytes),
+            "tensor_tflops": round(step_flops / (ms * 1e-3) / 1e12, 2),
+            "tensor_frac_of_fp8_peak": round(step_flops / (ms * 1e-3) / 1e12 / fp8_peak_tflops, 4),
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(args.steps),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------- reference arm
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle (fp64 definition) as the reference implementation; rank 0
+    alone runs it, on a bounded sample of each step's workload."""
+    if rank != 0:
+        return
+    from oracle import oracle
+
+    oracle.build()
+    sets = make_sets(args.config, 0, 1)
+    w = sets[0]
+    T, H, D = w["q"].shape
+    prob = oracle.Problem.from_workload(w)
+    cores = oracle.max_threads()
+    rng = np.random.default_rng(13)
+    probe = min(T * H, max(cores, 16))
+    pairs = np.stack([rng.integers(0, T, probe), rng.integers(0, H, probe)], axis=1)
+    t0 = time.perf_counter()
+    oracle.fp64(prob, pairs, threads=cores)
+    per_pair = (time.perf_counter() - t0) / probe
+    total_steps = max(1, args.steps + args.warmup)
+    budget = 120.0  # seconds for the whole run
+    n = int(max(1, min(T * H, budget / total_steps / max(per_pair, 1e-9))))
+    for _ in range(args.warmup):
+        pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
+        oracle.fp64(prob, pairs, threads=cores)
+    elapsed = 0.0
+    for _ in range(args.steps):
+        pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
+        t0 = time.perf_counter()
+        oracle.fp64(prob, pairs, threads=cores)
+        elapsed += time.perf_counter() - t0
+    per_call = elapsed / args.steps / n * T * H
+    value = bytes_alg(w) / per_call / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_call * 1e3, 3),
+        "us_per_call": round(per_call * 1e6, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": workload_name(args.config, w), "tokens": int(T), "heads": int(H),
+                   "width": int(w["indices"].shape[1]), "head_dim": int(D)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {T * H} (token, head) pairs per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

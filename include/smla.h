@@ -1,0 +1,138 @@
+/*
+ * smla.h -- C ABI of the sparse MLA decode library (libsmla.so, sm_103a).
+ *
+ * The operation (DeepSeek-V4.1 page "sparse_mla_cute", module docstring, "The
+ * problem" and "What this module computes"; Kimi K3.1 page "attn_sparse",
+ * module docstring and its "Precision" paragraph):
+ *
+ *   for each token t and head h, over the token's active columns c
+ *   (c < clamp(lens[t], 0, width) and indices[t, c] >= 0):
+ *     s_c  = bmm1_scale * q[t, h, :] . kv_c[:]          (all head_dim bytes)
+ *     out[t, h, j] = bmm2_scale * k_scale * sum_c p_c kv_c[j] / den,  j < 512
+ *     p_c  = exp(s_c - m),  den = sum_c p_c + exp(sink_h - m),  m = max(s, sink)
+ *     lse[t, h] = log2(den) + m * log2(e)               (base 2)
+ *   where kv_c is row indices[t, c] of pool 0 when c < pool_split and of pool 1
+ *   otherwise (a single pool serves every column when num_pools == 1).
+ *   A token without active columns gets out = +0.0 and lse = -inf.
+ *
+ * Datapath: E4M3 q and KV, FP32 logits, a base-2 online softmax over chunks of
+ * 128 columns, P rounded to E4M3 (RN, satfinite) at 448 of the running maximum
+ * of the split, FP32 sums of the unrounded P, FP32 accumulation, an FP32 merge
+ * of the key splits over distributed shared memory, one BF16 rounding.
+ *
+ * All functions are thread-safe. Device buffers are owned by the caller; the
+ * library allocates no device memory.
+ */
+#ifndef SMLA_H
+#define SMLA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define SMLA_OK 0
+#define SMLA_EINVAL (-1)       /* null pointer, bad shape, stride or alignment */
+#define SMLA_EUNSUPPORTED (-2) /* a shape outside what the kernels handle */
+#define SMLA_ECUDA (-3)        /* a CUDA runtime call failed (see smla_last_cuda_error) */
+#define SMLA_EDEVICE (-4)      /* the device reported an error (smla_device_error) */
+
+/* Device error bits, set by the kernels in the library's device error word. */
+#define SMLA_DEV_INDEX_RANGE 1 /* an index >= pool rows (that column was masked) */
+#define SMLA_DEV_TIMEOUT 2     /* a bounded wait gave up; outputs are invalid */
+
+/* One KV pool: `rows` rows of `row_bytes` E4M3 bytes, rows contiguous, in
+ * device memory; data 16-byte aligned. row_bytes must equal shape.head_dim. */
+typedef struct smla_pool {
+    const void* data;
+    int64_t rows;
+    int32_t row_bytes;
+    int32_t reserved; /* 0 */
+} smla_pool;
+
+/* Sizes and strides of one call.
+ *   tokens T >= 0, heads H (a positive multiple of 16, <= 1024), width W >= 0,
+ *   head_dim D in {512, 576} (576 = 512 latent + 64 rope; V is the first 512),
+ *   num_pools in {1, 2}, pool_split in [0, W] (used when num_pools == 2).
+ *   q element (t, h, d) at q + t*q_stride_token + h*q_stride_head + d (bytes;
+ *   both strides multiples of 16, q 16-byte aligned).
+ *   indices element (t, c) at indices[t*idx_stride_token + c] (int32 elements,
+ *   idx_stride_token >= W).
+ *   out element (t, h, j) at out[t*out_stride_token + h*out_stride_head + j]
+ *   (bf16 elements; strides even, out 4-byte aligned).
+ *   lse element (t, h) at lse[t*lse_stride_token + h] (float elements). */
+typedef struct smla_shape {
+    int32_t tokens, heads, width, head_dim;
+    int32_t num_pools, pool_split;
+    int64_t q_stride_token, q_stride_head;
+    int64_t idx_stride_token;
+    int64_t out_stride_token, out_stride_head;
+    int64_t lse_stride_token;
+} smla_shape;
+
+/* The launch the library picks for a shape (returned for tests, sweeps and
+ * the emulating oracle, which replays `splits` and `chunk`). */
+typedef struct smla_plan {
+    int32_t head_tile;        /* heads per CTA (16, 32 or 64) */
+    int32_t head_groups;      /* heads / head_tile */
+    int32_t chunk;            /* columns per chunk (128) */
+    int32_t chunks;           /* ceil(width / chunk) */
+    int32_t splits;           /* CTAs per (token, head group) = cluster size */
+    int32_t chunks_per_split; /* ceil(chunks / splits) */
+    int32_t ctas;             /* tokens * head_groups * splits */
+    int32_t threads;          /* threads per CTA */
+    int32_t smem_bytes;       /* dynamic shared memory per CTA */
+    int32_t tmem_columns;     /* tensor-memory columns allocated per CTA */
+    int32_t num_sms;          /* SM count the plan was made for */
+    int32_t reserved;
+} smla_plan;
+
+/* Fills *plan for `shape` on a GPU of `num_sms` SMs (num_sms <= 0: the current
+ * device's SM count, which needs a CUDA device). Pure host logic otherwise.
+ * The environment variable SMLA_SPLITS, when set to a positive integer, forces
+ * the split count (clamped to [1, min(chunks, 16)]).
+ * Returns SMLA_OK, SMLA_EINVAL or SMLA_EUNSUPPORTED. */
+int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* plan);
+
+/* Sparse MLA decode (the operation above), asynchronous on `stream`.
+ *   shape     host pointer, see smla_shape.
+ *   q         device, E4M3 [T, H, D] bytes.
+ *   kv_pools  host array of shape->num_pools descriptors (data in device memory).
+ *   indices   device, int32 [T, >= W], -1 marks a hole.
+ *   lens      device, int32 [T], active count per token, clamped to [0, W].
+ *   sinks     device, float [H] per-head sink in score units, or NULL.
+ *   bmm1_scale  multiplies the q.kv dot products (fold q and k scales in here).
+ *   bmm2_scale, k_scale  multiply the output.
+ *   out       device, BF16 [T, H, 512].
+ *   lse       device, float [T, H] base-2 log-sum-exp, or NULL.
+ *   stream    a cudaStream_t (NULL: the legacy default stream).
+ * Launched with programmatic dependent launch: the kernel reads its inputs only
+ * after the previous kernel in the stream has completed.
+ * Captureable in a CUDA graph (no allocation, no synchronisation).
+ * Errors: SMLA_EINVAL / SMLA_EUNSUPPORTED before anything is launched,
+ * SMLA_ECUDA when the launch fails. Device-side conditions (an index beyond its
+ * pool, a wait that timed out) are recorded in the device error word. */
+int smla_decode(const smla_shape* shape, const void* q, const smla_pool* kv_pools,
+                const int32_t* indices, const int32_t* lens, const float* sinks,
+                float bmm1_scale, float bmm2_scale, float k_scale, void* out, float* lse,
+                void* stream);
+
+/* Reads and clears the current device's error word (SMLA_DEV_* bits) after
+ * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
+int smla_device_error(int32_t* bits);
+
+/* A static string for a return code. */
+const char* smla_error_string(int code);
+
+/* The last CUDA error code seen by this thread (0 if none). */
+int smla_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int smla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMLA_H */

@@ -1,0 +1,17 @@
+"""Sparse MLA decode attention for GB300 (sm_103a).
+
+The compute lives in ``libsmla.so`` (hand-written CUDA, C ABI in
+``include/smla.h``); :mod:`sparse_mla_decode_gb300.smla` is its thin Python
+binding and :mod:`sparse_mla_decode_gb300.workloads` draws seeded inputs.
+"""
+
+from .smla import (  # noqa: F401
+    SmlaError,
+    decode,
+    load,
+    make_shape,
+    smla_decode,
+    smla_device_error,
+    smla_plan_for,
+    smla_version,
+)

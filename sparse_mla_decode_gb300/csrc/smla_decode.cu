@@ -1,0 +1,778 @@
+// smla_decode.cu -- sparse MLA decode attention for sm_103a, and the C ABI
+// declared in include/smla.h.
+//
+// The operation is the one stated on the DeepSeek-V4.1 "sparse_mla_cute" page
+// (module docstring, "What this module computes"): per token and head, softmax
+// attention over the token's active gathered KV rows, with optional per-head
+// sinks. The datapath follows the Kimi K3.1 "attn_sparse" page (module
+// docstring, per-chunk steps and "Precision"; SparseDcpDecode.merge): FP32
+// logits, base-2 online softmax per chunk, P rounded to E4M3 at 448 of the
+// running maximum, FP32 sums of the unrounded P, FP32 accumulation, an FP32
+// merge of the key splits across a thread-block cluster, one BF16 rounding.
+//
+// GB300 design (one CTA per SM, 288 threads):
+//   warps 0-3  softmax: one thread per key of a 128-key chunk (the TMEM lane of
+//              S^T), per-head maxima by warp reductions + shared memory, P as
+//              E4M3 into shared memory, rescale of O^T in TMEM, epilogue/merge;
+//   warp 4     allocates TMEM and issues the tcgen05 MMAs from one thread;
+//   warps 5-8  gather: 16-byte cp.async copies of the chunk's KV rows (and the
+//              Q tile) into 128B-swizzled K-major tiles, zero-filling masked
+//              columns; two stages so the next chunk streams during compute.
+// Both products put the long side on the MMA's M = 128 and the heads on N, as
+// the DeepSeek page sketches:
+//   S^T[key, head]   = KV[key, :] . Q[head, :]      (A = KV K-major, B = Q K-major)
+//   O^T[lat, head]  += V^T[lat, key] . P^T[key, head] (A = the same KV tile read
+//                      MN-major, B = P^T K-major), four 128-latent blocks.
+// TMEM holds two S^T buffers (2N columns) and O^T (4N columns).
+// Key splits of one (token, head tile) form a cluster and merge over DSMEM.
+// Every wait is bounded; a timeout sets an error bit and the kernel still
+// returns (and frees its TMEM).
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "smla.h"
+#include "smla_ptx.cuh"
+
+namespace smla {
+
+constexpr int kChunk = 128;  // keys per chunk = the MMA's M
+constexpr int kLatent = 512;
+constexpr int kThreads = 288;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kMmaWarp = 4;
+constexpr int kGatherBase = 160;
+constexpr int kGatherThreads = 128;
+constexpr int kMaxSplits = 16;
+constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
+
+__device__ int32_t g_device_error;
+
+struct Params {
+    const uint8_t* q;
+    int64_t q_stride_token, q_stride_head;
+    const uint8_t* pool0;
+    const uint8_t* pool1;
+    int64_t rows0, rows1;
+    const int32_t* indices;
+    int64_t idx_stride;
+    const int32_t* lens;
+    const float* sinks;
+    __nv_bfloat16* out;
+    int64_t out_stride_token, out_stride_head;
+    float* lse;
+    int64_t lse_stride_token;
+    int32_t width, pool_split, num_pools, splits, chunks_per_split;
+    float scale_log2, out_scale;
+};
+
+// Shared-memory map of one CTA for N heads and D-byte rows (offsets from a
+// 1024-byte aligned base; every MMA operand tile starts on 1024 bytes).
+template <int N, int D>
+struct Layout {
+    static constexpr int kBlocks = (D + 127) / 128;  // 128-byte K blocks per row (5 or 4)
+    static constexpr int kPieces = D / 16;           // 16-byte pieces per row
+    static constexpr int kStage = kBlocks * kChunk * 128;
+    static constexpr int kKv = 0;
+    static constexpr int kQ = 2 * kStage;
+    static constexpr int kP = kQ + kBlocks * N * 128;
+    static constexpr int kIdx = kP + N * 128;         // int32 [2][128] row of each key, -1 masked
+    static constexpr int kRed = kIdx + 2 * kChunk * 4;  // float [4][N] per-warp partials
+    static constexpr int kHead = kRed + 4 * N * 4;      // float [4][N]: m_run, bias, alpha, l
+    static constexpr int kBar = kHead + 4 * N * 4;      // 16 mbarriers
+    static constexpr int kMisc = kBar + 16 * 8;         // tmem base, abort flag
+    static constexpr int kBytes = kMisc + 64;
+    static constexpr int kAlloc = kBytes + 1024;
+    static constexpr int kTmemCols = 6 * N <= 128 ? 128 : (6 * N <= 256 ? 256 : 512);
+    static constexpr int kMergeLimit = kP;  // the merge reuses KV + Q space
+};
+
+// Byte offset of 16-byte piece `piece` of row `row` in a K-major tile of
+// `rows` rows made of 128-byte K blocks, 128B-swizzled (16-byte unit u of a
+// row lands at u ^ (row % 8)).
+__device__ __forceinline__ uint32_t swizzled_piece(int row, int piece, int rows) {
+    const int block = piece >> 3, unit = piece & 7;
+    return static_cast<uint32_t>(block * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
+                                 ((unit ^ (row & 7)) << 4));
+}
+
+// Byte offset of element (head, key) in the K-major 128B-swizzled P^T tile.
+__device__ __forceinline__ uint32_t p_offset(int head, int key) {
+    return static_cast<uint32_t>((head >> 3) * 1024 + (head & 7) * 128 +
+                                 ((((key >> 4) ^ (head & 7))) << 4) + (key & 15));
+}
+
+template <int N, int D>
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __grid_constant__ Params p) {
+    using L = Layout<N, D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+    uint64_t* kv_full = bars + 0;   // [2] gather of a stage landed (128 arrivals)
+    uint64_t* kv_empty = bars + 2;  // [2] PV of a stage done (commit)
+    uint64_t* s_full = bars + 4;    // [2] QK of a chunk done (commit)
+    uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (128 arrivals)
+    uint64_t* o_done = bars + 7;    // PV of a chunk done (commit)
+    uint64_t* drain = bars + 8;     // every MMA done (commit)
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::kIdx);
+    float* red = reinterpret_cast<float*>(smem + L::kRed);
+    float* m_run_s = reinterpret_cast<float*>(smem + L::kHead);
+    float* bias_s = m_run_s + N;
+    float* alpha_s = m_run_s + 2 * N;
+    float* l_s = m_run_s + 3 * N;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int splits = p.splits;
+    const int split = static_cast<int>(blockIdx.x) % splits;  // == rank in the cluster
+    const int head0 = (static_cast<int>(blockIdx.x) / splits) * N;
+    const int token = blockIdx.y;
+
+    // ---- set-up (reads no input, so it overlaps the previous kernel) -------
+    if (tid == 0) {
+        mbar_init(&kv_full[0], kGatherThreads);
+        mbar_init(&kv_full[1], kGatherThreads);
+        mbar_init(&kv_empty[0], 1);
+        mbar_init(&kv_empty[1], 1);
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(p_full, kSoftmaxThreads);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        misc[1] = 0;
+        mbar_init_fence();
+    }
+    if (tid < N) {
+        m_run_s[tid] = -INFINITY;
+        bias_s[tid] = -INFINITY;
+        alpha_s[tid] = 1.0f;
+        l_s[tid] = 0.0f;
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(misc, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    grid_dependency_wait();  // inputs are read only after this point
+    const int count = min(max(p.lens[token], 0), p.width);
+    const int chunks_total = (count + kChunk - 1) / kChunk;
+    const int c_first = split * p.chunks_per_split;
+    const int nch = max(0, min(p.chunks_per_split, chunks_total - c_first));
+    grid_launch_dependents();
+
+    bool ok = true;
+    if (warp >= kGatherBase / 32) {
+        // ================================================= gather warps
+        const int g = tid - kGatherBase;
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            if (c >= 2) ok &= mbar_wait_bounded(&kv_empty[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
+            const int col0 = (c_first + c) * kChunk;
+            {
+                const int col = col0 + g;
+                int32_t id = -1;
+                if (col < count) {
+                    const int32_t raw = p.indices[static_cast<int64_t>(token) * p.idx_stride + col];
+                    const bool second = p.num_pools == 2 && col >= p.pool_split;
+                    const int64_t rows = second ? p.rows1 : p.rows0;
+                    if (raw >= 0) {
+                        if (raw < rows)
+                            id = raw;
+                        else
+                            atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
+                    }
+                }
+                idx_s[b * kChunk + g] = id;
+            }
+            named_barrier(2, kGatherThreads);
+            if (c == 0) {  // the Q tile of this CTA's heads, once
+                const uint8_t* qt = p.q + static_cast<int64_t>(token) * p.q_stride_token +
+                                    static_cast<int64_t>(head0) * p.q_stride_head;
+                for (int i = g; i < N * L::kPieces; i += kGatherThreads) {
+                    const int h = i / L::kPieces, pc = i - h * L::kPieces;
+                    cp_async_16(sbase + L::kQ + swizzled_piece(h, pc, N),
+                                qt + static_cast<int64_t>(h) * p.q_stride_head + pc * 16, 16u);
+                }
+            }
+            const uint32_t stage = sbase + L::kKv + b * L::kStage;
+            for (int i = g; i < kChunk * L::kPieces; i += kGatherThreads) {
+                const int k = i / L::kPieces, pc = i - k * L::kPieces;
+                const int32_t id = idx_s[b * kChunk + k];
+                const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
+                const uint8_t* src = second ? p.pool1 : p.pool0;
+                uint32_t bytes = 0;
+                if (id >= 0) {
+                    src += static_cast<int64_t>(id) * D + pc * 16;
+                    bytes = 16;
+                }
+                cp_async_16(stage + swizzled_piece(k, pc, kChunk), src, bytes);
+            }
+            cp_async_commit();
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            mbar_arrive(&kv_full[b]);
+        }
+        cp_async_wait_all();
+    } else if (warp == kMmaWarp) {
+        // ================================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_e4m3(128, N, 0, 0);
+            constexpr uint32_t kIdescPV = idesc_e4m3(128, N, 1, 0);
+            auto issue_pv = [&](int c) {
+                const uint32_t stage = sbase + L::kKv + (c & 1) * L::kStage;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 32; ++kk) {
+                        const uint64_t a = smem_desc(stage + j * kChunk * 128 + kk * 32 * 128, 1024, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(sbase + L::kP + kk * 32, 1024, 1024, kSwizzle128B);
+                        mma_f8(tmem + 2 * N + j * N, a, bd, kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(o_done);
+                mma_commit(&kv_empty[c & 1]);
+            };
+            for (int c = 0; c < nch; ++c) {
+                const int b = c & 1;
+                ok &= mbar_wait_bounded(&kv_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+                tc_fence_after_sync();
+                const uint32_t stage = sbase + L::kKv + b * L::kStage;
+#pragma unroll
+                for (int kb = 0; kb < L::kBlocks; ++kb) {
+                    const int steps = (kb < 4) ? 4 : (D - 512) / 32;
+                    for (int ks = 0; ks < steps; ++ks) {
+                        const uint64_t a = smem_desc(stage + kb * kChunk * 128 + ks * 32, 1024, 1024, kSwizzle128B);
+                        const uint64_t bq = smem_desc(sbase + L::kQ + kb * N * 128 + ks * 32, 1024, 1024, kSwizzle128B);
+                        mma_f8(tmem + b * N, a, bq, kIdescQK, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(&s_full[b]);
+                if (c >= 1) {
+                    ok &= mbar_wait_bounded(p_full, (c - 1) & 1, abort_flag, kWaitLimitNs);
+                    tc_fence_after_sync();
+                    issue_pv(c - 1);
+                }
+            }
+            if (nch >= 1) {
+                ok &= mbar_wait_bounded(p_full, (nch - 1) & 1, abort_flag, kWaitLimitNs);
+                tc_fence_after_sync();
+                issue_pv(nch - 1);
+            }
+            mma_commit(drain);
+        }
+        __syncwarp();
+    } else {
+        // ===================================================== softmax
+        // Thread tid owns key tid of each chunk (TMEM lane tid of S^T) and,
+        // for O^T, latent rows 32 * warp + lane of each 128-latent block.
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const float scale_log2 = p.scale_log2;
+        float lsum[N];
+#pragma unroll
+        for (int h = 0; h < N; ++h) lsum[h] = 0.0f;
+        uint8_t* pt = smem + L::kP;
+
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            if (c > 0) ok &= mbar_wait_bounded(o_done, (c - 1) & 1, abort_flag, kWaitLimitNs);
+            ok &= mbar_wait_bounded(&kv_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+            ok &= mbar_wait_bounded(&s_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+            tc_fence_after_sync();
+            const bool active = idx_s[b * kChunk + tid] >= 0;
+            const uint32_t s_cols = tmem + lane_base + b * N;
+
+            // chunk maxima per head (log2 units; masked keys are -inf)
+#pragma unroll
+            for (int gq = 0; gq < N / 16; ++gq) {
+                float v[16];
+                tmem_load16(s_cols + gq * 16, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float x = active ? v[j] * scale_log2 : -INFINITY;
+                    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, float_to_ordered(x));
+                    if (lane == j) red[warp * N + gq * 16 + j] = ordered_to_float(m);
+                }
+            }
+            named_barrier(1, kSoftmaxThreads);
+            if (tid < N) {
+                const float cm = fmaxf(fmaxf(red[tid], red[N + tid]), fmaxf(red[2 * N + tid], red[3 * N + tid]));
+                const float mo = m_run_s[tid];
+                const float mn = fmaxf(mo, cm);
+                alpha_s[tid] = (mo == -INFINITY) ? 1.0f : fast_exp2(mo - mn);
+                bias_s[tid] = mn - kLog2P;
+                m_run_s[tid] = mn;
+            }
+            named_barrier(1, kSoftmaxThreads);
+
+            // P = 2^(s2 - m + log2 448) -> E4M3 into P^T; FP32 sums of the unrounded P
+#pragma unroll
+            for (int gq = 0; gq < N / 16; ++gq) {
+                float v[16];
+                tmem_load16(s_cols + gq * 16, v);
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const int h = gq * 16 + j;
+                    float p0 = 0.0f, p1 = 0.0f;
+                    if (active) {
+                        p0 = fast_exp2(v[j] * scale_log2 - bias_s[h]);
+                        p1 = fast_exp2(v[j + 1] * scale_log2 - bias_s[h + 1]);
+                    }
+                    lsum[h] = lsum[h] * alpha_s[h] + p0;
+                    lsum[h + 1] = lsum[h + 1] * alpha_s[h + 1] + p1;
+                    const uint32_t pair = e4m3x2(p0, p1);
+                    pt[p_offset(h, tid)] = static_cast<uint8_t>(pair & 0xFFu);
+                    pt[p_offset(h + 1, tid)] = static_cast<uint8_t>(pair >> 8);
+                }
+            }
+            // O^T *= alpha where a head's running maximum rose (PV(c-1) is done)
+            if (c > 0) {
+#pragma unroll
+                for (int gq = 0; gq < N / 16; ++gq) {
+                    float a[16];
+                    bool rescale = false;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        a[j] = alpha_s[gq * 16 + j];
+                        rescale |= a[j] != 1.0f;
+                    }
+                    if (rescale) {
+#pragma unroll
+                        for (int blk = 0; blk < 4; ++blk) {
+                            const uint32_t col = tmem + lane_base + 2 * N + blk * N + gq * 16;
+                            float v[16];
+                            tmem_load16(col, v);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[j] *= a[j];
+                            tmem_store16(col, v);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(p_full);
+        }
+        if (nch > 0) ok &= mbar_wait_bounded(o_done, (nch - 1) & 1, abort_flag, kWaitLimitNs);
+        tc_fence_after_sync();
+
+        // per-head totals of the per-thread partial sums
+#pragma unroll
+        for (int h = 0; h < N; ++h) {
+            float s = lsum[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+            if (lane == (h & 31)) red[warp * N + h] = s;
+        }
+        named_barrier(1, kSoftmaxThreads);
+        if (tid < N) l_s[tid] = (red[tid] + red[N + tid]) + (red[2 * N + tid] + red[3 * N + tid]);
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        atomicOr(&g_device_error, SMLA_DEV_TIMEOUT);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+
+    // ================================================ epilogue / merge
+    const bool split_empty = (m_run_s[0] == -INFINITY);  // no active key in this split
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    if (splits == 1) {
+        if (tid < N) {
+            const int h = head0 + tid;
+            const float m = m_run_s[tid];
+            float scale = 0.0f, lse2 = -INFINITY;
+            if (m != -INFINITY) {
+                float top = m, extra = 0.0f;
+                if (p.sinks != nullptr) {
+                    const float s2 = p.sinks[h] * kLog2e;
+                    top = fmaxf(m, s2);
+                    extra = 448.0f * fast_exp2(s2 - top);
+                }
+                const float w = fast_exp2(m - top);
+                const float total = l_s[tid] * w + extra;
+                scale = p.out_scale * w / total;
+                lse2 = top - kLog2P + log2f(total);
+            }
+            bias_s[tid] = scale;
+            if (p.lse != nullptr) p.lse[static_cast<int64_t>(token) * p.lse_stride_token + h] = lse2;
+        }
+        named_barrier(3, kThreads);
+        if (tid < kSoftmaxThreads) {
+            __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
+                                 static_cast<int64_t>(head0) * p.out_stride_head;
+#pragma unroll 1
+            for (int blk = 0; blk < 4; ++blk) {
+                const int lat = blk * 128 + warp * 32 + lane;
+#pragma unroll
+                for (int gq = 0; gq < N / 16; ++gq) {
+                    float v[16];
+                    if (!split_empty) tmem_load16(tmem + lane_base + 2 * N + blk * N + gq * 16, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float x = split_empty ? 0.0f : v[j] * bias_s[gq * 16 + j];
+                        out[static_cast<int64_t>(gq * 16 + j) * p.out_stride_head + lat] = __float2bfloat16_rn(x);
+                    }
+                }
+            }
+        }
+    } else {
+        // Partials of every split of this (token, head tile) meet at the CTA
+        // owning their latent slice: slice s (latent 32 s .. 32 s + 31, s < 16)
+        // belongs to rank s % splits. The areas reuse the KV and Q tiles.
+        const int slots = (16 + splits - 1) / splits;
+        const uint32_t inbox = sbase;                                   // float [S][slots][N][32]
+        const uint32_t stats = inbox + splits * slots * N * 32 * 4;     // float [S][2][N]
+        float* stats_f = reinterpret_cast<float*>(smem + splits * slots * N * 32 * 4);
+        float* weight_f = stats_f + splits * 2 * N;                     // float [S][N]
+        const float* inbox_f = reinterpret_cast<const float*>(smem);
+        cluster_sync_all();  // every CTA of the cluster is past its main loop
+        if (tid < N) {
+            for (int r = 0; r < splits; ++r) {
+                st_cluster_f32(map_to_rank(stats + ((split * 2 + 0) * N + tid) * 4, r), m_run_s[tid]);
+                st_cluster_f32(map_to_rank(stats + ((split * 2 + 1) * N + tid) * 4, r), l_s[tid]);
+            }
+        }
+        if (tid < kSoftmaxThreads && !split_empty) {
+#pragma unroll 1
+            for (int blk = 0; blk < 4; ++blk) {
+                const int slice = blk * 4 + warp;
+                const int owner = slice % splits, slot = slice / splits;
+                const uint32_t dst = map_to_rank(inbox + (((split * slots + slot) * N) * 32 + lane) * 4, owner);
+#pragma unroll
+                for (int gq = 0; gq < N / 16; ++gq) {
+                    float v[16];
+                    tmem_load16(tmem + lane_base + 2 * N + blk * N + gq * 16, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) st_cluster_f32(dst + (gq * 16 + j) * 32 * 4, v[j]);
+                }
+            }
+        }
+        cluster_sync_all();  // every partial has landed
+        if (tid < N) {
+            const int h = head0 + tid;
+            float top = -INFINITY;
+            for (int s = 0; s < splits; ++s) top = fmaxf(top, stats_f[(s * 2) * N + tid]);
+            float lse2 = -INFINITY;
+            if (top == -INFINITY) {
+                for (int s = 0; s < splits; ++s) weight_f[s * N + tid] = 0.0f;
+            } else {
+                float extra = 0.0f;
+                if (p.sinks != nullptr) {
+                    const float s2 = p.sinks[h] * kLog2e;
+                    top = fmaxf(top, s2);
+                    extra = 448.0f * fast_exp2(s2 - top);
+                }
+                float total = 0.0f;
+                for (int s = 0; s < splits; ++s) {
+                    const float m = stats_f[(s * 2) * N + tid];
+                    const float w = (m == -INFINITY) ? 0.0f : fast_exp2(m - top);
+                    weight_f[s * N + tid] = w;
+                    total += w * stats_f[(s * 2 + 1) * N + tid];
+                }
+                total += extra;
+                const float inverse = p.out_scale / total;
+                for (int s = 0; s < splits; ++s) weight_f[s * N + tid] *= inverse;
+                lse2 = top - kLog2P + log2f(total);
+            }
+            if (split == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(token) * p.lse_stride_token + h] = lse2;
+        }
+        named_barrier(3, kThreads);
+        if (tid < kSoftmaxThreads) {
+            const int owned = (16 - split + splits - 1) / splits;
+            __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
+                                 static_cast<int64_t>(head0) * p.out_stride_head;
+            for (int it = warp; it < owned * N; it += 4) {
+                const int k = it / N, h = it - k * N;
+                const int slice = split + k * splits;
+                float acc = 0.0f;
+                for (int s = 0; s < splits; ++s) {
+                    const float w = weight_f[s * N + h];
+                    if (w != 0.0f) acc += w * inbox_f[((s * slots + k) * N + h) * 32 + lane];
+                }
+                out[static_cast<int64_t>(h) * p.out_stride_head + slice * 32 + lane] = __float2bfloat16_rn(acc);
+            }
+        }
+    }
+
+    // ---- teardown: every MMA and TMEM access has finished -----------------
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        if (!mbar_wait_bounded(drain, 0, abort_flag, kWaitLimitNs)) {
+            if (lane == 0) atomicOr(&g_device_error, SMLA_DEV_TIMEOUT);
+        }
+        __syncwarp();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+// ============================================================== host side
+
+thread_local int t_last_cuda_error = 0;
+
+int head_tile_for(int heads) {
+    if (heads % 64 == 0) return 64;
+    if (heads % 32 == 0) return 32;
+    return 16;
+}
+
+template <int N, int D>
+constexpr int smem_bytes() {
+    return Layout<N, D>::kAlloc;
+}
+
+int smem_for(int n, int d) {
+    if (d == 576) return n == 64 ? smem_bytes<64, 576>() : n == 32 ? smem_bytes<32, 576>() : smem_bytes<16, 576>();
+    return n == 64 ? smem_bytes<64, 512>() : n == 32 ? smem_bytes<32, 512>() : smem_bytes<16, 512>();
+}
+
+int tmem_for(int n) { return 6 * n <= 128 ? 128 : (6 * n <= 256 ? 256 : 512); }
+
+// Largest split count whose merge area fits the KV + Q tiles it reuses.
+bool merge_fits(int n, int d, int splits) {
+    const int blocks = (d + 127) / 128;
+    const int limit = 2 * blocks * kChunk * 128 + blocks * n * 128;
+    const int slots = (16 + splits - 1) / splits;
+    return splits * slots * n * 32 * 4 + splits * 3 * n * 4 <= limit;
+}
+
+template <int N, int D>
+cudaError_t launch(const Params& p, dim3 grid, int splits, cudaStream_t stream) {
+    auto kernel = sparse_mla_decode_kernel<N, D>;
+    constexpr int kSmem = Layout<N, D>::kAlloc;
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+int device_sms() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev < 64) cache[dev] = sms;
+    return sms;
+}
+
+int validate(const smla_shape* s) {
+    if (s == nullptr) return SMLA_EINVAL;
+    if (s->tokens < 0 || s->width < 0 || s->heads <= 0) return SMLA_EINVAL;
+    if (s->heads % 16 != 0) return SMLA_EINVAL;
+    if (s->heads > 1024 || s->tokens > 65535) return SMLA_EUNSUPPORTED;
+    if (s->head_dim != 576 && s->head_dim != 512) return SMLA_EUNSUPPORTED;
+    if (s->num_pools != 1 && s->num_pools != 2) return SMLA_EUNSUPPORTED;
+    if (s->num_pools == 2 && (s->pool_split < 0 || s->pool_split > s->width)) return SMLA_EINVAL;
+    if (s->q_stride_token < 0 || s->q_stride_head < 0 || s->idx_stride_token < 0 || s->out_stride_head < 0)
+        return SMLA_EINVAL;
+    if (s->q_stride_token % 16 != 0 || s->q_stride_head % 16 != 0) return SMLA_EINVAL;
+    if (s->q_stride_head < s->head_dim && s->heads > 1) return SMLA_EINVAL;
+    if (s->idx_stride_token < s->width) return SMLA_EINVAL;
+    if (s->out_stride_head < kLatent && s->heads > 1) return SMLA_EINVAL;
+    if (s->out_stride_token < 0 || s->lse_stride_token < 0) return SMLA_EINVAL;
+    return SMLA_OK;
+}
+
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* plan) {
+    if (plan == nullptr) return SMLA_EINVAL;
+    const int rc = validate(shape);
+    if (rc != SMLA_OK) return rc;
+    if (num_sms <= 0) {
+        num_sms = device_sms();
+        if (num_sms <= 0) return SMLA_ECUDA;
+    }
+    const int n = head_tile_for(shape->heads);
+    const int groups = shape->heads / n;
+    const int chunks = (shape->width + kChunk - 1) / kChunk;
+    const long units = static_cast<long>(shape->tokens) * groups;
+
+    // Split count: the fewest rounds of chunk work per SM (one CTA per SM),
+    // charging each CTA's fixed work and the cluster merge.
+    int best = 1;
+    double best_cost = 1e300;
+    const int max_splits = chunks < 8 ? (chunks < 1 ? 1 : chunks) : 8;
+    for (int s = 1; s <= max_splits; ++s) {
+        if (!merge_fits(n, shape->head_dim, s)) continue;
+        const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
+        const int eff = per > 0 ? (chunks + per - 1) / per : 1;
+        if (eff != s) continue;
+        const long ctas = units * eff;
+        const long waves = ctas > 0 ? (ctas + num_sms - 1) / num_sms : 0;
+        const double cost = static_cast<double>(waves) * (per + 0.5) + (eff > 1 ? 0.5 : 0.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = eff;
+        }
+    }
+    if (const char* env = std::getenv("SMLA_SPLITS")) {
+        const int forced = std::atoi(env);
+        if (forced > 0) {
+            int s = forced;
+            const int cap = chunks < kMaxSplits ? (chunks < 1 ? 1 : chunks) : kMaxSplits;
+            if (s > cap) s = cap;
+            while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
+            const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
+            best = per > 0 ? (chunks + per - 1) / per : 1;
+        }
+    }
+    plan->head_tile = n;
+    plan->head_groups = groups;
+    plan->chunk = kChunk;
+    plan->chunks = chunks;
+    plan->splits = best;
+    plan->chunks_per_split = chunks > 0 ? (chunks + best - 1) / best : 0;
+    plan->ctas = static_cast<int32_t>(units * best);
+    plan->threads = kThreads;
+    plan->smem_bytes = smem_for(n, shape->head_dim);
+    plan->tmem_columns = tmem_for(n);
+    plan->num_sms = num_sms;
+    plan->reserved = 0;
+    return SMLA_OK;
+}
+
+extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_pool* kv_pools,
+                           const int32_t* indices, const int32_t* lens, const float* sinks,
+                           float bmm1_scale, float bmm2_scale, float k_scale, void* out, float* lse,
+                           void* stream) {
+    int rc = validate(shape);
+    if (rc != SMLA_OK) return rc;
+    if (shape->tokens == 0) return SMLA_OK;
+    if (q == nullptr || kv_pools == nullptr || indices == nullptr || lens == nullptr || out == nullptr)
+        return SMLA_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(out) & 3u) != 0)
+        return SMLA_EINVAL;
+    if (shape->out_stride_token % 2 != 0 || shape->out_stride_head % 2 != 0) return SMLA_EINVAL;
+    for (int i = 0; i < shape->num_pools; ++i) {
+        const smla_pool& pl = kv_pools[i];
+        if (pl.data == nullptr || pl.rows < 0 || pl.row_bytes != shape->head_dim) return SMLA_EINVAL;
+        if ((reinterpret_cast<uintptr_t>(pl.data) & 15u) != 0) return SMLA_EINVAL;
+        if (pl.rows > 0x7FFFFFFFll) return SMLA_EUNSUPPORTED;
+    }
+    if (!std::isfinite(bmm1_scale) || !std::isfinite(bmm2_scale) || !std::isfinite(k_scale)) return SMLA_EINVAL;
+
+    smla_plan plan;
+    rc = smla_plan_for(shape, 0, &plan);
+    if (rc != SMLA_OK) return rc;
+
+    Params p;
+    p.q = static_cast<const uint8_t*>(q);
+    p.q_stride_token = shape->q_stride_token;
+    p.q_stride_head = shape->q_stride_head;
+    p.pool0 = static_cast<const uint8_t*>(kv_pools[0].data);
+    p.rows0 = kv_pools[0].rows;
+    const smla_pool& second = shape->num_pools == 2 ? kv_pools[1] : kv_pools[0];
+    p.pool1 = static_cast<const uint8_t*>(second.data);
+    p.rows1 = second.rows;
+    p.indices = indices;
+    p.idx_stride = shape->idx_stride_token;
+    p.lens = lens;
+    p.sinks = sinks;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.out_stride_token = shape->out_stride_token;
+    p.out_stride_head = shape->out_stride_head;
+    p.lse = lse;
+    p.lse_stride_token = shape->lse_stride_token;
+    p.width = shape->width;
+    p.pool_split = shape->num_pools == 2 ? shape->pool_split : 0;
+    p.num_pools = shape->num_pools;
+    p.splits = plan.splits;
+    p.chunks_per_split = plan.chunks_per_split;
+    p.scale_log2 = static_cast<float>(static_cast<double>(bmm1_scale) * 1.4426950408889634);
+    p.out_scale = static_cast<float>(static_cast<double>(bmm2_scale) * static_cast<double>(k_scale));
+
+    const dim3 grid(static_cast<unsigned>(plan.head_groups * plan.splits), static_cast<unsigned>(shape->tokens), 1);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    const int n = plan.head_tile;
+    if (shape->head_dim == 576) {
+        e = n == 64 ? launch<64, 576>(p, grid, plan.splits, st)
+          : n == 32 ? launch<32, 576>(p, grid, plan.splits, st)
+                    : launch<16, 576>(p, grid, plan.splits, st);
+    } else {
+        e = n == 64 ? launch<64, 512>(p, grid, plan.splits, st)
+          : n == 32 ? launch<32, 512>(p, grid, plan.splits, st)
+                    : launch<16, 512>(p, grid, plan.splits, st);
+    }
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return SMLA_ECUDA;
+    }
+    return SMLA_OK;
+}
+
+extern "C" int smla_device_error(int32_t* bits) {
+    if (bits == nullptr) return SMLA_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    int32_t v = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+    const int32_t zero = 0;
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return SMLA_ECUDA;
+    }
+    *bits = v;
+    return SMLA_OK;
+}
+
+extern "C" const char* smla_error_string(int code) {
+    switch (code) {
+        case SMLA_OK: return "ok";
+        case SMLA_EINVAL: return "invalid argument (null pointer, shape, stride or alignment)";
+        case SMLA_EUNSUPPORTED: return "unsupported shape";
+        case SMLA_ECUDA: return "CUDA runtime error";
+        case SMLA_EDEVICE: return "device-side error";
+        default: return "unknown error";
+    }
+}
+
+extern "C" int smla_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" int smla_version(void) { return 100; }

@@ -1,0 +1,174 @@
+"""Python binding of libsmla.so: argument marshalling only.
+
+The names mirror the C ABI in ``include/smla.h``. Every step of the decode runs
+in the library's CUDA kernels; when the library is missing this module raises
+instead of computing anything itself.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE = 0, -1, -2, -3, -4
+DEV_INDEX_RANGE, DEV_TIMEOUT = 1, 2
+LATENT = 512
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SmlaPool(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("row_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class SmlaShape(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("width", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("num_pools", ctypes.c_int32), ("pool_split", ctypes.c_int32),
+        ("q_stride_token", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
+        ("idx_stride_token", ctypes.c_int64),
+        ("out_stride_token", ctypes.c_int64), ("out_stride_head", ctypes.c_int64),
+        ("lse_stride_token", ctypes.c_int64),
+    ]
+
+
+class SmlaPlan(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "head_tile", "head_groups", "chunk", "chunks", "splits", "chunks_per_split", "ctas",
+        "threads", "smem_bytes", "tmem_columns", "num_sms", "reserved")]
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        lib = _lib
+        text = lib.smla_error_string(code).decode() if lib is not None else str(code)
+        if code == ECUDA and lib is not None:
+            text += f" (cudaError {lib.smla_last_cuda_error()})"
+        super().__init__(f"{what}: {text} [{code}]")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load(path: str | None = None):
+    """Loads libsmla.so (built by ``sparse_mla_decode_gb300.build``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _build.LIBRARY
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m sparse_mla_decode_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        lib.smla_plan_for.argtypes = [ctypes.POINTER(SmlaShape), i32, ctypes.POINTER(SmlaPlan)]
+        lib.smla_plan_for.restype = i32
+        lib.smla_decode.argtypes = [ctypes.POINTER(SmlaShape), vp, ctypes.POINTER(SmlaPool), vp, vp,
+                                    vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, vp, vp, vp]
+        lib.smla_decode.restype = i32
+        lib.smla_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+        lib.smla_device_error.restype = i32
+        lib.smla_error_string.argtypes = [i32]
+        lib.smla_error_string.restype = ctypes.c_char_p
+        lib.smla_last_cuda_error.restype = i32
+        lib.smla_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def make_shape(tokens, heads, width, head_dim, num_pools=1, pool_split=0, q_strides=None,
+               idx_stride=None, out_strides=None, lse_stride=None) -> SmlaShape:
+    s = SmlaShape()
+    s.tokens, s.heads, s.width, s.head_dim = tokens, heads, width, head_dim
+    s.num_pools, s.pool_split = num_pools, pool_split
+    s.q_stride_token, s.q_stride_head = q_strides or (heads * head_dim, head_dim)
+    s.idx_stride_token = width if idx_stride is None else idx_stride
+    s.out_stride_token, s.out_stride_head = out_strides or (heads * LATENT, LATENT)
+    s.lse_stride_token = heads if lse_stride is None else lse_stride
+    return s
+
+
+def smla_plan_for(shape: SmlaShape, num_sms: int = 0) -> dict:
+    lib = load()
+    plan = SmlaPlan()
+    rc = lib.smla_plan_for(ctypes.byref(shape), int(num_sms), ctypes.byref(plan))
+    if rc != OK:
+        raise SmlaError(rc, "smla_plan_for")
+    return {name: getattr(plan, name) for name, _ in SmlaPlan._fields_ if name != "reserved"}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def smla_decode(q: torch.Tensor, kv_pools, indices: torch.Tensor, lens: torch.Tensor,
+                sinks: torch.Tensor | None, bmm1_scale: float, bmm2_scale: float, k_scale: float,
+                out: torch.Tensor, lse: torch.Tensor | None, stream=None, pool_split: int = 0):
+    """Sparse MLA decode through the C ABI.
+
+    q: uint8 (E4M3 bytes) or float8_e4m3fn [T, H, D] on the device, last dim
+    contiguous; kv_pools: list of 1 or 2 [rows, D] E4M3 tensors, rows
+    contiguous; indices int32 [T, >= W] (W = indices.shape[1]); lens int32 [T];
+    sinks float32 [H] or None; out bf16 [T, H, 512]; lse float32 [T, H] or None.
+    Runs on ``stream`` (default: torch's current stream) without synchronising.
+    """
+    lib = load()
+    T, H, D = q.shape
+    W = indices.shape[1]
+    if q.stride(2) != 1 or out.stride(2) != 1 or indices.stride(1) != 1:
+        raise ValueError("innermost dimensions must be contiguous")
+    pools = (SmlaPool * len(kv_pools))()
+    for i, pool in enumerate(kv_pools):
+        if pool.stride(1) != 1 or pool.stride(0) != D:
+            raise ValueError("pool rows must be contiguous")
+        pools[i].data = pool.data_ptr()
+        pools[i].rows = pool.shape[0]
+        pools[i].row_bytes = pool.shape[1]
+        pools[i].reserved = 0
+    shape = make_shape(T, H, W, D, len(kv_pools), pool_split,
+                       q_strides=(q.stride(0) * q.element_size(), q.stride(1) * q.element_size()),
+                       idx_stride=indices.stride(0), out_strides=(out.stride(0), out.stride(1)),
+                       lse_stride=None if lse is None else lse.stride(0))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib.smla_decode(ctypes.byref(shape), _ptr(q), pools, _ptr(indices), _ptr(lens), _ptr(sinks),
+                         float(bmm1_scale), float(bmm2_scale), float(k_scale), _ptr(out), _ptr(lse),
+                         ctypes.c_void_p(handle))
+    if rc != OK:
+        raise SmlaError(rc, "smla_decode")
+    return out, lse
+
+
+def smla_device_error() -> int:
+    """Reads and clears the device error word (synchronises the device)."""
+    lib = load()
+    bits = ctypes.c_int32(0)
+    rc = lib.smla_device_error(ctypes.byref(bits))
+    if rc != OK:
+        raise SmlaError(rc, "smla_device_error")
+    return int(bits.value)
+
+
+def smla_version() -> int:
+    return int(load().smla_version())
+
+
+def decode(q, kv_pools, indices, lens, sinks=None, bmm1_scale=1.0, bmm2_scale=1.0, k_scale=1.0,
+           pool_split=0, stream=None, with_lse=True):
+    """Allocates the outputs on q's device and calls :func:`smla_decode`."""
+    T, H, _ = q.shape
+    out = torch.empty((T, H, LATENT), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((T, H), dtype=torch.float32, device=q.device) if with_lse else None
+    return smla_decode(q, kv_pools, indices, lens, sinks, bmm1_scale, bmm2_scale, k_scale, out, lse,
+                       stream=stream, pool_split=pool_split)

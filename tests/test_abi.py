@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every function include/smla.h declares, plans
+launches, and rejects bad arguments before launching anything."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mla_decode_gb300 import build, smla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return smla.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "smla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(smla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "smla_decode" in names and "smla_plan_for" in names
+    for name in names:
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def shape(**kw):
+    base = dict(tokens=64, heads=128, width=2048, head_dim=576)
+    base.update(kw)
+    return smla.make_shape(**base)
+
+
+def test_plan_bandwidth_batch(lib):
+    p = smla.smla_plan_for(shape(), num_sms=152)
+    assert p["head_tile"] == 64 and p["head_groups"] == 2 and p["chunk"] == 128
+    assert p["chunks"] == 16 and p["splits"] * p["chunks_per_split"] >= 16
+    assert p["ctas"] == 64 * 2 * p["splits"]
+    assert p["smem_bytes"] <= 232448 and p["tmem_columns"] == 512
+
+
+@pytest.mark.parametrize("tokens,heads,width,dim", [(1, 16, 256, 576), (5, 128, 256, 576),
+                                                    (12, 16, 640, 512), (256, 64, 1024, 576)])
+def test_plan_fills_the_machine_without_empty_splits(lib, tokens, heads, width, dim):
+    p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width, head_dim=dim), num_sms=152)
+    assert 1 <= p["splits"] <= 16
+    assert (p["splits"] - 1) * p["chunks_per_split"] < p["chunks"]  # the last split has work
+    assert heads % p["head_tile"] == 0
+
+
+def test_forced_splits(lib, monkeypatch):
+    monkeypatch.setenv("SMLA_SPLITS", "5")
+    assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 4  # 16 chunks: 4 x 4 ... no empty split
+    monkeypatch.setenv("SMLA_SPLITS", "16")
+    assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 16
+    monkeypatch.setenv("SMLA_SPLITS", "99")
+    assert smla.smla_plan_for(shape(width=300), num_sms=152)["splits"] == 3
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(heads=24), smla.EINVAL),
+    (dict(heads=0), smla.EINVAL),
+    (dict(head_dim=256), smla.EUNSUPPORTED),
+    (dict(tokens=-1), smla.EINVAL),
+    (dict(num_pools=3), smla.EUNSUPPORTED),
+    (dict(num_pools=2, pool_split=4096), smla.EINVAL),
+])
+def test_plan_rejects_bad_shapes(lib, kw, code):
+    with pytest.raises(smla.SmlaError) as e:
+        smla.smla_plan_for(shape(**kw), num_sms=152)
+    assert e.value.code == code
+
+
+def test_decode_rejects_bad_arguments_without_launching(lib):
+    s = shape(tokens=2, heads=16, width=8)
+    pools = (smla.SmlaPool * 1)()
+    pools[0].data, pools[0].rows, pools[0].row_bytes = 4096, 10, 576
+    fake = ctypes.c_void_p(4096)
+    call = lambda sh, q=fake, p=pools: lib.smla_decode(  # noqa: E731
+        ctypes.byref(sh), q, p, fake, fake, None, 1.0, 1.0, 1.0, fake, None, None)
+    assert call(s, q=None) == smla.EINVAL
+    assert call(s, q=ctypes.c_void_p(4097)) == smla.EINVAL  # unaligned q
+    bad = smla.make_shape(2, 16, 8, 576, q_strides=(16 * 576, 8))
+    assert call(bad) == smla.EINVAL
+    pools[0].row_bytes = 512
+    assert call(s) == smla.EINVAL  # pool row bytes != head_dim
+    pools[0].row_bytes = 576
+    assert lib.smla_decode(ctypes.byref(smla.make_shape(0, 16, 8, 576)), None, None, None, None, None,
+                           1.0, 1.0, 1.0, None, None, None) == smla.OK  # nothing to do
+    assert lib.smla_error_string(smla.EINVAL).startswith(b"invalid")

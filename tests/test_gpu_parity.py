@@ -1,0 +1,165 @@
+"""GPU parity: libsmla.so (through its C ABI) against both oracle modes.
+
+Sizes run from the three small workloads of the pages (1 x 16 heads x 256
+keys; 5 verify rows x 128 heads with an empty row; 12 tokens x 16 heads over
+two pools with sinks) through ragged and degenerate cases to the full
+64 x 128 x 2048 batch, sampled per (token, head)."""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from sparse_mla_decode_gb300 import smla, workloads
+from tests.gpu_helpers import compare, plan_of, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def forced_splits():
+    old = os.environ.get("SMLA_SPLITS")
+
+    def set_splits(s):
+        if s is None:
+            os.environ.pop("SMLA_SPLITS", None)
+        else:
+            os.environ["SMLA_SPLITS"] = str(s)
+
+    yield set_splits
+    set_splits(old)
+
+
+def test_library_loads_and_reports_version():
+    assert smla.smla_version() == 100
+    assert smla.smla_device_error() == 0
+
+
+@pytest.mark.parametrize("make", [workloads.tiny, workloads.verify_rows, workloads.two_pool_sinks],
+                         ids=["tiny", "verify", "two_pool"])
+def test_page_workloads(make):
+    w = make()
+    got, bits, lse = run_gpu(w)
+    report = compare(w, got, bits, lse)
+    print(w["name"], plan_of(w), report)
+    assert smla.smla_device_error() == 0
+
+
+SMALL = [
+    # heads, head_dim, width, holes, sinks, lens (None = full)
+    (16, 576, 300, 0.0, False, None),
+    (16, 512, 130, 0.1, True, None),
+    (32, 576, 257, 0.05, False, None),
+    (48, 576, 200, 0.0, True, None),
+    (64, 576, 384, 0.1, True, [384, 1, 129]),
+    (64, 512, 250, 0.0, False, [250, 0, 77]),
+    (128, 576, 129, 0.2, False, None),
+    (80, 512, 600, 0.02, True, None),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"h{c[0]}_d{c[1]}_w{c[2]}" for c in SMALL])
+def test_small_shapes(case):
+    heads, dim, width, holes, sinks, lens = case
+    tokens = 3 if lens is not None else 2
+    w = workloads.small("small", seed=heads * 1000 + width, tokens=tokens, heads=heads, width=width,
+                        head_dim=dim, pool_rows=4096, holes=holes, sinks=sinks, lens=lens)
+    got, bits, lse = run_gpu(w)
+    print(case, plan_of(w), compare(w, got, bits, lse))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 5, 8, 16])
+def test_forced_split_counts(forced_splits, splits):
+    forced_splits(splits)
+    w = workloads.small("splits", seed=77, tokens=2, heads=64, width=2048, head_dim=576,
+                        pool_rows=8192, holes=0.05, sinks=True, lens=[2048, 1000])
+    plan = plan_of(w)
+    assert plan["splits"] == min(splits, 16)
+    got, bits, lse = run_gpu(w)
+    print(splits, plan, compare(w, got, bits, lse))
+
+
+def test_two_pools_ragged_split_boundary():
+    w = workloads.small("pools", seed=91, tokens=4, heads=16, width=333, head_dim=512,
+                        pool_rows=1000, two_pools=True, pool_split=77, holes=0.05, sinks=True,
+                        lens=[333, 76, 78, 200])
+    got, bits, lse = run_gpu(w)
+    print(compare(w, got, bits, lse))
+
+
+def test_degenerate_inputs():
+    w = workloads.small("degenerate", seed=5, tokens=6, heads=16, width=140, head_dim=576,
+                        pool_rows=512, lens=[0, -3, 500, 140, 1, 129], sinks=True)
+    w["indices"][3, :] = -1  # every column a hole
+    got, bits, lse = run_gpu(w)
+    compare(w, got, bits, lse)
+    assert np.all(bits[[0, 1, 3]] == 0) and np.all(np.isneginf(lse[[0, 1, 3]]))
+
+
+def test_zero_width_and_zero_tokens():
+    w = workloads.small("zero", seed=6, tokens=2, heads=16, width=0, head_dim=576)
+    got, bits, lse = run_gpu(w)
+    assert np.all(bits == 0) and np.all(np.isneginf(lse))
+    d = to_device(w)
+    q = d["q"][:0]
+    out = torch.empty((0, 16, 512), dtype=torch.bfloat16, device="cuda")
+    smla.smla_decode(q, d["pools"], d["indices"][:0], d["lens"][:0], None, 1.0, 1.0, 1.0, out, None)
+
+
+def test_index_beyond_pool_is_masked_and_flagged():
+    w = workloads.small("oob", seed=7, tokens=1, heads=16, width=64, head_dim=576, pool_rows=100)
+    w["indices"][0, 10] = 100  # one past the last row
+    w["indices"][0, 11] = 2 ** 30
+    got, bits, lse = run_gpu(w)
+    assert smla.smla_device_error() & smla.DEV_INDEX_RANGE
+    compare(w, got, bits, lse)  # the oracle treats them as holes too
+    assert smla.smla_device_error() == 0
+
+
+def test_strided_layouts_match_contiguous():
+    w = workloads.small("strided", seed=8, tokens=3, heads=32, width=200, head_dim=576,
+                        pool_rows=2048, holes=0.1, sinks=True)
+    d = to_device(w)
+    out0, lse0 = smla.decode(d["q"], d["pools"], d["indices"], d["lens"], d["sinks"],
+                             w["bmm1_scale"], w["bmm2_scale"], w["k_scale"])
+    T, H, D = w["q"].shape
+    qbig = torch.zeros((T, H + 16, D + 64), dtype=torch.uint8, device="cuda")
+    qbig[:, 8:8 + H, :D] = d["q"]
+    q = qbig[:, 8:8 + H, :D]
+    ibig = torch.full((T, 256), -1, dtype=torch.int32, device="cuda")
+    ibig[:, :200] = d["indices"]
+    obig = torch.zeros((T, H + 3, 640), dtype=torch.bfloat16, device="cuda")
+    out = obig[:, 1:1 + H, :512]
+    lbig = torch.zeros((T, 40), dtype=torch.float32, device="cuda")
+    lse = lbig[:, :H]
+    smla.smla_decode(q, d["pools"], ibig[:, :200], d["lens"], d["sinks"], w["bmm1_scale"],
+                     w["bmm2_scale"], w["k_scale"], out, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+    assert torch.equal(lse, lse0)
+    assert torch.all(obig[:, 0] == 0) and torch.all(obig[:, :, 512:] == 0)
+
+
+def test_repeated_calls_are_bitwise_deterministic():
+    w = workloads.small("det", seed=9, tokens=4, heads=64, width=700, head_dim=576,
+                        pool_rows=4096, holes=0.05)
+    d = to_device(w)
+    a = smla.decode(d["q"], d["pools"], d["indices"], d["lens"], None, w["bmm1_scale"], 1.0, 1.0)
+    b = smla.decode(d["q"], d["pools"], d["indices"], d["lens"], None, w["bmm1_scale"], 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1])
+
+
+def test_bandwidth_batch_full_size_sampled():
+    """64 tokens x 128 heads x 2048 keys on the 1M-row pool, in the launch
+    configuration the benchmark times; 96 (token, head) pairs against the
+    oracle, every LSE finite."""
+    w = workloads.bandwidth_batch()
+    got, bits, lse = run_gpu(w)
+    rng = np.random.default_rng(1)
+    pairs = np.stack([rng.integers(0, 64, 96), rng.integers(0, 128, 96)], axis=1)
+    print(plan_of(w), compare(w, got, bits, lse, pairs=pairs))
+    assert np.all(np.isfinite(lse))
