@@ -80,7 +80,8 @@ typedef struct smla_plan {
     int32_t chunk;            /* columns per chunk (128) */
     int32_t chunks;           /* ceil(width / chunk) */
     int32_t splits;           /* CTAs per (token, head group) = cluster size */
-    int32_t chunks_per_split; /* ceil(chunks / splits) */
+    int32_t chunks_per_split; /* ceil(chunks / splits); a token of c active-count
+                                 chunks gives each split ceil(c / splits) */
     int32_t ctas;             /* tokens * head_groups * splits */
     int32_t threads;          /* threads per CTA */
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
@@ -100,7 +101,7 @@ int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* plan);
  *   shape     host pointer, see smla_shape.
  *   q         device, E4M3 [T, H, D] bytes.
  *   kv_pools  host array of shape->num_pools descriptors (data in device memory).
- *   indices   device, int32 [T, >= W], -1 marks a hole.
+ *   indices   device, int32 [T, >= W], -1 marks a hole (may be NULL when W == 0).
  *   lens      device, int32 [T], active count per token, clamped to [0, W].
  *   sinks     device, float [H] per-head sink in score units, or NULL.
  *   bmm1_scale  multiplies the q.kv dot products (fold q and k scales in here).

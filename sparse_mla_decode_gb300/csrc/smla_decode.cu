@@ -70,7 +70,7 @@ struct Params {
     int64_t out_stride_token, out_stride_head;
     float* lse;
     int64_t lse_stride_token;
-    int32_t width, pool_split, num_pools, splits, chunks_per_split;
+    int32_t width, pool_split, num_pools, splits;
     float scale_log2, out_scale;
 };
 
@@ -170,9 +170,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
     grid_dependency_wait();  // inputs are read only after this point
     const int count = min(max(p.lens[token], 0), p.width);
+    // This split's chunks of the token: ceil(chunks / splits) consecutive
+    // chunks each, dealt over the token's own count (later splits may be empty).
     const int chunks_total = (count + kChunk - 1) / kChunk;
-    const int c_first = split * p.chunks_per_split;
-    const int nch = max(0, min(p.chunks_per_split, chunks_total - c_first));
+    const int per_split = (chunks_total + splits - 1) / splits;
+    const int c_first = split * per_split;
+    const int nch = max(0, min(per_split, chunks_total - c_first));
     grid_launch_dependents();
 
     bool ok = true;
@@ -684,8 +687,8 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
     int rc = validate(shape);
     if (rc != SMLA_OK) return rc;
     if (shape->tokens == 0) return SMLA_OK;
-    if (q == nullptr || kv_pools == nullptr || indices == nullptr || lens == nullptr || out == nullptr)
-        return SMLA_EINVAL;
+    if (q == nullptr || kv_pools == nullptr || lens == nullptr || out == nullptr) return SMLA_EINVAL;
+    if (indices == nullptr && shape->width > 0) return SMLA_EINVAL;
     if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(out) & 3u) != 0)
         return SMLA_EINVAL;
     if (shape->out_stride_token % 2 != 0 || shape->out_stride_head % 2 != 0) return SMLA_EINVAL;
@@ -723,7 +726,6 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
     p.pool_split = shape->num_pools == 2 ? shape->pool_split : 0;
     p.num_pools = shape->num_pools;
     p.splits = plan.splits;
-    p.chunks_per_split = plan.chunks_per_split;
     p.scale_log2 = static_cast<float>(static_cast<double>(bmm1_scale) * 1.4426950408889634);
     p.out_scale = static_cast<float>(static_cast<double>(bmm2_scale) * static_cast<double>(k_scale));
 

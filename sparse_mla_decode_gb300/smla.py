@@ -125,11 +125,12 @@ def smla_decode(q: torch.Tensor, kv_pools, indices: torch.Tensor, lens: torch.Te
     lib = load()
     T, H, D = q.shape
     W = indices.shape[1]
-    if q.stride(2) != 1 or out.stride(2) != 1 or indices.stride(1) != 1:
-        raise ValueError("innermost dimensions must be contiguous")
+    for name, t, dim in (("q", q, 2), ("out", out, 2), ("indices", indices, 1)):
+        if t.shape[dim] > 1 and t.stride(dim) != 1:
+            raise ValueError(f"{name}: innermost dimension must be contiguous")
     pools = (SmlaPool * len(kv_pools))()
     for i, pool in enumerate(kv_pools):
-        if pool.stride(1) != 1 or pool.stride(0) != D:
+        if pool.shape[0] > 1 and (pool.stride(1) != 1 or pool.stride(0) != D):
             raise ValueError("pool rows must be contiguous")
         pools[i].data = pool.data_ptr()
         pools[i].rows = pool.shape[0]
