@@ -59,6 +59,8 @@ def parse():
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--soak", type=float, default=0.6,
+                    help="seconds of untimed calls after the timed region, under the clock sampler")
     return ap.parse_args()
 
 
@@ -331,7 +333,7 @@ def run_ours(args, rank, world, local_rank):
     t_wall1 = time.time()
     # keep the GPU under the same load for the clock sampler when the timed
     # region was shorter than a few samples
-    soak_until = t_wall1 + max(0.0, 0.6 - (t_wall1 - t_wall0))
+    soak_until = t_wall1 + max(0.0, args.soak - (t_wall1 - t_wall0)) if args.soak > 0 else t_wall1
     i = 0
     while time.time() < soak_until:
         for _ in range(200):

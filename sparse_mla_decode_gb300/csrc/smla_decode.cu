@@ -79,12 +79,11 @@ struct Params {
 template <int N, int D>
 struct Layout {
     static constexpr int kBlocks = (D + 127) / 128;  // 128-byte K blocks per row (5 or 4)
-    static constexpr int kPieces = D / 16;           // 16-byte pieces per row
     static constexpr int kStage = kBlocks * kChunk * 128;
-    static constexpr int kKv = 0;
-    static constexpr int kQ = 2 * kStage;
-    static constexpr int kP = kQ + kBlocks * N * 128;
-    static constexpr int kIdx = kP + N * 128;         // int32 [2][128] row of each key, -1 masked
+    static constexpr int kKv = 0;                       // 2 stages of KV rows
+    static constexpr int kQ = 2 * kStage;               // the Q tile
+    static constexpr int kP = kQ + kBlocks * N * 128;   // 2 buffers of P^T (kChunk x N bytes)
+    static constexpr int kIdx = kP + 2 * kChunk * N;    // int32 [2][128] row of each key, -1 masked
     static constexpr int kRed = kIdx + 2 * kChunk * 4;  // float [4][N] per-warp partials
     static constexpr int kHead = kRed + 4 * N * 4;      // float [4][N]: m_run, bias, alpha, l
     static constexpr int kBar = kHead + 4 * N * 4;      // 16 mbarriers
@@ -92,22 +91,30 @@ struct Layout {
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;
     static constexpr int kTmemCols = 6 * N <= 128 ? 128 : (6 * N <= 256 ? 256 : 512);
-    static constexpr int kMergeLimit = kP;  // the merge reuses KV + Q space
 };
 
-// Byte offset of 16-byte piece `piece` of row `row` in a K-major tile of
-// `rows` rows made of 128-byte K blocks, 128B-swizzled (16-byte unit u of a
-// row lands at u ^ (row % 8)).
-__device__ __forceinline__ uint32_t swizzled_piece(int row, int piece, int rows) {
-    const int block = piece >> 3, unit = piece & 7;
-    return static_cast<uint32_t>(block * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
-                                 ((unit ^ (row & 7)) << 4));
+// P^T for PV: B operand of N heads x 128 keys, MN-major (each key's N heads
+// are contiguous). Rows of N bytes, 8-row atoms of 8N bytes, swizzled with the
+// atom width: 64 heads -> 64B swizzle, 32 -> 32B swizzle, 16 -> none.
+template <int N>
+__device__ __forceinline__ uint32_t p_unit(int key, int unit) {
+    int u = unit;
+    if constexpr (N == 64) u ^= (key >> 1) & 3;
+    if constexpr (N == 32) u ^= (key >> 2) & 1;
+    return static_cast<uint32_t>(key * N + (u << 4));
 }
 
-// Byte offset of element (head, key) in the K-major 128B-swizzled P^T tile.
-__device__ __forceinline__ uint32_t p_offset(int head, int key) {
-    return static_cast<uint32_t>((head >> 3) * 1024 + (head & 7) * 128 +
-                                 ((((key >> 4) ^ (head & 7))) << 4) + (key & 15));
+template <int N>
+constexpr uint32_t p_swizzle() {
+    return N == 64 ? kSwizzle64B : (N == 32 ? kSwizzle32B : kSwizzleNone);
+}
+
+// N consecutive TMEM columns of this warp's lanes.
+template <int N>
+__device__ __forceinline__ void load_columns(uint32_t taddr, float (&v)[N]) {
+    if constexpr (N == 16) tmem_load16x1(taddr, v);
+    if constexpr (N == 32) tmem_load32x1(taddr, v);
+    if constexpr (N == 64) tmem_load32x2(taddr, taddr + 32, v);
 }
 
 template <int N, int D>
@@ -118,10 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     const uint32_t sbase = smem_u32(smem);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint64_t* kv_full = bars + 0;   // [2] gather of a stage landed (128 arrivals)
+    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (64 gather arrivals)
     uint64_t* kv_empty = bars + 2;  // [2] PV of a stage done (commit)
     uint64_t* s_full = bars + 4;    // [2] QK of a chunk done (commit)
-    uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (128 arrivals)
+    uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (128 softmax arrivals)
     uint64_t* o_done = bars + 7;    // PV of a chunk done (commit)
     uint64_t* drain = bars + 8;     // every MMA done (commit)
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -141,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
     // ---- set-up (reads no input, so it overlaps the previous kernel) -------
     if (tid == 0) {
-        mbar_init(&kv_full[0], kGatherThreads);
-        mbar_init(&kv_full[1], kGatherThreads);
+        mbar_init(&kv_full[0], kGatherThreads / 2);
+        mbar_init(&kv_full[1], kGatherThreads / 2);
         mbar_init(&kv_empty[0], 1);
         mbar_init(&kv_empty[1], 1);
         mbar_init(&s_full[0], 1);
@@ -181,51 +188,82 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     bool ok = true;
     if (warp >= kGatherBase / 32) {
         // ================================================= gather warps
-        const int g = tid - kGatherBase;
-        for (int c = 0; c < nch; ++c) {
-            const int b = c & 1;
-            if (c >= 2) ok &= mbar_wait_bounded(&kv_empty[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
-            const int col0 = (c_first + c) * kChunk;
-            {
-                const int col = col0 + g;
-                int32_t id = -1;
-                if (col < count) {
-                    const int32_t raw = p.indices[static_cast<int64_t>(token) * p.idx_stride + col];
-                    const bool second = p.num_pools == 2 && col >= p.pool_split;
-                    const int64_t rows = second ? p.rows1 : p.rows0;
-                    if (raw >= 0) {
-                        if (raw < rows)
-                            id = raw;
-                        else
-                            atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
-                    }
-                }
-                idx_s[b * kChunk + g] = id;
+        // Two pairs of warps, one per stage: pair s loads chunks c = s, s+2,
+        // ... so both stages can be in flight; each thread signals its stage
+        // only after its own copies landed and were made visible to the
+        // tensor cores. Warp w of a pair copies keys 64 w .. 64 w + 63, one
+        // row per instruction (lane l: bytes 16 l .. 16 l + 15 of the latent
+        // part; the rope of 8 rows per instruction).
+        const int pair = (warp - kGatherBase / 32) >> 1;
+        const int pt = tid - kGatherBase - 64 * pair;  // 0..63 within the pair
+        const int pw = pt >> 5;
+        const uint8_t* qt = p.q + static_cast<int64_t>(token) * p.q_stride_token +
+                            static_cast<int64_t>(head0) * p.q_stride_head;
+        auto resolve = [&](int col) -> int32_t {  // the row of a column, -1 if masked
+            if (col >= count) return -1;
+            const int32_t raw = p.indices[static_cast<int64_t>(token) * p.idx_stride + col];
+            if (raw < 0) return -1;
+            const bool second = p.num_pools == 2 && col >= p.pool_split;
+            if (raw >= (second ? p.rows1 : p.rows0)) {
+                atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
+                return -1;
             }
-            named_barrier(2, kGatherThreads);
-            if (c == 0) {  // the Q tile of this CTA's heads, once
-                const uint8_t* qt = p.q + static_cast<int64_t>(token) * p.q_stride_token +
-                                    static_cast<int64_t>(head0) * p.q_stride_head;
-                for (int i = g; i < N * L::kPieces; i += kGatherThreads) {
-                    const int h = i / L::kPieces, pc = i - h * L::kPieces;
-                    cp_async_16(sbase + L::kQ + swizzled_piece(h, pc, N),
-                                qt + static_cast<int64_t>(h) * p.q_stride_head + pc * 16, 16u);
+            return raw;
+        };
+        auto row_ptr = [&](int col, int32_t id) -> const uint8_t* {
+            const bool second = p.num_pools == 2 && col >= p.pool_split;
+            return (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id) * D;
+        };
+        for (int c = pair; c < nch; c += 2) {
+            const int b = pair;
+            if (c >= 2) ok &= mbar_wait_bounded(&kv_empty[b], ((c >> 1) - 1) & 1, abort_flag, kWaitLimitNs);
+            const int col0 = (c_first + c) * kChunk;
+            idx_s[b * kChunk + pt] = resolve(col0 + pt);
+            idx_s[b * kChunk + pt + 64] = resolve(col0 + pt + 64);
+            named_barrier(2 + pair, 64);
+            if (c == 0) {  // the Q tile of this CTA's heads, with the first chunk
+                for (int h = pw; h < N; h += 2) {
+                    const uint32_t dst = sbase + L::kQ + (lane >> 3) * N * 128 + (h >> 3) * 1024 + (h & 7) * 128 +
+                                         (((lane & 7) ^ (h & 7)) << 4);
+                    cp_async_16(dst, qt + static_cast<int64_t>(h) * p.q_stride_head + lane * 16, 16u);
+                }
+                if constexpr (D == 576) {
+                    for (int j = pw; j < N / 8; j += 2) {
+                        const int h = j * 8 + (lane >> 2), u = lane & 3;
+                        const uint32_t dst = sbase + L::kQ + 4 * N * 128 + (h >> 3) * 1024 + (h & 7) * 128 +
+                                             ((u ^ (h & 7)) << 4);
+                        cp_async_16(dst, qt + static_cast<int64_t>(h) * p.q_stride_head + 512 + u * 16, 16u);
+                    }
                 }
             }
             const uint32_t stage = sbase + L::kKv + b * L::kStage;
-            for (int i = g; i < kChunk * L::kPieces; i += kGatherThreads) {
-                const int k = i / L::kPieces, pc = i - k * L::kPieces;
+            const uint32_t lane_part = (lane >> 3) * kChunk * 128;
+#pragma unroll 8
+            for (int i = 0; i < 64; ++i) {
+                const int k = pw * 64 + i;
                 const int32_t id = idx_s[b * kChunk + k];
-                const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
-                const uint8_t* src = second ? p.pool1 : p.pool0;
-                uint32_t bytes = 0;
-                if (id >= 0) {
-                    src += static_cast<int64_t>(id) * D + pc * 16;
-                    bytes = 16;
+                const uint8_t* src = id >= 0 ? row_ptr(col0 + k, id) + lane * 16 : p.pool0;
+                const uint32_t dst = stage + lane_part + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
+                cp_async_16(dst, src, id >= 0 ? 16u : 0u);
+            }
+            if constexpr (D == 576) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int k = pw * 64 + j * 8 + (lane >> 2), u = lane & 3;
+                    const int32_t id = idx_s[b * kChunk + k];
+                    const uint8_t* src = id >= 0 ? row_ptr(col0 + k, id) + 512 + u * 16 : p.pool0;
+                    const uint32_t dst = stage + 4 * kChunk * 128 + (k >> 3) * 1024 + (k & 7) * 128 + ((u ^ (k & 7)) << 4);
+                    cp_async_16(dst, src, id >= 0 ? 16u : 0u);
                 }
-                cp_async_16(stage + swizzled_piece(k, pc, kChunk), src, bytes);
             }
             cp_async_commit();
+            if (c + 2 < nch) {  // this pair's next chunk: start pulling its rows into L2
+                for (int k = pt; k < kChunk; k += 64) {
+                    const int col = col0 + 2 * kChunk + k;
+                    const int32_t id = resolve(col);
+                    if (id >= 0) prefetch_l2(row_ptr(col, id), D);
+                }
+            }
             cp_async_wait_all();
             fence_proxy_async_smem();
             mbar_arrive(&kv_full[b]);
@@ -235,15 +273,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         // ================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_e4m3(128, N, 0, 0);
-            constexpr uint32_t kIdescPV = idesc_e4m3(128, N, 1, 0);
+            constexpr uint32_t kIdescPV = idesc_e4m3(128, N, 1, 1);
             auto issue_pv = [&](int c) {
                 const uint32_t stage = sbase + L::kKv + (c & 1) * L::kStage;
+                const uint32_t pbuf = sbase + L::kP + (c & 1) * kChunk * N;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 32; ++kk) {
                         const uint64_t a = smem_desc(stage + j * kChunk * 128 + kk * 32 * 128, 1024, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(sbase + L::kP + kk * 32, 1024, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(pbuf + kk * 32 * N, 8 * N, 8 * N, p_swizzle<N>());
                         mma_f8(tmem + 2 * N + j * N, a, bd, kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
@@ -288,83 +327,94 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         float lsum[N];
 #pragma unroll
         for (int h = 0; h < N; ++h) lsum[h] = 0.0f;
-        uint8_t* pt = smem + L::kP;
 
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
-            if (c > 0) ok &= mbar_wait_bounded(o_done, (c - 1) & 1, abort_flag, kWaitLimitNs);
             ok &= mbar_wait_bounded(&kv_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             ok &= mbar_wait_bounded(&s_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             tc_fence_after_sync();
             const bool active = idx_s[b * kChunk + tid] >= 0;
-            const uint32_t s_cols = tmem + lane_base + b * N;
+            float s[N];
+            load_columns<N>(tmem + lane_base + b * N, s);
 
-            // chunk maxima per head (log2 units; masked keys are -inf)
+            // chunk maxima per head, in logit units (bmm1_scale > 0 keeps the
+            // order; masked keys are -inf)
+            float mine0 = -INFINITY, mine1 = -INFINITY;
 #pragma unroll
-            for (int gq = 0; gq < N / 16; ++gq) {
-                float v[16];
-                tmem_load16(s_cols + gq * 16, v);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float x = active ? v[j] * scale_log2 : -INFINITY;
-                    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, float_to_ordered(x));
-                    if (lane == j) red[warp * N + gq * 16 + j] = ordered_to_float(m);
-                }
+            for (int h = 0; h < N; ++h) {
+                const float m = warp_max(active ? s[h] : -INFINITY);
+                if (h < 32)
+                    mine0 = (lane == h) ? m : mine0;
+                else
+                    mine1 = (lane == h - 32) ? m : mine1;
             }
+            if (lane < N) red[warp * N + lane] = mine0;
+            if (N > 32) red[warp * N + 32 + lane] = mine1;
             named_barrier(1, kSoftmaxThreads);
             if (tid < N) {
                 const float cm = fmaxf(fmaxf(red[tid], red[N + tid]), fmaxf(red[2 * N + tid], red[3 * N + tid]));
                 const float mo = m_run_s[tid];
-                const float mn = fmaxf(mo, cm);
+                const float mn = fmaxf(mo, cm * scale_log2);
                 alpha_s[tid] = (mo == -INFINITY) ? 1.0f : fast_exp2(mo - mn);
                 bias_s[tid] = mn - kLog2P;
                 m_run_s[tid] = mn;
             }
             named_barrier(1, kSoftmaxThreads);
 
-            // P = 2^(s2 - m + log2 448) -> E4M3 into P^T; FP32 sums of the unrounded P
+            // P = 2^(s * scale_log2 - m + log2 448) as E4M3 into P^T[b] (PV of
+            // chunk c-2 has finished reading it); FP32 sums of the unrounded P
+            if (c >= 2) ok &= mbar_wait_bounded(o_done, (c - 2) & 1, abort_flag, kWaitLimitNs);
+            uint32_t words[N / 4];
 #pragma unroll
-            for (int gq = 0; gq < N / 16; ++gq) {
-                float v[16];
-                tmem_load16(s_cols + gq * 16, v);
-#pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const int h = gq * 16 + j;
-                    float p0 = 0.0f, p1 = 0.0f;
-                    if (active) {
-                        p0 = fast_exp2(v[j] * scale_log2 - bias_s[h]);
-                        p1 = fast_exp2(v[j + 1] * scale_log2 - bias_s[h + 1]);
-                    }
-                    lsum[h] = lsum[h] * alpha_s[h] + p0;
-                    lsum[h + 1] = lsum[h + 1] * alpha_s[h + 1] + p1;
-                    const uint32_t pair = e4m3x2(p0, p1);
-                    pt[p_offset(h, tid)] = static_cast<uint8_t>(pair & 0xFFu);
-                    pt[p_offset(h + 1, tid)] = static_cast<uint8_t>(pair >> 8);
+            for (int h4 = 0; h4 < N / 4; ++h4) {
+                const float4 bi = reinterpret_cast<const float4*>(bias_s)[h4];
+                const float4 al = reinterpret_cast<const float4*>(alpha_s)[h4];
+                float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (active) {
+                    pr[0] = fast_exp2(fmaf(s[4 * h4 + 0], scale_log2, -bi.x));
+                    pr[1] = fast_exp2(fmaf(s[4 * h4 + 1], scale_log2, -bi.y));
+                    pr[2] = fast_exp2(fmaf(s[4 * h4 + 2], scale_log2, -bi.z));
+                    pr[3] = fast_exp2(fmaf(s[4 * h4 + 3], scale_log2, -bi.w));
                 }
+                lsum[4 * h4 + 0] = fmaf(lsum[4 * h4 + 0], al.x, pr[0]);
+                lsum[4 * h4 + 1] = fmaf(lsum[4 * h4 + 1], al.y, pr[1]);
+                lsum[4 * h4 + 2] = fmaf(lsum[4 * h4 + 2], al.z, pr[2]);
+                lsum[4 * h4 + 3] = fmaf(lsum[4 * h4 + 3], al.w, pr[3]);
+                words[h4] = e4m3x2(pr[0], pr[1]) | (e4m3x2(pr[2], pr[3]) << 16);
             }
-            // O^T *= alpha where a head's running maximum rose (PV(c-1) is done)
-            if (c > 0) {
+            uint8_t* pbuf = smem + L::kP + b * kChunk * N;
+#pragma unroll
+            for (int u = 0; u < N / 16; ++u)
+                *reinterpret_cast<uint4*>(pbuf + p_unit<N>(tid, u)) =
+                    make_uint4(words[4 * u], words[4 * u + 1], words[4 * u + 2], words[4 * u + 3]);
+
+            // O^T *= alpha where a head's running maximum rose (PV of chunk c-1 is done)
+            if (c >= 1) {
+                ok &= mbar_wait_bounded(o_done, (c - 1) & 1, abort_flag, kWaitLimitNs);
+                tc_fence_after_sync();
 #pragma unroll
                 for (int gq = 0; gq < N / 16; ++gq) {
                     float a[16];
                     bool rescale = false;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        a[j] = alpha_s[gq * 16 + j];
-                        rescale |= a[j] != 1.0f;
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const float4 v4 = reinterpret_cast<const float4*>(alpha_s)[gq * 4 + j4];
+                        a[4 * j4 + 0] = v4.x;
+                        a[4 * j4 + 1] = v4.y;
+                        a[4 * j4 + 2] = v4.z;
+                        a[4 * j4 + 3] = v4.w;
+                        rescale |= (v4.x != 1.0f) | (v4.y != 1.0f) | (v4.z != 1.0f) | (v4.w != 1.0f);
                     }
                     if (rescale) {
+                        const uint32_t col = tmem + lane_base + 2 * N + gq * 16;
+                        float v[64];
+                        tmem_load16x4(col, col + N, col + 2 * N, col + 3 * N, v);
 #pragma unroll
-                        for (int blk = 0; blk < 4; ++blk) {
-                            const uint32_t col = tmem + lane_base + 2 * N + blk * N + gq * 16;
-                            float v[16];
-                            tmem_load16(col, v);
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) v[j] *= a[j];
-                            tmem_store16(col, v);
-                        }
+                        for (int i = 0; i < 64; ++i) v[i] *= a[i & 15];
+                        tmem_store16x4(col, col + N, col + 2 * N, col + 3 * N, v);
                     }
                 }
+                tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -376,10 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         // per-head totals of the per-thread partial sums
 #pragma unroll
         for (int h = 0; h < N; ++h) {
-            float s = lsum[h];
+            float t = lsum[h];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-            if (lane == (h & 31)) red[warp * N + h] = s;
+            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+            if (lane == (h & 31)) red[warp * N + h] = t;
         }
         named_barrier(1, kSoftmaxThreads);
         if (tid < N) l_s[tid] = (red[tid] + red[N + tid]) + (red[2 * N + tid] + red[3 * N + tid]);
@@ -422,15 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 #pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
                 const int lat = blk * 128 + warp * 32 + lane;
+                float v[N];
+                if (!split_empty) load_columns<N>(tmem + lane_base + 2 * N + blk * N, v);
 #pragma unroll
-                for (int gq = 0; gq < N / 16; ++gq) {
-                    float v[16];
-                    if (!split_empty) tmem_load16(tmem + lane_base + 2 * N + blk * N + gq * 16, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float x = split_empty ? 0.0f : v[j] * bias_s[gq * 16 + j];
-                        out[static_cast<int64_t>(gq * 16 + j) * p.out_stride_head + lat] = __float2bfloat16_rn(x);
-                    }
+                for (int j = 0; j < N; ++j) {
+                    const float x = split_empty ? 0.0f : v[j] * bias_s[j];
+                    out[static_cast<int64_t>(j) * p.out_stride_head + lat] = __float2bfloat16_rn(x);
                 }
             }
         }
@@ -457,13 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 const int slice = blk * 4 + warp;
                 const int owner = slice % splits, slot = slice / splits;
                 const uint32_t dst = map_to_rank(inbox + (((split * slots + slot) * N) * 32 + lane) * 4, owner);
+                float v[N];
+                load_columns<N>(tmem + lane_base + 2 * N + blk * N, v);
 #pragma unroll
-                for (int gq = 0; gq < N / 16; ++gq) {
-                    float v[16];
-                    tmem_load16(tmem + lane_base + 2 * N + blk * N + gq * 16, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) st_cluster_f32(dst + (gq * 16 + j) * 32 * 4, v[j]);
-                }
+                for (int j = 0; j < N; ++j) st_cluster_f32(dst + j * 32 * 4, v[j]);
             }
         }
         cluster_sync_all();  // every partial has landed
@@ -551,7 +595,7 @@ int tmem_for(int n) { return 6 * n <= 128 ? 128 : (6 * n <= 256 ? 256 : 512); }
 // Largest split count whose merge area fits the KV + Q tiles it reuses.
 bool merge_fits(int n, int d, int splits) {
     const int blocks = (d + 127) / 128;
-    const int limit = 2 * blocks * kChunk * 128 + blocks * n * 128;
+    const int limit = 2 * blocks * kChunk * 128 + blocks * n * 128;  // KV stages + Q tile
     const int slots = (16 + splits - 1) / splits;
     return splits * slots * n * 32 * 4 + splits * 3 * n * 4 <= limit;
 }
@@ -699,6 +743,7 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
         if (pl.rows > 0x7FFFFFFFll) return SMLA_EUNSUPPORTED;
     }
     if (!std::isfinite(bmm1_scale) || !std::isfinite(bmm2_scale) || !std::isfinite(k_scale)) return SMLA_EINVAL;
+    if (!(bmm1_scale > 0.0f)) return SMLA_EINVAL;  // a softmax scale; its sign orders the maxima
 
     smla_plan plan;
     rc = smla_plan_for(shape, 0, &plan);
