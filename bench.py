@@ -308,8 +308,9 @@ def run_ours(args, rank, world, local_rank):
     for i in range(max(3, args.warmup)):
         call(i)
     barrier()
-    if smla.smla_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+    bits = smla.smla_device_error()
+    if bits != 0:
+        raise RuntimeError(f"device error bits {bits} during warm-up")
     t_wall0 = time.time()
     if flush is None:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -341,8 +342,9 @@ def run_ours(args, rank, world, local_rank):
             i += 1
         torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, max(t_wall1, soak_until))
-    if smla.smla_device_error() != 0:
-        raise RuntimeError("device error during the timed region")
+    bits = smla.smla_device_error()
+    if bits != 0:
+        raise RuntimeError(f"device error bits {bits} during the timed region")
 
     step_bytes = float(np.mean([byts[i % len(byts)] for i in range(args.steps)]))
     step_flops = float(np.mean([flops[i % len(flops)] for i in range(args.steps)]))

@@ -126,10 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (64 gather arrivals)
-    uint64_t* kv_empty = bars + 2;  // [2] PV of a stage done (commit)
+    // pv_done[b]: PV of the chunk in stage b finished (its KV stage and P^T
+    // buffer are free, O^T holds it). One barrier per stage, so that no waiter
+    // is ever more than one phase behind the barrier it waits on.
+    uint64_t* pv_done = bars + 2;   // [2] commit
     uint64_t* s_full = bars + 4;    // [2] QK of a chunk done (commit)
     uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (128 softmax arrivals)
-    uint64_t* o_done = bars + 7;    // PV of a chunk done (commit)
     uint64_t* drain = bars + 8;     // every MMA done (commit)
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -150,12 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     if (tid == 0) {
         mbar_init(&kv_full[0], kGatherThreads / 2);
         mbar_init(&kv_full[1], kGatherThreads / 2);
-        mbar_init(&kv_empty[0], 1);
-        mbar_init(&kv_empty[1], 1);
+        mbar_init(&pv_done[0], 1);
+        mbar_init(&pv_done[1], 1);
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
         mbar_init(p_full, kSoftmaxThreads);
-        mbar_init(o_done, 1);
         mbar_init(drain, 1);
         misc[1] = 0;
         mbar_init_fence();
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         };
         for (int c = pair; c < nch; c += 2) {
             const int b = pair;
-            if (c >= 2) ok &= mbar_wait_bounded(&kv_empty[b], ((c >> 1) - 1) & 1, abort_flag, kWaitLimitNs);
+            if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             const int col0 = (c_first + c) * kChunk;
             idx_s[b * kChunk + pt] = resolve(col0 + pt);
             idx_s[b * kChunk + pt + 64] = resolve(col0 + pt + 64);
@@ -286,8 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                         mma_f8(tmem + 2 * N + j * N, a, bd, kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(o_done);
-                mma_commit(&kv_empty[c & 1]);
+                mma_commit(&pv_done[c & 1]);
             };
             for (int c = 0; c < nch; ++c) {
                 const int b = c & 1;
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
             // P = 2^(s * scale_log2 - m + log2 448) as E4M3 into P^T[b] (PV of
             // chunk c-2 has finished reading it); FP32 sums of the unrounded P
-            if (c >= 2) ok &= mbar_wait_bounded(o_done, (c - 2) & 1, abort_flag, kWaitLimitNs);
+            if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             uint32_t words[N / 4];
 #pragma unroll
             for (int h4 = 0; h4 < N / 4; ++h4) {
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
             // O^T *= alpha where a head's running maximum rose (PV of chunk c-1 is done)
             if (c >= 1) {
-                ok &= mbar_wait_bounded(o_done, (c - 1) & 1, abort_flag, kWaitLimitNs);
+                ok &= mbar_wait_bounded(&pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
                 tc_fence_after_sync();
 #pragma unroll
                 for (int gq = 0; gq < N / 16; ++gq) {
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             tc_fence_before_sync();
             mbar_arrive(p_full);
         }
-        if (nch > 0) ok &= mbar_wait_bounded(o_done, (nch - 1) & 1, abort_flag, kWaitLimitNs);
+        if (nch > 0) ok &= mbar_wait_bounded(&pv_done[(nch - 1) & 1], ((nch - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
         tc_fence_after_sync();
 
         // per-head totals of the per-thread partial sums

@@ -46,6 +46,9 @@ def run_gpu(w, d=None, stream=None):
                            w["bmm1_scale"], w["bmm2_scale"], w["k_scale"],
                            pool_split=w.get("pool_split", 0), stream=stream)
     torch.cuda.synchronize()
+    bits = smla.smla_device_error()
+    assert bits & smla.DEV_TIMEOUT == 0, f"a bounded wait timed out (device error bits {bits})"
+    run_gpu.last_error_bits = bits
     return out.float().cpu().numpy(), out.view(torch.int16).cpu().numpy().view(np.uint16), \
         lse.cpu().numpy()
 

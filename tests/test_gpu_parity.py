@@ -114,7 +114,7 @@ def test_index_beyond_pool_is_masked_and_flagged():
     w["indices"][0, 10] = 100  # one past the last row
     w["indices"][0, 11] = 2 ** 30
     got, bits, lse = run_gpu(w)
-    assert smla.smla_device_error() & smla.DEV_INDEX_RANGE
+    assert run_gpu.last_error_bits == smla.DEV_INDEX_RANGE
     compare(w, got, bits, lse)  # the oracle treats them as holes too
     assert smla.smla_device_error() == 0
 
@@ -138,6 +138,7 @@ def test_strided_layouts_match_contiguous():
     smla.smla_decode(q, d["pools"], ibig[:, :200], d["lens"], d["sinks"], w["bmm1_scale"],
                      w["bmm2_scale"], w["k_scale"], out, lse)
     torch.cuda.synchronize()
+    assert smla.smla_device_error() == 0
     assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
     assert torch.equal(lse, lse0)
     assert torch.all(obig[:, 0] == 0) and torch.all(obig[:, :, 512:] == 0)
@@ -150,6 +151,7 @@ def test_repeated_calls_are_bitwise_deterministic():
     a = smla.decode(d["q"], d["pools"], d["indices"], d["lens"], None, w["bmm1_scale"], 1.0, 1.0)
     b = smla.decode(d["q"], d["pools"], d["indices"], d["lens"], None, w["bmm1_scale"], 1.0, 1.0)
     torch.cuda.synchronize()
+    assert smla.smla_device_error() == 0
     assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
     assert torch.equal(a[1], b[1])
 
@@ -164,3 +166,25 @@ def test_bandwidth_batch_full_size_sampled():
     pairs = np.stack([rng.integers(0, 64, 96), rng.integers(0, 128, 96)], axis=1)
     print(plan_of(w), compare(w, got, bits, lse, pairs=pairs))
     assert np.all(np.isfinite(lse))
+
+
+def test_back_to_back_calls_with_dependent_launch():
+    """Many calls in a row on one stream (programmatic dependent launch lets
+    each start before the previous ends) over rotating inputs: no bounded wait
+    may time out and every result must equal its single-call result."""
+    sets = [workloads.small("b2b", seed=100 + r, tokens=8, heads=128, width=2048, head_dim=576,
+                            pool_rows=1 << 15, holes=0.02) for r in range(3)]
+    devs = [to_device(w) for w in sets]
+    ref = []
+    for w, d in zip(sets, devs):
+        o, l = smla.decode(d["q"], d["pools"], d["indices"], d["lens"], None, w["bmm1_scale"], 1.0, 1.0)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), l.clone()))
+    outs = [smla.decode(devs[i % 3]["q"], devs[i % 3]["pools"], devs[i % 3]["indices"],
+                        devs[i % 3]["lens"], None, sets[i % 3]["bmm1_scale"], 1.0, 1.0)
+            for i in range(60)]
+    torch.cuda.synchronize()
+    assert smla.smla_device_error() == 0
+    for i, (o, l) in enumerate(outs):
+        assert torch.equal(o.view(torch.int16), ref[i % 3][0].view(torch.int16))
+        assert torch.equal(l, ref[i % 3][1])
