@@ -105,7 +105,7 @@ __device__ __forceinline__ uint32_t p_unit(int key, int unit) {
 }
 
 template <int N>
-constexpr uint32_t p_swizzle() {
+__host__ __device__ constexpr uint32_t p_swizzle() {
     return N == 64 ? kSwizzle64B : (N == 32 ? kSwizzle32B : kSwizzleNone);
 }
 
