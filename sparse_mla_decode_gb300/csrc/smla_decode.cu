@@ -10,14 +10,18 @@
 // running maximum, FP32 sums of the unrounded P, FP32 accumulation, an FP32
 // merge of the key splits across a thread-block cluster, one BF16 rounding.
 //
-// GB300 design (one CTA per SM, 288 threads):
+// GB300 design (one CTA per SM, 192 threads):
 //   warps 0-3  softmax: one thread per key of a 128-key chunk (the TMEM lane of
 //              S^T), per-head maxima by warp reductions + shared memory, P as
 //              E4M3 into shared memory, rescale of O^T in TMEM, epilogue/merge;
-//   warp 4     allocates TMEM and issues the tcgen05 MMAs from one thread;
-//   warps 5-8  gather: 16-byte cp.async copies of the chunk's KV rows (and the
-//              Q tile) into 128B-swizzled K-major tiles, zero-filling masked
-//              columns; two stages so the next chunk streams during compute.
+//   warp 4     allocates TMEM and issues the tcgen05 MMAs from one thread,
+//              QK of the next chunk as soon as its rows landed and PV of the
+//              previous one as soon as its P is ready;
+//   warp 5     producer: TMA gathers of the chunk's KV rows, four rows per
+//              instruction (tile::gather4), straight into the swizzled K-major
+//              tiles the MMAs read (masked columns read a row outside the pool
+//              and so arrive as zeros), and TMA tile loads of the Q tile; two
+//              stages, plus an L2 prefetch of the stage's next chunk.
 // Both products put the long side on the MMA's M = 128 and the heads on N, as
 // the DeepSeek page sketches:
 //   S^T[key, head]   = KV[key, :] . Q[head, :]      (A = KV K-major, B = Q K-major)
@@ -28,13 +32,16 @@
 // Every wait is bounded; a timeout sets an error bit and the kernel still
 // returns (and frees its TMEM).
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "smla.h"
@@ -44,11 +51,10 @@ namespace smla {
 
 constexpr int kChunk = 128;  // keys per chunk = the MMA's M
 constexpr int kLatent = 512;
-constexpr int kThreads = 288;
+constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMmaWarp = 4;
-constexpr int kGatherBase = 160;
-constexpr int kGatherThreads = 128;
+constexpr int kProducerWarp = 5;
 constexpr int kMaxSplits = 16;
 constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -57,6 +63,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 __device__ int32_t g_device_error;
 
 struct Params {
+    // Tensor maps (64-byte aligned kernel parameters): per pool the 512-byte
+    // latent part as 128-byte boxes one row high (128B swizzle) and the 64-byte
+    // rope part (64B swizzle); the Q tile of one token and head group.
+    CUtensorMap kv_latent[2];
+    CUtensorMap kv_rope[2];
+    CUtensorMap q_latent;
+    CUtensorMap q_rope;
+    int32_t oob_row[2];  // a row index outside each pool's map: reads as zeros
     const uint8_t* q;
     int64_t q_stride_token, q_stride_head;
     const uint8_t* pool0;
@@ -78,11 +92,15 @@ struct Params {
 // 1024-byte aligned base; every MMA operand tile starts on 1024 bytes).
 template <int N, int D>
 struct Layout {
-    static constexpr int kBlocks = (D + 127) / 128;  // 128-byte K blocks per row (5 or 4)
-    static constexpr int kStage = kBlocks * kChunk * 128;
-    static constexpr int kKv = 0;                       // 2 stages of KV rows
-    static constexpr int kQ = 2 * kStage;               // the Q tile
-    static constexpr int kP = kQ + kBlocks * N * 128;   // 2 buffers of P^T (kChunk x N bytes)
+    // A tile of R rows: four 128-byte latent K blocks (128B swizzle, 8-row
+    // atoms of 1 KB) then, for 576-byte rows, the 64-byte rope block (64B
+    // swizzle, 8-row atoms of 512 bytes).
+    static constexpr bool kRope = D == 576;
+    static constexpr int kStage = 4 * kChunk * 128 + (kRope ? kChunk * 64 : 0);
+    static constexpr int kKv = 0;                                 // 2 stages of KV rows
+    static constexpr int kQ = 2 * kStage;                         // the Q tile
+    static constexpr int kQBytes = 4 * N * 128 + (kRope ? N * 64 : 0);
+    static constexpr int kP = kQ + kQBytes;                       // 2 buffers of P^T (kChunk x N bytes)
     static constexpr int kIdx = kP + 2 * kChunk * N;    // int32 [2][128] row of each key, -1 masked
     static constexpr int kRed = kIdx + 2 * kChunk * 4;  // float [4][N] per-warp partials
     static constexpr int kHead = kRed + 4 * N * 4;      // float [4][N]: m_run, bias, alpha, l
@@ -125,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     const uint32_t sbase = smem_u32(smem);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (64 gather arrivals)
+    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (TMA transaction bytes)
     // pv_done[b]: PV of the chunk in stage b finished (its KV stage and P^T
     // buffer are free, O^T holds it). One barrier per stage, so that no waiter
     // is ever more than one phase behind the barrier it waits on.
@@ -150,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
     // ---- set-up (reads no input, so it overlaps the previous kernel) -------
     if (tid == 0) {
-        mbar_init(&kv_full[0], kGatherThreads / 2);
-        mbar_init(&kv_full[1], kGatherThreads / 2);
+        mbar_init(&kv_full[0], 1);
+        mbar_init(&kv_full[1], 1);
         mbar_init(&pv_done[0], 1);
         mbar_init(&pv_done[1], 1);
         mbar_init(&s_full[0], 1);
@@ -171,6 +189,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         tmem_alloc(misc, L::kTmemCols);
         tmem_relinquish();
     }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensor_map(&p.kv_latent[0]);
+        prefetch_tensor_map(&p.kv_latent[1]);
+        prefetch_tensor_map(&p.q_latent);
+        if constexpr (L::kRope) {
+            prefetch_tensor_map(&p.kv_rope[0]);
+            prefetch_tensor_map(&p.kv_rope[1]);
+            prefetch_tensor_map(&p.q_rope);
+        }
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -187,22 +215,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     grid_launch_dependents();
 
     bool ok = true;
-    if (warp >= kGatherBase / 32) {
-        // ================================================= gather warps
-        // Two pairs of warps, one per stage: pair s loads chunks c = s, s+2,
-        // ... so both stages can be in flight; each thread signals its stage
-        // only after its own copies landed and were made visible to the
-        // tensor cores. Warp w of a pair copies keys 64 w .. 64 w + 63, one
-        // row per instruction (lane l: bytes 16 l .. 16 l + 15 of the latent
-        // part; the rope of 8 rows per instruction).
-        const int pair = (warp - kGatherBase / 32) >> 1;
-        const int pt = tid - kGatherBase - 64 * pair;  // 0..63 within the pair
-        const int pw = pt >> 5;
-        const uint8_t* qt = p.q + static_cast<int64_t>(token) * p.q_stride_token +
-                            static_cast<int64_t>(head0) * p.q_stride_head;
+    if (warp == kProducerWarp) {
+        // ================================================== producer
+        // Lane l gathers keys 4l .. 4l + 3 of the chunk: one tile::gather4 per
+        // 128-byte latent block and one for the rope block. A masked key asks
+        // for a row outside its pool's map and arrives as zeros.
+        const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
         auto resolve = [&](int col) -> int32_t {  // the row of a column, -1 if masked
             if (col >= count) return -1;
-            const int32_t raw = p.indices[static_cast<int64_t>(token) * p.idx_stride + col];
+            const int32_t raw = idx_row[col];
             if (raw < 0) return -1;
             const bool second = p.num_pools == 2 && col >= p.pool_split;
             if (raw >= (second ? p.rows1 : p.rows0)) {
@@ -211,109 +232,133 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             }
             return raw;
         };
-        auto row_ptr = [&](int col, int32_t id) -> const uint8_t* {
-            const bool second = p.num_pools == 2 && col >= p.pool_split;
-            return (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id) * D;
-        };
-        for (int c = pair; c < nch; c += 2) {
-            const int b = pair;
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             const int col0 = (c_first + c) * kChunk;
-            idx_s[b * kChunk + pt] = resolve(col0 + pt);
-            idx_s[b * kChunk + pt + 64] = resolve(col0 + pt + 64);
-            named_barrier(2 + pair, 64);
-            if (c == 0) {  // the Q tile of this CTA's heads, with the first chunk
-                for (int h = pw; h < N; h += 2) {
-                    const uint32_t dst = sbase + L::kQ + (lane >> 3) * N * 128 + (h >> 3) * 1024 + (h & 7) * 128 +
-                                         (((lane & 7) ^ (h & 7)) << 4);
-                    cp_async_16(dst, qt + static_cast<int64_t>(h) * p.q_stride_head + lane * 16, 16u);
+            const int k0 = 4 * lane;
+            int32_t row[4];
+            bool second[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = col0 + k0 + j;
+                row[j] = resolve(col);
+                idx_s[b * kChunk + k0 + j] = row[j];
+                second[j] = p.num_pools == 2 && col >= p.pool_split;
+                if (row[j] < 0) row[j] = p.oob_row[second[j] ? 1 : 0];
+            }
+            __syncwarp();  // every lane's idx_s entries precede the arrival (release)
+            if (lane == 0)
+                mbar_arrive_expect_tx(&kv_full[b], kChunk * D + (c == 0 ? N * D : 0));
+            __syncwarp();
+            if (c == 0 && lane == 0) {  // the Q tile of this CTA's heads, with the first chunk
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_load_3d(sbase + L::kQ + kb * N * 128, &p.q_latent, kb * 128, head0, token, &kv_full[0]);
+                if constexpr (L::kRope)
+                    tma_load_3d(sbase + L::kQ + 4 * N * 128, &p.q_rope, 512, head0, token, &kv_full[0]);
+            }
+            const uint32_t stage = sbase + L::kKv + b * L::kStage;
+            const uint32_t lat_dst = stage + (k0 >> 3) * 1024 + (k0 & 7) * 128;
+            const uint32_t rope_dst = stage + 4 * kChunk * 128 + (k0 >> 3) * 512 + (k0 & 7) * 64;
+            if (second[0] == second[3]) {
+                const int m = second[0] ? 1 : 0;
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_gather4(lat_dst + kb * kChunk * 128, &p.kv_latent[m], kb * 128, row[0], row[1], row[2],
+                                row[3], &kv_full[b]);
+                if constexpr (L::kRope)
+                    tma_gather4(rope_dst, &p.kv_rope[m], 512, row[0], row[1], row[2], row[3], &kv_full[b]);
+            } else {  // the group straddles the two pools: one row per copy
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int m = second[j] ? 1 : 0;
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb)
+                        tma_load_2d(lat_dst + kb * kChunk * 128 + j * 128, &p.kv_latent[m], kb * 128, row[j],
+                                    &kv_full[b]);
+                    if constexpr (L::kRope)
+                        tma_load_2d(rope_dst + j * 64, &p.kv_rope[m], 512, row[j], &kv_full[b]);
                 }
-                if constexpr (D == 576) {
-                    for (int j = pw; j < N / 8; j += 2) {
-                        const int h = j * 8 + (lane >> 2), u = lane & 3;
-                        const uint32_t dst = sbase + L::kQ + 4 * N * 128 + (h >> 3) * 1024 + (h & 7) * 128 +
-                                             ((u ^ (h & 7)) << 4);
-                        cp_async_16(dst, qt + static_cast<int64_t>(h) * p.q_stride_head + 512 + u * 16, 16u);
+            }
+            if (c + 2 < nch) {  // this stage's next chunk: start pulling its rows into L2
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int col = col0 + 2 * kChunk + k0 + j;
+                    const int32_t id = resolve(col);
+                    if (id >= 0) {
+                        const bool sec = p.num_pools == 2 && col >= p.pool_split;
+                        prefetch_l2((sec ? p.pool1 : p.pool0) + static_cast<int64_t>(id) * D, D);
                     }
                 }
             }
-            const uint32_t stage = sbase + L::kKv + b * L::kStage;
-            const uint32_t lane_part = (lane >> 3) * kChunk * 128;
-#pragma unroll 8
-            for (int i = 0; i < 64; ++i) {
-                const int k = pw * 64 + i;
-                const int32_t id = idx_s[b * kChunk + k];
-                const uint8_t* src = id >= 0 ? row_ptr(col0 + k, id) + lane * 16 : p.pool0;
-                const uint32_t dst = stage + lane_part + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
-                cp_async_16(dst, src, id >= 0 ? 16u : 0u);
-            }
-            if constexpr (D == 576) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int k = pw * 64 + j * 8 + (lane >> 2), u = lane & 3;
-                    const int32_t id = idx_s[b * kChunk + k];
-                    const uint8_t* src = id >= 0 ? row_ptr(col0 + k, id) + 512 + u * 16 : p.pool0;
-                    const uint32_t dst = stage + 4 * kChunk * 128 + (k >> 3) * 1024 + (k & 7) * 128 + ((u ^ (k & 7)) << 4);
-                    cp_async_16(dst, src, id >= 0 ? 16u : 0u);
-                }
-            }
-            cp_async_commit();
-            if (c + 2 < nch) {  // this pair's next chunk: start pulling its rows into L2
-                for (int k = pt; k < kChunk; k += 64) {
-                    const int col = col0 + 2 * kChunk + k;
-                    const int32_t id = resolve(col);
-                    if (id >= 0) prefetch_l2(row_ptr(col, id), D);
-                }
-            }
-            cp_async_wait_all();
-            fence_proxy_async_smem();
-            mbar_arrive(&kv_full[b]);
         }
-        cp_async_wait_all();
     } else if (warp == kMmaWarp) {
         // ================================================== MMA issuer
+        // QK(c) as soon as chunk c landed and S buffer c % 2 is free (the
+        // softmax of chunk c - 2 is done, i.e. PV(c - 2) was issued); PV(c) as
+        // soon as P(c) is ready. Whichever is due goes first.
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_e4m3(128, N, 0, 0);
             constexpr uint32_t kIdescPV = idesc_e4m3(128, N, 1, 1);
-            auto issue_pv = [&](int c) {
-                const uint32_t stage = sbase + L::kKv + (c & 1) * L::kStage;
-                const uint32_t pbuf = sbase + L::kP + (c & 1) * kChunk * N;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                    for (int kk = 0; kk < kChunk / 32; ++kk) {
-                        const uint64_t a = smem_desc(stage + j * kChunk * 128 + kk * 32 * 128, 1024, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(pbuf + kk * 32 * N, 8 * N, 8 * N, p_swizzle<N>());
-                        mma_f8(tmem + 2 * N + j * N, a, bd, kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
-                mma_commit(&pv_done[c & 1]);
-            };
-            for (int c = 0; c < nch; ++c) {
-                const int b = c & 1;
-                ok &= mbar_wait_bounded(&kv_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
-                tc_fence_after_sync();
-                const uint32_t stage = sbase + L::kKv + b * L::kStage;
-#pragma unroll
-                for (int kb = 0; kb < L::kBlocks; ++kb) {
-                    const int steps = (kb < 4) ? 4 : (D - 512) / 32;
-                    for (int ks = 0; ks < steps; ++ks) {
-                        const uint64_t a = smem_desc(stage + kb * kChunk * 128 + ks * 32, 1024, 1024, kSwizzle128B);
-                        const uint64_t bq = smem_desc(sbase + L::kQ + kb * N * 128 + ks * 32, 1024, 1024, kSwizzle128B);
-                        mma_f8(tmem + b * N, a, bq, kIdescQK, (kb | ks) != 0 ? 1u : 0u);
-                    }
-                }
-                mma_commit(&s_full[b]);
-                if (c >= 1) {
-                    ok &= mbar_wait_bounded(p_full, (c - 1) & 1, abort_flag, kWaitLimitNs);
+            int next_qk = 0, next_pv = 0;
+            uint64_t idle_since = 0;
+            while (next_pv < nch) {
+                bool progressed = false;
+                if (next_qk < nch && next_qk <= next_pv + 1 &&
+                    mbar_test_wait(&kv_full[next_qk & 1], (next_qk >> 1) & 1)) {
+                    const int c = next_qk;
                     tc_fence_after_sync();
-                    issue_pv(c - 1);
+                    const uint32_t stage = sbase + L::kKv + (c & 1) * L::kStage;
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t a = smem_desc(stage + kb * kChunk * 128 + ks * 32, 1024, 1024, kSwizzle128B);
+                            const uint64_t bq = smem_desc(sbase + L::kQ + kb * N * 128 + ks * 32, 1024, 1024, kSwizzle128B);
+                            mma_f8(tmem + (c & 1) * N, a, bq, kIdescQK, (kb | ks) != 0 ? 1u : 0u);
+                        }
+                    }
+                    if constexpr (L::kRope) {
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            const uint64_t a = smem_desc(stage + 4 * kChunk * 128 + ks * 32, 512, 512, kSwizzle64B);
+                            const uint64_t bq = smem_desc(sbase + L::kQ + 4 * N * 128 + ks * 32, 512, 512, kSwizzle64B);
+                            mma_f8(tmem + (c & 1) * N, a, bq, kIdescQK, 1u);
+                        }
+                    }
+                    mma_commit(&s_full[c & 1]);
+                    ++next_qk;
+                    progressed = true;
                 }
-            }
-            if (nch >= 1) {
-                ok &= mbar_wait_bounded(p_full, (nch - 1) & 1, abort_flag, kWaitLimitNs);
-                tc_fence_after_sync();
-                issue_pv(nch - 1);
+                if (next_pv < next_qk && mbar_test_wait(p_full, next_pv & 1)) {
+                    const int c = next_pv;
+                    tc_fence_after_sync();
+                    const uint32_t stage = sbase + L::kKv + (c & 1) * L::kStage;
+                    const uint32_t pbuf = sbase + L::kP + (c & 1) * kChunk * N;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int kk = 0; kk < kChunk / 32; ++kk) {
+                            const uint64_t a = smem_desc(stage + j * kChunk * 128 + kk * 32 * 128, 1024, 1024, kSwizzle128B);
+                            const uint64_t bd = smem_desc(pbuf + kk * 32 * N, 8 * N, 8 * N, p_swizzle<N>());
+                            mma_f8(tmem + 2 * N + j * N, a, bd, kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&pv_done[c & 1]);
+                    ++next_pv;
+                    progressed = true;
+                }
+                if (progressed) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = global_timer_ns();
+                    if (idle_since == 0) idle_since = now;
+                    if (*abort_flag || now - idle_since > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
             mma_commit(drain);
         }
@@ -594,8 +639,8 @@ int tmem_for(int n) { return 6 * n <= 128 ? 128 : (6 * n <= 256 ? 256 : 512); }
 
 // Largest split count whose merge area fits the KV + Q tiles it reuses.
 bool merge_fits(int n, int d, int splits) {
-    const int blocks = (d + 127) / 128;
-    const int limit = 2 * blocks * kChunk * 128 + blocks * n * 128;  // KV stages + Q tile
+    const int stage = 4 * kChunk * 128 + (d == 576 ? kChunk * 64 : 0);
+    const int limit = 2 * stage + 4 * n * 128 + (d == 576 ? n * 64 : 0);  // KV stages + Q tile
     const int slots = (16 + splits - 1) / splits;
     return splits * slots * n * 32 * 4 + splits * 3 * n * 4 <= limit;
 }
@@ -630,6 +675,54 @@ cudaError_t launch(const Params& p, dim3 grid, int splits, cudaStream_t stream) 
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A pool seen as `rows` rows of `d` bytes, read in boxes of `box` bytes of one
+// row (tile::gather4 reads four such rows).
+bool encode_pool_map(CUtensorMap* map, const void* base, int64_t rows, int d, int box, CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d)};
+    const cuuint32_t boxes[2] = {static_cast<cuuint32_t>(box), 1};
+    const cuuint32_t steps[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, boxes, steps,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Q as [T][H][D] bytes with the caller's strides, read in boxes of `box`
+// bytes x n heads of one token.
+bool encode_q_map(CUtensorMap* map, const void* q, const smla_shape* s, int n, int box, CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const int64_t head_stride = s->q_stride_head;
+    int64_t token_stride = s->q_stride_token;
+    if (s->tokens == 1 && token_stride < head_stride * s->heads) token_stride = head_stride * s->heads;  // unused
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->head_dim), static_cast<cuuint64_t>(s->heads),
+                                static_cast<cuuint64_t>(s->tokens)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_stride), static_cast<cuuint64_t>(token_stride)};
+    const cuuint32_t boxes[3] = {static_cast<cuuint32_t>(box), static_cast<cuuint32_t>(n), 1};
+    const cuuint32_t steps[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q), dims, strides, boxes, steps,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int device_sms() {
@@ -750,6 +843,21 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
     if (rc != SMLA_OK) return rc;
 
     Params p;
+    std::memset(&p, 0, sizeof(p));
+    {
+        const int n = plan.head_tile;
+        const bool rope = shape->head_dim == 576;
+        for (int i = 0; i < 2; ++i) {
+            const smla_pool& pl = kv_pools[shape->num_pools == 2 ? i : 0];
+            if (!encode_pool_map(&p.kv_latent[i], pl.data, pl.rows, shape->head_dim, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+                return SMLA_EUNSUPPORTED;
+            if (rope && !encode_pool_map(&p.kv_rope[i], pl.data, pl.rows, shape->head_dim, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+                return SMLA_EUNSUPPORTED;
+            p.oob_row[i] = static_cast<int32_t>(pl.rows > 0 ? pl.rows : 1);
+        }
+        if (!encode_q_map(&p.q_latent, q, shape, n, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
+        if (rope && !encode_q_map(&p.q_rope, q, shape, n, 64, CU_TENSOR_MAP_SWIZZLE_64B)) return SMLA_EUNSUPPORTED;
+    }
     p.q = static_cast<const uint8_t*>(q);
     p.q_stride_token = shape->q_stride_token;
     p.q_stride_head = shape->q_stride_head;
