@@ -10,18 +10,21 @@
 // running maximum, FP32 sums of the unrounded P, FP32 accumulation, an FP32
 // merge of the key splits across a thread-block cluster, one BF16 rounding.
 //
-// GB300 design (one CTA per SM, 192 threads):
+// GB300 design (one CTA per SM, 288 threads):
 //   warps 0-3  softmax: one thread per key of a 128-key chunk (the TMEM lane of
 //              S^T), per-head maxima by warp reductions + shared memory, P as
 //              E4M3 into shared memory, rescale of O^T in TMEM, epilogue/merge;
 //   warp 4     allocates TMEM and issues the tcgen05 MMAs from one thread,
 //              QK of the next chunk as soon as its rows landed and PV of the
 //              previous one as soon as its P is ready;
-//   warp 5     producer: TMA gathers of the chunk's KV rows, four rows per
-//              instruction (tile::gather4), straight into the swizzled K-major
-//              tiles the MMAs read (masked columns read a row outside the pool
-//              and so arrive as zeros), and TMA tile loads of the Q tile; two
-//              stages, plus an L2 prefetch of the stage's next chunk.
+//   warps 5-8  producers: 16-byte cp.async copies of the chunk's KV rows, one
+//              row per warp instruction, straight into the swizzled K-major
+//              tiles the MMAs read (masked columns are zero-filled); each
+//              thread's arrival on the stage barrier fires when its copies
+//              land, so both stages stream while the other is computed. The Q
+//              tile comes by TMA tile loads. (Random 576-byte rows stream
+//              fastest this way: TMA tile::gather4 reaches only about 60% of
+//              the cp.async rate on L2 hits and needs as many issuing warps.)
 // Both products put the long side on the MMA's M = 128 and the heads on N, as
 // the DeepSeek page sketches:
 //   S^T[key, head]   = KV[key, :] . Q[head, :]      (A = KV K-major, B = Q K-major)
@@ -51,10 +54,11 @@ namespace smla {
 
 constexpr int kChunk = 128;  // keys per chunk = the MMA's M
 constexpr int kLatent = 512;
-constexpr int kThreads = 192;
+constexpr int kThreads = 288;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMmaWarp = 4;
-constexpr int kProducerWarp = 5;
+constexpr int kProducerWarp = 5;  // first of four
+constexpr int kProducerThreads = 128;
 constexpr int kMaxSplits = 16;
 constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -63,14 +67,11 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
 __device__ int32_t g_device_error;
 
 struct Params {
-    // Tensor maps (64-byte aligned kernel parameters): per pool the 512-byte
-    // latent part as 128-byte boxes one row high (128B swizzle) and the 64-byte
-    // rope part (64B swizzle); the Q tile of one token and head group.
-    CUtensorMap kv_latent[2];
-    CUtensorMap kv_rope[2];
+    // Tensor maps (64-byte aligned kernel parameters) of the Q tile of one
+    // token and head group: 128-byte latent boxes (128B swizzle) and the
+    // 64-byte rope box (64B swizzle).
     CUtensorMap q_latent;
     CUtensorMap q_rope;
-    int32_t oob_row[2];  // a row index outside each pool's map: reads as zeros
     const uint8_t* q;
     int64_t q_stride_token, q_stride_head;
     const uint8_t* pool0;
@@ -136,14 +137,14 @@ __device__ __forceinline__ void load_columns(uint32_t taddr, float (&v)[N]) {
 }
 
 template <int N, int D>
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __grid_constant__ Params p) {
+__global__ void __maxnreg__(224) sparse_mla_decode_kernel(const __grid_constant__ Params p) {
     using L = Layout<N, D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (TMA transaction bytes)
+    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (128 cp.async arrivals + 1)
     // pv_done[b]: PV of the chunk in stage b finished (its KV stage and P^T
     // buffer are free, O^T holds it). One barrier per stage, so that no waiter
     // is ever more than one phase behind the barrier it waits on.
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     uint64_t* s_full = bars + 4;    // [2] QK of a chunk done (commit)
     uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (128 softmax arrivals)
     uint64_t* drain = bars + 8;     // every MMA done (commit)
+    uint64_t* q_full = bars + 9;    // the Q tile landed (TMA transaction bytes)
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::kIdx);
@@ -168,8 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
     // ---- set-up (reads no input, so it overlaps the previous kernel) -------
     if (tid == 0) {
-        mbar_init(&kv_full[0], 1);
-        mbar_init(&kv_full[1], 1);
+        mbar_init(&kv_full[0], kProducerThreads + 1);
+        mbar_init(&kv_full[1], kProducerThreads + 1);
+        mbar_init(q_full, 1);
         mbar_init(&pv_done[0], 1);
         mbar_init(&pv_done[1], 1);
         mbar_init(&s_full[0], 1);
@@ -190,14 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
-        prefetch_tensor_map(&p.kv_latent[0]);
-        prefetch_tensor_map(&p.kv_latent[1]);
         prefetch_tensor_map(&p.q_latent);
-        if constexpr (L::kRope) {
-            prefetch_tensor_map(&p.kv_rope[0]);
-            prefetch_tensor_map(&p.kv_rope[1]);
-            prefetch_tensor_map(&p.q_rope);
-        }
+        if constexpr (L::kRope) prefetch_tensor_map(&p.q_rope);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -215,84 +212,69 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     grid_launch_dependents();
 
     bool ok = true;
-    if (warp == kProducerWarp) {
-        // ================================================== producer
-        // Lane l gathers keys 4l .. 4l + 3 of the chunk: one tile::gather4 per
-        // 128-byte latent block and one for the rope block. A masked key asks
-        // for a row outside its pool's map and arrives as zeros.
+    if (warp >= kProducerWarp) {
+        // ================================================== producers
+        // Thread g resolves key g's row; warp w then copies keys 32 w ..
+        // 32 w + 31, one 512-byte latent row per instruction (lane l: bytes
+        // 16 l .. 16 l + 15) and the 64-byte ropes of eight keys per
+        // instruction. Masked keys are zero-filled.
+        const int g = tid - kProducerWarp * 32;
+        const int pw = g >> 5;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
-        auto resolve = [&](int col) -> int32_t {  // the row of a column, -1 if masked
-            if (col >= count) return -1;
-            const int32_t raw = idx_row[col];
-            if (raw < 0) return -1;
-            const bool second = p.num_pools == 2 && col >= p.pool_split;
-            if (raw >= (second ? p.rows1 : p.rows0)) {
-                atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
-                return -1;
-            }
-            return raw;
-        };
+        if (g == 0 && nch > 0) {  // the Q tile of this CTA's heads
+            mbar_arrive_expect_tx(q_full, N * D);
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb)
+                tma_load_3d(sbase + L::kQ + kb * N * 128, &p.q_latent, kb * 128, head0, token, q_full);
+            if constexpr (L::kRope) tma_load_3d(sbase + L::kQ + 4 * N * 128, &p.q_rope, 512, head0, token, q_full);
+        }
+        const uint32_t lane_part = (lane >> 3) * kChunk * 128;
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             const int col0 = (c_first + c) * kChunk;
-            const int k0 = 4 * lane;
-            int32_t row[4];
-            bool second[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int col = col0 + k0 + j;
-                row[j] = resolve(col);
-                idx_s[b * kChunk + k0 + j] = row[j];
-                second[j] = p.num_pools == 2 && col >= p.pool_split;
-                if (row[j] < 0) row[j] = p.oob_row[second[j] ? 1 : 0];
-            }
-            __syncwarp();  // every lane's idx_s entries precede the arrival (release)
-            if (lane == 0)
-                mbar_arrive_expect_tx(&kv_full[b], kChunk * D + (c == 0 ? N * D : 0));
-            __syncwarp();
-            if (c == 0 && lane == 0) {  // the Q tile of this CTA's heads, with the first chunk
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-                    tma_load_3d(sbase + L::kQ + kb * N * 128, &p.q_latent, kb * 128, head0, token, &kv_full[0]);
-                if constexpr (L::kRope)
-                    tma_load_3d(sbase + L::kQ + 4 * N * 128, &p.q_rope, 512, head0, token, &kv_full[0]);
-            }
-            const uint32_t stage = sbase + L::kKv + b * L::kStage;
-            const uint32_t lat_dst = stage + (k0 >> 3) * 1024 + (k0 & 7) * 128;
-            const uint32_t rope_dst = stage + 4 * kChunk * 128 + (k0 >> 3) * 512 + (k0 & 7) * 64;
-            if (second[0] == second[3]) {
-                const int m = second[0] ? 1 : 0;
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-                    tma_gather4(lat_dst + kb * kChunk * 128, &p.kv_latent[m], kb * 128, row[0], row[1], row[2],
-                                row[3], &kv_full[b]);
-                if constexpr (L::kRope)
-                    tma_gather4(rope_dst, &p.kv_rope[m], 512, row[0], row[1], row[2], row[3], &kv_full[b]);
-            } else {  // the group straddles the two pools: one row per copy
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int m = second[j] ? 1 : 0;
-#pragma unroll
-                    for (int kb = 0; kb < 4; ++kb)
-                        tma_load_2d(lat_dst + kb * kChunk * 128 + j * 128, &p.kv_latent[m], kb * 128, row[j],
-                                    &kv_full[b]);
-                    if constexpr (L::kRope)
-                        tma_load_2d(rope_dst + j * 64, &p.kv_rope[m], 512, row[j], &kv_full[b]);
-                }
-            }
-            if (c + 2 < nch) {  // this stage's next chunk: start pulling its rows into L2
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int col = col0 + 2 * kChunk + k0 + j;
-                    const int32_t id = resolve(col);
-                    if (id >= 0) {
-                        const bool sec = p.num_pools == 2 && col >= p.pool_split;
-                        prefetch_l2((sec ? p.pool1 : p.pool0) + static_cast<int64_t>(id) * D, D);
+            {
+                const int col = col0 + g;
+                int32_t id = -1;
+                if (col < count) {
+                    const int32_t raw = idx_row[col];
+                    const bool second = p.num_pools == 2 && col >= p.pool_split;
+                    if (raw >= 0) {
+                        if (raw < (second ? p.rows1 : p.rows0))
+                            id = raw;
+                        else
+                            atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
                     }
                 }
+                idx_s[b * kChunk + g] = id;
             }
+            named_barrier(2, kProducerThreads);
+            if (g == 0) mbar_arrive(&kv_full[b]);  // every producer's idx_s entries (release)
+            const uint32_t stage = sbase + L::kKv + b * L::kStage;
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i) {
+                const int k = pw * 32 + i;
+                const int32_t id = idx_s[b * kChunk + k];
+                const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
+                const uint8_t* src = (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + lane * 16;
+                const uint32_t dst = stage + lane_part + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
+                cp_async_16(dst, src, id >= 0 ? 16u : 0u);
+            }
+            if constexpr (L::kRope) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int k = pw * 32 + j * 8 + (lane >> 2), u = lane & 3;
+                    const int32_t id = idx_s[b * kChunk + k];
+                    const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
+                    const uint8_t* src =
+                        (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + 512 + u * 16;
+                    const uint32_t dst = stage + 4 * kChunk * 128 + (k >> 3) * 512 + (k & 7) * 64 + ((u ^ ((k >> 1) & 3)) << 4);
+                    cp_async_16(dst, src, id >= 0 ? 16u : 0u);
+                }
+            }
+            cp_async_arrive_noinc(&kv_full[b]);
         }
+        cp_async_wait_all();
     } else if (warp == kMmaWarp) {
         // ================================================== MMA issuer
         // QK(c) as soon as chunk c landed and S buffer c % 2 is free (the
@@ -301,31 +283,41 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_e4m3(128, N, 0, 0);
             constexpr uint32_t kIdescPV = idesc_e4m3(128, N, 1, 1);
+            // Descriptors of every operand tile; moving a descriptor by b
+            // bytes adds b >> 4 to its start field (no carry: shared
+            // addresses stay below 256 KB).
+            const uint64_t d_q = smem_desc(sbase + L::kQ, 1024, 1024, kSwizzle128B);
+            const uint64_t d_q_rope = smem_desc(sbase + L::kQ + 4 * N * 128, 512, 512, kSwizzle64B);
+            const uint64_t d_kv = smem_desc(sbase + L::kKv, 1024, 1024, kSwizzle128B);
+            const uint64_t d_kv_rope = smem_desc(sbase + L::kKv + 4 * kChunk * 128, 512, 512, kSwizzle64B);
+            const uint64_t d_p = smem_desc(sbase + L::kP, 8 * N, 8 * N, p_swizzle<N>());
             int next_qk = 0, next_pv = 0;
+            bool q_ready = false;
             uint64_t idle_since = 0;
             while (next_pv < nch) {
                 bool progressed = false;
-                if (next_qk < nch && next_qk <= next_pv + 1 &&
+                if (!q_ready) q_ready = mbar_test_wait(q_full, 0);
+                if (q_ready && next_qk < nch && next_qk <= next_pv + 1 &&
                     mbar_test_wait(&kv_full[next_qk & 1], (next_qk >> 1) & 1)) {
                     const int c = next_qk;
+                    fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
                     tc_fence_after_sync();
-                    const uint32_t stage = sbase + L::kKv + (c & 1) * L::kStage;
+                    const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
+                    const uint32_t d_tmem = tmem + (c & 1) * N;
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t a = smem_desc(stage + kb * kChunk * 128 + ks * 32, 1024, 1024, kSwizzle128B);
-                            const uint64_t bq = smem_desc(sbase + L::kQ + kb * N * 128 + ks * 32, 1024, 1024, kSwizzle128B);
-                            mma_f8(tmem + (c & 1) * N, a, bq, kIdescQK, (kb | ks) != 0 ? 1u : 0u);
+                            const uint32_t a_off = stage16 + ((kb * kChunk * 128 + ks * 32) >> 4);
+                            const uint32_t b_off = (kb * N * 128 + ks * 32) >> 4;
+                            mma_f8(d_tmem, d_kv + a_off, d_q + b_off, kIdescQK, (kb | ks) != 0 ? 1u : 0u);
                         }
                     }
                     if constexpr (L::kRope) {
 #pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const uint64_t a = smem_desc(stage + 4 * kChunk * 128 + ks * 32, 512, 512, kSwizzle64B);
-                            const uint64_t bq = smem_desc(sbase + L::kQ + 4 * N * 128 + ks * 32, 512, 512, kSwizzle64B);
-                            mma_f8(tmem + (c & 1) * N, a, bq, kIdescQK, 1u);
-                        }
+                        for (int ks = 0; ks < 2; ++ks)
+                            mma_f8(d_tmem, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
+                                   kIdescQK, 1u);
                     }
                     mma_commit(&s_full[c & 1]);
                     ++next_qk;
@@ -334,15 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 if (next_pv < next_qk && mbar_test_wait(p_full, next_pv & 1)) {
                     const int c = next_pv;
                     tc_fence_after_sync();
-                    const uint32_t stage = sbase + L::kKv + (c & 1) * L::kStage;
-                    const uint32_t pbuf = sbase + L::kP + (c & 1) * kChunk * N;
+                    const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
+                    const uint32_t p16 = static_cast<uint32_t>((c & 1) * kChunk * N) >> 4;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
 #pragma unroll
                         for (int kk = 0; kk < kChunk / 32; ++kk) {
-                            const uint64_t a = smem_desc(stage + j * kChunk * 128 + kk * 32 * 128, 1024, 1024, kSwizzle128B);
-                            const uint64_t bd = smem_desc(pbuf + kk * 32 * N, 8 * N, 8 * N, p_swizzle<N>());
-                            mma_f8(tmem + 2 * N + j * N, a, bd, kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
+                            const uint32_t a_off = stage16 + ((j * kChunk * 128 + kk * 32 * 128) >> 4);
+                            const uint32_t b_off = p16 + ((kk * 32 * N) >> 4);
+                            mma_f8(tmem + 2 * N + j * N, d_kv + a_off, d_p + b_off, kIdescPV,
+                                   (c > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
                     mma_commit(&pv_done[c & 1]);
@@ -693,20 +686,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A pool seen as `rows` rows of `d` bytes, read in boxes of `box` bytes of one
-// row (tile::gather4 reads four such rows).
-bool encode_pool_map(CUtensorMap* map, const void* base, int64_t rows, int d, int box, CUtensorMapSwizzle swizzle) {
-    auto enc = tensor_map_encoder();
-    if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d)};
-    const cuuint32_t boxes[2] = {static_cast<cuuint32_t>(box), 1};
-    const cuuint32_t steps[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, boxes, steps,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Q as [T][H][D] bytes with the caller's strides, read in boxes of `box`
 // bytes x n heads of one token.
 bool encode_q_map(CUtensorMap* map, const void* q, const smla_shape* s, int n, int box, CUtensorMapSwizzle swizzle) {
@@ -847,14 +826,6 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
     {
         const int n = plan.head_tile;
         const bool rope = shape->head_dim == 576;
-        for (int i = 0; i < 2; ++i) {
-            const smla_pool& pl = kv_pools[shape->num_pools == 2 ? i : 0];
-            if (!encode_pool_map(&p.kv_latent[i], pl.data, pl.rows, shape->head_dim, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-                return SMLA_EUNSUPPORTED;
-            if (rope && !encode_pool_map(&p.kv_rope[i], pl.data, pl.rows, shape->head_dim, 64, CU_TENSOR_MAP_SWIZZLE_64B))
-                return SMLA_EUNSUPPORTED;
-            p.oob_row[i] = static_cast<int32_t>(pl.rows > 0 ? pl.rows : 1);
-        }
         if (!encode_q_map(&p.q_latent, q, shape, n, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
         if (rope && !encode_q_map(&p.q_rope, q, shape, n, 64, CU_TENSOR_MAP_SWIZZLE_64B)) return SMLA_EUNSUPPORTED;
     }

@@ -141,6 +141,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                  : "memory");
 }
 
+// Arrives on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's count must include this arrival: .noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
