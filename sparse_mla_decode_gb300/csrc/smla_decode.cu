@@ -137,7 +137,7 @@ __device__ __forceinline__ void load_columns(uint32_t taddr, float (&v)[N]) {
 }
 
 template <int N, int D>
-__global__ void __maxnreg__(200) sparse_mla_decode_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __grid_constant__ Params p) {
     using L = Layout<N, D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
