@@ -30,7 +30,8 @@
 //   S^T[key, head]   = KV[key, :] . Q[head, :]      (A = KV K-major, B = Q K-major)
 //   O^T[lat, head]  += V^T[lat, key] . P^T[key, head] (A = the same KV tile read
 //                      MN-major, B = P^T K-major), four 128-latent blocks.
-// TMEM holds two S^T buffers (2N columns) and O^T (4N columns).
+// TMEM holds two S^T buffers, each as two partial sums over halves of the
+// row (independent accumulator chains keep the tensor pipe busy), and O^T.
 // Key splits of one (token, head tile) form a cluster and merge over DSMEM.
 // Every wait is bounded; a timeout sets an error bit and the kernel still
 // returns (and frees its TMEM).
@@ -109,7 +110,9 @@ struct Layout {
     static constexpr int kMisc = kBar + 16 * 8;         // tmem base, abort flag
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;
-    static constexpr int kTmemCols = 6 * N <= 128 ? 128 : (6 * N <= 256 ? 256 : 512);
+    // TMEM columns: S^T chain 0 of buffers 0/1 at [0, 2N), O^T blocks at
+    // [2N, 6N), S^T chain 1 of buffers 0/1 at [6N, 8N).
+    static constexpr int kTmemCols = 8 * N;
 };
 
 // P^T for PV: B operand of N heads x 128 keys, MN-major (each key's N heads
@@ -128,12 +131,44 @@ __host__ __device__ constexpr uint32_t p_swizzle() {
     return N == 64 ? kSwizzle64B : (N == 32 ? kSwizzle32B : kSwizzleNone);
 }
 
+// 16 heads' logits: the sum of the two partial-sum chains of S^T.
+__device__ __forceinline__ void load_logits16(uint32_t chain0, uint32_t chain1, float (&s)[16]) {
+    float v[32];
+    tmem_load16x2(chain0, chain1, v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s[j] = v[j] + v[16 + j];
+}
+
 // N consecutive TMEM columns of this warp's lanes.
 template <int N>
 __device__ __forceinline__ void load_columns(uint32_t taddr, float (&v)[N]) {
     if constexpr (N == 16) tmem_load16x1(taddr, v);
     if constexpr (N == 32) tmem_load32x1(taddr, v);
     if constexpr (N == 64) tmem_load32x2(taddr, taddr + 32, v);
+}
+
+// Writes the BF16 tile [N heads][512] from shared memory to out[token][head0
+// + h][:], 16 bytes per thread per step when the output rows allow it.
+template <int N>
+__device__ __forceinline__ void store_rows(const Params& p, const __nv_bfloat16* tile, int token, int head0,
+                                           int tid) {
+    __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
+                         static_cast<int64_t>(head0) * p.out_stride_head;
+    const bool wide = ((reinterpret_cast<uintptr_t>(p.out) | static_cast<uintptr_t>(p.out_stride_token * 2) |
+                        static_cast<uintptr_t>(p.out_stride_head * 2)) & 15u) == 0;
+    if (wide) {
+        for (int i = tid; i < N * kLatent / 8; i += kSoftmaxThreads) {
+            const int h = i / (kLatent / 8), e = (i % (kLatent / 8)) * 8;
+            *reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
+                *reinterpret_cast<const uint4*>(tile + h * kLatent + e);
+        }
+    } else {
+        for (int i = tid; i < N * kLatent / 2; i += kSoftmaxThreads) {
+            const int h = i / (kLatent / 2), e = (i % (kLatent / 2)) * 2;
+            *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
+                *reinterpret_cast<const uint32_t*>(tile + h * kLatent + e);
+        }
+    }
 }
 
 template <int N, int D>
@@ -303,20 +338,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
                     tc_fence_after_sync();
                     const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
-                    const uint32_t d_tmem = tmem + (c & 1) * N;
+                    // chain 0: latent bytes 0..255; chain 1: 256..511 and the
+                    // rope; their MMAs alternate so neither waits on itself
+                    const uint32_t d_s0 = tmem + (c & 1) * N;
+                    const uint32_t d_s1 = tmem + 6 * N + (c & 1) * N;
 #pragma unroll
-                    for (int kb = 0; kb < 4; ++kb) {
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint32_t a_off = stage16 + ((kb * kChunk * 128 + ks * 32) >> 4);
-                            const uint32_t b_off = (kb * N * 128 + ks * 32) >> 4;
-                            mma_f8(d_tmem, d_kv + a_off, d_q + b_off, kIdescQK, (kb | ks) != 0 ? 1u : 0u);
-                        }
+                    for (int i = 0; i < 8; ++i) {
+                        const int kb = i >> 2, ks = i & 3;
+                        const uint32_t a0 = stage16 + ((kb * kChunk * 128 + ks * 32) >> 4);
+                        const uint32_t b0 = (kb * N * 128 + ks * 32) >> 4;
+                        mma_f8(d_s0, d_kv + a0, d_q + b0, kIdescQK, i != 0 ? 1u : 0u);
+                        const uint32_t a1 = stage16 + (((kb + 2) * kChunk * 128 + ks * 32) >> 4);
+                        const uint32_t b1 = ((kb + 2) * N * 128 + ks * 32) >> 4;
+                        mma_f8(d_s1, d_kv + a1, d_q + b1, kIdescQK, i != 0 ? 1u : 0u);
                     }
                     if constexpr (L::kRope) {
 #pragma unroll
                         for (int ks = 0; ks < 2; ++ks)
-                            mma_f8(d_tmem, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
+                            mma_f8(d_s1, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
                                    kIdescQK, 1u);
                     }
                     mma_commit(&s_full[c & 1]);
@@ -329,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
                     const uint32_t p16 = static_cast<uint32_t>((c & 1) * kChunk * N) >> 4;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int kk = 0; kk < kChunk / 32; ++kk) {  // the four latent blocks are independent chains
 #pragma unroll
-                        for (int kk = 0; kk < kChunk / 32; ++kk) {
+                        for (int j = 0; j < 4; ++j) {
                             const uint32_t a_off = stage16 + ((j * kChunk * 128 + kk * 32 * 128) >> 4);
                             const uint32_t b_off = p16 + ((kk * 32 * N) >> 4);
                             mma_f8(tmem + 2 * N + j * N, d_kv + a_off, d_p + b_off, kIdescPV,
@@ -372,19 +411,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             ok &= mbar_wait_bounded(&s_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             tc_fence_after_sync();
             const bool active = idx_s[b * kChunk + tid] >= 0;
-            float s[N];
-            load_columns<N>(tmem + lane_base + b * N, s);
+            const uint32_t chain0 = tmem + lane_base + b * N, chain1 = tmem + lane_base + 6 * N + b * N;
 
             // chunk maxima per head, in logit units (bmm1_scale > 0 keeps the
-            // order; masked keys are -inf)
+            // order; masked keys are -inf); 16 heads per TMEM batch
             float mine0 = -INFINITY, mine1 = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < N; ++h) {
-                const float m = warp_max(active ? s[h] : -INFINITY);
-                if (h < 32)
-                    mine0 = (lane == h) ? m : mine0;
-                else
-                    mine1 = (lane == h - 32) ? m : mine1;
+            for (int g = 0; g < N / 16; ++g) {
+                float s16[16];
+                load_logits16(chain0 + 16 * g, chain1 + 16 * g, s16);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int h = 16 * g + j;
+                    const float m = warp_max(active ? s16[j] : -INFINITY);
+                    if (h < 32)
+                        mine0 = (lane == h) ? m : mine0;
+                    else
+                        mine1 = (lane == h - 32) ? m : mine1;
+                }
             }
             if (lane < N) red[warp * N + lane] = mine0;
             if (N > 32) red[warp * N + 32 + lane] = mine1;
@@ -402,29 +446,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             // P = 2^(s * scale_log2 - m + log2 448) as E4M3 into P^T[b] (PV of
             // chunk c-2 has finished reading it); FP32 sums of the unrounded P
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
-            uint32_t words[N / 4];
-#pragma unroll
-            for (int h4 = 0; h4 < N / 4; ++h4) {
-                const float4 bi = reinterpret_cast<const float4*>(bias_s)[h4];
-                const float4 al = reinterpret_cast<const float4*>(alpha_s)[h4];
-                float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                if (active) {
-                    pr[0] = fast_exp2(fmaf(s[4 * h4 + 0], scale_log2, -bi.x));
-                    pr[1] = fast_exp2(fmaf(s[4 * h4 + 1], scale_log2, -bi.y));
-                    pr[2] = fast_exp2(fmaf(s[4 * h4 + 2], scale_log2, -bi.z));
-                    pr[3] = fast_exp2(fmaf(s[4 * h4 + 3], scale_log2, -bi.w));
-                }
-                lsum[4 * h4 + 0] = fmaf(lsum[4 * h4 + 0], al.x, pr[0]);
-                lsum[4 * h4 + 1] = fmaf(lsum[4 * h4 + 1], al.y, pr[1]);
-                lsum[4 * h4 + 2] = fmaf(lsum[4 * h4 + 2], al.z, pr[2]);
-                lsum[4 * h4 + 3] = fmaf(lsum[4 * h4 + 3], al.w, pr[3]);
-                words[h4] = e4m3x2(pr[0], pr[1]) | (e4m3x2(pr[2], pr[3]) << 16);
-            }
             uint8_t* pbuf = smem + L::kP + b * kChunk * N;
 #pragma unroll
-            for (int u = 0; u < N / 16; ++u)
-                *reinterpret_cast<uint4*>(pbuf + p_unit<N>(tid, u)) =
-                    make_uint4(words[4 * u], words[4 * u + 1], words[4 * u + 2], words[4 * u + 3]);
+            for (int g = 0; g < N / 16; ++g) {
+                float s16[16];
+                load_logits16(chain0 + 16 * g, chain1 + 16 * g, s16);
+                uint32_t words[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int h4 = 4 * g + q4;
+                    const float4 bi = reinterpret_cast<const float4*>(bias_s)[h4];
+                    const float4 al = reinterpret_cast<const float4*>(alpha_s)[h4];
+                    float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    if (active) {
+                        pr[0] = fast_exp2(fmaf(s16[4 * q4 + 0], scale_log2, -bi.x));
+                        pr[1] = fast_exp2(fmaf(s16[4 * q4 + 1], scale_log2, -bi.y));
+                        pr[2] = fast_exp2(fmaf(s16[4 * q4 + 2], scale_log2, -bi.z));
+                        pr[3] = fast_exp2(fmaf(s16[4 * q4 + 3], scale_log2, -bi.w));
+                    }
+                    lsum[4 * h4 + 0] = fmaf(lsum[4 * h4 + 0], al.x, pr[0]);
+                    lsum[4 * h4 + 1] = fmaf(lsum[4 * h4 + 1], al.y, pr[1]);
+                    lsum[4 * h4 + 2] = fmaf(lsum[4 * h4 + 2], al.z, pr[2]);
+                    lsum[4 * h4 + 3] = fmaf(lsum[4 * h4 + 3], al.w, pr[3]);
+                    words[q4] = e4m3x2(pr[0], pr[1]) | (e4m3x2(pr[2], pr[3]) << 16);
+                }
+                *reinterpret_cast<uint4*>(pbuf + p_unit<N>(tid, g)) = make_uint4(words[0], words[1], words[2], words[3]);
+            }
 
             // O^T *= alpha where a head's running maximum rose (PV of chunk c-1 is done)
             if (c >= 1) {
@@ -444,12 +491,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                         rescale |= (v4.x != 1.0f) | (v4.y != 1.0f) | (v4.z != 1.0f) | (v4.w != 1.0f);
                     }
                     if (rescale) {
-                        const uint32_t col = tmem + lane_base + 2 * N + gq * 16;
-                        float v[64];
-                        tmem_load16x4(col, col + N, col + 2 * N, col + 3 * N, v);
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) v[i] *= a[i & 15];
-                        tmem_store16x4(col, col + N, col + 2 * N, col + 3 * N, v);
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t col = tmem + lane_base + 2 * N + 2 * half * N + gq * 16;
+                            float v[32];
+                            tmem_load16x2(col, col + N, v);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] *= a[i & 15];
+                            tmem_store16x2(col, col + N, v);
+                        }
                     }
                 }
                 tmem_wait_st();
@@ -505,19 +555,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         }
         named_barrier(3, kThreads);
         if (tid < kSoftmaxThreads) {
-            __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
-                                 static_cast<int64_t>(head0) * p.out_stride_head;
+            // O^T rows (one latent index per thread, N heads) -> BF16 [N][512]
+            // in shared memory (the KV tiles are free now), then whole head
+            // rows to global memory with coalesced stores.
+            __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + L::kKv);
 #pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
                 const int lat = blk * 128 + warp * 32 + lane;
-                float v[N];
-                if (!split_empty) load_columns<N>(tmem + lane_base + 2 * N + blk * N, v);
 #pragma unroll
-                for (int j = 0; j < N; ++j) {
-                    const float x = split_empty ? 0.0f : v[j] * bias_s[j];
-                    out[static_cast<int64_t>(j) * p.out_stride_head + lat] = __float2bfloat16_rn(x);
+                for (int g = 0; g < N / 16; ++g) {
+                    float v[16];
+                    if (!split_empty) tmem_load16x1(tmem + lane_base + 2 * N + blk * N + 16 * g, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float x = split_empty ? 0.0f : v[j] * bias_s[16 * g + j];
+                        tile[(16 * g + j) * kLatent + lat] = __float2bfloat16_rn(x);
+                    }
                 }
             }
+            named_barrier(1, kSoftmaxThreads);
+            store_rows<N>(p, tile, token, head0, tid);
         }
     } else {
         // Partials of every split of this (token, head tile) meet at the CTA
@@ -628,7 +685,7 @@ int smem_for(int n, int d) {
     return n == 64 ? smem_bytes<64, 512>() : n == 32 ? smem_bytes<32, 512>() : smem_bytes<16, 512>();
 }
 
-int tmem_for(int n) { return 6 * n <= 128 ? 128 : (6 * n <= 256 ? 256 : 512); }
+int tmem_for(int n) { return 8 * n; }
 
 // Largest split count whose merge area fits the KV + Q tiles it reuses.
 bool merge_fits(int n, int d, int splits) {
