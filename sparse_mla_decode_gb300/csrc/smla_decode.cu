@@ -10,14 +10,16 @@
 // running maximum, FP32 sums of the unrounded P, FP32 accumulation, an FP32
 // merge of the key splits across a thread-block cluster, one BF16 rounding.
 //
-// GB300 design (one CTA per SM, 288 threads):
-//   warps 0-3  softmax: one thread per key of a 128-key chunk (the TMEM lane of
-//              S^T), per-head maxima by warp reductions + shared memory, P as
-//              E4M3 into shared memory, rescale of O^T in TMEM, epilogue/merge;
-//   warp 4     allocates TMEM and issues the tcgen05 MMAs from one thread,
+// GB300 design (one CTA per SM, 512 threads, 16 warps = 4 per SM sub-partition):
+//   warps 0-7  softmax: for a 64-head tile two warpgroups of 32 heads each, for
+//              16 or 32 heads one warpgroup; one thread per key of a 128-key
+//              chunk (the TMEM lane of S^T), per-head maxima by warp
+//              reductions + shared memory, P as E4M3 into shared memory,
+//              rescale of O^T in TMEM, epilogue/merge;
+//   warp 8     allocates TMEM and issues the tcgen05 MMAs from one thread,
 //              QK of the next chunk as soon as its rows landed and PV of the
 //              previous one as soon as its P is ready;
-//   warps 5-8  producers: 16-byte cp.async copies of the chunk's KV rows, one
+//   warps 9-15 producers: 16-byte cp.async copies of the chunk's KV rows, one
 //              row per warp instruction, straight into the swizzled K-major
 //              tiles the MMAs read (masked columns are zero-filled); each
 //              thread's arrival on the stage barrier fires when its copies
@@ -55,11 +57,11 @@ namespace smla {
 
 constexpr int kChunk = 128;  // keys per chunk = the MMA's M
 constexpr int kLatent = 512;
-constexpr int kThreads = 288;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kMmaWarp = 4;
-constexpr int kProducerWarp = 5;  // first of four
-constexpr int kProducerThreads = 128;
+constexpr int kThreads = 512;
+constexpr int kSoftmaxRange = 256;  // warps 0-7: one or two softmax warpgroups
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp = 9;  // first of seven
+constexpr int kProducerThreads = 224;
 constexpr int kMaxSplits = 16;
 constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -131,22 +133,6 @@ __host__ __device__ constexpr uint32_t p_swizzle() {
     return N == 64 ? kSwizzle64B : (N == 32 ? kSwizzle32B : kSwizzleNone);
 }
 
-// 16 heads' logits: the sum of the two partial-sum chains of S^T.
-__device__ __forceinline__ void load_logits16(uint32_t chain0, uint32_t chain1, float (&s)[16]) {
-    float v[32];
-    tmem_load16x2(chain0, chain1, v);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) s[j] = v[j] + v[16 + j];
-}
-
-// N consecutive TMEM columns of this warp's lanes.
-template <int N>
-__device__ __forceinline__ void load_columns(uint32_t taddr, float (&v)[N]) {
-    if constexpr (N == 16) tmem_load16x1(taddr, v);
-    if constexpr (N == 32) tmem_load32x1(taddr, v);
-    if constexpr (N == 64) tmem_load32x2(taddr, taddr + 32, v);
-}
-
 // Writes the BF16 tile [N heads][512] from shared memory to out[token][head0
 // + h][:], 16 bytes per thread per step when the output rows allow it.
 template <int N>
@@ -157,13 +143,13 @@ __device__ __forceinline__ void store_rows(const Params& p, const __nv_bfloat16*
     const bool wide = ((reinterpret_cast<uintptr_t>(p.out) | static_cast<uintptr_t>(p.out_stride_token * 2) |
                         static_cast<uintptr_t>(p.out_stride_head * 2)) & 15u) == 0;
     if (wide) {
-        for (int i = tid; i < N * kLatent / 8; i += kSoftmaxThreads) {
+        for (int i = tid; i < N * kLatent / 8; i += kSoftmaxRange) {
             const int h = i / (kLatent / 8), e = (i % (kLatent / 8)) * 8;
             *reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
                 *reinterpret_cast<const uint4*>(tile + h * kLatent + e);
         }
     } else {
-        for (int i = tid; i < N * kLatent / 2; i += kSoftmaxThreads) {
+        for (int i = tid; i < N * kLatent / 2; i += kSoftmaxRange) {
             const int h = i / (kLatent / 2), e = (i % (kLatent / 2)) * 2;
             *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
                 *reinterpret_cast<const uint32_t*>(tile + h * kLatent + e);
@@ -171,21 +157,43 @@ __device__ __forceinline__ void store_rows(const Params& p, const __nv_bfloat16*
     }
 }
 
+// Logits of the H heads at two TMEM chain addresses (H = 16 or 32): the sum of
+// the two partial-sum chains of S^T, one TMEM round trip.
+template <int H>
+__device__ __forceinline__ void load_logits(uint32_t chain0, uint32_t chain1, float (&s)[H]) {
+    if constexpr (H == 16) {
+        float v[32];
+        tmem_load16x2(chain0, chain1, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) s[j] = v[j] + v[16 + j];
+    } else {
+        float v[64];
+        tmem_load16x4(chain0, chain1, chain0 + 16, chain1 + 16, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            s[j] = v[j] + v[16 + j];
+            s[16 + j] = v[32 + j] + v[48 + j];
+        }
+    }
+}
+
 template <int N, int D>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __grid_constant__ Params p) {
     using L = Layout<N, D>;
+    constexpr int NG = N == 64 ? 2 : 1;  // softmax warpgroups
+    constexpr int HW = N / NG;           // heads per softmax warpgroup (16 or 32)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (128 cp.async arrivals + 1)
+    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (224 cp.async arrivals + 1)
     // pv_done[b]: PV of the chunk in stage b finished (its KV stage and P^T
     // buffer are free, O^T holds it). One barrier per stage, so that no waiter
     // is ever more than one phase behind the barrier it waits on.
     uint64_t* pv_done = bars + 2;   // [2] commit
     uint64_t* s_full = bars + 4;    // [2] QK of a chunk done (commit)
-    uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (128 softmax arrivals)
+    uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (softmax arrivals)
     uint64_t* drain = bars + 8;     // every MMA done (commit)
     uint64_t* q_full = bars + 9;    // the Q tile landed (TMA transaction bytes)
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         mbar_init(&pv_done[1], 1);
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
-        mbar_init(p_full, kSoftmaxThreads);
+        mbar_init(p_full, NG * 128);
         mbar_init(drain, 1);
         misc[1] = 0;
         mbar_init_fence();
@@ -249,10 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     bool ok = true;
     if (warp >= kProducerWarp) {
         // ================================================== producers
-        // Thread g resolves key g's row; warp w then copies keys 32 w ..
-        // 32 w + 31, one 512-byte latent row per instruction (lane l: bytes
-        // 16 l .. 16 l + 15) and the 64-byte ropes of eight keys per
-        // instruction. Masked keys are zero-filled.
+        // Thread g < 128 resolves key g's row; warp w then copies keys w,
+        // w + 7, ..., one 512-byte latent row per instruction (lane l: bytes
+        // 16 l .. 16 l + 15), and the 64-byte ropes of eight keys per
+        // instruction. Masked keys are zero-filled. Thread 0 also arrives
+        // after the index barrier, so that the stage barrier releases idx_s.
         const int g = tid - kProducerWarp * 32;
         const int pw = g >> 5;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
@@ -263,12 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 tma_load_3d(sbase + L::kQ + kb * N * 128, &p.q_latent, kb * 128, head0, token, q_full);
             if constexpr (L::kRope) tma_load_3d(sbase + L::kQ + 4 * N * 128, &p.q_rope, 512, head0, token, q_full);
         }
-        const uint32_t lane_part = (lane >> 3) * kChunk * 128;
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             const int col0 = (c_first + c) * kChunk;
-            {
+            if (g < kChunk) {
                 const int col = col0 + g;
                 int32_t id = -1;
                 if (col < count) {
@@ -283,22 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 }
                 idx_s[b * kChunk + g] = id;
             }
-            named_barrier(2, kProducerThreads);
-            if (g == 0) mbar_arrive(&kv_full[b]);  // every producer's idx_s entries (release)
+            named_barrier(3, kProducerThreads);
+            if (g == 0) mbar_arrive(&kv_full[b]);
             const uint32_t stage = sbase + L::kKv + b * L::kStage;
-#pragma unroll 8
-            for (int i = 0; i < 32; ++i) {
-                const int k = pw * 32 + i;
+            const uint32_t lane_part = stage + (lane >> 3) * kChunk * 128;
+            for (int k = pw; k < kChunk; k += kProducerThreads / 32) {
                 const int32_t id = idx_s[b * kChunk + k];
                 const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
                 const uint8_t* src = (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + lane * 16;
-                const uint32_t dst = stage + lane_part + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
+                const uint32_t dst = lane_part + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
                 cp_async_16(dst, src, id >= 0 ? 16u : 0u);
             }
             if constexpr (L::kRope) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int k = pw * 32 + j * 8 + (lane >> 2), u = lane & 3;
+                for (int j = pw; j < kChunk / 8; j += kProducerThreads / 32) {
+                    const int k = j * 8 + (lane >> 2), u = lane & 3;
                     const int32_t id = idx_s[b * kChunk + k];
                     const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
                     const uint8_t* src =
@@ -339,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     tc_fence_after_sync();
                     const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
                     // chain 0: latent bytes 0..255; chain 1: 256..511 and the
-                    // rope; their MMAs alternate so neither waits on itself
+                    // rope; their MMAs alternate
                     const uint32_t d_s0 = tmem + (c & 1) * N;
                     const uint32_t d_s1 = tmem + 6 * N + (c & 1) * N;
 #pragma unroll
@@ -395,82 +401,82 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             mma_commit(drain);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 4 * NG) {
         // ===================================================== softmax
-        // Thread tid owns key tid of each chunk (TMEM lane tid of S^T) and,
-        // for O^T, latent rows 32 * warp + lane of each 128-latent block.
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        // Warpgroup wg owns heads hb .. hb + HW - 1. Thread t owns key t of
+        // each chunk (TMEM lane t of S^T) and, for O^T, latent rows t of each
+        // 128-latent block.
+        const int wg = warp >> 2, t = tid & 127, hb = wg * HW;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const float scale_log2 = p.scale_log2;
-        float lsum[N];
+        float lsum[HW];
 #pragma unroll
-        for (int h = 0; h < N; ++h) lsum[h] = 0.0f;
+        for (int h = 0; h < HW; ++h) lsum[h] = 0.0f;
 
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
             ok &= mbar_wait_bounded(&kv_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             ok &= mbar_wait_bounded(&s_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             tc_fence_after_sync();
-            const bool active = idx_s[b * kChunk + tid] >= 0;
-            const uint32_t chain0 = tmem + lane_base + b * N, chain1 = tmem + lane_base + 6 * N + b * N;
+            const bool active = idx_s[b * kChunk + t] >= 0;
+            const uint32_t chain0 = tmem + lane_base + b * N + hb, chain1 = tmem + lane_base + 6 * N + b * N + hb;
 
             // chunk maxima per head, in logit units (bmm1_scale > 0 keeps the
-            // order; masked keys are -inf); 16 heads per TMEM batch
-            float mine0 = -INFINITY, mine1 = -INFINITY;
+            // order; masked keys are -inf)
+            {
+                float s[HW];
+                load_logits<HW>(chain0, chain1, s);
+                float mine = -INFINITY;
 #pragma unroll
-            for (int g = 0; g < N / 16; ++g) {
-                float s16[16];
-                load_logits16(chain0 + 16 * g, chain1 + 16 * g, s16);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int h = 16 * g + j;
-                    const float m = warp_max(active ? s16[j] : -INFINITY);
-                    if (h < 32)
-                        mine0 = (lane == h) ? m : mine0;
-                    else
-                        mine1 = (lane == h - 32) ? m : mine1;
+                for (int j = 0; j < HW; ++j) {
+                    const float m = warp_max(active ? s[j] : -INFINITY);
+                    mine = (lane == j) ? m : mine;
                 }
+                if (lane < HW) red[(warp & 3) * N + hb + lane] = mine;
             }
-            if (lane < N) red[warp * N + lane] = mine0;
-            if (N > 32) red[warp * N + 32 + lane] = mine1;
-            named_barrier(1, kSoftmaxThreads);
-            if (tid < N) {
-                const float cm = fmaxf(fmaxf(red[tid], red[N + tid]), fmaxf(red[2 * N + tid], red[3 * N + tid]));
-                const float mo = m_run_s[tid];
+            named_barrier(1 + wg, 128);
+            if (t < HW) {
+                const int h = hb + t;
+                const float cm = fmaxf(fmaxf(red[h], red[N + h]), fmaxf(red[2 * N + h], red[3 * N + h]));
+                const float mo = m_run_s[h];
                 const float mn = fmaxf(mo, cm * scale_log2);
-                alpha_s[tid] = (mo == -INFINITY) ? 1.0f : fast_exp2(mo - mn);
-                bias_s[tid] = mn - kLog2P;
-                m_run_s[tid] = mn;
+                alpha_s[h] = (mo == -INFINITY) ? 1.0f : fast_exp2(mo - mn);
+                bias_s[h] = mn - kLog2P;
+                m_run_s[h] = mn;
             }
-            named_barrier(1, kSoftmaxThreads);
+            named_barrier(1 + wg, 128);
 
             // P = 2^(s * scale_log2 - m + log2 448) as E4M3 into P^T[b] (PV of
             // chunk c-2 has finished reading it); FP32 sums of the unrounded P
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
-            uint8_t* pbuf = smem + L::kP + b * kChunk * N;
+            {
+                float s[HW];
+                load_logits<HW>(chain0, chain1, s);
+                uint8_t* pbuf = smem + L::kP + b * kChunk * N;
 #pragma unroll
-            for (int g = 0; g < N / 16; ++g) {
-                float s16[16];
-                load_logits16(chain0 + 16 * g, chain1 + 16 * g, s16);
-                uint32_t words[4];
+                for (int g = 0; g < HW / 16; ++g) {
+                    uint32_t words[4];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int h4 = 4 * g + q4;
-                    const float4 bi = reinterpret_cast<const float4*>(bias_s)[h4];
-                    const float4 al = reinterpret_cast<const float4*>(alpha_s)[h4];
-                    float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    if (active) {
-                        pr[0] = fast_exp2(fmaf(s16[4 * q4 + 0], scale_log2, -bi.x));
-                        pr[1] = fast_exp2(fmaf(s16[4 * q4 + 1], scale_log2, -bi.y));
-                        pr[2] = fast_exp2(fmaf(s16[4 * q4 + 2], scale_log2, -bi.z));
-                        pr[3] = fast_exp2(fmaf(s16[4 * q4 + 3], scale_log2, -bi.w));
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int j = 16 * g + 4 * q4;
+                        const float4 bi = reinterpret_cast<const float4*>(bias_s + hb)[j / 4];
+                        const float4 al = reinterpret_cast<const float4*>(alpha_s + hb)[j / 4];
+                        float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        if (active) {
+                            pr[0] = fast_exp2(fmaf(s[j + 0], scale_log2, -bi.x));
+                            pr[1] = fast_exp2(fmaf(s[j + 1], scale_log2, -bi.y));
+                            pr[2] = fast_exp2(fmaf(s[j + 2], scale_log2, -bi.z));
+                            pr[3] = fast_exp2(fmaf(s[j + 3], scale_log2, -bi.w));
+                        }
+                        lsum[j + 0] = fmaf(lsum[j + 0], al.x, pr[0]);
+                        lsum[j + 1] = fmaf(lsum[j + 1], al.y, pr[1]);
+                        lsum[j + 2] = fmaf(lsum[j + 2], al.z, pr[2]);
+                        lsum[j + 3] = fmaf(lsum[j + 3], al.w, pr[3]);
+                        words[q4] = e4m3x2(pr[0], pr[1]) | (e4m3x2(pr[2], pr[3]) << 16);
                     }
-                    lsum[4 * h4 + 0] = fmaf(lsum[4 * h4 + 0], al.x, pr[0]);
-                    lsum[4 * h4 + 1] = fmaf(lsum[4 * h4 + 1], al.y, pr[1]);
-                    lsum[4 * h4 + 2] = fmaf(lsum[4 * h4 + 2], al.z, pr[2]);
-                    lsum[4 * h4 + 3] = fmaf(lsum[4 * h4 + 3], al.w, pr[3]);
-                    words[q4] = e4m3x2(pr[0], pr[1]) | (e4m3x2(pr[2], pr[3]) << 16);
+                    *reinterpret_cast<uint4*>(pbuf + p_unit<N>(t, hb / 16 + g)) =
+                        make_uint4(words[0], words[1], words[2], words[3]);
                 }
-                *reinterpret_cast<uint4*>(pbuf + p_unit<N>(tid, g)) = make_uint4(words[0], words[1], words[2], words[3]);
             }
 
             // O^T *= alpha where a head's running maximum rose (PV of chunk c-1 is done)
@@ -478,12 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 ok &= mbar_wait_bounded(&pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
                 tc_fence_after_sync();
 #pragma unroll
-                for (int gq = 0; gq < N / 16; ++gq) {
+                for (int g = 0; g < HW / 16; ++g) {
                     float a[16];
                     bool rescale = false;
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
-                        const float4 v4 = reinterpret_cast<const float4*>(alpha_s)[gq * 4 + j4];
+                        const float4 v4 = reinterpret_cast<const float4*>(alpha_s + hb + 16 * g)[j4];
                         a[4 * j4 + 0] = v4.x;
                         a[4 * j4 + 1] = v4.y;
                         a[4 * j4 + 2] = v4.z;
@@ -491,15 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                         rescale |= (v4.x != 1.0f) | (v4.y != 1.0f) | (v4.z != 1.0f) | (v4.w != 1.0f);
                     }
                     if (rescale) {
+                        const uint32_t col = tmem + lane_base + 2 * N + hb + 16 * g;
+                        float v[64];
+                        tmem_load16x4(col, col + N, col + 2 * N, col + 3 * N, v);
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const uint32_t col = tmem + lane_base + 2 * N + 2 * half * N + gq * 16;
-                            float v[32];
-                            tmem_load16x2(col, col + N, v);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] *= a[i & 15];
-                            tmem_store16x2(col, col + N, v);
-                        }
+                        for (int i = 0; i < 64; ++i) v[i] *= a[i & 15];
+                        tmem_store16x4(col, col + N, col + 2 * N, col + 3 * N, v);
                     }
                 }
                 tmem_wait_st();
@@ -513,14 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
         // per-head totals of the per-thread partial sums
 #pragma unroll
-        for (int h = 0; h < N; ++h) {
-            float t = lsum[h];
+        for (int j = 0; j < HW; ++j) {
+            float v = lsum[j];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
-            if (lane == (h & 31)) red[warp * N + h] = t;
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+            if (lane == j) red[(warp & 3) * N + hb + j] = v;
         }
-        named_barrier(1, kSoftmaxThreads);
-        if (tid < N) l_s[tid] = (red[tid] + red[N + tid]) + (red[2 * N + tid] + red[3 * N + tid]);
+        named_barrier(1 + wg, 128);
+        if (t < HW) {
+            const int h = hb + t;
+            l_s[h] = (red[h] + red[N + h]) + (red[2 * N + h] + red[3 * N + h]);
+        }
     }
     if (!ok) {
         *abort_flag = 1;
@@ -531,8 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     tc_fence_after_sync();
 
     // ================================================ epilogue / merge
+    // Warps 0-7 (softmax range); warpgroup wg < NG holds heads hb .. hb + HW - 1.
     const bool split_empty = (m_run_s[0] == -INFINITY);  // no active key in this split
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int wg = warp >> 2, hb = wg * HW;
+    const bool has_heads = warp < 4 * NG;
     if (splits == 1) {
         if (tid < N) {
             const int h = head0 + tid;
@@ -553,29 +562,30 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             bias_s[tid] = scale;
             if (p.lse != nullptr) p.lse[static_cast<int64_t>(token) * p.lse_stride_token + h] = lse2;
         }
-        named_barrier(3, kThreads);
-        if (tid < kSoftmaxThreads) {
-            // O^T rows (one latent index per thread, N heads) -> BF16 [N][512]
-            // in shared memory (the KV tiles are free now), then whole head
-            // rows to global memory with coalesced stores.
-            __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + L::kKv);
+        named_barrier(4, kThreads);
+        __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + L::kKv);
+        if (has_heads) {
+            // O^T rows (one latent index per thread, this warpgroup's heads)
+            // -> BF16 [N][512] in shared memory (the KV tiles are free now)
 #pragma unroll 1
-            for (int blk = 0; blk < 4; ++blk) {
-                const int lat = blk * 128 + warp * 32 + lane;
+            for (int blk = 0; blk < 4; blk += 64 / HW) {  // 64 values per TMEM round trip
+                float v[64];
+                const uint32_t col = tmem + lane_base + 2 * N + hb;
+                if constexpr (HW == 32)
+                    tmem_load16x4(col + blk * N, col + blk * N + 16, col + (blk + 1) * N, col + (blk + 1) * N + 16, v);
+                else
+                    tmem_load16x4(col, col + N, col + 2 * N, col + 3 * N, v);
 #pragma unroll
-                for (int g = 0; g < N / 16; ++g) {
-                    float v[16];
-                    if (!split_empty) tmem_load16x1(tmem + lane_base + 2 * N + blk * N + 16 * g, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float x = split_empty ? 0.0f : v[j] * bias_s[16 * g + j];
-                        tile[(16 * g + j) * kLatent + lat] = __float2bfloat16_rn(x);
-                    }
+                for (int i = 0; i < 64; ++i) {
+                    const int bb = HW == 32 ? blk + i / 32 : i / 16;  // latent block of value i
+                    const int j = HW == 32 ? i % 32 : i % 16;        // head within the warpgroup
+                    const float x = split_empty ? 0.0f : v[i] * bias_s[hb + j];
+                    tile[(hb + j) * kLatent + bb * 128 + (warp & 3) * 32 + lane] = __float2bfloat16_rn(x);
                 }
             }
-            named_barrier(1, kSoftmaxThreads);
-            store_rows<N>(p, tile, token, head0, tid);
         }
+        named_barrier(4, kThreads);
+        if (tid < kSoftmaxRange) store_rows<N>(p, tile, token, head0, tid);
     } else {
         // Partials of every split of this (token, head tile) meet at the CTA
         // owning their latent slice: slice s (latent 32 s .. 32 s + 31, s < 16)
@@ -593,16 +603,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 st_cluster_f32(map_to_rank(stats + ((split * 2 + 1) * N + tid) * 4, r), l_s[tid]);
             }
         }
-        if (tid < kSoftmaxThreads && !split_empty) {
+        if (has_heads && !split_empty) {
 #pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
-                const int slice = blk * 4 + warp;
+                const int slice = blk * 4 + (warp & 3);
                 const int owner = slice % splits, slot = slice / splits;
-                const uint32_t dst = map_to_rank(inbox + (((split * slots + slot) * N) * 32 + lane) * 4, owner);
-                float v[N];
-                load_columns<N>(tmem + lane_base + 2 * N + blk * N, v);
+                const uint32_t dst = map_to_rank(inbox + (((split * slots + slot) * N + hb) * 32 + lane) * 4, owner);
+                float v[HW];
+                const uint32_t col = tmem + lane_base + 2 * N + blk * N + hb;
+                if constexpr (HW == 32)
+                    tmem_load32x1(col, v);
+                else
+                    tmem_load16x1(col, v);
 #pragma unroll
-                for (int j = 0; j < N; ++j) st_cluster_f32(dst + j * 32 * 4, v[j]);
+                for (int j = 0; j < HW; ++j) st_cluster_f32(dst + j * 32 * 4, v[j]);
             }
         }
         cluster_sync_all();  // every partial has landed
@@ -634,12 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             }
             if (split == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(token) * p.lse_stride_token + h] = lse2;
         }
-        named_barrier(3, kThreads);
-        if (tid < kSoftmaxThreads) {
+        named_barrier(4, kThreads);
+        if (tid < kSoftmaxRange) {
             const int owned = (16 - split + splits - 1) / splits;
             __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
                                  static_cast<int64_t>(head0) * p.out_stride_head;
-            for (int it = warp; it < owned * N; it += 4) {
+            for (int it = warp; it < owned * N; it += kSoftmaxRange / 32) {
                 const int k = it / N, h = it - k * N;
                 const int slice = split + k * splits;
                 float acc = 0.0f;
