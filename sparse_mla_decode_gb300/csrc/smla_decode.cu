@@ -245,6 +245,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     const uint32_t tmem = misc[0];
 
     grid_dependency_wait();  // inputs are read only after this point
+    if (warp == kProducerWarp && lane == 0) {
+        // The Q tile of this CTA's heads, before anything else is known.
+        mbar_arrive_expect_tx(q_full, N * D);
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+            tma_load_3d(sbase + L::kQ + kb * N * 128, &p.q_latent, kb * 128, head0, token, q_full);
+        if constexpr (L::kRope) tma_load_3d(sbase + L::kQ + 4 * N * 128, &p.q_rope, 512, head0, token, q_full);
+    }
+    if (warp == kProducerWarp && lane < 4 && p.width > 0) {
+        // The first chunk's indices, pulled into L2 while the count loads
+        // (assuming the full width; a shorter count only leaves them unused).
+        const int chunks_w = (p.width + kChunk - 1) / kChunk;
+        const int col = split * ((chunks_w + splits - 1) / splits) * kChunk + 32 * lane;
+        if (col < p.width) prefetch_l2_line(p.indices + static_cast<int64_t>(token) * p.idx_stride + col);
+    }
     const int count = min(max(p.lens[token], 0), p.width);
     // This split's chunks of the token: ceil(chunks / splits) consecutive
     // chunks each, dealt over the token's own count (later splits may be empty).
@@ -265,13 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         const int g = tid - kProducerWarp * 32;
         const int pw = g >> 5;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
-        if (g == 0 && nch > 0) {  // the Q tile of this CTA's heads
-            mbar_arrive_expect_tx(q_full, N * D);
-#pragma unroll
-            for (int kb = 0; kb < 4; ++kb)
-                tma_load_3d(sbase + L::kQ + kb * N * 128, &p.q_latent, kb * 128, head0, token, q_full);
-            if constexpr (L::kRope) tma_load_3d(sbase + L::kQ + 4 * N * 128, &p.q_rope, 512, head0, token, q_full);
-        }
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
@@ -398,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     }
                 }
             }
+            if (!q_ready) ok &= mbar_wait_bounded(q_full, 0, abort_flag, kWaitLimitNs);  // no copy outlives the CTA
             mma_commit(drain);
         }
         __syncwarp();
@@ -649,19 +658,39 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             if (split == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(token) * p.lse_stride_token + h] = lse2;
         }
         named_barrier(4, kThreads);
-        if (tid < kSoftmaxRange) {
+        {
+            // Every thread: eight latent values of one (owned slice, head),
+            // merged from the splits' partials and stored as 16 bytes.
             const int owned = (16 - split + splits - 1) / splits;
             __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
                                  static_cast<int64_t>(head0) * p.out_stride_head;
-            for (int it = warp; it < owned * N; it += kSoftmaxRange / 32) {
-                const int k = it / N, h = it - k * N;
+            const bool wide = ((reinterpret_cast<uintptr_t>(p.out) | static_cast<uintptr_t>(p.out_stride_token * 2) |
+                                static_cast<uintptr_t>(p.out_stride_head * 2)) & 15u) == 0;
+            for (int it = tid; it < owned * N * 4; it += kThreads) {
+                const int q8 = it & 3, h = (it >> 2) % N, k = (it >> 2) / N;
                 const int slice = split + k * splits;
-                float acc = 0.0f;
+                float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
                 for (int s = 0; s < splits; ++s) {
                     const float w = weight_f[s * N + h];
-                    if (w != 0.0f) acc += w * inbox_f[((s * slots + k) * N + h) * 32 + lane];
+                    if (w == 0.0f) continue;
+                    const float4* src = reinterpret_cast<const float4*>(inbox_f + ((s * slots + k) * N + h) * 32 + q8 * 8);
+                    const float4 a = src[0], b = src[1];
+                    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+                    acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
                 }
-                out[static_cast<int64_t>(h) * p.out_stride_head + slice * 32 + lane] = __float2bfloat16_rn(acc);
+                __nv_bfloat16* dst = out + static_cast<int64_t>(h) * p.out_stride_head + slice * 32 + q8 * 8;
+                uint32_t packed[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 two = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+                    packed[e] = *reinterpret_cast<const uint32_t*>(&two);
+                }
+                if (wide) {
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) reinterpret_cast<uint32_t*>(dst)[e] = packed[e];
+                }
             }
         }
     }

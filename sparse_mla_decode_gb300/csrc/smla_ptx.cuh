@@ -157,6 +157,11 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Pulls the 128-byte line holding `ptr` into L2.
+__device__ __forceinline__ void prefetch_l2_line(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr) : "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (the tensor cores read their operands through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
