@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (softmax arrivals)
     uint64_t* drain = bars + 8;     // every MMA done (commit)
     uint64_t* q_full = bars + 9;    // the Q tile landed (TMA transaction bytes)
+    uint64_t* kv_first = bars + 10; // chunk 0 landed (256 cp.async arrivals + 1); later chunks use kv_full
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::kIdx);
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         mbar_init(&s_full[1], 1);
         mbar_init(p_full, NG * 128);
         mbar_init(drain, 1);
+        mbar_init(kv_first, kSoftmaxRange + 1);
         misc[1] = 0;
         mbar_init_fence();
     }
@@ -268,8 +270,59 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     const int c_first = split * per_split;
     const int nch = max(0, min(per_split, chunks_total - c_first));
     grid_launch_dependents();
+    // Chunk c's stage barrier and the parity of its phase: chunk 0 has its own
+    // barrier; stage 1 serves chunks 1, 3, 5, ..., stage 0 chunks 2, 4, ...
+    auto kv_bar = [&](int c) -> uint64_t* { return c == 0 ? kv_first : &kv_full[c & 1]; };
+    auto kv_parity = [](int c) -> uint32_t {
+        return c == 0 ? 0u : static_cast<uint32_t>(((c >> 1) - ((c & 1) ? 0 : 1)) & 1);
+    };
 
     bool ok = true;
+    if (warp < kSoftmaxRange / 32 && nch > 0) {
+        // ============================= chunk 0 by the softmax-range warps
+        // (idle until the first QK): the first gather is on every CTA's
+        // critical path, and more issuing warps stream it faster.
+        const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
+        const int col0 = c_first * kChunk;
+        if (tid < kChunk) {
+            const int col = col0 + tid;
+            int32_t id = -1;
+            if (col < count) {
+                const int32_t raw = idx_row[col];
+                const bool second = p.num_pools == 2 && col >= p.pool_split;
+                if (raw >= 0) {
+                    if (raw < (second ? p.rows1 : p.rows0))
+                        id = raw;
+                    else
+                        atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
+                }
+            }
+            idx_s[tid] = id;
+        }
+        named_barrier(5, kSoftmaxRange);
+        if (tid == 0) mbar_arrive(kv_first);  // every idx_s entry (release)
+        const uint32_t stage = sbase + L::kKv;
+        const uint32_t lane_part = stage + (lane >> 3) * kChunk * 128;
+        for (int k = warp; k < kChunk; k += kSoftmaxRange / 32) {
+            const int32_t id = idx_s[k];
+            const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
+            const uint8_t* src = (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + lane * 16;
+            const uint32_t dst = lane_part + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
+            cp_async_16(dst, src, id >= 0 ? 16u : 0u);
+        }
+        if constexpr (L::kRope) {
+            for (int j = warp; j < kChunk / 8; j += kSoftmaxRange / 32) {
+                const int k = j * 8 + (lane >> 2), u = lane & 3;
+                const int32_t id = idx_s[k];
+                const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
+                const uint8_t* src =
+                    (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + 512 + u * 16;
+                const uint32_t dst = stage + 4 * kChunk * 128 + (k >> 3) * 512 + (k & 7) * 64 + ((u ^ ((k >> 1) & 3)) << 4);
+                cp_async_16(dst, src, id >= 0 ? 16u : 0u);
+            }
+        }
+        cp_async_arrive_noinc(kv_first);
+    }
     if (warp >= kProducerWarp) {
         // ================================================== producers
         // Thread g < 128 resolves key g's row; warp w then copies keys w,
@@ -280,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         const int g = tid - kProducerWarp * 32;
         const int pw = g >> 5;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
-        for (int c = 0; c < nch; ++c) {
+        for (int c = 1; c < nch; ++c) {  // chunk 0 is gathered by the softmax-range warps
             const int b = c & 1;
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             const int col0 = (c_first + c) * kChunk;
@@ -347,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 bool progressed = false;
                 if (!q_ready) q_ready = mbar_test_wait(q_full, 0);
                 if (q_ready && next_qk < nch && next_qk <= next_pv + 1 &&
-                    mbar_test_wait(&kv_full[next_qk & 1], (next_qk >> 1) & 1)) {
+                    mbar_test_wait(kv_bar(next_qk), kv_parity(next_qk))) {
                     const int c = next_qk;
                     fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
                     tc_fence_after_sync();
@@ -424,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
-            ok &= mbar_wait_bounded(&kv_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+            ok &= mbar_wait_bounded(kv_bar(c), kv_parity(c), abort_flag, kWaitLimitNs);
             ok &= mbar_wait_bounded(&s_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             tc_fence_after_sync();
             const bool active = idx_s[b * kChunk + t] >= 0;
@@ -541,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         *abort_flag = 1;
         atomicOr(&g_device_error, SMLA_DEV_TIMEOUT);
     }
+    cp_async_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -584,12 +638,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     tmem_load16x4(col + blk * N, col + blk * N + 16, col + (blk + 1) * N, col + (blk + 1) * N + 16, v);
                 else
                     tmem_load16x4(col, col + N, col + 2 * N, col + 3 * N, v);
+                // Heads j, j + 1 of latents d, d + 1 (lanes l, l ^ 1) as two
+                // BF16 words: the even lane stores head j, the odd lane head
+                // j + 1, each after one exchange with its neighbour.
+                const bool odd = lane & 1;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
+                for (int i = 0; i < 64; i += 2) {
                     const int bb = HW == 32 ? blk + i / 32 : i / 16;  // latent block of value i
-                    const int j = HW == 32 ? i % 32 : i % 16;        // head within the warpgroup
-                    const float x = split_empty ? 0.0f : v[i] * bias_s[hb + j];
-                    tile[(hb + j) * kLatent + bb * 128 + (warp & 3) * 32 + lane] = __float2bfloat16_rn(x);
+                    const int j = HW == 32 ? i % 32 : i % 16;        // head (even) within the warpgroup
+                    const float x0 = split_empty ? 0.0f : v[i] * bias_s[hb + j];
+                    const float x1 = split_empty ? 0.0f : v[i + 1] * bias_s[hb + j + 1];
+                    const float other = __shfl_xor_sync(0xFFFFFFFFu, odd ? x0 : x1, 1);
+                    const __nv_bfloat162 two = odd ? __floats2bfloat162_rn(other, x1) : __floats2bfloat162_rn(x0, other);
+                    const int lat = bb * 128 + (warp & 3) * 32 + (lane & ~1);
+                    *reinterpret_cast<__nv_bfloat162*>(tile + (hb + j + (odd ? 1 : 0)) * kLatent + lat) = two;
                 }
             }
         }
@@ -605,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         float* stats_f = reinterpret_cast<float*>(smem + splits * slots * N * 32 * 4);
         float* weight_f = stats_f + splits * 2 * N;                     // float [S][N]
         const float* inbox_f = reinterpret_cast<const float*>(smem);
-        cluster_sync_all();  // every CTA of the cluster is past its main loop
+        cluster_sync_relaxed();  // every CTA of the cluster is past its main loop
         if (tid < N) {
             for (int r = 0; r < splits; ++r) {
                 st_cluster_f32(map_to_rank(stats + ((split * 2 + 0) * N + tid) * 4, r), m_run_s[tid]);

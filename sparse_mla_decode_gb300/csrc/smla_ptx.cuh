@@ -367,6 +367,12 @@ __device__ __forceinline__ void cluster_sync_all() {  // every thread of every C
                      : "memory");
 }
 
+// The same barrier without release semantics: orders only the reuse of
+// buffers whose readers have finished.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
