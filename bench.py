@@ -59,6 +59,9 @@ def parse():
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
+                    help="time the K calls replayed from one CUDA graph (device time, no host launch "
+                         "cost), or as K library calls from Python")
     ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
                     help="small workloads: rotate over enough input sets with distinct rows to exceed "
                          "2x L2 (back-to-back calls), or flush L2 before every timed call")
@@ -320,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
     def call(i):
         w, d = sets[i % len(sets)], dsets[i % len(sets)]
         smla.smla_decode(d["q"], d["pools"], d["indices"], d["lens"], d["sinks"], w["bmm1_scale"],
-                         w["bmm2_scale"], w["k_scale"], d["out"], d["lse"], stream=stream,
+                         w["bmm2_scale"], w["k_scale"], d["out"], d["lse"], stream=None,
                          pool_split=w.get("pool_split", 0))
 
     dist = None
@@ -342,8 +345,25 @@ def run_ours(args, rank, world, local_rank):
     bits = smla.smla_device_error()
     if bits != 0:
         raise RuntimeError(f"device error bits {bits} during warm-up")
+    graph = None
+    if flush is None and args.launch == "graph":
+        # the K timed calls, captured once; the capture stream becomes the
+        # current stream inside the context, which the calls launch on
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                call(i)
+        graph.replay()
+        barrier()
     t_wall0 = time.time()
-    if flush is None:
+    if graph is not None:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = start.elapsed_time(end)
+    elif flush is None:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(args.steps):
@@ -368,9 +388,12 @@ def run_ours(args, rank, world, local_rank):
     soak_until = t_wall1 + max(0.0, args.soak - (t_wall1 - t_wall0)) if args.soak > 0 else t_wall1
     i = 0
     while time.time() < soak_until:
-        for _ in range(200):
-            call(i)
-            i += 1
+        if graph is not None:
+            graph.replay()
+        else:
+            for _ in range(200):
+                call(i)
+                i += 1
         torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, max(t_wall1, soak_until))
     bits = smla.smla_device_error()
@@ -470,6 +493,8 @@ def run_ours(args, rank, world, local_rank):
                    "back-to-back calls" % (len(sets), np.mean(byts) / 1e6, np.mean(byts) * len(sets) / 1e6))
                   if flush is None else
                   "L2 flushed (256 MB write) before every timed call",
+            "launch": ("one CUDA graph of the %d timed library calls, replayed once" % args.steps)
+                      if graph is not None else "%d library calls from Python" % args.steps,
             "plan": plan,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },

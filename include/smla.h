@@ -87,11 +87,16 @@ typedef struct smla_plan {
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t tmem_columns;     /* tensor-memory columns allocated per CTA */
     int32_t num_sms;          /* SM count the plan was made for */
-    int32_t reserved;
+    int32_t resident_ctas;    /* CTAs in clusters of `splits` the GPU holds at
+                                 once (occupancy query; with an explicit
+                                 num_sms: splits * floor(num_sms / splits)) */
 } smla_plan;
 
 /* Fills *plan for `shape` on a GPU of `num_sms` SMs (num_sms <= 0: the current
- * device's SM count, which needs a CUDA device). Pure host logic otherwise.
+ * device, whose SM count and cluster occupancy are queried; needs a CUDA
+ * device). Pure host logic otherwise. Splits are made only while all
+ * tokens * head_groups * splits CTAs are resident at once: the largest such
+ * split count that gives each CTA fewer chunks, else 1.
  * The environment variable SMLA_SPLITS, when set to a positive integer, forces
  * the split count (clamped to [1, min(chunks, 16)]).
  * Returns SMLA_OK, SMLA_EINVAL or SMLA_EUNSUPPORTED. */

@@ -800,8 +800,10 @@ bool merge_fits(int n, int d, int splits) {
     return splits * slots * n * 32 * 4 + splits * 3 * n * 4 <= limit;
 }
 
+// Opts the kernel into its shared-memory size and non-portable clusters, once
+// per device.
 template <int N, int D>
-cudaError_t launch(const Params& p, dim3 grid, int splits, cudaStream_t stream) {
+cudaError_t configure() {
     auto kernel = sparse_mla_decode_kernel<N, D>;
     constexpr int kSmem = Layout<N, D>::kAlloc;
     static std::atomic<uint64_t> configured{0};
@@ -815,6 +817,65 @@ cudaError_t launch(const Params& p, dim3 grid, int splits, cudaStream_t stream) 
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
+    return cudaSuccess;
+}
+
+// CTAs in clusters of `splits` that the current device holds at once (the
+// occupancy API's cluster count x splits; GPC boundaries make it smaller than
+// the SM count for wide clusters). 0 when the query fails.
+template <int N, int D>
+int resident_ctas_query(int splits) {
+    if (configure<N, D>() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(splits), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Layout<N, D>::kAlloc;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(splits);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, sparse_mla_decode_kernel<N, D>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters * splits;
+}
+
+int resident_ctas_on_device(int n, int d, int splits) {
+    static std::mutex mu;
+    static int cache[64][3][2][kMaxSplits + 1] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || splits < 1 || splits > kMaxSplits) return 0;
+    const int ni = n == 64 ? 0 : n == 32 ? 1 : 2;
+    const int di = d == 576 ? 0 : 1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache[dev][ni][di][splits] != 0) return cache[dev][ni][di][splits];
+    }
+    int r = 0;
+    if (d == 576)
+        r = n == 64 ? resident_ctas_query<64, 576>(splits) : n == 32 ? resident_ctas_query<32, 576>(splits)
+                                                                    : resident_ctas_query<16, 576>(splits);
+    else
+        r = n == 64 ? resident_ctas_query<64, 512>(splits) : n == 32 ? resident_ctas_query<32, 512>(splits)
+                                                                    : resident_ctas_query<16, 512>(splits);
+    if (r > 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache[dev][ni][di][splits] = r;
+    }
+    return r;
+}
+
+template <int N, int D>
+cudaError_t launch(const Params& p, dim3 grid, int splits, cudaStream_t stream) {
+    auto kernel = sparse_mla_decode_kernel<N, D>;
+    constexpr int kSmem = Layout<N, D>::kAlloc;
+    cudaError_t e = configure<N, D>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -905,7 +966,8 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     if (plan == nullptr) return SMLA_EINVAL;
     const int rc = validate(shape);
     if (rc != SMLA_OK) return rc;
-    if (num_sms <= 0) {
+    const bool query_device = num_sms <= 0;
+    if (query_device) {
         num_sms = device_sms();
         if (num_sms <= 0) return SMLA_ECUDA;
     }
@@ -914,22 +976,29 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     const int chunks = (shape->width + kChunk - 1) / kChunk;
     const long units = static_cast<long>(shape->tokens) * groups;
 
-    // Split count: the fewest rounds of chunk work per SM (one CTA per SM),
-    // charging each CTA's fixed work and the cluster merge.
+    // Split count. One CTA runs per SM, each pays a fixed cost (Q, TMEM,
+    // epilogue) besides its chunks, and a chunk's gather runs faster the fewer
+    // CTAs share the HBM. So: while every cluster of the launch fits on the
+    // device at once, more splits shorten the critical path (fewer chunks per
+    // CTA, one cluster merge); once the launch needs a second wave, a split
+    // only adds fixed costs and merges, and none is made.
+    const bool on_device = query_device;
+    auto resident = [&](int s) {
+        const int r = on_device ? resident_ctas_on_device(n, shape->head_dim, s) : 0;
+        return r > 0 ? r : (num_sms / s) * s;
+    };
     int best = 1;
-    double best_cost = 1e300;
+    int best_resident = resident(1);
     const int max_splits = chunks < 8 ? (chunks < 1 ? 1 : chunks) : 8;
-    for (int s = 1; s <= max_splits; ++s) {
-        if (!merge_fits(n, shape->head_dim, s)) continue;
-        const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
-        const int eff = per > 0 ? (chunks + per - 1) / per : 1;
-        if (eff != s) continue;
-        const long ctas = units * eff;
-        const long waves = ctas > 0 ? (ctas + num_sms - 1) / num_sms : 0;
-        const double cost = static_cast<double>(waves) * (per + 0.5) + (eff > 1 ? 0.5 : 0.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = eff;
+    if (units <= best_resident) {
+        for (int s = 2; s <= max_splits; ++s) {
+            if (!merge_fits(n, shape->head_dim, s)) continue;
+            const int per = (chunks + s - 1) / s;
+            if ((chunks + per - 1) / per != s) continue;  // same chunks per CTA as a smaller count
+            const int r = resident(s);
+            if (units * s > r) continue;
+            best = s;
+            best_resident = r;
         }
     }
     if (const char* env = std::getenv("SMLA_SPLITS")) {
@@ -941,6 +1010,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
             while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
             const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
             best = per > 0 ? (chunks + per - 1) / per : 1;
+            best_resident = resident(best);
         }
     }
     plan->head_tile = n;
@@ -954,7 +1024,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     plan->smem_bytes = smem_for(n, shape->head_dim);
     plan->tmem_columns = tmem_for(n);
     plan->num_sms = num_sms;
-    plan->reserved = 0;
+    plan->resident_ctas = best_resident;
     return SMLA_OK;
 }
 

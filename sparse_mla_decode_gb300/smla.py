@@ -42,7 +42,7 @@ class SmlaShape(ctypes.Structure):
 class SmlaPlan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "head_tile", "head_groups", "chunk", "chunks", "splits", "chunks_per_split", "ctas",
-        "threads", "smem_bytes", "tmem_columns", "num_sms", "reserved")]
+        "threads", "smem_bytes", "tmem_columns", "num_sms", "resident_ctas")]
 
 
 class SmlaError(RuntimeError):
@@ -104,7 +104,7 @@ def smla_plan_for(shape: SmlaShape, num_sms: int = 0) -> dict:
     rc = lib.smla_plan_for(ctypes.byref(shape), int(num_sms), ctypes.byref(plan))
     if rc != OK:
         raise SmlaError(rc, "smla_plan_for")
-    return {name: getattr(plan, name) for name, _ in SmlaPlan._fields_ if name != "reserved"}
+    return {name: getattr(plan, name) for name, _ in SmlaPlan._fields_}
 
 
 def _ptr(t):

@@ -56,6 +56,15 @@ def test_plan_fills_the_machine_without_empty_splits(lib, tokens, heads, width, 
     assert heads % p["head_tile"] == 0
 
 
+@pytest.mark.parametrize("tokens,heads,width,want", [(1, 16, 2048, 8), (1, 128, 256, 2), (64, 128, 2048, 1),
+                                                     (128, 128, 2048, 1), (256, 16, 2048, 1), (32, 16, 1024, 4)])
+def test_plan_splits_only_while_resident(lib, tokens, heads, width, want):
+    p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width), num_sms=152)
+    assert p["splits"] == want
+    assert p["resident_ctas"] == (152 // p["splits"]) * p["splits"]
+    assert p["splits"] == 1 or p["ctas"] <= p["resident_ctas"]
+
+
 def test_forced_splits(lib, monkeypatch):
     monkeypatch.setenv("SMLA_SPLITS", "5")
     assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 4  # 16 chunks: 4 x 4 ... no empty split
