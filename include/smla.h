@@ -94,12 +94,17 @@ typedef struct smla_plan {
 
 /* Fills *plan for `shape` on a GPU of `num_sms` SMs (num_sms <= 0: the current
  * device, whose SM count and cluster occupancy are queried; needs a CUDA
- * device). Pure host logic otherwise. Splits are made only while all
- * tokens * head_groups * splits CTAs are resident at once: the largest such
- * split count that gives each CTA fewer chunks, else 1.
- * The environment variable SMLA_SPLITS, when set to a positive integer, forces
- * the split count (clamped to [1, min(chunks, 16)]).
- * Returns SMLA_OK, SMLA_EINVAL or SMLA_EUNSUPPORTED. */
+ * device). Pure host logic otherwise.
+ * The head tile (16, 32 or 64 heads per CTA, dividing `heads`) and the split
+ * count are chosen together: among the choices whose tokens * head_groups *
+ * splits CTAs are all resident at once, the least estimated time (a fixed cost
+ * per CTA that grows with the tile, plus the chunks per CTA at a rate that
+ * grows with the CTAs sharing the HBM); when no choice fits one wave, the
+ * widest tile without splits.
+ * Environment overrides (for measurement): SMLA_HEAD_TILE=16|32|64 forces the
+ * tile when it divides `heads`; SMLA_SPLITS=n (n > 0) forces the split count,
+ * clamped to [1, min(chunks, 16)], with the widest tile unless one is forced.
+ * Returns SMLA_OK, SMLA_EINVAL, SMLA_EUNSUPPORTED or SMLA_ECUDA. */
 int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* plan);
 
 /* Sparse MLA decode (the operation above), asynchronous on `stream`.

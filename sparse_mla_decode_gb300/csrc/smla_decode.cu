@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -971,48 +972,66 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         num_sms = device_sms();
         if (num_sms <= 0) return SMLA_ECUDA;
     }
-    const int n = head_tile_for(shape->heads);
-    const int groups = shape->heads / n;
     const int chunks = (shape->width + kChunk - 1) / kChunk;
-    const long units = static_cast<long>(shape->tokens) * groups;
-
-    // Split count. One CTA runs per SM, each pays a fixed cost (Q, TMEM,
-    // epilogue) besides its chunks, and a chunk's gather runs faster the fewer
-    // CTAs share the HBM. So: while every cluster of the launch fits on the
-    // device at once, more splits shorten the critical path (fewer chunks per
-    // CTA, one cluster merge); once the launch needs a second wave, a split
-    // only adds fixed costs and merges, and none is made.
-    const bool on_device = query_device;
-    auto resident = [&](int s) {
-        const int r = on_device ? resident_ctas_on_device(n, shape->head_dim, s) : 0;
+    const int max_tile = head_tile_for(shape->heads);
+    int forced_tile = 0, forced_splits = 0;
+    if (const char* env = std::getenv("SMLA_HEAD_TILE")) {
+        const int f = std::atoi(env);
+        if ((f == 16 || f == 32 || f == 64) && shape->heads % f == 0) forced_tile = f;
+    }
+    if (const char* env = std::getenv("SMLA_SPLITS")) forced_splits = std::max(0, std::atoi(env));
+    auto resident = [&](int tile, int s) {
+        const int r = query_device ? resident_ctas_on_device(tile, shape->head_dim, s) : 0;
         return r > 0 ? r : (num_sms / s) * s;
     };
+
+    // Head tile and split count. One CTA runs per SM and pays a fixed cost
+    // (Q, TMEM, epilogue; larger for wider head tiles) besides its chunks, and
+    // a chunk costs more the more CTAs share the HBM. Among the (tile, splits)
+    // whose clusters are all resident at once, the one of least estimated
+    // time wins:
+    //   a(tile) + 0.71 log2(splits) + per * (b(tile) + 0.62 ctas / num_sms) us,
+    // per = chunks per CTA; a = 5.1 / 6.3 / 8.0 and b = 2.24 / 2.28 / 2.82 for
+    // 16 / 32 / 64 heads (a least-squares fit of the tokens x heads x top-k
+    // sweep on GB300). A launch that needs a second wave at any tile takes the
+    // widest tile and no split: splitting then only adds fixed costs and
+    // merges, and wider tiles read each gathered row for more heads.
+    int n = forced_tile > 0 ? forced_tile : max_tile;
     int best = 1;
-    int best_resident = resident(1);
+    double best_cost = 1e300;
     const int max_splits = chunks < 8 ? (chunks < 1 ? 1 : chunks) : 8;
-    if (units <= best_resident) {
-        for (int s = 2; s <= max_splits; ++s) {
-            if (!merge_fits(n, shape->head_dim, s)) continue;
-            const int per = (chunks + s - 1) / s;
-            if ((chunks + per - 1) / per != s) continue;  // same chunks per CTA as a smaller count
-            const int r = resident(s);
-            if (units * s > r) continue;
-            best = s;
-            best_resident = r;
+    if (forced_splits == 0) {
+        for (int tile = 64; tile >= 16; tile /= 2) {
+            if (shape->heads % tile != 0 || (forced_tile > 0 && tile != forced_tile)) continue;
+            const long units = static_cast<long>(shape->tokens) * (shape->heads / tile);
+            const double a = tile == 64 ? 8.05 : tile == 32 ? 6.34 : 5.13;
+            const double b = tile == 64 ? 2.82 : tile == 32 ? 2.28 : 2.24;
+            for (int s = 1; s <= max_splits; ++s) {
+                if (s > 1 && !merge_fits(tile, shape->head_dim, s)) continue;
+                const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
+                if (per > 0 && (chunks + per - 1) / per != s) continue;  // same chunks per CTA as fewer splits
+                const long ctas = units * s;
+                if (ctas > resident(tile, s)) continue;
+                const double cost = a + 0.71 * std::log2(static_cast<double>(s)) +
+                                    per * (b + 0.62 * static_cast<double>(ctas) / num_sms);
+                if (cost < best_cost - 1e-9) {
+                    best_cost = cost;
+                    n = tile;
+                    best = s;
+                }
+            }
         }
+    } else {
+        int s = forced_splits;
+        const int cap = chunks < kMaxSplits ? (chunks < 1 ? 1 : chunks) : kMaxSplits;
+        if (s > cap) s = cap;
+        while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
+        const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
+        best = per > 0 ? (chunks + per - 1) / per : 1;
     }
-    if (const char* env = std::getenv("SMLA_SPLITS")) {
-        const int forced = std::atoi(env);
-        if (forced > 0) {
-            int s = forced;
-            const int cap = chunks < kMaxSplits ? (chunks < 1 ? 1 : chunks) : kMaxSplits;
-            if (s > cap) s = cap;
-            while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
-            const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
-            best = per > 0 ? (chunks + per - 1) / per : 1;
-            best_resident = resident(best);
-        }
-    }
+    const int groups = shape->heads / n;
+    const long units = static_cast<long>(shape->tokens) * groups;
+    const int best_resident = resident(n, best);
     plan->head_tile = n;
     plan->head_groups = groups;
     plan->chunk = kChunk;

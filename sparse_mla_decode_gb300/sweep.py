@@ -54,7 +54,7 @@ def index_sets(T, k, R, gen, device):
     return idx, lens
 
 
-def point(T, H, k, pool, steps, device, seed, scan=()):
+def point(T, H, k, pool, steps, device, seed, scan=(), tiles=()):
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     per_call = T * 0.9 * 0.75 * k * D
@@ -112,6 +112,15 @@ def point(T, H, k, pool, steps, device, seed, scan=()):
         return e0.elapsed_time(e1) * 1e3 / (steps * reps), us_eager
 
     us, us_eager = timed(True)
+    by_tile = {}
+    for n in tiles:
+        os.environ["SMLA_HEAD_TILE"] = str(n)
+        try:
+            pl = smla.smla_plan_for(smla.make_shape(T, H, k, D))
+            if pl["head_tile"] == n:
+                by_tile[n] = [round(timed(False)[0], 3), pl["splits"]]
+        finally:
+            del os.environ["SMLA_HEAD_TILE"]
     by_splits = {}
     for s in scan:
         os.environ["SMLA_SPLITS"] = str(s)
@@ -126,7 +135,9 @@ def point(T, H, k, pool, steps, device, seed, scan=()):
     return {"tokens": T, "heads": H, "topk": k, "us_per_call": round(us, 3), "us_eager": round(us_eager, 3),
             "gbs": round(bytes_alg / (us * 1e-6) / 1e9, 1), "tflops": round(flops / (us * 1e-6) / 1e12, 1),
             "splits": plan["splits"], "ctas": plan["ctas"], "resident_ctas": plan["resident_ctas"], "input_sets": R, "device_error": bits,
-            **({"us_by_splits": by_splits} if scan else {})}
+            "head_tile": plan["head_tile"],
+            **({"us_by_splits": by_splits} if scan else {}),
+            **({"us_splits_by_head_tile": by_tile} if tiles else {})}
 
 
 def main():
@@ -135,6 +146,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--out", default=None, help="write the rows as JSON lines here")
     ap.add_argument("--scan-splits", default="", help="also time these forced split counts, e.g. 1,2,4,8")
+    ap.add_argument("--scan-tiles", default="", help="also time these forced head tiles, e.g. 16,32,64")
     ap.add_argument("--points", default="", help="only these points, e.g. 1x16x256,64x128x2048")
     args = ap.parse_args()
     import __graft_entry__
@@ -153,7 +165,9 @@ def main():
     rows = []
     for i, (t, h, k) in enumerate(points):
         scan = tuple(int(v) for v in args.scan_splits.split(",") if v)
-        row = point(t, h, k, pool, args.steps, device, seed=2000 + 7919 * t + 104729 * h + k, scan=scan)
+        tiles = tuple(int(v) for v in args.scan_tiles.split(",") if v)
+        row = point(t, h, k, pool, args.steps, device, seed=2000 + 7919 * t + 104729 * h + k, scan=scan,
+                    tiles=tiles)
         rows.append(row)
         print(json.dumps(row), flush=True)
         if row["device_error"] != 0:

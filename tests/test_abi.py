@@ -65,6 +65,21 @@ def test_plan_splits_only_while_resident(lib, tokens, heads, width, want):
     assert p["splits"] == 1 or p["ctas"] <= p["resident_ctas"]
 
 
+@pytest.mark.parametrize("tokens,heads,width,tile,splits", [(1, 128, 256, 16, 2), (64, 128, 2048, 64, 1),
+                                                            (32, 128, 256, 32, 1), (256, 64, 1024, 64, 1)])
+def test_plan_head_tile(lib, tokens, heads, width, tile, splits):
+    p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width), num_sms=152)
+    assert (p["head_tile"], p["splits"]) == (tile, splits)
+    assert p["head_groups"] * p["head_tile"] == heads
+
+
+def test_forced_head_tile(lib, monkeypatch):
+    monkeypatch.setenv("SMLA_HEAD_TILE", "32")
+    assert smla.smla_plan_for(shape(), num_sms=152)["head_tile"] == 32
+    monkeypatch.setenv("SMLA_HEAD_TILE", "64")
+    assert smla.smla_plan_for(shape(heads=48), num_sms=152)["head_tile"] == 16  # 64 does not divide 48
+
+
 def test_forced_splits(lib, monkeypatch):
     monkeypatch.setenv("SMLA_SPLITS", "5")
     assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 4  # 16 chunks: 4 x 4 ... no empty split
