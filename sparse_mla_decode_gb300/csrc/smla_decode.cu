@@ -336,13 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
         for (int c = 1; c < nch; ++c) {  // chunk 0 is gathered by the softmax-range warps
             const int b = c & 1;
-            if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             const int col0 = (c_first + c) * kChunk;
+            // This chunk's index is loaded before the wait for its stage, so
+            // that its latency overlaps the wait.
+            const int32_t raw = (g < kChunk && col0 + g < count) ? idx_row[col0 + g] : -1;
+            if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             if (g < kChunk) {
                 const int col = col0 + g;
                 int32_t id = -1;
                 if (col < count) {
-                    const int32_t raw = idx_row[col];
                     const bool second = p.num_pools == 2 && col >= p.pool_split;
                     if (raw >= 0) {
                         if (raw < (second ? p.rows1 : p.rows0))
