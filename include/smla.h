@@ -87,9 +87,13 @@ typedef struct smla_plan {
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t tmem_columns;     /* tensor-memory columns allocated per CTA */
     int32_t num_sms;          /* SM count the plan was made for */
-    int32_t resident_ctas;    /* CTAs in clusters of `splits` the GPU holds at
-                                 once (occupancy query; with an explicit
-                                 num_sms: splits * floor(num_sms / splits)) */
+    int32_t resident_ctas;    /* CTAs in clusters of pair * splits the GPU holds
+                                 at once (occupancy query; with an explicit
+                                 num_sms: c * floor(num_sms / c), c the cluster) */
+    int32_t pair;             /* head groups sharing each gathered chunk: 2 when
+                                 one pool and an even number of head groups
+                                 (the pair's CTAs each gather half of a chunk's
+                                 rows into both), else 1 */
 } smla_plan;
 
 /* Fills *plan for `shape` on a GPU of `num_sms` SMs (num_sms <= 0: the current
@@ -102,8 +106,10 @@ typedef struct smla_plan {
  * grows with the CTAs sharing the HBM); when no choice fits one wave, the
  * widest tile without splits.
  * Environment overrides (for measurement): SMLA_HEAD_TILE=16|32|64 forces the
- * tile when it divides `heads`; SMLA_SPLITS=n (n > 0) forces the split count,
- * clamped to [1, min(chunks, 16)], with the widest tile unless one is forced.
+ * tile when it divides `heads`; SMLA_PAIR=0 turns pairing off; SMLA_SPLITS=n
+ * (n > 0) forces the split count,
+ * clamped to [1, min(chunks, 16 / pair)], with the widest tile unless one is
+ * forced.
  * Returns SMLA_OK, SMLA_EINVAL, SMLA_EUNSUPPORTED or SMLA_ECUDA. */
 int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* plan);
 

@@ -76,6 +76,10 @@ struct Params {
     // 64-byte rope box (64B swizzle).
     CUtensorMap q_latent;
     CUtensorMap q_rope;
+    // Row gathers of pool 0 for paired CTAs (tile::gather4, one row high):
+    // 128-byte latent boxes (128B swizzle) and the 64-byte rope box.
+    CUtensorMap kv_latent;
+    CUtensorMap kv_rope;
     const uint8_t* q;
     int64_t q_stride_token, q_stride_head;
     const uint8_t* pool0;
@@ -90,6 +94,7 @@ struct Params {
     float* lse;
     int64_t lse_stride_token;
     int32_t width, pool_split, num_pools, splits;
+    int32_t pair;  // head groups sharing each gathered chunk (1 or 2; 2 needs one pool)
     float scale_log2, out_scale;
 };
 
@@ -198,6 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     uint64_t* drain = bars + 8;     // every MMA done (commit)
     uint64_t* q_full = bars + 9;    // the Q tile landed (TMA transaction bytes)
     uint64_t* kv_first = bars + 10; // chunk 0 landed (256 cp.async arrivals + 1); later chunks use kv_full
+    // stage_free[b] (paired): PV of the chunk in stage b finished in both CTAs
+    // of the pair (one multicast commit from each), so either may refill the
+    // stage in both.
+    uint64_t* stage_free = bars + 11;  // [2]
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::kIdx);
@@ -209,14 +218,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int splits = p.splits;
-    const int split = static_cast<int>(blockIdx.x) % splits;  // == rank in the cluster
+    const bool paired = p.pair == 2;
+    // The cluster holds the splits of `pair` consecutive head groups of one
+    // token: rank = half * splits + split.
+    const int rank = static_cast<int>(blockIdx.x) % (splits * p.pair);
+    const int split = rank % splits;
+    const int half = rank / splits;
     const int head0 = (static_cast<int>(blockIdx.x) / splits) * N;
+    // the CTA of the same split in the other head group of the pair, and both
+    const uint16_t pair_mask = static_cast<uint16_t>((1u << split) | (1u << (splits + split)));
     const int token = blockIdx.y;
 
     // ---- set-up (reads no input, so it overlaps the previous kernel) -------
     if (tid == 0) {
-        mbar_init(&kv_full[0], kProducerThreads + 1);
-        mbar_init(&kv_full[1], kProducerThreads + 1);
+        // paired: the producer's expect-tx arrival; else every producer
+        // thread's cp.async arrival and one index-release arrival
+        mbar_init(&kv_full[0], paired ? 1 : kProducerThreads + 1);
+        mbar_init(&kv_full[1], paired ? 1 : kProducerThreads + 1);
+        mbar_init(&stage_free[0], 2);
+        mbar_init(&stage_free[1], 2);
         mbar_init(q_full, 1);
         mbar_init(&pv_done[0], 1);
         mbar_init(&pv_done[1], 1);
@@ -241,9 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensor_map(&p.q_latent);
         if constexpr (L::kRope) prefetch_tensor_map(&p.q_rope);
+        if (paired) {
+            prefetch_tensor_map(&p.kv_latent);
+            if constexpr (L::kRope) prefetch_tensor_map(&p.kv_rope);
+        }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if (paired)
+        cluster_sync_all();  // the partner's barriers are initialised before anything reaches them
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = misc[0];
 
@@ -273,13 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     grid_launch_dependents();
     // Chunk c's stage barrier and the parity of its phase: chunk 0 has its own
     // barrier; stage 1 serves chunks 1, 3, 5, ..., stage 0 chunks 2, 4, ...
-    auto kv_bar = [&](int c) -> uint64_t* { return c == 0 ? kv_first : &kv_full[c & 1]; };
-    auto kv_parity = [](int c) -> uint32_t {
+    // Paired CTAs use the two stage barriers from chunk 0 on.
+    auto kv_bar = [&](int c) -> uint64_t* { return (c == 0 && !paired) ? kv_first : &kv_full[c & 1]; };
+    auto kv_parity = [&](int c) -> uint32_t {
+        if (paired) return static_cast<uint32_t>((c >> 1) & 1);
         return c == 0 ? 0u : static_cast<uint32_t>(((c >> 1) - ((c & 1) ? 0 : 1)) & 1);
     };
 
     bool ok = true;
-    if (warp < kSoftmaxRange / 32 && nch > 0) {
+    if (warp < kSoftmaxRange / 32 && nch > 0 && !paired) {
         // ============================= chunk 0 by the softmax-range warps
         // (idle until the first QK): the first gather is on every CTA's
         // critical path, and more issuing warps stream it faster.
@@ -324,7 +353,61 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         }
         cp_async_arrive_noinc(kv_first);
     }
-    if (warp >= kProducerWarp) {
+    if (warp >= kProducerWarp && paired) {
+        // =========================================== paired producers
+        // Both CTAs of the pair hold the same token and split, so the same
+        // chunks. Each resolves all 128 indices (the softmax masks by them)
+        // and gathers its half of the rows with tile::gather4, multicast into
+        // the stage of both CTAs; a stage is refilled once PV has released it
+        // in both. Masked keys get a row past the pool's end (zero fill).
+        const int g = tid - kProducerWarp * 32;
+        const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
+        const int32_t past_end = static_cast<int32_t>(p.rows0);
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            const int col0 = (c_first + c) * kChunk;
+            const int32_t raw = (g < kChunk && col0 + g < count) ? idx_row[col0 + g] : -1;
+            if (c >= 2) ok &= mbar_wait_bounded(&stage_free[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
+            if (g < kChunk) {
+                int32_t id = -1;
+                if (raw >= 0) {
+                    if (raw < p.rows0)
+                        id = raw;
+                    else
+                        atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
+                }
+                idx_s[b * kChunk + g] = id;
+            }
+            named_barrier(3, kProducerThreads);
+            if (g == 0) mbar_arrive_expect_tx(&kv_full[b], L::kStage);  // both halves; also releases idx_s
+            if (lane == 0) {
+                // one lane per producer warp: the TMA instructions of one
+                // thread issue one after another, several threads overlap
+                const uint32_t stage = sbase + L::kKv + b * L::kStage;
+                for (int k = half * (kChunk / 2) + 4 * (g >> 5); k < (half + 1) * (kChunk / 2);
+                     k += 4 * (kProducerThreads / 32)) {
+                    int32_t r[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int32_t id = idx_s[b * kChunk + k + i];
+                        r[i] = id >= 0 ? id : past_end;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tma_gather4_multicast(stage + j * kChunk * 128 + (k >> 3) * 1024 + (k & 7) * 128, &p.kv_latent,
+                                              j * 128, r[0], r[1], r[2], r[3], &kv_full[b], pair_mask);
+                    if constexpr (L::kRope)
+                        tma_gather4_multicast(stage + 4 * kChunk * 128 + (k >> 3) * 512 + (k & 7) * 64, &p.kv_rope,
+                                              512, r[0], r[1], r[2], r[3], &kv_full[b], pair_mask);
+                }
+            }
+        }
+        // The partner's commits for the last chunks have reached this CTA's
+        // stage barriers before either CTA moves on to its exit.
+        if (g == 0)
+            for (int c = max(0, nch - 2); c < nch; ++c)
+                ok &= mbar_wait_bounded(&stage_free[c & 1], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+    } else if (warp >= kProducerWarp) {
         // ================================================== producers
         // Thread g < 128 resolves key g's row; warp w then copies keys w,
         // w + 7, ..., one 512-byte latent row per instruction (lane l: bytes
@@ -448,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                         }
                     }
                     mma_commit(&pv_done[c & 1]);
+                    if (paired) mma_commit_multicast(&stage_free[c & 1], pair_mask);
                     ++next_pv;
                     progressed = true;
                 }
@@ -673,8 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         cluster_sync_relaxed();  // every CTA of the cluster is past its main loop
         if (tid < N) {
             for (int r = 0; r < splits; ++r) {
-                st_cluster_f32(map_to_rank(stats + ((split * 2 + 0) * N + tid) * 4, r), m_run_s[tid]);
-                st_cluster_f32(map_to_rank(stats + ((split * 2 + 1) * N + tid) * 4, r), l_s[tid]);
+                st_cluster_f32(map_to_rank(stats + ((split * 2 + 0) * N + tid) * 4, half * splits + r), m_run_s[tid]);
+                st_cluster_f32(map_to_rank(stats + ((split * 2 + 1) * N + tid) * 4, half * splits + r), l_s[tid]);
             }
         }
         if (has_heads && !split_empty) {
@@ -682,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             for (int blk = 0; blk < 4; ++blk) {
                 const int slice = blk * 4 + (warp & 3);
                 const int owner = slice % splits, slot = slice / splits;
-                const uint32_t dst = map_to_rank(inbox + (((split * slots + slot) * N + hb) * 32 + lane) * 4, owner);
+                const uint32_t dst =
+                    map_to_rank(inbox + (((split * slots + slot) * N + hb) * 32 + lane) * 4, half * splits + owner);
                 float v[HW];
                 const uint32_t col = tmem + lane_base + 2 * N + blk * N + hb;
                 if constexpr (HW == 32)
@@ -771,6 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         __syncwarp();
         tmem_dealloc(tmem, L::kTmemCols);
     }
+    if (paired) cluster_sync_all();  // neither CTA of a pair leaves while the other may still signal it
 }
 
 // ============================================================== host side
@@ -874,7 +960,7 @@ int resident_ctas_on_device(int n, int d, int splits) {
 }
 
 template <int N, int D>
-cudaError_t launch(const Params& p, dim3 grid, int splits, cudaStream_t stream) {
+cudaError_t launch(const Params& p, dim3 grid, int cluster, cudaStream_t stream) {
     auto kernel = sparse_mla_decode_kernel<N, D>;
     constexpr int kSmem = Layout<N, D>::kAlloc;
     cudaError_t e = configure<N, D>();
@@ -886,7 +972,7 @@ cudaError_t launch(const Params& p, dim3 grid, int splits, cudaStream_t stream) 
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attrs[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
     attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -927,6 +1013,19 @@ bool encode_q_map(CUtensorMap* map, const void* q, const smla_shape* s, int n, i
     const cuuint32_t steps[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q), dims, strides, boxes, steps,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Pool rows of `d` bytes, read by tile::gather4 in boxes of `box` bytes x 1 row.
+bool encode_kv_map(CUtensorMap* map, const void* pool, int64_t rows, int d, int box, CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr || rows <= 0) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d)};
+    const cuuint32_t boxes[2] = {static_cast<cuuint32_t>(box), 1};
+    const cuuint32_t steps[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, boxes, steps,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -982,6 +1081,11 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         if ((f == 16 || f == 32 || f == 64) && shape->heads % f == 0) forced_tile = f;
     }
     if (const char* env = std::getenv("SMLA_SPLITS")) forced_splits = std::max(0, std::atoi(env));
+    int pair_mode = 1;  // 0: never pair; 1: pair whenever the shape allows
+    if (const char* env = std::getenv("SMLA_PAIR")) pair_mode = std::atoi(env) != 0 ? 1 : 0;
+    auto can_pair = [&](int tile) {
+        return pair_mode != 0 && shape->num_pools == 1 && (shape->heads / tile) % 2 == 0;
+    };
     auto resident = [&](int tile, int s) {
         const int r = query_device ? resident_ctas_on_device(tile, shape->head_dim, s) : 0;
         return r > 0 ? r : (num_sms / s) * s;
@@ -1006,14 +1110,16 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         for (int tile = 64; tile >= 16; tile /= 2) {
             if (shape->heads % tile != 0 || (forced_tile > 0 && tile != forced_tile)) continue;
             const long units = static_cast<long>(shape->tokens) * (shape->heads / tile);
+            const int pair = can_pair(tile) ? 2 : 1;
             const double a = tile == 64 ? 8.05 : tile == 32 ? 6.34 : 5.13;
             const double b = tile == 64 ? 2.82 : tile == 32 ? 2.28 : 2.24;
             for (int s = 1; s <= max_splits; ++s) {
                 if (s > 1 && !merge_fits(tile, shape->head_dim, s)) continue;
                 const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
                 if (per > 0 && (chunks + per - 1) / per != s) continue;  // same chunks per CTA as fewer splits
+                if (pair * s > kMaxSplits) continue;
                 const long ctas = units * s;
-                if (ctas > resident(tile, s)) continue;
+                if (ctas > resident(tile, pair * s)) continue;
                 const double cost = a + 0.71 * std::log2(static_cast<double>(s)) +
                                     per * (b + 0.62 * static_cast<double>(ctas) / num_sms);
                 if (cost < best_cost - 1e-9) {
@@ -1028,12 +1134,14 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         const int cap = chunks < kMaxSplits ? (chunks < 1 ? 1 : chunks) : kMaxSplits;
         if (s > cap) s = cap;
         while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
+        if (can_pair(n) && 2 * s > kMaxSplits) s = kMaxSplits / 2;
         const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
         best = per > 0 ? (chunks + per - 1) / per : 1;
     }
     const int groups = shape->heads / n;
     const long units = static_cast<long>(shape->tokens) * groups;
-    const int best_resident = resident(n, best);
+    const int pair = can_pair(n) ? 2 : 1;
+    const int best_resident = resident(n, pair * best);
     plan->head_tile = n;
     plan->head_groups = groups;
     plan->chunk = kChunk;
@@ -1046,6 +1154,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     plan->tmem_columns = tmem_for(n);
     plan->num_sms = num_sms;
     plan->resident_ctas = best_resident;
+    plan->pair = pair;
     return SMLA_OK;
 }
 
@@ -1103,21 +1212,31 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
     p.pool_split = shape->num_pools == 2 ? shape->pool_split : 0;
     p.num_pools = shape->num_pools;
     p.splits = plan.splits;
+    p.pair = plan.pair;
+    if (plan.pair == 2) {
+        const bool rope = shape->head_dim == 576;
+        if (!encode_kv_map(&p.kv_latent, kv_pools[0].data, kv_pools[0].rows, shape->head_dim, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+            (rope && !encode_kv_map(&p.kv_rope, kv_pools[0].data, kv_pools[0].rows, shape->head_dim, 64,
+                                    CU_TENSOR_MAP_SWIZZLE_64B)))
+            p.pair = 1;  // an empty pool (nothing to gather): unpaired
+    }
     p.scale_log2 = static_cast<float>(static_cast<double>(bmm1_scale) * 1.4426950408889634);
     p.out_scale = static_cast<float>(static_cast<double>(bmm2_scale) * static_cast<double>(k_scale));
 
     const dim3 grid(static_cast<unsigned>(plan.head_groups * plan.splits), static_cast<unsigned>(shape->tokens), 1);
+    const int cluster = plan.splits * p.pair;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     const int n = plan.head_tile;
     if (shape->head_dim == 576) {
-        e = n == 64 ? launch<64, 576>(p, grid, plan.splits, st)
-          : n == 32 ? launch<32, 576>(p, grid, plan.splits, st)
-                    : launch<16, 576>(p, grid, plan.splits, st);
+        e = n == 64 ? launch<64, 576>(p, grid, cluster, st)
+          : n == 32 ? launch<32, 576>(p, grid, cluster, st)
+                    : launch<16, 576>(p, grid, cluster, st);
     } else {
-        e = n == 64 ? launch<64, 512>(p, grid, plan.splits, st)
-          : n == 32 ? launch<32, 512>(p, grid, plan.splits, st)
-                    : launch<16, 512>(p, grid, plan.splits, st);
+        e = n == 64 ? launch<64, 512>(p, grid, cluster, st)
+          : n == 32 ? launch<32, 512>(p, grid, cluster, st)
+                    : launch<16, 512>(p, grid, cluster, st);
     }
     if (e != cudaSuccess) {
         t_last_cuda_error = static_cast<int>(e);
@@ -1154,4 +1273,4 @@ extern "C" const char* smla_error_string(int code) {
 
 extern "C" int smla_last_cuda_error(void) { return t_last_cuda_error; }
 
-extern "C" int smla_version(void) { return 100; }
+extern "C" int smla_version(void) { return 200; }

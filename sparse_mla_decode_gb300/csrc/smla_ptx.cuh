@@ -114,6 +114,20 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int32
         : "memory");
 }
 
+// tile::gather4 with cluster multicast: the four rows land at `dst` (the same
+// shared offset) in every CTA of `cta_mask`, and each of those CTAs' barrier
+// at `bar`'s offset receives the bytes as transaction count.
+__device__ __forceinline__ void tma_gather4_multicast(uint32_t dst, const void* map, int32_t x, int32_t r0,
+                                                      int32_t r1, int32_t r2, int32_t r3, uint64_t* bar,
+                                                      uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int32_t x, int32_t y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
@@ -211,6 +225,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// The same commit, arriving once on the barrier at `bar`'s offset in every CTA
+// of `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 

@@ -42,7 +42,7 @@ class SmlaShape(ctypes.Structure):
 class SmlaPlan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "head_tile", "head_groups", "chunk", "chunks", "splits", "chunks_per_split", "ctas",
-        "threads", "smem_bytes", "tmem_columns", "num_sms", "resident_ctas")]
+        "threads", "smem_bytes", "tmem_columns", "num_sms", "resident_ctas", "pair")]
 
 
 class SmlaError(RuntimeError):

@@ -73,6 +73,15 @@ def test_plan_head_tile(lib, tokens, heads, width, tile, splits):
     assert p["head_groups"] * p["head_tile"] == heads
 
 
+@pytest.mark.parametrize("heads,pools,pair", [(128, 1, 2), (64, 1, 1), (128, 2, 1), (16, 1, 1), (32, 1, 1)])
+def test_plan_pairs_head_groups(lib, heads, pools, pair):
+    kw = dict(tokens=64, heads=heads, width=2048)
+    p = smla.smla_plan_for(smla.make_shape(kw["tokens"], heads, kw["width"], 576, pools, 1024 if pools == 2 else 0),
+                           num_sms=152)
+    assert p["pair"] == pair
+    assert p["head_groups"] % p["pair"] == 0
+
+
 def test_forced_head_tile(lib, monkeypatch):
     monkeypatch.setenv("SMLA_HEAD_TILE", "32")
     assert smla.smla_plan_for(shape(), num_sms=152)["head_tile"] == 32
@@ -84,7 +93,10 @@ def test_forced_splits(lib, monkeypatch):
     monkeypatch.setenv("SMLA_SPLITS", "5")
     assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 4  # 16 chunks: 4 x 4 ... no empty split
     monkeypatch.setenv("SMLA_SPLITS", "16")
+    assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 8  # paired: clusters of 2 x 8 at most
+    monkeypatch.setenv("SMLA_PAIR", "0")
     assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 16
+    monkeypatch.delenv("SMLA_PAIR")
     monkeypatch.setenv("SMLA_SPLITS", "99")
     assert smla.smla_plan_for(shape(width=300), num_sms=152)["splits"] == 3
 

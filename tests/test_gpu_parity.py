@@ -33,7 +33,7 @@ def forced_splits():
 
 
 def test_library_loads_and_reports_version():
-    assert smla.smla_version() == 100
+    assert smla.smla_version() == 200
     assert smla.smla_device_error() == 0
 
 
