@@ -91,9 +91,9 @@ typedef struct smla_plan {
                                  at once (occupancy query; with an explicit
                                  num_sms: c * floor(num_sms / c), c the cluster) */
     int32_t pair;             /* head groups sharing each gathered chunk: 2 when
-                                 one pool and an even number of head groups
-                                 (the pair's CTAs each gather half of a chunk's
-                                 rows into both), else 1 */
+                                 one pool, an even number of head groups and at
+                                 least 4 chunks per CTA (the pair's CTAs each
+                                 gather half of a chunk's rows into both), else 1 */
 } smla_plan;
 
 /* Fills *plan for `shape` on a GPU of `num_sms` SMs (num_sms <= 0: the current
@@ -106,7 +106,8 @@ typedef struct smla_plan {
  * grows with the CTAs sharing the HBM); when no choice fits one wave, the
  * widest tile without splits.
  * Environment overrides (for measurement): SMLA_HEAD_TILE=16|32|64 forces the
- * tile when it divides `heads`; SMLA_PAIR=0 turns pairing off; SMLA_SPLITS=n
+ * tile when it divides `heads`; SMLA_PAIR=0 / 1 turns pairing off / on wherever
+ * the shape allows it; SMLA_SPLITS=n
  * (n > 0) forces the split count,
  * clamped to [1, min(chunks, 16 / pair)], with the widest tile unless one is
  * forced.

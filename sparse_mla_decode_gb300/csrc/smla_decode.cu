@@ -1081,7 +1081,11 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         if ((f == 16 || f == 32 || f == 64) && shape->heads % f == 0) forced_tile = f;
     }
     if (const char* env = std::getenv("SMLA_SPLITS")) forced_splits = std::max(0, std::atoi(env));
-    int pair_mode = 1;  // 0: never pair; 1: pair whenever the shape allows
+    // Pairing (two head groups share each gathered chunk) pays once a CTA
+    // streams at least four chunks, where the gather bounds the pipeline
+    // (up to 12% at 128-256 tokens x 128 heads on GB300); at one or two
+    // chunks per CTA its multicast latency costs up to 8%.
+    int pair_mode = -1;  // -1: by chunks per CTA; 0: never; 1: whenever the shape allows
     if (const char* env = std::getenv("SMLA_PAIR")) pair_mode = std::atoi(env) != 0 ? 1 : 0;
     auto can_pair = [&](int tile) {
         return pair_mode != 0 && shape->num_pools == 1 && (shape->heads / tile) % 2 == 0;
@@ -1110,7 +1114,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         for (int tile = 64; tile >= 16; tile /= 2) {
             if (shape->heads % tile != 0 || (forced_tile > 0 && tile != forced_tile)) continue;
             const long units = static_cast<long>(shape->tokens) * (shape->heads / tile);
-            const int pair = can_pair(tile) ? 2 : 1;
+            const int pair = 1;  // pairing is decided for the chosen tile and splits
             const double a = tile == 64 ? 8.05 : tile == 32 ? 6.34 : 5.13;
             const double b = tile == 64 ? 2.82 : tile == 32 ? 2.28 : 2.24;
             for (int s = 1; s <= max_splits; ++s) {
@@ -1134,13 +1138,17 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         const int cap = chunks < kMaxSplits ? (chunks < 1 ? 1 : chunks) : kMaxSplits;
         if (s > cap) s = cap;
         while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
-        if (can_pair(n) && 2 * s > kMaxSplits) s = kMaxSplits / 2;
+        if (can_pair(n) && pair_mode == 1 && 2 * s > kMaxSplits) s = kMaxSplits / 2;
         const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
         best = per > 0 ? (chunks + per - 1) / per : 1;
     }
     const int groups = shape->heads / n;
     const long units = static_cast<long>(shape->tokens) * groups;
-    const int pair = can_pair(n) ? 2 : 1;
+    const int per_cta = chunks > 0 ? (chunks + best - 1) / best : 0;
+    int pair = 1;
+    if (can_pair(n) && (pair_mode == 1 || per_cta >= 4) && 2 * best <= kMaxSplits &&
+        (units * best <= resident(n, best) ? units * best <= resident(n, 2 * best) : true))
+        pair = 2;
     const int best_resident = resident(n, pair * best);
     plan->head_tile = n;
     plan->head_groups = groups;

@@ -93,9 +93,11 @@ def test_forced_splits(lib, monkeypatch):
     monkeypatch.setenv("SMLA_SPLITS", "5")
     assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 4  # 16 chunks: 4 x 4 ... no empty split
     monkeypatch.setenv("SMLA_SPLITS", "16")
-    assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 8  # paired: clusters of 2 x 8 at most
-    monkeypatch.setenv("SMLA_PAIR", "0")
-    assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 16
+    p = smla.smla_plan_for(shape(), num_sms=152)
+    assert (p["splits"], p["pair"]) == (16, 1)  # one chunk per CTA: unpaired
+    monkeypatch.setenv("SMLA_PAIR", "1")
+    p = smla.smla_plan_for(shape(), num_sms=152)
+    assert (p["splits"], p["pair"]) == (8, 2)  # forced pairing: clusters of 2 x 8 at most
     monkeypatch.delenv("SMLA_PAIR")
     monkeypatch.setenv("SMLA_SPLITS", "99")
     assert smla.smla_plan_for(shape(width=300), num_sms=152)["splits"] == 3
