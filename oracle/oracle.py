@@ -9,6 +9,9 @@ through :func:`build`) and exposes the two oracle modes over numpy arrays:
 * :func:`emulate` -- the Kimi K3.1 ``attn_sparse`` datapath (module docstring,
   the per-chunk softmax with E4M3 P at 448 of the running max, and
   ``SparseDcpDecode.merge``) replayed on a given (splits, chunk) partition.
+* :func:`merge` / :func:`merge_f64` -- the LSE merge of partial (out, lse) sets
+  of the Kimi K3.1 ``mla/dcp`` page (``DcpValue``: weights exp2(lse - max) /
+  sum, an FP32 weighted sum of the BF16 rows, one BF16 rounding).
 
 It shares no code with the CUDA path and never imports it.
 """
@@ -57,6 +60,22 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _MergeProblem(ctypes.Structure):
+    _fields_ = [
+        ("sources", ctypes.c_int32),
+        ("tokens", ctypes.c_int32),
+        ("heads", ctypes.c_int32),
+        ("parts", ctypes.c_void_p),
+        ("part_stride_source", ctypes.c_int64),
+        ("part_stride_token", ctypes.c_int64),
+        ("part_stride_head", ctypes.c_int64),
+        ("lses", ctypes.c_void_p),
+        ("lse_stride_source", ctypes.c_int64),
+        ("lse_stride_token", ctypes.c_int64),
+        ("lens", ctypes.c_void_p),
+    ]
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/_build`` (gcc, OpenMP, no FP contraction)."""
     if not force and os.path.exists(LIBRARY) and os.path.getmtime(LIBRARY) >= max(
@@ -91,6 +110,8 @@ def _load():
             lib.smla_oracle_fp64_pairs.argtypes = [P, vp, vp, i32, vp, vp, i32]
             lib.smla_oracle_emulate_pairs.argtypes = [P, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
             lib.smla_oracle_max_threads.restype = i32
+            lib.smla_oracle_merge_f64.argtypes = [i32, vp, vp, vp, vp]
+            lib.smla_oracle_merge_pairs.argtypes = [ctypes.POINTER(_MergeProblem), vp, vp, i32, vp, vp, vp, i32]
             del i64
             _lib = lib
     return _lib
@@ -195,4 +216,56 @@ def emulate(problem: Problem, splits: int, chunk: int, pairs=None, flags: int = 
                                        threads)
     if rc != 0:
         raise ValueError("oracle emulate: bad partition")
+    return value, bits, lse
+
+
+def merge_f64(rows, lses):
+    """The merge in double of ``rows`` [S, 512] with base-2 ``lses`` [S].
+    Returns (out [512] float64, lse2 float)."""
+    lib = _load()
+    rows = _c(rows, np.float64).reshape(-1, LATENT)
+    lses = _c(lses, np.float64).reshape(-1)
+    assert rows.shape[0] == lses.size
+    out = np.zeros(LATENT, np.float64)
+    lse = np.zeros(1, np.float64)
+    lib.smla_oracle_merge_f64(int(lses.size), rows.ctypes.data, lses.ctypes.data, out.ctypes.data,
+                              lse.ctypes.data)
+    return out, float(lse[0])
+
+
+class MergeProblem:
+    """Host copy of one merge problem: ``parts`` BF16 bits uint16 [S, T, H, 512],
+    ``lses`` float32 [S, T, H] (base 2), ``lens`` int32 [T] or None."""
+
+    def __init__(self, parts, lses, lens=None):
+        self.parts = _c(parts, np.uint16)
+        self.lses = _c(lses, np.float32)
+        self.lens = None if lens is None else _c(lens, np.int32)
+        S, T, H, J = self.parts.shape
+        assert J == LATENT and self.lses.shape == (S, T, H)
+        m = _MergeProblem()
+        m.sources, m.tokens, m.heads = S, T, H
+        m.parts = self.parts.ctypes.data
+        m.part_stride_source, m.part_stride_token, m.part_stride_head = T * H * J, H * J, J
+        m.lses = self.lses.ctypes.data
+        m.lse_stride_source, m.lse_stride_token = T * H, H
+        m.lens = None if self.lens is None else self.lens.ctypes.data
+        self.struct = m
+        self.tokens, self.heads = T, H
+
+
+def merge(problem: MergeProblem, pairs=None, threads: int = 0):
+    """LSE merge of the (token, head) ``pairs`` (all, row-major, when None).
+    Returns (value [n, 512] float64 before rounding, bf16 [n, 512] uint16 bits,
+    lse2 [n] float64)."""
+    lib = _load()
+    tok, head = _pairs(problem, pairs)
+    n = tok.size
+    value = np.zeros((n, LATENT), np.float64)
+    bits = np.zeros((n, LATENT), np.uint16)
+    lse = np.zeros(n, np.float64)
+    rc = lib.smla_oracle_merge_pairs(ctypes.byref(problem.struct), tok.ctypes.data, head.ctypes.data, n,
+                                     value.ctypes.data, bits.ctypes.data, lse.ctypes.data, threads)
+    if rc != 0:
+        raise MemoryError("oracle merge")
     return value, bits, lse

@@ -325,6 +325,89 @@ int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, 
     return 0;
 }
 
+/* ----------------------------------------------- LSE merge of partial sets */
+/*
+ * [DCP]  vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.dcp --
+ *        DcpValue (class docstring and merge): the owner weights each source
+ *        s of a (token, head) by exp2(lse_s - max) / sum over the sources, in
+ *        FP32; a source whose LSE is NaN, -inf or +inf (or a token of count
+ *        0) is empty and weighs nothing; the weighted sum of the sources' BF16
+ *        rows is taken in FP32 and rounded to BF16 once. A token with no
+ *        source left gets zeros.
+ * Readings: an LSE that is not finite marks an empty source; the merged LSE,
+ * which the page does not output, is max + log2(sum of weights) (base 2),
+ * -inf for an empty result.
+ */
+
+/* The merge in double: `sources` rows of 512 values with base-2 LSEs. */
+int smla_oracle_merge_f64(int sources, const double* rows, const double* lses, double* out, double* lse2) {
+    double top = -INFINITY;
+    for (int s = 0; s < sources; ++s)
+        if (isfinite(lses[s]) && lses[s] > top) top = lses[s];
+    double total = 0.0;
+    for (int s = 0; s < sources; ++s)
+        if (isfinite(lses[s])) total += exp2(lses[s] - top);
+    for (int j = 0; j < LATENT; ++j) out[j] = 0.0;
+    if (!(total > 0.0)) {
+        *lse2 = -INFINITY;
+        return 0;
+    }
+    for (int s = 0; s < sources; ++s) {
+        if (!isfinite(lses[s])) continue;
+        double weight = exp2(lses[s] - top) / total;
+        for (int j = 0; j < LATENT; ++j) out[j] += weight * rows[(size_t)s * LATENT + j];
+    }
+    *lse2 = top + log2(total);
+    return 0;
+}
+
+/* The merge of (t, h) from BF16 rows: out_value (double, before rounding),
+ * out_bf16 (bits) and the merged LSE; any may be NULL. */
+int smla_oracle_merge(const smla_oracle_merge_problem* m, int t, int h, double* out_value,
+                      uint16_t* out_bf16, double* lse2_out) {
+    double* rows = (double*)malloc(sizeof(double) * (size_t)m->sources * LATENT);
+    double* lses = (double*)malloc(sizeof(double) * (size_t)(m->sources > 0 ? m->sources : 1));
+    double out[LATENT];
+    double lse2 = -INFINITY;
+    if (!rows || !lses) {
+        free(rows);
+        free(lses);
+        return -1;
+    }
+    int live = !(m->lens && m->lens[t] <= 0);
+    for (int s = 0; s < m->sources; ++s) {
+        const uint16_t* part = m->parts + s * m->part_stride_source + (int64_t)t * m->part_stride_token +
+                               (int64_t)h * m->part_stride_head;
+        for (int j = 0; j < LATENT; ++j) rows[(size_t)s * LATENT + j] = smla_oracle_bf16_to_float(part[j]);
+        lses[s] = live ? (double)m->lses[s * m->lse_stride_source + (int64_t)t * m->lse_stride_token + h]
+                       : -INFINITY;
+    }
+    smla_oracle_merge_f64(m->sources, rows, lses, out, &lse2);
+    for (int j = 0; j < LATENT; ++j) {
+        if (out_value) out_value[j] = out[j];
+        if (out_bf16) out_bf16[j] = smla_oracle_bf16_from_float((float)out[j]);
+    }
+    if (lse2_out) *lse2_out = lse2;
+    free(rows);
+    free(lses);
+    return 0;
+}
+
+int smla_oracle_merge_pairs(const smla_oracle_merge_problem* m, const int32_t* tokens,
+                            const int32_t* heads, int n, double* out_value, uint16_t* out_bf16,
+                            double* lse2, int threads) {
+    int bad = 0;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+#endif
+    for (int i = 0; i < n; ++i)
+        bad |= smla_oracle_merge(m, tokens[i], heads[i], out_value ? out_value + (size_t)i * LATENT : NULL,
+                                 out_bf16 ? out_bf16 + (size_t)i * LATENT : NULL, lse2 ? lse2 + i : NULL) != 0;
+    (void)threads;
+    return bad ? -1 : 0;
+}
+
 /* ------------------------------------------------------------ batch drivers */
 
 /* FP64 definition over every (token, head); OpenMP over the pairs. */

@@ -60,6 +60,29 @@ int smla_oracle_emulate_pairs(const smla_oracle_problem* p, const int32_t* token
                               double* out_value, uint16_t* out_bf16, double* lse2, int threads);
 int smla_oracle_max_threads(void);
 
+/* LSE merge of partial sets (the DCP owner's merge).
+ * parts: BF16 bits, element (s, t, h, j) at s*part_stride_source +
+ *        t*part_stride_token + h*part_stride_head + j, j < 512.
+ * lses:  float, (s, t, h) at s*lse_stride_source + t*lse_stride_token + h
+ *        (base 2; not finite = empty source).
+ * lens:  int32 [tokens] or NULL; a token of count <= 0 merges to zeros. */
+typedef struct smla_oracle_merge_problem {
+    int32_t sources, tokens, heads;
+    const uint16_t* parts;
+    int64_t part_stride_source, part_stride_token, part_stride_head;
+    const float* lses;
+    int64_t lse_stride_source, lse_stride_token;
+    const int32_t* lens;
+} smla_oracle_merge_problem;
+
+/* The merge in double of `sources` rows [sources][512] with base-2 LSEs. */
+int smla_oracle_merge_f64(int sources, const double* rows, const double* lses, double* out, double* lse2);
+int smla_oracle_merge(const smla_oracle_merge_problem* m, int t, int h, double* out_value,
+                      uint16_t* out_bf16, double* lse2_out);
+int smla_oracle_merge_pairs(const smla_oracle_merge_problem* m, const int32_t* tokens,
+                            const int32_t* heads, int n, double* out_value, uint16_t* out_bf16,
+                            double* lse2, int threads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -296,3 +296,114 @@ def test_one_chunk_matches_a_float32_library_evaluation():
         assert np.abs(got - ref).max() <= 2e-6 * np.abs(ref).max()
         ref_lse = (m[:, 0] - math.log2(448.0) + torch.log2(l[:, 0])).numpy()
         assert np.abs(lse[t * 16:(t + 1) * 16] - ref_lse).max() <= 1e-5
+
+
+# ------------------------------------------------ LSE merge of partial sets
+# (Kimi K3.1 mla/dcp page, DcpValue: weights exp2(lse - max) / sum, FP32 merge
+# of the BF16 rows, one BF16 rounding; empty sources weigh nothing.)
+
+
+def _column_subset(w, t_cols):
+    """The workload with only the columns in ``t_cols[t]`` kept (others -1)."""
+    sub = dict(w)
+    sub["indices"] = np.full_like(w["indices"], -1)
+    for t, cols in enumerate(t_cols):
+        cols = np.asarray(cols, dtype=np.int64)
+        sub["indices"][t, cols] = w["indices"][t, cols]
+    return sub
+
+
+@pytest.mark.parametrize("layout", ["blocks", "interleaved", "with_empty_part"])
+def test_merge_of_key_disjoint_parts_equals_the_definition(layout):
+    """Decoding disjoint column subsets separately and merging the parts by
+    their LSEs reassembles the decode of all columns (the softmax over a union
+    of keys): pins the weights' base, sign and normalisation to the decode
+    definition."""
+    w = workloads.small("merge_pin", seed=404, tokens=2, heads=16, width=60, head_dim=576,
+                        pool_rows=300, holes=0.1, lens=[60, 45])
+    W = w["indices"].shape[1]
+    if layout == "blocks":
+        parts = [list(range(0, 20)), list(range(20, 41)), list(range(41, W))]
+    elif layout == "interleaved":
+        parts = [list(range(s, W, 3)) for s in range(3)]
+    else:
+        parts = [list(range(0, 30)), [], list(range(30, W))]
+    whole = oracle.Problem.from_workload(w)
+    ref, ref_lse = oracle.fp64(whole)
+    outs, lses = [], []
+    for cols in parts:
+        sub = oracle.Problem.from_workload(_column_subset(w, [cols, cols]))
+        o, l = oracle.fp64(sub)
+        outs.append(o)
+        lses.append(l)
+    outs = np.stack(outs)  # [S, T*H, 512]
+    lses = np.stack(lses)  # [S, T*H]
+    for i in range(ref.shape[0]):
+        got, got_lse = oracle.merge_f64(outs[:, i], lses[:, i])
+        np.testing.assert_allclose(got, ref[i], rtol=1e-12, atol=1e-14)
+        assert abs(got_lse - ref_lse[i]) < 1e-12
+
+
+def _bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_value(bits):
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).float().numpy()
+
+
+def test_merge_with_one_valid_source_passes_it_through():
+    rng = np.random.default_rng(1)
+    parts = _bf16_bits(rng.standard_normal((4, 1, 2, 512)))
+    lses = np.array([[[-np.inf, 3.0]], [[2.5, np.nan]], [[np.nan, -np.inf]], [[np.inf, np.inf]]], np.float32)
+    _, bits, lse = oracle.merge(oracle.MergeProblem(parts, lses))
+    assert np.array_equal(bits[0], parts[1, 0, 0]) and lse[0] == 2.5
+    assert np.array_equal(bits[1], parts[0, 0, 1]) and lse[1] == 3.0
+
+
+def test_merge_of_equal_lses_is_the_mean_row():
+    rng = np.random.default_rng(2)
+    parts = _bf16_bits(rng.standard_normal((5, 2, 3, 512)))
+    lses = np.full((5, 2, 3), 7.25, np.float32)
+    value, _, lse = oracle.merge(oracle.MergeProblem(parts, lses))
+    mean = _bf16_value(parts).astype(np.float64).mean(axis=0).reshape(-1, 512)
+    np.testing.assert_allclose(value, mean, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse, 7.25 + math.log2(5.0), rtol=0, atol=1e-12)
+
+
+def test_merge_weights_in_closed_form():
+    """Two sources: out = (a * 2^la + b * 2^lb) / (2^la + 2^lb)."""
+    rng = np.random.default_rng(3)
+    parts = _bf16_bits(rng.standard_normal((2, 1, 1, 512)))
+    la, lb = 1.0, -2.5
+    lses = np.array([[[la]], [[lb]]], np.float32)
+    value, _, lse = oracle.merge(oracle.MergeProblem(parts, lses))
+    a, b = _bf16_value(parts[0, 0, 0]).astype(np.float64), _bf16_value(parts[1, 0, 0]).astype(np.float64)
+    expect = (a * 2.0 ** la + b * 2.0 ** lb) / (2.0 ** la + 2.0 ** lb)
+    np.testing.assert_allclose(value[0], expect, rtol=1e-14, atol=1e-16)
+    assert abs(lse[0] - math.log2(2.0 ** la + 2.0 ** lb)) < 1e-12
+
+
+def test_merge_is_shift_and_permutation_invariant():
+    rng = np.random.default_rng(4)
+    parts = _bf16_bits(rng.standard_normal((6, 2, 2, 512)))
+    lses = (np.round(rng.uniform(-5, 5, (6, 2, 2)) * 1024) / 1024).astype(np.float32)  # + 16 is exact
+    v0, b0, l0 = oracle.merge(oracle.MergeProblem(parts, lses))
+    v1, b1, l1 = oracle.merge(oracle.MergeProblem(parts, lses + np.float32(16.0)))
+    np.testing.assert_allclose(v1, v0, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l1, l0 + 16.0, rtol=0, atol=1e-9)
+    perm = rng.permutation(6)
+    v2, _, l2 = oracle.merge(oracle.MergeProblem(parts[perm], lses[perm]))
+    np.testing.assert_allclose(v2, v0, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l2, l0, rtol=0, atol=1e-12)
+
+
+def test_merge_empty_rows_are_zero_and_minus_inf():
+    rng = np.random.default_rng(5)
+    parts = _bf16_bits(rng.standard_normal((3, 3, 1, 512)))
+    lses = rng.uniform(-2, 2, (3, 3, 1)).astype(np.float32)
+    lses[:, 1, 0] = -np.inf  # every source empty
+    value, bits, lse = oracle.merge(oracle.MergeProblem(parts, lses, lens=np.array([5, 5, 0], np.int32)))
+    for i in (1, 2):  # all sources empty; token count 0
+        assert np.all(bits[i] == 0) and np.all(value[i] == 0.0) and lse[i] == -np.inf
+    assert np.isfinite(lse[0])
