@@ -2,7 +2,7 @@
 """Benchmark: sparse MLA decode on GB300 (µs per call, achieved HBM GB/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config batch|tiny|verify|two_pool]
+                    [--config batch|tiny|verify|two_pool|merge]
 
 A step is one smla_decode call over one batch of seeded synthetic inputs. The
 default workload is the bandwidth-bound batch: 64 tokens x 128 heads x 2048
@@ -54,7 +54,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool"], default="batch")
+    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge"], default="batch",
+                    help="merge: the LSE merge of 8 partial (out, lse) sets of the 64 x 128 batch shape")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
@@ -564,13 +565,210 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+MERGE_METRIC = "µs/call and achieved HBM GB/s for the LSE merge of partial (out, lse) sets"
+
+
+def merge_bytes(S, T, H) -> int:
+    """Algorithmic bytes of one merge: every source row and LSE read once, the
+    merged row and LSE written once."""
+    return S * T * H * (512 * 2 + 4) + T * H * (512 * 2 + 4) + T * 4
+
+
+def run_merge(args, rank, world, local_rank):
+    """--config merge: smla_merge of 8 partial sets of the 64 x 128 batch shape,
+    rotating over input sets whose bytes exceed 2.5x the L2."""
+    import torch
+
+    import __graft_entry__
+    from sparse_mla_decode_gb300 import smla, workloads
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    S, T, H = 8, 64, 128
+    per_call = merge_bytes(S, T, H)
+    R = int(math.ceil(2.5 * L2_BYTES / per_call))
+    sets = [workloads.merge_sets(1005 + 17 * r + 1000 * rank, S, T, H, device=dev) for r in range(R)]
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+    def call(i):
+        parts, lses, lens = sets[i % R]
+        smla.smla_merge(parts, lses, lens, out, lse)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(max(3, args.warmup)):
+        call(i)
+    barrier()
+    graph = None
+    if args.launch == "graph":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                call(i)
+        graph.replay()
+        barrier()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            call(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    elapsed_ms = start.elapsed_time(end)
+    t_wall1 = time.time()
+    soak_until = t_wall1 + max(0.0, args.soak - (t_wall1 - t_wall0)) if args.soak > 0 else t_wall1
+    while time.time() < soak_until:
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(200):
+                call(i)
+        torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, max(t_wall1, soak_until))
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms = elapsed_ms / args.steps
+    total_bytes = per_call * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        hp = [sets[k][0].cpu().pin_memory() for k in range(R)]
+        hl = [sets[k][1].cpu().pin_memory() for k in range(R)]
+        ho = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+        hlse = torch.empty((T, H), dtype=torch.float32).pin_memory()
+
+        def e2e_step(i):
+            k = i % R
+            sets[k][0].copy_(hp[k], non_blocking=True)
+            sets[k][1].copy_(hl[k], non_blocking=True)
+            call(k)
+            ho.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        barrier()
+        steps = min(args.steps, 200)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(steps):
+            e2e_step(i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1) / steps
+        h2d = hp[0].numel() * 2 + hl[0].numel() * 4
+        e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(ho.numel() * 2 + hlse.numel() * 4)}
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu:
+        cpu = merge_cpu_rate(sets[0], args.cpu_seconds)
+    peak, peak_src = measured_hbm_peak()
+    achieved = per_call / (ms * 1e-3) / 1e9
+    line = {
+        "metric": MERGE_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "us_per_call": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16/f32", "data": "synthetic",
+        "config": {"workload": f"merge_s{S}_t{T}_h{H}: {S} partial (BF16 [T, H, 512], base-2 LSE) sets of "
+                               f"the {T} x {H} batch shape, 3% empty sources, one count-0 token",
+                   "sources": S, "tokens": T, "heads": H, "input_sets": R,
+                   "l2": "rotating %d input sets (%.1f MB per call, %.0f MB in all) between back-to-back calls"
+                         % (R, per_call / 1e6, R * per_call / 1e6),
+                   "launch": ("one CUDA graph of the %d timed library calls, replayed once" % args.steps)
+                             if graph is not None else "%d library calls from Python" % args.steps,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "bytes_alg_per_launch": int(per_call)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def merge_cpu_rate(first_set, seconds: float):
+    """The oracle's merge on all host cores over a bounded sample of rows."""
+    from oracle import oracle
+
+    oracle.build()
+    parts, lses, lens = (x.cpu() for x in first_set)
+    S, T, H, _ = parts.shape
+    prob = oracle.MergeProblem(parts.view(torch_int16()).numpy().view(np.uint16), lses.numpy(), lens.numpy())
+    cores = oracle.max_threads()
+    rng = np.random.default_rng(11)
+    n = min(T * H, 256)
+    t0 = time.perf_counter()
+    done = 0
+    while time.perf_counter() - t0 < seconds and done < 64 * T * H:
+        rows = rng.integers(0, T * H, n)
+        oracle.merge(prob, np.stack([rows // H, rows % H], 1), threads=cores)
+        done += n
+    elapsed = time.perf_counter() - t0
+    per_call = elapsed / done * T * H
+    return {"value": round(merge_bytes(S, T, H) / per_call / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "sample": f"{done} merged rows in batches of {n} drawn from the {T * H} rows of one call",
+            "us_per_call": round(per_call * 1e6, 1)}
+
+
+def torch_int16():
+    import torch
+
+    return torch.int16
+
+
+def run_merge_reference(args, rank, world):
+    """The oracle's merge as the reference arm; rank 0 alone, bounded samples."""
+    if rank != 0:
+        return
+    from sparse_mla_decode_gb300 import workloads
+
+    S, T, H = 8, 64, 128
+    total = max(1, args.steps + args.warmup)
+    cpu = merge_cpu_rate(workloads.merge_sets(1005, S, T, H), min(60.0, 2.0 * total) / total * args.steps)
+    line = {
+        "metric": MERGE_METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(cpu["us_per_call"] / 1e3, 3),
+        "us_per_call": cpu["us_per_call"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"merge_s{S}_t{T}_h{H}", "sources": S, "tokens": T, "heads": H},
+        "cpu_baseline": cpu,
+        "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        if args.config == "merge":
+            run_merge_reference(args, rank, world)
+        else:
+            run_reference(args, rank, world)
         return
     if world > 1:
         import torch
@@ -579,7 +777,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.config == "merge":
+            run_merge(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -137,6 +137,49 @@ int smla_decode(const smla_shape* shape, const void* q, const smla_pool* kv_pool
                 float bmm1_scale, float bmm2_scale, float k_scale, void* out, float* lse,
                 void* stream);
 
+/* ---------------------------------------------------------------- LSE merge
+ * The merge of partial (out, lse) sets of one decode step, e.g. the key
+ * shards of a context-parallel decode, after the Kimi K3.1 `mla/dcp` page
+ * (DcpValue, class docstring and merge): for each (token t, head h), source
+ * s weighs w_s = exp2(lse_s - M) / sum_s' exp2(lse_s' - M) with M the largest
+ * finite lse_s (FP32); a source whose LSE is not finite (NaN, +-inf) weighs
+ * nothing, and so does every source of a token whose count is <= 0;
+ * out[t, h, :] = BF16_RN(sum_s w_s * parts[s, t, h, :]) with the sum in FP32;
+ * lse_out[t, h] = M + log2(sum_s exp2(lse_s - M)), base 2. A (token, head)
+ * with no weight left gets +0.0 and LSE -inf. */
+typedef struct smla_merge_shape {
+    int32_t sources;  /* S partial sets (0: every row is empty) */
+    int32_t tokens;   /* T */
+    int32_t heads;    /* H */
+    int32_t reserved; /* 0 */
+    /* BF16 elements between consecutive sources / tokens / heads of `parts`
+     * (multiples of 8; the 512 latents of a row are contiguous) */
+    int64_t part_stride_source, part_stride_token, part_stride_head;
+    /* float elements between consecutive sources / tokens of `lses` (heads
+     * contiguous) */
+    int64_t lse_stride_source, lse_stride_token;
+    /* BF16 elements between consecutive tokens / heads of `out` (multiples of 8) */
+    int64_t out_stride_token, out_stride_head;
+    /* float elements between consecutive tokens of `lse_out` (heads contiguous) */
+    int64_t lse_out_stride_token;
+} smla_merge_shape;
+
+/* Merges S partial sets into out (and lse_out).
+ *   parts    device, BF16 [S, T, H, 512] at the shape's strides, 16-byte aligned.
+ *   lses     device, float [S, T, H] base-2 LSEs at the shape's strides.
+ *   lens     device, int32 [T] counts (<= 0: the token is empty), or NULL.
+ *   out      device, BF16 [T, H, 512] at the shape's strides, 16-byte aligned;
+ *            must not overlap the inputs.
+ *   lse_out  device, float [T, H], or NULL.
+ *   stream   a cudaStream_t (NULL: the legacy default stream).
+ * Every buffer belongs to the caller; nothing is allocated. Launched with
+ * programmatic dependent launch (inputs are read after the previous kernel in
+ * the stream completed); captureable in a CUDA graph.
+ * Errors: SMLA_EINVAL (null buffers, negative sizes or strides, unaligned rows)
+ * before anything is launched; SMLA_ECUDA when the launch fails. */
+int smla_merge(const smla_merge_shape* shape, const void* parts, const float* lses,
+               const int32_t* lens, void* out, float* lse_out, void* stream);
+
 /* Reads and clears the current device's error word (SMLA_DEV_* bits) after
  * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
 int smla_device_error(int32_t* bits);

@@ -10,8 +10,10 @@ from .smla import (  # noqa: F401
     decode,
     load,
     make_shape,
+    merge,
     smla_decode,
     smla_device_error,
+    smla_merge,
     smla_plan_for,
     smla_version,
 )

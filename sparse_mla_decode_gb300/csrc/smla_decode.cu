@@ -863,6 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
 thread_local int t_last_cuda_error = 0;
 
+void note_cuda_error(int code) { t_last_cuda_error = code; }
+
 int head_tile_for(int heads) {
     if (heads % 64 == 0) return 64;
     if (heads % 32 == 0) return 32;

@@ -1,0 +1,238 @@
+// LSE merge of partial (out, lse) sets on one GPU.
+//
+// What it computes follows the Kimi K3.1 `mla/dcp` page, DcpValue (class
+// docstring and merge): each source s of a (token, head) weighs
+// exp2(lse_s - max) / sum over the sources, in FP32; a source whose LSE is not
+// finite (NaN, -inf, +inf), or every source of a token of count <= 0, weighs
+// nothing; the sources' BF16 rows are summed with these weights in FP32 and
+// rounded to BF16 once. A (token, head) with no weight left gets +0.0 and LSE
+// -inf. The merged LSE (base 2) is max + log2(sum of weights).
+//
+// The pass streams every source row once and writes the merged row once, so
+// it is bound by HBM bandwidth: one warp per (token, head) row, each lane 16
+// consecutive latents (two 16-byte loads per source, four sources in flight),
+// up to eight CTAs per SM, a grid-stride loop beyond that.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "smla.h"
+
+namespace smla {
+void note_cuda_error(int code);  // the thread's last CUDA error, for smla_last_cuda_error
+}
+
+namespace lse_merge {
+
+constexpr int kLatent = 512;
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kGroup = 4;  // sources whose row loads are in flight together
+
+struct Params {
+    const __nv_bfloat16* parts;
+    int64_t part_stride_source, part_stride_token, part_stride_head;  // elements
+    const float* lses;
+    int64_t lse_stride_source, lse_stride_token;  // elements (heads contiguous)
+    const int32_t* lens;                           // [tokens] or null
+    __nv_bfloat16* out;
+    int64_t out_stride_token, out_stride_head;  // elements
+    float* lse_out;                             // or null
+    int64_t lse_out_stride_token;
+    int32_t sources, tokens, heads;
+};
+
+__device__ __forceinline__ uint4 load_nc(const void* ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// acc[0..7] += w * the eight BF16 values of v
+__device__ __forceinline__ void add_weighted(float* acc, float w, const uint4& v) {
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 two;
+        memcpy(&two, &words[e], 4);
+        const float2 f = __bfloat1622float2(two);
+        acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
+    }
+}
+
+__device__ __forceinline__ uint4 pack_bf16(const float* x) {
+    uint32_t words[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 two = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        memcpy(&words[e], &two, 4);
+    }
+    return make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+__global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_constant__ Params p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = static_cast<int64_t>(p.tokens) * p.heads;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kWarps;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial sets are read only after this point
+
+    for (int64_t row = first; row < rows; row += step) {
+        const int t = static_cast<int>(row / p.heads), h = static_cast<int>(row % p.heads);
+        const bool live = p.lens == nullptr || p.lens[t] > 0;
+        const float* lse_th = p.lses + static_cast<int64_t>(t) * p.lse_stride_token + h;
+
+        // the largest finite LSE and the sum of the weights (lanes stride the sources)
+        float top = -INFINITY;
+        if (live)
+            for (int s = lane; s < p.sources; s += 32) {
+                const float l = lse_th[s * p.lse_stride_source];
+                if (isfinite(l)) top = fmaxf(top, l);
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) top = fmaxf(top, __shfl_xor_sync(0xFFFFFFFFu, top, o));
+        float total = 0.0f;
+        if (top != -INFINITY)
+            for (int s = lane; s < p.sources; s += 32) {
+                const float l = lse_th[s * p.lse_stride_source];
+                if (isfinite(l)) total += exp2_approx(l - top);
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        if (total > 0.0f) {
+            const float inverse = 1.0f / total;
+            const __nv_bfloat16* base = p.parts + static_cast<int64_t>(t) * p.part_stride_token +
+                                        static_cast<int64_t>(h) * p.part_stride_head + 16 * lane;
+            int s = 0;
+            for (; s + kGroup <= p.sources; s += kGroup) {  // kGroup sources' loads in flight
+                float w[kGroup];
+                uint4 v[2 * kGroup];
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k) {
+                    const float l = lse_th[(s + k) * p.lse_stride_source];
+                    w[k] = isfinite(l) ? exp2_approx(l - top) * inverse : 0.0f;
+                    if (w[k] != 0.0f) {  // the same for every lane: an empty source's row is never read
+                        const __nv_bfloat16* src = base + (s + k) * p.part_stride_source;
+                        v[2 * k] = load_nc(src);
+                        v[2 * k + 1] = load_nc(src + 8);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k)
+                    if (w[k] != 0.0f) {
+                        add_weighted(acc, w[k], v[2 * k]);
+                        add_weighted(acc + 8, w[k], v[2 * k + 1]);
+                    }
+            }
+            for (; s < p.sources; ++s) {
+                const float l = lse_th[s * p.lse_stride_source];
+                const float w = isfinite(l) ? exp2_approx(l - top) * inverse : 0.0f;
+                if (w != 0.0f) {
+                    const __nv_bfloat16* src = base + s * p.part_stride_source;
+                    add_weighted(acc, w, load_nc(src));
+                    add_weighted(acc + 8, w, load_nc(src + 8));
+                }
+            }
+        }
+        __nv_bfloat16* dst = p.out + static_cast<int64_t>(t) * p.out_stride_token +
+                             static_cast<int64_t>(h) * p.out_stride_head + 16 * lane;
+        reinterpret_cast<uint4*>(dst)[0] = pack_bf16(acc);
+        reinterpret_cast<uint4*>(dst)[1] = pack_bf16(acc + 8);
+        if (p.lse_out != nullptr && lane == 0)
+            p.lse_out[static_cast<int64_t>(t) * p.lse_out_stride_token + h] =
+                total > 0.0f ? top + log2f(total) : -INFINITY;
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return sms;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+}  // namespace lse_merge
+
+using namespace lse_merge;
+
+extern "C" int smla_merge(const smla_merge_shape* shape, const void* parts, const float* lses,
+                          const int32_t* lens, void* out, float* lse_out, void* stream) {
+    if (shape == nullptr) return SMLA_EINVAL;
+    const smla_merge_shape& s = *shape;
+    if (s.sources < 0 || s.tokens < 0 || s.heads < 0) return SMLA_EINVAL;
+    if (s.tokens == 0 || s.heads == 0) return SMLA_OK;
+    if (out == nullptr || (s.sources > 0 && (parts == nullptr || lses == nullptr))) return SMLA_EINVAL;
+    // 16-byte loads and stores of each row
+    if (!aligned16(out) || (s.sources > 0 && !aligned16(parts))) return SMLA_EINVAL;
+    if (s.part_stride_source % 8 || s.part_stride_token % 8 || s.part_stride_head % 8 || s.out_stride_token % 8 ||
+        s.out_stride_head % 8)
+        return SMLA_EINVAL;
+    if (s.part_stride_source < 0 || s.part_stride_token < 0 || s.part_stride_head < 0 || s.lse_stride_source < 0 ||
+        s.lse_stride_token < 0 || s.out_stride_token < 0 || s.out_stride_head < 0 || s.lse_out_stride_token < 0)
+        return SMLA_EINVAL;
+    if (s.heads > 1 && (s.out_stride_head < kLatent || (s.sources > 0 && s.part_stride_head < kLatent)))
+        return SMLA_EINVAL;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.parts = static_cast<const __nv_bfloat16*>(parts);
+    p.part_stride_source = s.part_stride_source;
+    p.part_stride_token = s.part_stride_token;
+    p.part_stride_head = s.part_stride_head;
+    p.lses = lses;
+    p.lse_stride_source = s.lse_stride_source;
+    p.lse_stride_token = s.lse_stride_token;
+    p.lens = lens;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.out_stride_token = s.out_stride_token;
+    p.out_stride_head = s.out_stride_head;
+    p.lse_out = lse_out;
+    p.lse_out_stride_token = s.lse_out_stride_token;
+    p.sources = s.sources;
+    p.tokens = s.tokens;
+    p.heads = s.heads;
+
+    const int sms = device_sms();
+    if (sms <= 0) return SMLA_ECUDA;
+    // One row per warp up to eight CTAs per SM (the CTA scheduler keeps the SMs
+    // busy as rows finish); beyond that, a grid-stride loop.
+    const int64_t rows = static_cast<int64_t>(s.tokens) * s.heads;
+    const int64_t want = (rows + kWarps - 1) / kWarps;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel, p);
+    if (e != cudaSuccess) {
+        smla::note_cuda_error(static_cast<int>(e));
+        return SMLA_ECUDA;
+    }
+    return SMLA_OK;
+}

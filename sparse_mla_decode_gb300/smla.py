@@ -45,6 +45,18 @@ class SmlaPlan(ctypes.Structure):
         "threads", "smem_bytes", "tmem_columns", "num_sms", "resident_ctas", "pair")]
 
 
+class SmlaMergeShape(ctypes.Structure):
+    _fields_ = [
+        ("sources", ctypes.c_int32), ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("part_stride_source", ctypes.c_int64), ("part_stride_token", ctypes.c_int64),
+        ("part_stride_head", ctypes.c_int64),
+        ("lse_stride_source", ctypes.c_int64), ("lse_stride_token", ctypes.c_int64),
+        ("out_stride_token", ctypes.c_int64), ("out_stride_head", ctypes.c_int64),
+        ("lse_out_stride_token", ctypes.c_int64),
+    ]
+
+
 class SmlaError(RuntimeError):
     def __init__(self, code: int, what: str):
         lib = _lib
@@ -82,6 +94,8 @@ def load(path: str | None = None):
         lib.smla_error_string.restype = ctypes.c_char_p
         lib.smla_last_cuda_error.restype = i32
         lib.smla_version.restype = i32
+        lib.smla_merge.argtypes = [ctypes.POINTER(SmlaMergeShape), vp, vp, vp, vp, vp, vp]
+        lib.smla_merge.restype = i32
         _lib = lib
         return lib
 
@@ -173,3 +187,43 @@ def decode(q, kv_pools, indices, lens, sinks=None, bmm1_scale=1.0, bmm2_scale=1.
     lse = torch.empty((T, H), dtype=torch.float32, device=q.device) if with_lse else None
     return smla_decode(q, kv_pools, indices, lens, sinks, bmm1_scale, bmm2_scale, k_scale, out, lse,
                        stream=stream, pool_split=pool_split)
+
+
+def smla_merge(parts: torch.Tensor, lses: torch.Tensor, lens: torch.Tensor | None, out: torch.Tensor,
+               lse_out: torch.Tensor | None, stream=None):
+    """LSE merge of partial sets through the C ABI (see ``smla_merge`` in smla.h).
+
+    parts: bfloat16 [S, T, H, 512] on the device, latents contiguous; lses:
+    float32 [S, T, H] (base 2), heads contiguous; lens: int32 [T] or None;
+    out: bfloat16 [T, H, 512]; lse_out: float32 [T, H] or None. Runs on
+    ``stream`` (default: torch's current stream) without synchronising."""
+    lib = load()
+    S, T, H, J = parts.shape
+    if J != LATENT or tuple(lses.shape) != (S, T, H) or tuple(out.shape) != (T, H, LATENT):
+        raise ValueError("merge: parts [S, T, H, 512], lses [S, T, H], out [T, H, 512]")
+    if parts.stride(3) != 1 or out.stride(2) != 1 or (H > 1 and lses.stride(2) != 1):
+        raise ValueError("merge: latents and heads must be contiguous")
+    if lse_out is not None and H > 1 and lse_out.stride(1) != 1:
+        raise ValueError("merge: lse_out heads must be contiguous")
+    shape = SmlaMergeShape()
+    shape.sources, shape.tokens, shape.heads, shape.reserved = S, T, H, 0
+    shape.part_stride_source, shape.part_stride_token, shape.part_stride_head = parts.stride()[:3]
+    shape.lse_stride_source, shape.lse_stride_token = lses.stride()[:2]
+    shape.out_stride_token, shape.out_stride_head = out.stride()[:2]
+    shape.lse_out_stride_token = 0 if lse_out is None else lse_out.stride(0)
+    if stream is None:
+        stream = torch.cuda.current_stream(out.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib.smla_merge(ctypes.byref(shape), _ptr(parts), _ptr(lses), _ptr(lens), _ptr(out), _ptr(lse_out),
+                        ctypes.c_void_p(handle))
+    if rc != OK:
+        raise SmlaError(rc, "smla_merge")
+    return out, lse_out
+
+
+def merge(parts, lses, lens=None, stream=None, with_lse=True):
+    """Allocates the outputs on parts' device and calls :func:`smla_merge`."""
+    S, T, H, _ = parts.shape
+    out = torch.empty((T, H, LATENT), dtype=torch.bfloat16, device=parts.device)
+    lse_out = torch.empty((T, H), dtype=torch.float32, device=parts.device) if with_lse else None
+    return smla_merge(parts, lses, lens, out, lse_out, stream=stream)

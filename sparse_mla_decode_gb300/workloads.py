@@ -251,3 +251,25 @@ def unique_active_rows(w: dict) -> int:
             rows.append(r)
         seen.append(np.unique(np.concatenate(rows)).size if rows else 0)
     return int(sum(seen))
+
+
+def merge_sets(seed: int = 1005, sources: int = 8, tokens: int = 64, heads: int = 128, device=None):
+    """Partial (out, lse) sets of one decode step split over ``sources`` key
+    shards (a DCP8 step of the 64 x 128 batch by default): BF16 rows N(0, 1),
+    base-2 LSEs U(4, 12), 3 % of the (source, token, head) entries empty
+    (LSE -inf), token 5 with count 0. Torch tensors on ``device`` (a seeded
+    torch generator there): parts bfloat16 [S, T, H, 512], lses float32
+    [S, T, H], lens int32 [T]."""
+    import torch
+
+    device = torch.device(device or "cpu")
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    parts = torch.randn((sources, tokens, heads, 512), generator=gen, device=device).to(torch.bfloat16)
+    lses = torch.rand((sources, tokens, heads), generator=gen, device=device) * 8.0 + 4.0
+    empty = torch.rand((sources, tokens, heads), generator=gen, device=device) < 0.03
+    lses = torch.where(empty, torch.full_like(lses, float("-inf")), lses)
+    lens = torch.full((tokens,), 2048, dtype=torch.int32, device=device)
+    if tokens > 5:
+        lens[5] = 0
+    return parts, lses, lens

@@ -134,3 +134,33 @@ def test_decode_rejects_bad_arguments_without_launching(lib):
     assert lib.smla_decode(ctypes.byref(smla.make_shape(0, 16, 8, 576)), None, None, None, None, None,
                            1.0, 1.0, 1.0, None, None, None) == smla.OK  # nothing to do
     assert lib.smla_error_string(smla.EINVAL).startswith(b"invalid")
+
+
+def _merge_shape(**kw):
+    s = smla.SmlaMergeShape()
+    base = dict(sources=2, tokens=3, heads=16, reserved=0, part_stride_source=3 * 16 * 512,
+                part_stride_token=16 * 512, part_stride_head=512, lse_stride_source=48, lse_stride_token=16,
+                out_stride_token=16 * 512, out_stride_head=512, lse_out_stride_token=16)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(s, k, v)
+    return s
+
+
+@pytest.mark.parametrize("kw,ptrs", [
+    (dict(sources=-1), (16, 16, 16)),
+    (dict(part_stride_head=500), (16, 16, 16)),       # rows not 16-byte aligned
+    (dict(out_stride_token=12), (16, 16, 16)),
+    (dict(out_stride_head=256), (16, 16, 16)),        # heads overlap
+    (dict(), (0, 16, 16)),                            # no parts
+    (dict(), (16, 16, 0)),                            # no out
+    (dict(), (8, 16, 16)),                            # parts misaligned
+])
+def test_merge_rejects_bad_arguments_before_any_launch(lib, kw, ptrs):
+    parts, lses, out = (ctypes.c_void_p(p) if p else None for p in ptrs)
+    rc = lib.smla_merge(ctypes.byref(_merge_shape(**kw)), parts, lses, None, out, None, None)
+    assert rc == smla.EINVAL
+
+
+def test_merge_of_nothing_is_ok_without_a_device(lib):
+    assert lib.smla_merge(ctypes.byref(_merge_shape(tokens=0)), None, None, None, None, None, None) == smla.OK
