@@ -17,7 +17,8 @@ One JSON line on rank 0:
   roofline    achieved GB/s of the decode kernel vs the measured HBM copy peak
   e2e         the same metric with host buffers: per step the H2D copy of q,
               indices and lens from pinned memory, the call, and the D2H copy
-              of out and lse, all inside the timed region
+              of out and lse, all inside the timed region (consecutive steps
+              pipelined over three streams)
   cpu_baseline the CPU oracle (fp64 definition) on a bounded sample, all cores
 With --impl reference the same line is produced by the CPU oracle alone.
 Under torchrun (--gpus N > 1) every rank runs an independent replica on its
@@ -257,6 +258,79 @@ def cpu_oracle_rate(sets, seconds: float):
 # --------------------------------------------------------------- our arm
 
 
+def pipelined_e2e(torch, host_inputs, dev_like, run, out_like, steps, warmup=3, graph=True):
+    """End to end through the library call with host buffers: every step copies
+    its inputs from pinned host memory to the device, runs the call, and reads
+    its outputs back to pinned host memory. Steps are pipelined over three
+    streams and three device slots (the H2D copy of step i + 1 and the D2H copy
+    of step i - 1 overlap the call of step i); events order every reuse of a
+    slot. With ``graph`` the timed steps (copies included) are captured once in
+    a CUDA graph and replayed, so that host launch cost does not bound small
+    steps. Returns the mean time per step in ms (CUDA events).
+
+    host_inputs: list (cycled over steps) of tuples of pinned host tensors;
+    dev_like: one such tuple on the device (shapes and dtypes of a slot);
+    run(inputs, outputs): launches the call on the current stream;
+    out_like: tuple of device tensors shaped like the outputs."""
+    slots = 3
+    d_in = [tuple(torch.empty_like(x) for x in dev_like) for _ in range(slots)]
+    d_out = [tuple(torch.empty_like(x) for x in out_like) for _ in range(slots)]
+    h_out = [tuple(torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in out_like) for _ in range(slots)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event() for _ in range(slots)]  # noqa: E731
+    e_in, e_comp, e_out = ev(), ev(), ev()
+
+    def issue(first, n):
+        comp = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(comp)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        for i in range(first, first + n):
+            b = i % slots
+            src = host_inputs[i % len(host_inputs)]
+            with torch.cuda.stream(s_in):
+                if i - first >= slots:
+                    s_in.wait_event(e_comp[b])  # the call of step i - 3 has read this slot
+                for d, h in zip(d_in[b], src):
+                    d.copy_(h, non_blocking=True)
+                e_in[b].record(s_in)
+            comp.wait_event(e_in[b])
+            if i - first >= slots:
+                comp.wait_event(e_out[b])  # step i - 3's outputs have left this slot
+            run(d_in[b], d_out[b])
+            e_comp[b].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e_comp[b])
+                for h, d in zip(h_out[b], d_out[b]):
+                    h.copy_(d, non_blocking=True)
+                e_out[b].record(s_out)
+        for s_ in (s_in, s_out):  # join
+            e = torch.cuda.Event()
+            e.record(s_)
+            comp.wait_event(e)
+
+    issue(0, warmup)
+    torch.cuda.synchronize()
+    comp = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            issue(warmup, steps)
+        g.replay()
+        torch.cuda.synchronize()
+        t0.record(comp)
+        g.replay()
+        t1.record(comp)
+    else:
+        t0.record(comp)
+        issue(warmup, steps)
+        t1.record(comp)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -418,42 +492,28 @@ def run_ours(args, rank, world, local_rank):
     # end to end through the public API, host buffers in pinned memory
     e2e = None
     if not args.no_e2e:
-        hq = [d["q"].cpu().pin_memory() for d in dsets]
-        hi = [d["indices"].cpu().pin_memory() for d in dsets]
-        hl = [d["lens"].cpu().pin_memory() for d in dsets]
-        ho = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
-        hlse = torch.empty((T, H), dtype=torch.float32).pin_memory()
-        h2d = hq[0].numel() + hi[0].numel() * 4 + hl[0].numel() * 4
-        d2h = ho.numel() * 2 + hlse.numel() * 4
+        # q, indices and lens of each input set, resident on the host
+        host = [(d["q"].cpu().pin_memory(), d["indices"].cpu().pin_memory(), d["lens"].cpu().pin_memory())
+                for d in dsets[:64]]
+        h2d = sum(x.numel() * x.element_size() for x in host[0])
+        d2h = T * H * 512 * 2 + T * H * 4
+        w0 = sets[0]
 
-        def e2e_step(i):
-            k = i % len(sets)
-            d = dsets[k]
-            d["q"].copy_(hq[k], non_blocking=True)
-            d["indices"].copy_(hi[k], non_blocking=True)
-            d["lens"].copy_(hl[k], non_blocking=True)
-            call(k)
-            ho.copy_(d["out"], non_blocking=True)
-            hlse.copy_(d["lse"], non_blocking=True)
+        def e2e_run(inp, outp):
+            q, idx, lens = inp
+            smla.smla_decode(q, dsets[0]["pools"], idx, lens, dsets[0]["sinks"], w0["bmm1_scale"],
+                             w0["bmm2_scale"], w0["k_scale"], outp[0], outp[1], pool_split=w0.get("pool_split", 0))
 
-        for i in range(3):
-            e2e_step(i)
-        barrier()
         steps = min(args.steps, 500)
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for i in range(steps):
-            e2e_step(i)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = s0.elapsed_time(s1) / steps
+        e_ms = pipelined_e2e(torch, host, (dsets[0]["q"], dsets[0]["indices"], dsets[0]["lens"]), e2e_run,
+                             (dsets[0]["out"], dsets[0]["lse"]), steps)
         if dist is not None:
             t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h)}
+               "d2h_bytes_per_step": int(d2h), "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
 
     if rank != 0:
         return
@@ -652,34 +712,17 @@ def run_merge(args, rank, world, local_rank):
 
     e2e = None
     if not args.no_e2e:
-        hp = [sets[k][0].cpu().pin_memory() for k in range(R)]
-        hl = [sets[k][1].cpu().pin_memory() for k in range(R)]
-        ho = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
-        hlse = torch.empty((T, H), dtype=torch.float32).pin_memory()
+        host = [(sets[k][0].cpu().pin_memory(), sets[k][1].cpu().pin_memory()) for k in range(R)]
+        h2d = sum(x.numel() * x.element_size() for x in host[0])
 
-        def e2e_step(i):
-            k = i % R
-            sets[k][0].copy_(hp[k], non_blocking=True)
-            sets[k][1].copy_(hl[k], non_blocking=True)
-            call(k)
-            ho.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+        def e2e_run(inp, outp):
+            smla.smla_merge(inp[0], inp[1], sets[0][2], outp[0], outp[1])
 
-        for i in range(3):
-            e2e_step(i)
-        barrier()
-        steps = min(args.steps, 200)
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for i in range(steps):
-            e2e_step(i)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = s0.elapsed_time(s1) / steps
-        h2d = hp[0].numel() * 2 + hl[0].numel() * 4
+        e_ms = pipelined_e2e(torch, host, (sets[0][0], sets[0][1]), e2e_run, (out, lse), min(args.steps, 200))
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(ho.numel() * 2 + hlse.numel() * 4)}
+               "d2h_bytes_per_step": int(T * H * (512 * 2 + 4)),
+               "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
     if rank != 0:
         return
     cpu = None
