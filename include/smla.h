@@ -127,7 +127,8 @@ int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* plan);
  *   lse       device, float [T, H] base-2 log-sum-exp, or NULL.
  *   stream    a cudaStream_t (NULL: the legacy default stream).
  * Launched with programmatic dependent launch: the kernel reads its inputs only
- * after the previous kernel in the stream has completed.
+ * after the previous kernel in the stream has completed (SMLA_PDL=0 in the
+ * environment launches without it, for measurement).
  * Captureable in a CUDA graph (no allocation, no synchronisation).
  * Errors: SMLA_EINVAL / SMLA_EUNSUPPORTED before anything is launched,
  * SMLA_ECUDA when the launch fails. Device-side conditions (an index beyond its

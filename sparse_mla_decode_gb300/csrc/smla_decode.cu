@@ -891,6 +891,17 @@ bool merge_fits(int n, int d, int splits) {
     return splits * slots * n * 32 * 4 + splits * 3 * n * 4 <= limit;
 }
 
+// Programmatic dependent launch (the kernel's set-up overlaps the previous
+// kernel in the stream) unless the environment variable SMLA_PDL is "0", for
+// measuring what it gains.
+bool dependent_launch() {
+    static const bool on = [] {
+        const char* env = std::getenv("SMLA_PDL");
+        return !(env != nullptr && env[0] == '0');
+    }();
+    return on;
+}
+
 // Opts the kernel into its shared-memory size and non-portable clusters, once
 // per device.
 template <int N, int D>
@@ -978,7 +989,7 @@ cudaError_t launch(const Params& p, dim3 grid, int cluster, cudaStream_t stream)
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
     attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].val.programmaticStreamSerializationAllowed = dependent_launch() ? 1 : 0;
     cfg.attrs = attrs;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, p);
