@@ -9,6 +9,8 @@ through :func:`build`) and exposes the two oracle modes over numpy arrays:
 * :func:`emulate` -- the Kimi K3.1 ``attn_sparse`` datapath (module docstring,
   the per-chunk softmax with E4M3 P at 448 of the running max, and
   ``SparseDcpDecode.merge``) replayed on a given (splits, chunk) partition.
+* :func:`mxfp4_q_quant` -- the MXFP4 quantisation of the indexer query (Kimi
+  K3.1 ``dsa_indexer_mxfp4`` page: UE8M0 scale per 32 values, E2M1 codes).
 * :func:`merge` / :func:`merge_f64` -- the LSE merge of partial (out, lse) sets
   of the Kimi K3.1 ``mla/dcp`` page (``DcpValue``: weights exp2(lse - max) /
   sum, an FP32 weighted sum of the BF16 rows, one BF16 rounding).
@@ -111,6 +113,11 @@ def _load():
             lib.smla_oracle_emulate_pairs.argtypes = [P, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
             lib.smla_oracle_max_threads.restype = i32
             lib.smla_oracle_merge_f64.argtypes = [i32, vp, vp, vp, vp]
+            lib.smla_oracle_e2m1_from_float.argtypes = [ctypes.c_float]
+            lib.smla_oracle_e2m1_from_float.restype = ctypes.c_uint8
+            lib.smla_oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+            lib.smla_oracle_e2m1_to_double.restype = ctypes.c_double
+            lib.smla_oracle_mxfp4_q_quant.argtypes = [i32, i32, vp, vp, ctypes.c_float, vp, vp, vp]
             lib.smla_oracle_merge_pairs.argtypes = [ctypes.POINTER(_MergeProblem), vp, vp, i32, vp, vp, vp, i32]
             del i64
             _lib = lib
@@ -269,3 +276,30 @@ def merge(problem: MergeProblem, pairs=None, threads: int = 0):
     if rc != 0:
         raise MemoryError("oracle merge")
     return value, bits, lse
+
+
+def e2m1_from_float(value: float) -> int:
+    return int(_load().smla_oracle_e2m1_from_float(float(value)))
+
+
+def e2m1_to_double(code: int) -> float:
+    return float(_load().smla_oracle_e2m1_to_double(int(code)))
+
+
+def mxfp4_q_quant(q, weights, weight_scale: float, padded_heads: int):
+    """MXFP4 of the indexer query ``q`` float32 [T, H, 128] (values as FP32)
+    and the scaled ``weights`` float32 [T, H]. Returns (packed uint8 [T, P, 64],
+    scale int32 [T, P], weights float32 [T, P])."""
+    lib = _load()
+    q = _c(q, np.float32)
+    weights = _c(weights, np.float32)
+    T, H, D = q.shape
+    assert D == 128 and weights.shape == (T, H) and padded_heads >= H
+    P = int(padded_heads)
+    packed = np.zeros((T, P, 64), np.uint8)
+    scale = np.zeros((T, P), np.int32)
+    w_out = np.zeros((T, P), np.float32)
+    for t in range(T):
+        lib.smla_oracle_mxfp4_q_quant(H, P, q[t].ctypes.data, weights[t].ctypes.data, float(weight_scale),
+                                      packed[t].ctypes.data, scale[t].ctypes.data, w_out[t].ctypes.data)
+    return packed, scale, w_out

@@ -408,6 +408,87 @@ int smla_oracle_merge_pairs(const smla_oracle_merge_problem* m, const int32_t* t
     return bad ? -1 : 0;
 }
 
+/* ------------------------------------------ MXFP4 quantisation of the query */
+/*
+ * [MXFP4] vllm.models.kimi_k3.nvidia.ops.dsa_indexer_mxfp4 -- mxfp4_q_quant,
+ *         _mxfp4_q_quant_kernel and _mxfp4_quant: each head's 128 query
+ *         values (taken as FP32) form 4 blocks of 32; a block's UE8M0 scale is
+ *         2^e with e = ceil(log2(max(amax, 6 * 2^-126) / 6)) clamped to
+ *         [-127, 127] and stored as e + 127; the values divided by 2^e are
+ *         rounded to FP4 E2M1 and packed two per byte, the even element in
+ *         the low nibble; a head's four scale bytes form one int32 (block b
+ *         in byte b); the head weights are multiplied by weight_scale in FP32;
+ *         heads [H, P) of the padded outputs are zero.
+ * Readings: the ceiling of log2 is taken exactly on the FP32 quotient (a power
+ * of two gives its own exponent, anything above it the next one); E2M1 is the
+ * OCP MX element format (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), rounded to
+ * nearest with ties to the even code, saturating at 6, keeping the sign of
+ * zero.
+ */
+
+/* FP32 -> E2M1 code (sign in bit 3), round to nearest even, saturating. */
+uint8_t smla_oracle_e2m1_from_float(float value) {
+    static const float grid[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    uint8_t sign = signbit(value) ? 8u : 0u;
+    float a = fabsf(value);
+    if (a >= 6.0f) return (uint8_t)(sign | 7u);
+    int best = 0;
+    for (int c = 1; c < 8; ++c) {
+        float d_best = fabsf(a - grid[best]), d = fabsf(a - grid[c]);
+        if (d < d_best || (d == d_best && (c & 1) == 0)) best = c;
+    }
+    return (uint8_t)(sign | (uint8_t)best);
+}
+
+double smla_oracle_e2m1_to_double(uint8_t code) {
+    static const double grid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    double v = grid[code & 7u];
+    return (code & 8u) ? -v : v;
+}
+
+/* e = ceil(log2(q)) for a positive finite float q, exactly. */
+static int ceil_log2_exact(float q) {
+    int e;
+    double m = frexp((double)q, &e); /* q = m * 2^e, m in [0.5, 1) */
+    return m == 0.5 ? e - 1 : e;
+}
+
+/* One token: q [heads][128] FP32 values, weights [heads]; outputs for the
+ * padded heads: packed [padded][64] bytes, scale [padded] int32, w_out [padded]. */
+int smla_oracle_mxfp4_q_quant(int heads, int padded, const float* q, const float* weights, float weight_scale,
+                              uint8_t* packed, int32_t* scale, float* w_out) {
+    const int D = 128, B = 32;
+    for (int h = 0; h < padded; ++h) {
+        if (h >= heads) {
+            memset(packed + (size_t)h * (D / 2), 0, D / 2);
+            scale[h] = 0;
+            w_out[h] = 0.0f;
+            continue;
+        }
+        const float* x = q + (size_t)h * D;
+        uint32_t bytes = 0;
+        for (int b = 0; b < D / B; ++b) {
+            float amax = 0.0f;
+            for (int i = 0; i < B; ++i) amax = fmaxf(amax, fabsf(x[b * B + i]));
+            float floor_amax = 6.0f * ldexpf(1.0f, -126);
+            float quotient = fmaxf(amax, floor_amax) / 6.0f;
+            int e = ceil_log2_exact(quotient);
+            if (e < -127) e = -127;
+            if (e > 127) e = 127;
+            bytes |= (uint32_t)(uint8_t)(e + 127) << (8 * b);
+            for (int i = 0; i < B; i += 2) {
+                float lo = (float)ldexp((double)x[b * B + i], -e);     /* exact: a power-of-two scaling */
+                float hi = (float)ldexp((double)x[b * B + i + 1], -e);
+                packed[(size_t)h * (D / 2) + (b * B + i) / 2] =
+                    (uint8_t)(smla_oracle_e2m1_from_float(lo) | (smla_oracle_e2m1_from_float(hi) << 4));
+            }
+        }
+        memcpy(&scale[h], &bytes, 4);
+        w_out[h] = weights[h] * weight_scale;
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------ batch drivers */
 
 /* FP64 definition over every (token, head); OpenMP over the pairs. */

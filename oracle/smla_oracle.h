@@ -83,6 +83,12 @@ int smla_oracle_merge_pairs(const smla_oracle_merge_problem* m, const int32_t* t
                             const int32_t* heads, int n, double* out_value, uint16_t* out_bf16,
                             double* lse2, int threads);
 
+/* MXFP4 quantisation of the indexer query (one token, head_dim 128). */
+uint8_t smla_oracle_e2m1_from_float(float value);
+double smla_oracle_e2m1_to_double(uint8_t code);
+int smla_oracle_mxfp4_q_quant(int heads, int padded, const float* q, const float* weights, float weight_scale,
+                              uint8_t* packed, int32_t* scale, float* w_out);
+
 #ifdef __cplusplus
 }
 #endif

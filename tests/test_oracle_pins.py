@@ -407,3 +407,87 @@ def test_merge_empty_rows_are_zero_and_minus_inf():
     for i in (1, 2):  # all sources empty; token count 0
         assert np.all(bits[i] == 0) and np.all(value[i] == 0.0) and lse[i] == -np.inf
     assert np.isfinite(lse[0])
+
+
+# -------------------------------- MXFP4 quantisation of the indexer query
+# (Kimi K3.1 dsa_indexer_mxfp4 page: UE8M0 scale 2^ceil(log2(amax / 6)) per 32
+# values, E2M1 codes with the even element in the low nibble.)
+
+E2M1_GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_grid_round_trips_and_ties_go_to_even_codes():
+    for code in range(16):
+        v = oracle.e2m1_to_double(code)
+        assert abs(v) == E2M1_GRID[code & 7] and (v < 0) == (code >= 8 and code != 8)
+        if code != 8:  # -0 decodes to 0 and re-encodes to +0 (0.0 has no sign)
+            assert oracle.e2m1_from_float(v) == code
+    # midpoints between neighbours: the code with mantissa bit 0 wins
+    for lo in range(7):
+        mid = (E2M1_GRID[lo] + E2M1_GRID[lo + 1]) / 2
+        even = lo if lo % 2 == 0 else lo + 1
+        assert oracle.e2m1_from_float(mid) == even
+        assert oracle.e2m1_from_float(-mid) == 8 | even
+    assert oracle.e2m1_from_float(6.5) == 7 and oracle.e2m1_from_float(1e30) == 7  # saturating
+    assert oracle.e2m1_from_float(-1e-6) == 8  # the sign of a zero result is kept
+
+
+def test_e2m1_rounds_to_the_nearest_grid_value():
+    rng = np.random.default_rng(6)
+    grid = np.array(E2M1_GRID)
+    for x in rng.uniform(-7, 7, 3000).astype(np.float32):
+        v = oracle.e2m1_to_double(oracle.e2m1_from_float(float(x)))
+        a = min(abs(float(x)), 6.0)
+        assert abs(abs(v) - a) <= np.min(np.abs(grid - a)) + 1e-12
+
+
+def _mxfp4_inputs(seed, T=3, H=5):
+    rng = np.random.default_rng(seed)
+    q = (rng.standard_normal((T, H, 128)) * rng.uniform(1e-3, 1e3, (T, H, 1))).astype(np.float32)
+    q[0, 0, 32:64] = 0.0  # an all-zero block
+    q[0, 1, 0:32] = 6.0 * 2.0 ** -3  # amax exactly 6 * 2^-3
+    q[0, 1, 32:64] = np.float32(6.0 * 2.0 ** -3) * np.float32(1 + 2 ** -20)  # just above
+    w = rng.standard_normal((T, H)).astype(np.float32)
+    return q, w
+
+
+def test_mxfp4_scale_is_the_smallest_power_of_two_covering_the_block():
+    q, w = _mxfp4_inputs(7)
+    packed, scale, _ = oracle.mxfp4_q_quant(q, w, 0.5, 8)
+    T, H, _ = q.shape
+    for t in range(T):
+        for h in range(H):
+            for b in range(4):
+                e = int((int(scale[t, h]) >> (8 * b)) & 0xFF) - 127
+                amax = float(np.abs(q[t, h, 32 * b:32 * b + 32]).max())
+                if amax <= 6.0 * 2.0 ** -126:
+                    assert e == -126
+                else:
+                    assert amax <= 6.0 * 2.0 ** e and amax > 6.0 * 2.0 ** (e - 1)
+    assert (int(scale[0, 1]) & 0xFF) - 127 == -3 and ((int(scale[0, 1]) >> 8) & 0xFF) - 127 == -2
+
+
+def test_mxfp4_dequantised_values_are_within_half_a_grid_step():
+    q, w = _mxfp4_inputs(8)
+    packed, scale, _ = oracle.mxfp4_q_quant(q, w, 1.0, 5)
+    grid = np.array(E2M1_GRID)
+    T, H, _ = q.shape
+    for t in range(T):
+        for h in range(H):
+            for i in range(128):
+                byte = int(packed[t, h, i // 2])
+                code = byte & 0xF if i % 2 == 0 else byte >> 4  # even element in the low nibble
+                e = int((int(scale[t, h]) >> (8 * (i // 32))) & 0xFF) - 127
+                y = float(q[t, h, i]) / 2.0 ** e
+                back = oracle.e2m1_to_double(code)
+                gap = np.min(np.abs(grid - min(abs(y), 6.0)))
+                assert abs(abs(back) - min(abs(y), 6.0)) <= gap + 1e-12
+                assert back == 0.0 or np.sign(back) == np.sign(y)
+
+
+def test_mxfp4_zero_blocks_weights_and_padding():
+    q, w = _mxfp4_inputs(9, T=2, H=3)
+    packed, scale, w_out = oracle.mxfp4_q_quant(q, w, 0.125, 8)
+    assert ((int(scale[0, 0]) >> 8) & 0xFF) == 1 and np.all(packed[0, 0, 16:32] == 0)  # zero block: 2^-126
+    np.testing.assert_array_equal(w_out[:, :3], w * np.float32(0.125))
+    assert np.all(packed[:, 3:] == 0) and np.all(scale[:, 3:] == 0) and np.all(w_out[:, 3:] == 0)
