@@ -2,7 +2,7 @@
 """Benchmark: sparse MLA decode on GB300 (µs per call, achieved HBM GB/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config batch|tiny|verify|two_pool|merge]
+                    [--config batch|tiny|verify|two_pool|merge|mxfp4]
 
 A step is one smla_decode call over one batch of seeded synthetic inputs. The
 default workload is the bandwidth-bound batch: 64 tokens x 128 heads x 2048
@@ -55,8 +55,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge"], default="batch",
-                    help="merge: the LSE merge of 8 partial (out, lse) sets of the 64 x 128 batch shape")
+    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge", "mxfp4"], default="batch",
+                    help="merge: the LSE merge of 8 partial (out, lse) sets of the 64 x 128 batch shape; "
+                         "mxfp4: the MXFP4 indexer-query quantisation of 16384 tokens x 32 heads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
@@ -775,6 +776,149 @@ def merge_cpu_rate(first_set, seconds: float):
             "us_per_call": round(per_call * 1e6, 1)}
 
 
+MXFP4_METRIC = "µs/call and achieved HBM GB/s for the MXFP4 indexer-query quantisation"
+
+
+def mxfp4_bytes(T, H) -> int:
+    """BF16 query and FP32 weights read; packed codes, scales and weights written."""
+    return T * H * (128 * 2 + 4) + T * H * (64 + 4 + 4)
+
+
+def run_mxfp4(args, rank, world, local_rank):
+    """--config mxfp4: smla_mxfp4_q_quant of a BF16 query [16384, 32, 128]."""
+    import torch
+
+    import __graft_entry__
+    from sparse_mla_decode_gb300 import smla
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T, H = 16384, 32
+    per_call = mxfp4_bytes(T, H)
+    R = max(2, int(math.ceil(2.5 * L2_BYTES / per_call)))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242 + rank)
+    sets = [(torch.randn((T, H, 128), generator=gen, device=dev).to(torch.bfloat16),
+             torch.randn((T, H), generator=gen, device=dev)) for _ in range(R)]
+    outs = [(torch.empty((T, H, 64), dtype=torch.uint8, device=dev), torch.empty((T, H), dtype=torch.int32, device=dev),
+             torch.empty((T, H), dtype=torch.float32, device=dev)) for _ in range(R)]
+
+    def call(i):
+        q, w = sets[i % R]
+        smla.smla_mxfp4_q_quant(q, w, 0.0625, *outs[i % R])
+
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(max(3, args.warmup)):
+        call(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(args.steps):
+            call(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    while time.time() < t_wall0 + args.soak:
+        graph.replay()
+        torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, max(t_wall1, t_wall0 + args.soak))
+    ms = start.elapsed_time(end) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    achieved = per_call / (ms * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        host = [(sets[k][0].cpu().pin_memory(), sets[k][1].cpu().pin_memory()) for k in range(R)]
+
+        def e2e_run(inp, outp):
+            smla.smla_mxfp4_q_quant(inp[0], inp[1], 0.0625, *outp)
+
+        e_ms = pipelined_e2e(torch, host, sets[0], e2e_run, outs[0], min(args.steps, 100))
+        e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(T * H * (256 + 4)),
+               "d2h_bytes_per_step": int(T * H * 72),
+               "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu:
+        cpu = mxfp4_cpu_rate(sets[0], args.cpu_seconds)
+    peak, peak_src = measured_hbm_peak()
+    line = {
+        "metric": MXFP4_METRIC, "value": round(per_call * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "us_per_call": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16->e2m1", "data": "synthetic",
+        "config": {"workload": f"mxfp4_q_t{T}_h{H}_d128: BF16 query N(0, 1), FP32 weights",
+                   "tokens": T, "heads": H, "head_dim": 128, "input_sets": R,
+                   "l2": "rotating %d input sets (%.1f MB per call)" % (R, per_call / 1e6),
+                   "launch": "one CUDA graph of the %d timed library calls, replayed once" % args.steps,
+                   "pages_context": "the pages' Triton kernel: ~35 us at 16K tokens x 32 heads on GB300"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "bytes_alg_per_launch": int(per_call)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def mxfp4_cpu_rate(first_set, seconds: float):
+    """The oracle's quantisation on the host (one thread per call) over a
+    bounded sample of tokens."""
+    from oracle import oracle
+
+    oracle.build()
+    q, w = (x.cpu() for x in first_set)
+    T, H, _ = q.shape
+    qf = q.float().numpy()
+    wf = w.numpy()
+    rng = np.random.default_rng(3)
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds and done < T:
+        rows = rng.integers(0, T, 64)
+        oracle.mxfp4_q_quant(qf[rows], wf[rows], 0.0625, H)
+        done += 64
+    per_call = (time.perf_counter() - t0) / done * T
+    return {"value": round(mxfp4_bytes(T, H) / per_call / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {T} tokens in batches of 64", "us_per_call": round(per_call * 1e6, 1)}
+
+
+def run_mxfp4_reference(args, rank, world):
+    if rank != 0:
+        return
+    import torch
+
+    T, H = 16384, 32
+    gen = torch.Generator()
+    gen.manual_seed(4242)
+    first = (torch.randn((T, H, 128), generator=gen).to(torch.bfloat16), torch.randn((T, H), generator=gen))
+    total = max(1, args.steps + args.warmup)
+    cpu = mxfp4_cpu_rate(first, min(60.0, 2.0 * total) / total * args.steps)
+    line = {
+        "metric": MXFP4_METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(cpu["us_per_call"] / 1e3, 3), "us_per_call": cpu["us_per_call"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "impl": "reference", "config": {"workload": f"mxfp4_q_t{T}_h{H}_d128", "tokens": T, "heads": H},
+        "cpu_baseline": cpu,
+        "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def torch_int16():
     import torch
 
@@ -810,6 +954,8 @@ def main():
     if args.impl == "reference":
         if args.config == "merge":
             run_merge_reference(args, rank, world)
+        elif args.config == "mxfp4":
+            run_mxfp4_reference(args, rank, world)
         else:
             run_reference(args, rank, world)
         return
@@ -822,6 +968,8 @@ def main():
     try:
         if args.config == "merge":
             run_merge(args, rank, world, local_rank)
+        elif args.config == "mxfp4":
+            run_mxfp4(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

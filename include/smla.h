@@ -181,6 +181,48 @@ typedef struct smla_merge_shape {
 int smla_merge(const smla_merge_shape* shape, const void* parts, const float* lses,
                const int32_t* lens, void* out, float* lse_out, void* stream);
 
+/* -------------------------------------------- MXFP4 indexer query quantisation
+ * The step before the decode: the indexer's query in the MXFP4 format of its
+ * key cache, after the Kimi K3.1 `dsa_indexer_mxfp4` page (mxfp4_q_quant and
+ * _mxfp4_quant). For token t and head h < H, the 128 values q[t, h, :] (taken
+ * as FP32) form 4 blocks of 32; block b's scale is 2^e, e = ceil(log2(max(amax,
+ * 6 * 2^-126) / 6)) clamped to [-127, 127], stored as the byte e + 127 in byte b
+ * of q_scale[t, h]; q_packed[t, h, j] = E2M1(q[t, h, 2j] / 2^e) | E2M1(q[t, h,
+ * 2j + 1] / 2^e) << 4 with E2M1 rounding to nearest (ties to the even code,
+ * saturating at 6, keeping the sign of zero); w_out[t, h] = weights[t, h] *
+ * weight_scale (FP32). Heads H <= h < padded_heads get zeros in all three. */
+#define SMLA_DTYPE_BF16 1
+#define SMLA_DTYPE_F32 2
+
+typedef struct smla_mxfp4_shape {
+    int32_t tokens;       /* T */
+    int32_t heads;        /* H */
+    int32_t padded_heads; /* P >= H */
+    int32_t head_dim;     /* 128 */
+    int32_t q_dtype;      /* SMLA_DTYPE_BF16 or SMLA_DTYPE_F32 */
+    int32_t reserved;     /* 0 */
+    int64_t q_stride_token, q_stride_head; /* q elements (multiples of 8); values contiguous */
+    int64_t w_stride_token;                /* float elements of `weights`; heads contiguous */
+    int64_t packed_stride_token;           /* bytes of q_packed (multiple of 4); heads contiguous, 64 bytes each */
+    int64_t scale_stride_token;            /* int32 elements of q_scale; heads contiguous */
+    int64_t w_out_stride_token;            /* float elements of w_out; heads contiguous */
+} smla_mxfp4_shape;
+
+/* Quantises the indexer query.
+ *   q          device, [T, H, 128] of q_dtype, 16-byte aligned.
+ *   weights    device, float [T, H].
+ *   q_packed   device, uint8 [T, P, 64], 4-byte aligned.
+ *   q_scale    device, int32 [T, P].
+ *   w_out      device, float [T, P].
+ * Every buffer belongs to the caller; nothing is allocated. Launched with
+ * programmatic dependent launch; captureable in a CUDA graph.
+ * Errors: SMLA_EINVAL (null buffers, negative sizes or strides, misalignment),
+ * SMLA_EUNSUPPORTED (head_dim != 128, unknown dtype, tokens * padded_heads >=
+ * 2^31 - 64) before any launch;
+ * SMLA_ECUDA when the launch fails. */
+int smla_mxfp4_q_quant(const smla_mxfp4_shape* shape, const void* q, const float* weights, float weight_scale,
+                       void* q_packed, int32_t* q_scale, float* w_out, void* stream);
+
 /* Reads and clears the current device's error word (SMLA_DEV_* bits) after
  * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
 int smla_device_error(int32_t* bits);

@@ -11,9 +11,11 @@ from .smla import (  # noqa: F401
     load,
     make_shape,
     merge,
+    mxfp4_q_quant,
     smla_decode,
     smla_device_error,
     smla_merge,
+    smla_mxfp4_q_quant,
     smla_plan_for,
     smla_version,
 )

@@ -57,6 +57,20 @@ class SmlaMergeShape(ctypes.Structure):
     ]
 
 
+class SmlaMxfp4Shape(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("padded_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("q_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("q_stride_token", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
+        ("w_stride_token", ctypes.c_int64), ("packed_stride_token", ctypes.c_int64),
+        ("scale_stride_token", ctypes.c_int64), ("w_out_stride_token", ctypes.c_int64),
+    ]
+
+
+DTYPE_BF16 = 1
+DTYPE_F32 = 2
+
+
 class SmlaError(RuntimeError):
     def __init__(self, code: int, what: str):
         lib = _lib
@@ -96,6 +110,8 @@ def load(path: str | None = None):
         lib.smla_version.restype = i32
         lib.smla_merge.argtypes = [ctypes.POINTER(SmlaMergeShape), vp, vp, vp, vp, vp, vp]
         lib.smla_merge.restype = i32
+        lib.smla_mxfp4_q_quant.argtypes = [ctypes.POINTER(SmlaMxfp4Shape), vp, vp, ctypes.c_float, vp, vp, vp, vp]
+        lib.smla_mxfp4_q_quant.restype = i32
         _lib = lib
         return lib
 
@@ -227,3 +243,49 @@ def merge(parts, lses, lens=None, stream=None, with_lse=True):
     out = torch.empty((T, H, LATENT), dtype=torch.bfloat16, device=parts.device)
     lse_out = torch.empty((T, H), dtype=torch.float32, device=parts.device) if with_lse else None
     return smla_merge(parts, lses, lens, out, lse_out, stream=stream)
+
+
+def smla_mxfp4_q_quant(q: torch.Tensor, weights: torch.Tensor, weight_scale: float, q_packed: torch.Tensor,
+                       q_scale: torch.Tensor, w_out: torch.Tensor, stream=None):
+    """MXFP4 quantisation of the indexer query through the C ABI (see
+    ``smla_mxfp4_q_quant`` in smla.h). q: bfloat16 or float32 [T, H, 128],
+    values contiguous; weights float32 [T, H]; q_packed uint8 [T, P, 64];
+    q_scale int32 [T, P]; w_out float32 [T, P]."""
+    lib = load()
+    T, H, D = q.shape
+    P = q_packed.shape[1]
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("mxfp4: q must be bfloat16 or float32")
+    if tuple(weights.shape) != (T, H) or tuple(q_packed.shape) != (T, P, D // 2) or tuple(q_scale.shape) != (T, P) \
+            or tuple(w_out.shape) != (T, P):
+        raise ValueError("mxfp4: shapes")
+    if q.stride(2) != 1 or (H > 1 and weights.stride(1) != 1) or q_packed.stride(2) != 1 \
+            or (P > 1 and (q_packed.stride(1) != D // 2 or q_scale.stride(1) != 1 or w_out.stride(1) != 1)):
+        raise ValueError("mxfp4: inner dimensions must be contiguous")
+    shape = SmlaMxfp4Shape()
+    shape.tokens, shape.heads, shape.padded_heads, shape.head_dim = T, H, P, D
+    shape.q_dtype = DTYPE_F32 if q.dtype == torch.float32 else DTYPE_BF16
+    shape.reserved = 0
+    shape.q_stride_token, shape.q_stride_head = q.stride(0), q.stride(1)
+    shape.w_stride_token = weights.stride(0)
+    shape.packed_stride_token = q_packed.stride(0)
+    shape.scale_stride_token = q_scale.stride(0)
+    shape.w_out_stride_token = w_out.stride(0)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_packed.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib.smla_mxfp4_q_quant(ctypes.byref(shape), _ptr(q), _ptr(weights), float(weight_scale), _ptr(q_packed),
+                                _ptr(q_scale), _ptr(w_out), ctypes.c_void_p(handle))
+    if rc != OK:
+        raise SmlaError(rc, "smla_mxfp4_q_quant")
+    return q_packed, q_scale, w_out
+
+
+def mxfp4_q_quant(q, weights, weight_scale: float, padded_heads: int | None = None, stream=None):
+    """Allocates the outputs on q's device and calls :func:`smla_mxfp4_q_quant`."""
+    T, H, D = q.shape
+    P = H if padded_heads is None else int(padded_heads)
+    packed = torch.empty((T, P, D // 2), dtype=torch.uint8, device=q.device)
+    scale = torch.empty((T, P), dtype=torch.int32, device=q.device)
+    w_out = torch.empty((T, P), dtype=torch.float32, device=q.device)
+    return smla_mxfp4_q_quant(q, weights, weight_scale, packed, scale, w_out, stream=stream)
