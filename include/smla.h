@@ -203,7 +203,7 @@ typedef struct smla_mxfp4_shape {
     int32_t reserved;     /* 0 */
     int64_t q_stride_token, q_stride_head; /* q elements (multiples of 8); values contiguous */
     int64_t w_stride_token;                /* float elements of `weights`; heads contiguous */
-    int64_t packed_stride_token;           /* bytes of q_packed (multiple of 4); heads contiguous, 64 bytes each */
+    int64_t packed_stride_token;           /* bytes of q_packed (multiple of 8); heads contiguous, 64 bytes each */
     int64_t scale_stride_token;            /* int32 elements of q_scale; heads contiguous */
     int64_t w_out_stride_token;            /* float elements of w_out; heads contiguous */
 } smla_mxfp4_shape;
@@ -211,14 +211,14 @@ typedef struct smla_mxfp4_shape {
 /* Quantises the indexer query.
  *   q          device, [T, H, 128] of q_dtype, 16-byte aligned.
  *   weights    device, float [T, H].
- *   q_packed   device, uint8 [T, P, 64], 4-byte aligned.
+ *   q_packed   device, uint8 [T, P, 64], 8-byte aligned.
  *   q_scale    device, int32 [T, P].
  *   w_out      device, float [T, P].
  * Every buffer belongs to the caller; nothing is allocated. Launched with
  * programmatic dependent launch; captureable in a CUDA graph.
  * Errors: SMLA_EINVAL (null buffers, negative sizes or strides, misalignment),
- * SMLA_EUNSUPPORTED (head_dim != 128, unknown dtype, tokens * padded_heads >=
- * 2^31 - 64) before any launch;
+ * SMLA_EUNSUPPORTED (head_dim != 128, unknown dtype, tokens * padded_heads
+ * within 2^10 of 2^31) before any launch;
  * SMLA_ECUDA when the launch fails. */
 int smla_mxfp4_q_quant(const smla_mxfp4_shape* shape, const void* q, const float* weights, float weight_scale,
                        void* q_packed, int32_t* q_scale, float* w_out, void* stream);

@@ -11,12 +11,12 @@
 // weights are multiplied by weight_scale; heads [H, P) of the padded outputs
 // are zero. The ceiling of log2 is taken exactly on the FP32 quotient.
 //
-// One warp per 16 (BF16) or 8 (FP32) (token, padded head) rows, two per step:
-// a half-warp holds a head, each lane 8 consecutive values and a 4-lane group
-// one block (maxima by shuffles); all steps' loads (and head weights) are
-// issued first and kept as raw words, so that enough bytes are in flight to
-// stream from HBM; a head's 64 packed bytes leave as 16 coalesced 4-byte
-// stores.
+// One warp per 16 (BF16) or 8 (FP32) (token, padded head) rows over 4 steps:
+// a head is 8 lanes of 16 BF16 values (or 16 lanes of 8 FP32 values), a
+// 32-value block 2 (or 4) lanes, maxima and scale bytes by shuffles; all
+// steps' loads (and head weights) are issued first and kept as raw words, so
+// that enough bytes are in flight to stream from HBM; a head's 64 packed
+// bytes leave as coalesced 8- (or 4-) byte stores.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -76,48 +76,43 @@ __device__ __forceinline__ uint4 load_stream(const uint4* ptr) {
     return v;
 }
 
-// The 8 values of one lane as FP32, from the raw 16-byte (BF16) or 32-byte
-// (FP32) words.
+// The values one lane holds: 16 BF16 or 8 FP32 values, 32 raw bytes either
+// way, kept as words until they are used.
 template <bool kF32>
-struct Lane8 {
-    uint4 w[kF32 ? 2 : 1];
+struct LaneValues {
+    static constexpr int kCount = kF32 ? 8 : 16;
+    uint4 w[2];
     __device__ __forceinline__ void load(const void* base, int64_t at) {
-        if constexpr (kF32) {
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(base) + at);
-            w[0] = load_stream(src);
-            w[1] = load_stream(src + 1);
-        } else {
-            w[0] = load_stream(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + at));
-        }
+        const uint4* src = kF32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(base) + at)
+                                : reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + at);
+        w[0] = load_stream(src);
+        w[1] = load_stream(src + 1);
     }
-    __device__ __forceinline__ void zero() {
-        w[0] = make_uint4(0u, 0u, 0u, 0u);
-        if constexpr (kF32) w[1] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    // max |value| over the 8 values as FP32 bits (finite values: the bit
-    // patterns of |x| order like the values)
+    __device__ __forceinline__ void zero() { w[0] = w[1] = make_uint4(0u, 0u, 0u, 0u); }
+    // max |value| as FP32 bits (finite values: the bit patterns of |x| order
+    // like the values)
     __device__ __forceinline__ uint32_t abs_max_bits() const {
+        const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
         if constexpr (kF32) {
-            const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
             uint32_t m = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) m = max(m, u[i] & 0x7FFFFFFFu);
             return m;
         } else {  // per-halfword maxima of the BF16 patterns, then the larger half
-            const uint32_t m = __vmaxu2(__vmaxu2(w[0].x & 0x7FFF7FFFu, w[0].y & 0x7FFF7FFFu),
-                                        __vmaxu2(w[0].z & 0x7FFF7FFFu, w[0].w & 0x7FFF7FFFu));
+            uint32_t m = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = __vmaxu2(m, u[i] & 0x7FFF7FFFu);
             return max(m << 16, m & 0xFFFF0000u);
         }
     }
     __device__ __forceinline__ void values(float* x) const {
+        const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
         if constexpr (kF32) {
-            const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(u[i]);
         } else {
-            const uint32_t u[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {  // BF16 -> FP32: the upper half of the word
+            for (int e = 0; e < 8; ++e) {  // BF16 -> FP32: the upper half of the word
                 x[2 * e] = __uint_as_float(u[e] << 16);
                 x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
             }
@@ -125,29 +120,41 @@ struct Lane8 {
     }
 };
 
+// Rows (token, padded head) per CTA: kWarps warps x kSteps steps x the heads
+// a warp holds per step.
+template <bool kF32>
+constexpr int rows_per_cta() {
+    return kWarps * 4 * (32 / (128 / LaneValues<kF32>::kCount));
+}
+
 template <bool kF32>
 __global__ void __launch_bounds__(kThreads) mxfp4_q_quant_kernel(const __grid_constant__ Params p) {
-    constexpr int kSteps = kF32 ? 4 : 8;     // two heads per step
-    constexpr int kRowsPerWarp = 2 * kSteps;  // (token, head) rows per warp
+    using V = LaneValues<kF32>;
+    constexpr int kVals = V::kCount;                     // values per lane
+    constexpr int kLanesPerHead = kHeadDim / kVals;      // 8 (BF16) or 16 (FP32)
+    constexpr int kHeadsPerStep = 32 / kLanesPerHead;    // 4 or 2
+    constexpr int kLanesPerBlock = 32 / kVals;           // a 32-value block: 2 or 4 lanes
+    constexpr int kSteps = 4;
+    constexpr int kRowsPerWarp = kHeadsPerStep * kSteps;
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, sub = lane & 15;  // a half-warp holds one head: 8 values per lane
+    const int slot = lane / kLanesPerHead, sub = lane % kLanesPerHead;
     // rows = tokens * padded < 2^31 (checked on the host): 32-bit indices
     const uint32_t rows = static_cast<uint32_t>(p.tokens) * static_cast<uint32_t>(p.padded);
     const uint32_t first = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
     const uint32_t padded = static_cast<uint32_t>(p.padded);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // every step's loads first (kSteps x 16 or 32 bytes per lane in flight)
-    Lane8<kF32> x[kSteps];
-    float wt[kSteps];  // the head weight of each step (first lane of a half-warp)
+    // every step's loads first (kSteps x 32 bytes per lane in flight)
+    V x[kSteps];
+    float wt[kSteps];  // the head weight of each step (first lane of the head)
     int tok[kSteps], head[kSteps];
-    {  // (token, head) of step 0 by one division; later steps add 2 heads
-        const uint32_t row = first + half;
+    {  // (token, head) of step 0 by one division; later steps add kHeadsPerStep heads
+        const uint32_t row = first + slot;
         tok[0] = static_cast<int>(row / padded);
         head[0] = static_cast<int>(row - static_cast<uint32_t>(tok[0]) * padded);
 #pragma unroll
         for (int k = 1; k < kSteps; ++k) {
-            int t_ = tok[k - 1], h_ = head[k - 1] + 2;
+            int t_ = tok[k - 1], h_ = head[k - 1] + kHeadsPerStep;
             while (h_ >= p.padded) h_ -= p.padded, ++t_;
             tok[k] = t_;
             head[k] = h_;
@@ -155,28 +162,26 @@ __global__ void __launch_bounds__(kThreads) mxfp4_q_quant_kernel(const __grid_co
     }
 #pragma unroll
     for (int k = 0; k < kSteps; ++k) {
-        const uint32_t row = first + 2 * k + half;
+        const uint32_t row = first + kHeadsPerStep * k + slot;
         const bool live = row < rows && head[k] < p.heads;
         const int t = live ? tok[k] : 0, h = live ? head[k] : 0;
         wt[k] = (live && sub == 0) ? p.w[static_cast<int64_t>(t) * p.w_stride_token + h] : 0.0f;
         if (live)
             x[k].load(p.q, static_cast<int64_t>(t) * p.q_stride_token + static_cast<int64_t>(h) * p.q_stride_head +
-                               8 * sub);
+                               kVals * sub);
         else
             x[k].zero();
     }
 #pragma unroll
     for (int k = 0; k < kSteps; ++k) {
         // every lane takes part in the shuffles; rows past the end store nothing
-        const bool in = first + 2 * k + half < rows;
+        const bool in = first + kHeadsPerStep * k + slot < rows;
         const int t = in ? tok[k] : 0, h = in ? head[k] : 0;
         const bool live = h < p.heads;
-        float v[8];
-        x[k].values(v);
-        // block maxima of |x|; a block of 32 values is 4 lanes
+        // block maxima of |x|
         uint32_t amax = x[k].abs_max_bits();
-        amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+#pragma unroll
+        for (int o = 1; o < kLanesPerBlock; o <<= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         // e = ceil(log2(RN(a / 6))) for a = max(amax, 6 * 2^-126) = m * 2^E,
         // m in [1, 2): RN(a / 6) is a power of two only for m = 1.5 (then
         // 2^(E - 2)); otherwise its exponent is E - 2 for m > 1.5 and E - 3
@@ -188,16 +193,23 @@ __global__ void __launch_bounds__(kThreads) mxfp4_q_quant_kernel(const __grid_co
         // x / 2^e as x * 2^-e: the factor is a normal power of two, so the
         // product is the correctly rounded quotient
         const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        float v[kVals];
+        x[k].values(v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], inv);
-        const uint32_t codes = e2m1x8(v);
+        for (int i = 0; i < kVals; ++i) v[i] = __fmul_rn(v[i], inv);
         uint8_t* packed = p.packed + static_cast<int64_t>(t) * p.packed_stride_token + h * (kHeadDim / 2);
-        if (in) reinterpret_cast<uint32_t*>(packed)[sub] = live ? codes : 0u;
+        if constexpr (kVals == 16) {
+            const uint2 codes = make_uint2(e2m1x8(v), e2m1x8(v + 8));
+            if (in) reinterpret_cast<uint2*>(packed)[sub] = live ? codes : make_uint2(0u, 0u);
+        } else {
+            const uint32_t codes = e2m1x8(v);
+            if (in) reinterpret_cast<uint32_t*>(packed)[sub] = live ? codes : 0u;
+        }
         // the head's four scale bytes: block b's byte in byte b, OR-reduced
-        // over the four blocks' lanes (every lane of a block holds its e)
-        uint32_t word = static_cast<uint32_t>(e + 127) << (8 * (sub >> 2));
-        word |= __shfl_xor_sync(0xFFFFFFFFu, word, 4);
-        word |= __shfl_xor_sync(0xFFFFFFFFu, word, 8);
+        // over the head's lanes (every lane of a block holds its e)
+        uint32_t word = static_cast<uint32_t>(e + 127) << (8 * (sub / kLanesPerBlock));
+#pragma unroll
+        for (int o = kLanesPerBlock; o < kLanesPerHead; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
         if (in && sub == 0) {
             p.scale[static_cast<int64_t>(t) * p.scale_stride_token + h] = live ? static_cast<int32_t>(word) : 0;
             p.w_out[static_cast<int64_t>(t) * p.w_out_stride_token + h] = live ? __fmul_rn(wt[k], p.weight_scale) : 0.0f;
@@ -222,9 +234,9 @@ extern "C" int smla_mxfp4_q_quant(const smla_mxfp4_shape* shape, const void* q, 
     if (s.tokens == 0 || s.padded_heads == 0) return SMLA_OK;
     if (q_packed == nullptr || q_scale == nullptr || w_out == nullptr) return SMLA_EINVAL;
     if (s.heads > 0 && (q == nullptr || weights == nullptr)) return SMLA_EINVAL;
-    // 16-byte loads of 8 values (two for FP32); 4-byte packed stores
-    if ((s.heads > 0 && !aligned(q, 16)) || !aligned(q_packed, 4)) return SMLA_EINVAL;
-    if (s.q_stride_token % 8 || s.q_stride_head % 8 || s.packed_stride_token % 4) return SMLA_EINVAL;
+    // two 16-byte loads per lane (16 BF16 or 8 FP32 values); 8-byte packed stores
+    if ((s.heads > 0 && !aligned(q, 16)) || !aligned(q_packed, 8)) return SMLA_EINVAL;
+    if (s.q_stride_token % 8 || s.q_stride_head % 8 || s.packed_stride_token % 8) return SMLA_EINVAL;
     if (s.q_stride_token < 0 || s.q_stride_head < 0 || s.w_stride_token < 0 || s.packed_stride_token < 0 ||
         s.scale_stride_token < 0 || s.w_out_stride_token < 0)
         return SMLA_EINVAL;
@@ -250,9 +262,9 @@ extern "C" int smla_mxfp4_q_quant(const smla_mxfp4_shape* shape, const void* q, 
     p.q_is_f32 = s.q_dtype == SMLA_DTYPE_F32;
 
     const int64_t rows = static_cast<int64_t>(s.tokens) * s.padded_heads;
-    if (rows + kWarps * 16 >= (int64_t{1} << 31)) return SMLA_EUNSUPPORTED;
+    if (rows + 2 * rows_per_cta<false>() >= (int64_t{1} << 31)) return SMLA_EUNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
-    const int64_t per_cta = static_cast<int64_t>(kWarps) * (p.q_is_f32 ? 8 : 16);  // rows per CTA
+    const int64_t per_cta = p.q_is_f32 ? rows_per_cta<true>() : rows_per_cta<false>();
     cfg.gridDim = dim3(static_cast<unsigned>((rows + per_cta - 1) / per_cta), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.stream = static_cast<cudaStream_t>(stream);
