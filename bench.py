@@ -43,6 +43,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+from sparse_mla_decode_gb300.replicas import job_rate, reduce_over_ranks  # noqa: E402
+
 METRIC = "µs/call and achieved HBM GB/s (% of 8 TB/s) for sparse MLA decode"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
@@ -79,14 +81,16 @@ def parse():
 def make_sets(config: str, rank: int, sets: int):
     from sparse_mla_decode_gb300 import workloads
 
+    from sparse_mla_decode_gb300.replicas import rank_seed
+
     if config == "batch":
-        rng = np.random.default_rng(5000 + rank)
+        rng = np.random.default_rng(rank_seed(5000, rank))
         pool = workloads.e4m3_normal(rng, (1 << 20, 576))
-        return [workloads.bandwidth_batch(seed=1003 + 101 * rank + r, pool=pool) for r in range(sets)]
+        return [workloads.bandwidth_batch(seed=rank_seed(1003, rank, r), pool=pool) for r in range(sets)]
     make = {"tiny": workloads.tiny, "verify": workloads.verify_rows,
             "two_pool": workloads.two_pool_sinks}[config]
     base = {"tiny": 1000, "verify": 1001, "two_pool": 1002}[config]
-    return [make(seed=base + 101 * rank + r) for r in range(sets)]
+    return [make(seed=rank_seed(base, rank, r)) for r in range(sets)]
 
 
 def bytes_alg(w) -> int:
@@ -478,17 +482,7 @@ def run_ours(args, rank, world, local_rank):
 
     step_bytes = float(np.mean([byts[i % len(byts)] for i in range(args.steps)]))
     step_flops = float(np.mean([flops[i % len(flops)] for i in range(args.steps)]))
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        b = torch.tensor([step_bytes], dtype=torch.float64, device=dev)
-        dist.all_reduce(b, op=dist.ReduceOp.SUM)
-        total_bytes = float(b.item())
-    else:
-        total_bytes = step_bytes
-    ms = elapsed_ms / args.steps
-    value = total_bytes / (ms * 1e-3) / 1e9
+    ms, total_bytes, value = job_rate(dist, elapsed_ms, step_bytes, args.steps, device=dev)
 
     # end to end through the public API, host buffers in pinned memory
     e2e = None
@@ -508,10 +502,7 @@ def run_ours(args, rank, world, local_rank):
         steps = min(args.steps, 500)
         e_ms = pipelined_e2e(torch, host, (dsets[0]["q"], dsets[0]["indices"], dsets[0]["lens"]), e2e_run,
                              (dsets[0]["out"], dsets[0]["lse"]), steps)
-        if dist is not None:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
@@ -703,13 +694,7 @@ def run_merge(args, rank, world, local_rank):
                 call(i)
         torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, max(t_wall1, soak_until))
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    ms = elapsed_ms / args.steps
-    total_bytes = per_call * world
-    value = total_bytes / (ms * 1e-3) / 1e9
+    ms, total_bytes, value = job_rate(dist, elapsed_ms, per_call, args.steps, device=dev)
 
     e2e = None
     if not args.no_e2e:
@@ -720,6 +705,7 @@ def run_merge(args, rank, world, local_rank):
             smla.smla_merge(inp[0], inp[1], sets[0][2], outp[0], outp[1])
 
         e_ms = pipelined_e2e(torch, host, (sets[0][0], sets[0][1]), e2e_run, (out, lse), min(args.steps, 200))
+        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(T * H * (512 * 2 + 4)),
@@ -832,13 +818,10 @@ def run_mxfp4(args, rank, world, local_rank):
         graph.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, max(t_wall1, t_wall0 + args.soak))
-    ms = start.elapsed_time(end) / args.steps
+    dist = None
     if world > 1:
         import torch.distributed as dist
-
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, _, _ = job_rate(dist, start.elapsed_time(end), per_call, args.steps, device=dev)
     achieved = per_call / (ms * 1e-3) / 1e9
     e2e = None
     if not args.no_e2e:
@@ -848,6 +831,7 @@ def run_mxfp4(args, rank, world, local_rank):
             smla.smla_mxfp4_q_quant(inp[0], inp[1], 0.0625, *outp)
 
         e_ms = pipelined_e2e(torch, host, sets[0], e2e_run, outs[0], min(args.steps, 100))
+        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(T * H * (256 + 4)),
                "d2h_bytes_per_step": int(T * H * 72),
