@@ -11,6 +11,8 @@ through :func:`build`) and exposes the two oracle modes over numpy arrays:
   ``SparseDcpDecode.merge``) replayed on a given (splits, chunk) partition.
 * :func:`mxfp4_q_quant` -- the MXFP4 quantisation of the indexer query (Kimi
   K3.1 ``dsa_indexer_mxfp4`` page: UE8M0 scale per 32 values, E2M1 codes).
+* :func:`value_gate` -- the value projection (W_UV) and sigmoid gate after
+  the merge (the ``mla/dcp`` page, ``DcpValue``).
 * :func:`merge` / :func:`merge_f64` -- the LSE merge of partial (out, lse) sets
   of the Kimi K3.1 ``mla/dcp`` page (``DcpValue``: weights exp2(lse - max) /
   sum, an FP32 weighted sum of the BF16 rows, one BF16 rounding).
@@ -118,6 +120,7 @@ def _load():
             lib.smla_oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
             lib.smla_oracle_e2m1_to_double.restype = ctypes.c_double
             lib.smla_oracle_mxfp4_q_quant.argtypes = [i32, i32, vp, vp, ctypes.c_float, vp, vp, vp]
+            lib.smla_oracle_value_gate.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
             lib.smla_oracle_merge_pairs.argtypes = [ctypes.POINTER(_MergeProblem), vp, vp, i32, vp, vp, vp, i32]
             del i64
             _lib = lib
@@ -303,3 +306,21 @@ def mxfp4_q_quant(q, weights, weight_scale: float, padded_heads: int):
         lib.smla_oracle_mxfp4_q_quant(H, P, q[t].ctypes.data, weights[t].ctypes.data, float(weight_scale),
                                       packed[t].ctypes.data, scale[t].ctypes.data, w_out[t].ctypes.data)
     return packed, scale, w_out
+
+
+def value_gate(latent_bits, w_bits, gate_bits, lens=None):
+    """out[t, h*128 + v] = BF16(BF16(sum_j latent[t,h,j] W[h,j,v]) * sigmoid(gate[t, h*128+v])).
+    latent_bits uint16 [T, H, 512], w_bits uint16 [H, 512, 128], gate_bits
+    uint16 [T, H*128]; returns (value [T, H*128] float64, bits uint16)."""
+    lib = _load()
+    latent = _c(latent_bits, np.uint16)
+    w = _c(w_bits, np.uint16)
+    gate = _c(gate_bits, np.uint16)
+    T, H, J = latent.shape
+    assert J == LATENT and w.shape == (H, LATENT, 128) and gate.shape == (T, H * 128)
+    lens = None if lens is None else _c(lens, np.int32)
+    value = np.zeros((T, H * 128), np.float64)
+    bits = np.zeros((T, H * 128), np.uint16)
+    lib.smla_oracle_value_gate(T, H, latent.ctypes.data, w.ctypes.data, gate.ctypes.data,
+                               None if lens is None else lens.ctypes.data, value.ctypes.data, bits.ctypes.data)
+    return value, bits

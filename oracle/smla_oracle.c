@@ -489,6 +489,40 @@ int smla_oracle_mxfp4_q_quant(int heads, int padded, const float* q, const float
     return 0;
 }
 
+/* ------------------------------- value projection and gate after the merge */
+/*
+ * [DCP]  DcpValue (class docstring and merge, the lines after the merged
+ *        rows): out[t, h*128 + v] = BF16(BF16(sum_j latent[t, h, j] *
+ *        W[h, j, v]) * sigmoid(gate[t, h*128 + v])), the sum over the 512
+ *        latents (BF16 operands, FP32 accumulation on the page), sigmoid(x) =
+ *        1 / (1 + e^-x); rows of a token whose count is <= 0 are zero.
+ * Readings: the count is per token (the page's per-request totals with one
+ * token per request); the sum is taken exactly (double) before its BF16
+ * rounding.
+ */
+int smla_oracle_value_gate(int tokens, int heads, const uint16_t* latent, const uint16_t* w_uv,
+                           const uint16_t* gate, const int32_t* lens, double* out_value, uint16_t* out_bf16) {
+    const int J = LATENT, V = 128;
+    for (int t = 0; t < tokens; ++t)
+        for (int h = 0; h < heads; ++h)
+            for (int v = 0; v < V; ++v) {
+                size_t o = ((size_t)t * heads + h) * V + v;
+                double value = 0.0;
+                if (!(lens && lens[t] <= 0)) {
+                    double acc = 0.0;
+                    for (int j = 0; j < J; ++j)
+                        acc += (double)smla_oracle_bf16_to_float(latent[((size_t)t * heads + h) * J + j]) *
+                               (double)smla_oracle_bf16_to_float(w_uv[((size_t)h * J + j) * V + v]);
+                    double rounded = smla_oracle_bf16_to_float(smla_oracle_bf16_from_float((float)acc));
+                    double g = smla_oracle_bf16_to_float(gate[o]);
+                    value = rounded * (1.0 / (1.0 + exp(-g)));
+                }
+                if (out_value) out_value[o] = value;
+                if (out_bf16) out_bf16[o] = smla_oracle_bf16_from_float((float)value);
+            }
+    return 0;
+}
+
 /* ------------------------------------------------------------ batch drivers */
 
 /* FP64 definition over every (token, head); OpenMP over the pairs. */

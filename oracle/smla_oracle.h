@@ -89,6 +89,12 @@ double smla_oracle_e2m1_to_double(uint8_t code);
 int smla_oracle_mxfp4_q_quant(int heads, int padded, const float* q, const float* weights, float weight_scale,
                               uint8_t* packed, int32_t* scale, float* w_out);
 
+/* Value projection and sigmoid gate after the merge: latent BF16 [T][H][512],
+ * w_uv BF16 [H][512][128], gate BF16 [T][H * 128], lens [T] or NULL; outputs
+ * [T][H * 128] (value before the final rounding, and BF16 bits). */
+int smla_oracle_value_gate(int tokens, int heads, const uint16_t* latent, const uint16_t* w_uv,
+                           const uint16_t* gate, const int32_t* lens, double* out_value, uint16_t* out_bf16);
+
 #ifdef __cplusplus
 }
 #endif

@@ -491,3 +491,55 @@ def test_mxfp4_zero_blocks_weights_and_padding():
     assert ((int(scale[0, 0]) >> 8) & 0xFF) == 1 and np.all(packed[0, 0, 16:32] == 0)  # zero block: 2^-126
     np.testing.assert_array_equal(w_out[:, :3], w * np.float32(0.125))
     assert np.all(packed[:, 3:] == 0) and np.all(scale[:, 3:] == 0) and np.all(w_out[:, 3:] == 0)
+
+
+# ------------------- value projection and sigmoid gate (mla/dcp, DcpValue)
+
+
+def _bf(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _val(bits):
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def _value_gate_inputs(seed, T=3, H=2):
+    rng = np.random.default_rng(seed)
+    latent = _bf(rng.standard_normal((T, H, 512)) * 0.5)
+    w = _bf(rng.standard_normal((H, 512, 128)) * 0.05)
+    gate = _bf(rng.standard_normal((T, H * 128)) * 2.0)
+    return latent, w, gate
+
+
+def test_value_gate_matches_a_library_matmul():
+    """The oracle's loops against numpy's float64 matmul of the same BF16
+    values, with the roundings and the sigmoid applied on top."""
+    latent, w, gate = _value_gate_inputs(21)
+    value, bits = oracle.value_gate(latent, w, gate)
+    acc = np.einsum("thj,hjv->thv", _val(latent), _val(w))
+    rounded = _val(_bf(acc.astype(np.float32)))
+    expect = (rounded * (1.0 / (1.0 + np.exp(-_val(gate).reshape(rounded.shape))))).reshape(value.shape)
+    np.testing.assert_allclose(value, expect, rtol=1e-12, atol=1e-14)
+    assert np.array_equal(bits, _bf(expect.astype(np.float32)))
+
+
+def test_value_gate_with_an_identity_projection_is_the_gated_latent():
+    latent, _, gate = _value_gate_inputs(22, T=2, H=3)
+    w = np.zeros((3, 512, 128), np.float32)
+    for v in range(128):
+        w[:, 2 * v, v] = 1.0  # v reads latent 2v
+    value, _ = oracle.value_gate(latent, _bf(w), gate)
+    lat = _val(latent)[:, :, 0:256:2].reshape(2, 3 * 128)
+    np.testing.assert_allclose(value, lat / (1.0 + np.exp(-_val(gate))), rtol=1e-14)
+
+
+def test_value_gate_saturated_gates_and_empty_tokens():
+    latent, w, gate = _value_gate_inputs(23)
+    gate = _bf(np.where(np.arange(3 * 0 + 2 * 128)[None, :] % 2 == 0, 40.0, -40.0) * np.ones((3, 1)))
+    value, bits = oracle.value_gate(latent, w, gate, lens=np.array([5, 0, 1], np.int32))
+    acc = np.einsum("thj,hjv->thv", _val(latent), _val(w)).reshape(3, 256)
+    rounded = _val(_bf(acc.astype(np.float32)))
+    np.testing.assert_allclose(value[[0, 2]][:, ::2], rounded[[0, 2]][:, ::2], rtol=1e-12)  # sigmoid(40) = 1 - 4e-18
+    assert np.all(np.abs(value[[0, 2]][:, 1::2]) <= np.abs(rounded[[0, 2]][:, 1::2]) * 1e-17)  # sigmoid(-40)
+    assert np.all(value[1] == 0.0) and np.all(bits[1] == 0)  # a token of count 0
