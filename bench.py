@@ -2,7 +2,7 @@
 """Benchmark: sparse MLA decode on GB300 (µs per call, achieved HBM GB/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config batch|tiny|verify|two_pool|merge|mxfp4]
+                    [--config batch|tiny|verify|two_pool|merge|mxfp4|value]
 
 A step is one smla_decode call over one batch of seeded synthetic inputs. The
 default workload is the bandwidth-bound batch: 64 tokens x 128 heads x 2048
@@ -57,9 +57,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge", "mxfp4"], default="batch",
+    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge", "mxfp4", "value"],
+                    default="batch",
                     help="merge: the LSE merge of 8 partial (out, lse) sets of the 64 x 128 batch shape; "
-                         "mxfp4: the MXFP4 indexer-query quantisation of 16384 tokens x 32 heads")
+                         "mxfp4: the MXFP4 indexer-query quantisation of 16384 tokens x 32 heads; "
+                         "value: the value projection (W_UV) and sigmoid gate of the 64 x 128 batch shape")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
@@ -905,6 +907,162 @@ def run_mxfp4_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+VALUE_METRIC = "µs/call and achieved HBM GB/s for the value projection (W_UV) and sigmoid gate"
+
+
+def value_bytes(T, H) -> int:
+    """Merged BF16 rows, the BF16 W_UV of every head and the BF16 gates read;
+    BF16 values written (lens: 4 bytes a token)."""
+    return T * H * 512 * 2 + H * 512 * 128 * 2 + 2 * T * H * 128 * 2 + 4 * T
+
+
+def value_sets(T, H, R, seed, device):
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    sets = []
+    for _ in range(R):
+        latent = torch.randn((T, H, 512), generator=gen, device=device).to(torch.bfloat16)
+        w = (torch.randn((H, 512, 128), generator=gen, device=device) / 512 ** 0.5).to(torch.bfloat16)
+        gate = (2.0 * torch.randn((T, H * 128), generator=gen, device=device)).to(torch.bfloat16)
+        lens = torch.full((T,), 2048, dtype=torch.int32, device=device)
+        sets.append((latent, w, gate, lens))
+    return sets
+
+
+def run_value(args, rank, world, local_rank):
+    """--config value: smla_value_gate of the 64 x 128 batch shape (one W_UV
+    per input set, as for consecutive layers)."""
+    import torch
+
+    import __graft_entry__
+    from sparse_mla_decode_gb300 import smla
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T, H = 64, 128
+    per_call = value_bytes(T, H)
+    R = max(2, int(math.ceil(2.5 * L2_BYTES / per_call)))
+    sets = value_sets(T, H, R, 5151 + rank, dev)
+    outs = [torch.empty((T, H * 128), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+    def call(i):
+        smla.smla_value_gate(*sets[i % R], outs[i % R])
+
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(max(3, args.warmup)):
+        call(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(args.steps):
+            call(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    while time.time() < t_wall0 + args.soak:
+        graph.replay()
+        torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, max(t_wall1, t_wall0 + args.soak))
+    if smla.smla_value_gate_error() != 0:
+        raise RuntimeError("value kernel reported a device error")
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    ms, _, _ = job_rate(dist, start.elapsed_time(end), per_call, args.steps, device=dev)
+    achieved = per_call / (ms * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        # the weights stay resident (a layer's W_UV does not travel per call);
+        # the merged rows, gates and counts go up, the values come back
+        host = [(sets[k][0].cpu().pin_memory(), sets[k][2].cpu().pin_memory(), sets[k][3].cpu().pin_memory())
+                for k in range(R)]
+        dev_like = (sets[0][0], sets[0][2], sets[0][3])
+
+        def e2e_run(inp, outp):
+            smla.smla_value_gate(inp[0], sets[0][1], inp[1], inp[2], outp[0])
+
+        e_ms = pipelined_e2e(torch, host, dev_like, e2e_run, (outs[0],), min(args.steps, 100))
+        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
+        e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(T * H * 512 * 2 + T * H * 256 + 4 * T),
+               "d2h_bytes_per_step": int(T * H * 256),
+               "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA "
+                           "graph; W_UV resident"}
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu:
+        cpu = value_cpu_rate(sets[0], args.cpu_seconds)
+    peak, peak_src = measured_hbm_peak()
+    line = {
+        "metric": VALUE_METRIC, "value": round(per_call * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "us_per_call": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"value_gate_t{T}_h{H}: merged BF16 rows N(0, 1), W_UV N(0, 1/512), gates N(0, 4)",
+                   "tokens": T, "heads": H, "latent": 512, "values": 128, "input_sets": R,
+                   "l2": "rotating %d input sets, W_UV included (%.1f MB per call)" % (R, per_call / 1e6),
+                   "launch": "one CUDA graph of the %d timed library calls, replayed once" % args.steps},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "bytes_alg_per_launch": int(per_call)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def value_cpu_rate(first_set, seconds: float):
+    """The oracle's projection and gate on the host (one thread) over a
+    bounded sample of tokens."""
+    from oracle import oracle
+
+    oracle.build()
+    latent, w, gate, lens = (x.cpu() for x in first_set)
+    T, H, _ = latent.shape
+    lat_b = latent.view(torch_int16()).numpy().view(np.uint16)
+    w_b = w.view(torch_int16()).numpy().view(np.uint16)
+    g_b = gate.view(torch_int16()).numpy().view(np.uint16)
+    rng = np.random.default_rng(4)
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds and done < T:
+        rows = rng.integers(0, T, 2)
+        oracle.value_gate(lat_b[rows], w_b, g_b[rows], lens.numpy()[rows])
+        done += 2
+    per_call = (time.perf_counter() - t0) / done * T
+    return {"value": round(value_bytes(T, H) / per_call / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {T} tokens, all heads, in batches of 2", "us_per_call": round(per_call * 1e6, 1)}
+
+
+def run_value_reference(args, rank, world):
+    if rank != 0:
+        return
+    T, H = 64, 128
+    first = value_sets(T, H, 1, 5151, "cpu")[0]
+    total = max(1, args.steps + args.warmup)
+    cpu = value_cpu_rate(first, min(60.0, 2.0 * total) / total * args.steps)
+    line = {
+        "metric": VALUE_METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(cpu["us_per_call"] / 1e3, 3), "us_per_call": cpu["us_per_call"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference", "config": {"workload": f"value_gate_t{T}_h{H}", "tokens": T, "heads": H},
+        "cpu_baseline": cpu,
+        "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def torch_int16():
     import torch
 
@@ -942,6 +1100,8 @@ def main():
             run_merge_reference(args, rank, world)
         elif args.config == "mxfp4":
             run_mxfp4_reference(args, rank, world)
+        elif args.config == "value":
+            run_value_reference(args, rank, world)
         else:
             run_reference(args, rank, world)
         return
@@ -956,6 +1116,8 @@ def main():
             run_merge(args, rank, world, local_rank)
         elif args.config == "mxfp4":
             run_mxfp4(args, rank, world, local_rank)
+        elif args.config == "value":
+            run_value(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -223,6 +223,44 @@ typedef struct smla_mxfp4_shape {
 int smla_mxfp4_q_quant(const smla_mxfp4_shape* shape, const void* q, const float* weights, float weight_scale,
                        void* q_packed, int32_t* q_scale, float* w_out, void* stream);
 
+/* ---------------------------------------------------- value projection + gate
+ * The step after the merge, after the Kimi K3.1 `mla/dcp` page (DcpValue,
+ * after the merged rows): each merged latent row is projected by its head's
+ * W_UV to 128 values and gated by a sigmoid. For token t < T, head h < H and
+ * value v < 128:
+ *   acc = sum over j < 512 of latent[t, h, j] * w_uv[h, j, v]  (BF16 x BF16, FP32 accumulation)
+ *   out[t, h*128 + v] = BF16(float(BF16(acc)) * 1 / (1 + exp(-gate[t, h*128 + v])))
+ * and out[t, h*128 + v] = +0.0 when lens is given and lens[t] <= 0. */
+typedef struct smla_value_shape {
+    int32_t tokens;   /* T */
+    int32_t heads;    /* H */
+    int32_t reserved[2];
+    int64_t latent_stride_token, latent_stride_head; /* BF16 elements, positive multiples of 8; latents contiguous */
+    int64_t gate_stride_token;                       /* BF16 elements (multiple of 8); H*128 contiguous */
+    int64_t out_stride_token;                        /* BF16 elements (multiple of 8); H*128 contiguous */
+} smla_value_shape;
+
+/* Projects and gates.
+ *   latent  device, BF16 [T, H, 512] (the merged rows), 16-byte aligned.
+ *   w_uv    device, BF16 [H, 512, 128], contiguous, 16-byte aligned.
+ *   gate    device, BF16 [T, H*128], 16-byte aligned.
+ *   lens    device, int32 [T], or NULL (every token live).
+ *   out     device, BF16 [T, H*128], 16-byte aligned.
+ * Every buffer belongs to the caller; nothing is allocated. Launched with
+ * programmatic dependent launch; captureable in a CUDA graph. A bounded wait
+ * that gives up sets SMLA_DEV_TIMEOUT in the word smla_value_gate_error reads.
+ * Errors: SMLA_EINVAL (null buffers, negative sizes, latent strides not
+ * positive multiples of 8, gate or out token strides below H*128 or not
+ * multiples of 8, misalignment), SMLA_EUNSUPPORTED (T above
+ * 65535 * 64 or H above 65535, no tensor-map encoder) before any launch;
+ * SMLA_ECUDA when the launch fails. T = 0 or H = 0 launches nothing. */
+int smla_value_gate(const smla_value_shape* shape, const void* latent, const void* w_uv, const void* gate,
+                    const int32_t* lens, void* out, void* stream);
+
+/* Reads and clears the value kernel's error word (SMLA_DEV_* bits) after
+ * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
+int smla_value_gate_error(int32_t* bits);
+
 /* Reads and clears the current device's error word (SMLA_DEV_* bits) after
  * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
 int smla_device_error(int32_t* bits);

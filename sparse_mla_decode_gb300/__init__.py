@@ -17,5 +17,8 @@ from .smla import (  # noqa: F401
     smla_merge,
     smla_mxfp4_q_quant,
     smla_plan_for,
+    smla_value_gate,
+    smla_value_gate_error,
     smla_version,
+    value_gate,
 )

@@ -67,8 +67,17 @@ class SmlaMxfp4Shape(ctypes.Structure):
     ]
 
 
+class SmlaValueShape(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
+        ("latent_stride_token", ctypes.c_int64), ("latent_stride_head", ctypes.c_int64),
+        ("gate_stride_token", ctypes.c_int64), ("out_stride_token", ctypes.c_int64),
+    ]
+
+
 DTYPE_BF16 = 1
 DTYPE_F32 = 2
+VALUE_DIM = 128
 
 
 class SmlaError(RuntimeError):
@@ -112,6 +121,10 @@ def load(path: str | None = None):
         lib.smla_merge.restype = i32
         lib.smla_mxfp4_q_quant.argtypes = [ctypes.POINTER(SmlaMxfp4Shape), vp, vp, ctypes.c_float, vp, vp, vp, vp]
         lib.smla_mxfp4_q_quant.restype = i32
+        lib.smla_value_gate.argtypes = [ctypes.POINTER(SmlaValueShape), vp, vp, vp, vp, vp, vp]
+        lib.smla_value_gate.restype = i32
+        lib.smla_value_gate_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+        lib.smla_value_gate_error.restype = i32
         _lib = lib
         return lib
 
@@ -289,3 +302,52 @@ def mxfp4_q_quant(q, weights, weight_scale: float, padded_heads: int | None = No
     scale = torch.empty((T, P), dtype=torch.int32, device=q.device)
     w_out = torch.empty((T, P), dtype=torch.float32, device=q.device)
     return smla_mxfp4_q_quant(q, weights, weight_scale, packed, scale, w_out, stream=stream)
+
+
+def smla_value_gate(latent: torch.Tensor, w_uv: torch.Tensor, gate: torch.Tensor, lens: torch.Tensor | None,
+                    out: torch.Tensor, stream=None):
+    """Value projection and sigmoid gate through the C ABI (see
+    ``smla_value_gate`` in smla.h). latent: bfloat16 [T, H, 512], latents
+    contiguous; w_uv: bfloat16 [H, 512, 128] contiguous; gate and out:
+    bfloat16 [T, H*128], rows contiguous; lens: int32 [T] or None."""
+    lib = load()
+    T, H, J = latent.shape
+    if latent.dtype != torch.bfloat16 or w_uv.dtype != torch.bfloat16 or gate.dtype != torch.bfloat16 \
+            or out.dtype != torch.bfloat16:
+        raise ValueError("value_gate: latent, w_uv, gate and out must be bfloat16")
+    if J != LATENT or tuple(w_uv.shape) != (H, LATENT, VALUE_DIM) or tuple(gate.shape) != (T, H * VALUE_DIM) \
+            or tuple(out.shape) != (T, H * VALUE_DIM):
+        raise ValueError("value_gate: shapes")
+    if not w_uv.is_contiguous() or latent.stride(2) != 1 or gate.stride(1) != 1 or out.stride(1) != 1:
+        raise ValueError("value_gate: inner dimensions must be contiguous")
+    if lens is not None and (lens.dtype != torch.int32 or tuple(lens.shape) != (T,) or lens.stride(0) != 1):
+        raise ValueError("value_gate: lens must be contiguous int32 [T]")
+    shape = SmlaValueShape()
+    shape.tokens, shape.heads = T, H
+    shape.latent_stride_token, shape.latent_stride_head = latent.stride(0), latent.stride(1)
+    shape.gate_stride_token, shape.out_stride_token = gate.stride(0), out.stride(0)
+    if stream is None:
+        stream = torch.cuda.current_stream(out.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib.smla_value_gate(ctypes.byref(shape), _ptr(latent), _ptr(w_uv), _ptr(gate),
+                             None if lens is None else _ptr(lens), _ptr(out), ctypes.c_void_p(handle))
+    if rc != OK:
+        raise SmlaError(rc, "smla_value_gate")
+    return out
+
+
+def value_gate(latent, w_uv, gate, lens=None, stream=None):
+    """Allocates the output on latent's device and calls :func:`smla_value_gate`."""
+    T, H, _ = latent.shape
+    out = torch.empty((T, H * VALUE_DIM), dtype=torch.bfloat16, device=latent.device)
+    return smla_value_gate(latent, w_uv, gate, lens, out, stream=stream)
+
+
+def smla_value_gate_error() -> int:
+    """Reads and clears the value kernel's error word (after a device sync)."""
+    lib = load()
+    bits = ctypes.c_int32(0)
+    rc = lib.smla_value_gate_error(ctypes.byref(bits))
+    if rc != OK:
+        raise SmlaError(rc, "smla_value_gate_error")
+    return int(bits.value)

@@ -91,8 +91,10 @@ def e4m3_p_bound(w, pairs):
 
 
 def bf16_ulp(x):
+    """Spacing of BF16 numbers at |x| (8 significand bits; FP32's exponent
+    range, so 2^-133 throughout the subnormal range below 2^-126)."""
     a = np.abs(np.asarray(x, np.float64))
-    a = np.maximum(a, 2.0 ** -133)
+    a = np.maximum(a, 2.0 ** -126)
     e = np.floor(np.log2(a))
     return 2.0 ** (e - 7)
 

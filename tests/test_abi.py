@@ -164,3 +164,35 @@ def test_merge_rejects_bad_arguments_before_any_launch(lib, kw, ptrs):
 
 def test_merge_of_nothing_is_ok_without_a_device(lib):
     assert lib.smla_merge(ctypes.byref(_merge_shape(tokens=0)), None, None, None, None, None, None) == smla.OK
+
+
+def _value_shape(**kw):
+    s = smla.SmlaValueShape()
+    base = dict(tokens=3, heads=4, latent_stride_token=4 * 512, latent_stride_head=512,
+                gate_stride_token=4 * 128, out_stride_token=4 * 128)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(s, k, v)
+    return s
+
+
+@pytest.mark.parametrize("kw,ptrs", [
+    (dict(tokens=-1), (16, 16, 16, 16)),
+    (dict(latent_stride_head=0), (16, 16, 16, 16)),
+    (dict(latent_stride_token=100), (16, 16, 16, 16)),  # rows not 16-byte aligned
+    (dict(gate_stride_token=4 * 128 - 8), (16, 16, 16, 16)),
+    (dict(out_stride_token=4 * 128 - 8), (16, 16, 16, 16)),  # output rows overlap
+    (dict(), (0, 16, 16, 16)),                           # no latent
+    (dict(), (16, 16, 16, 0)),                           # no out
+    (dict(), (16, 8, 16, 16)),                           # w_uv misaligned
+    (dict(), (16, 16, 24, 16)),                          # gate misaligned
+])
+def test_value_gate_rejects_bad_arguments_before_any_launch(lib, kw, ptrs):
+    latent, w, gate, out = (ctypes.c_void_p(p) if p else None for p in ptrs)
+    rc = lib.smla_value_gate(ctypes.byref(_value_shape(**kw)), latent, w, gate, None, out, None)
+    assert rc == smla.EINVAL
+
+
+def test_value_gate_of_nothing_is_ok_without_a_device(lib):
+    assert lib.smla_value_gate(ctypes.byref(_value_shape(tokens=0)), None, None, None, None, None, None) == smla.OK
+    assert lib.smla_value_gate(ctypes.byref(_value_shape(heads=0)), None, None, None, None, None, None) == smla.OK
