@@ -211,12 +211,16 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha() -> str:
-    """Hash of the decode kernel's sources (the committed DRAM traffic holds
-    only while they are unchanged)."""
+KERNEL_SOURCES = {"value": ("smla_value.cu", "smla_ptx.cuh")}
+
+
+def kernel_sha(config: str = "batch") -> str:
+    """Hash of the sources of the kernel a config times (the decode kernel
+    unless listed in KERNEL_SOURCES): the committed DRAM traffic holds only
+    while they are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc")
-    for name in ("smla_decode.cu", "smla_ptx.cuh"):
+    for name in KERNEL_SOURCES.get(config, ("smla_decode.cu", "smla_ptx.cuh")):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -233,7 +237,7 @@ def ncu_traffic(config: str):
     except (OSError, ValueError):
         return None
     entry = data.get(config)
-    if not entry or entry.get("kernel_sha") != kernel_sha():
+    if not entry or entry.get("kernel_sha") != kernel_sha(config):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -1016,7 +1020,7 @@ def run_value(args, rank, world, local_rank):
                    "l2": "rotating %d input sets, W_UV included (%.1f MB per call)" % (R, per_call / 1e6),
                    "launch": "one CUDA graph of the %d timed library calls, replayed once" % args.steps},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic("value"),
                      "bytes_alg_per_launch": int(per_call)},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
     }

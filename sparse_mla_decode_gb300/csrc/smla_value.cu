@@ -45,7 +45,7 @@ constexpr int kTile = 64;   // tokens per CTA (N)
 constexpr int kJ = 512;     // latents (K)
 constexpr int kV = 128;     // values per head (M)
 constexpr int kBlocks = kJ / 64;              // 64-latent blocks, one swizzle atom wide
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps: thread 0 issues TMA and MMA; all eight run the epilogue
 constexpr int kWBlockBytes = 64 * kV * 2;     // 64 latent rows x 128 values: two 8 KB MN atoms
 constexpr int kLBlockBytes = kTile * 128;     // 64 tokens x 64 latents
 constexpr int kGateBytes = kTile * kV * 2;    // 64 tokens x 128 values, unswizzled
@@ -54,13 +54,12 @@ constexpr int kL = kW + kBlocks * kWBlockBytes;
 constexpr int kG = kL + kBlocks * kLBlockBytes;
 constexpr int kBar = kG + kGateBytes;
 constexpr int kMisc = kBar + 8 * (kBlocks + 2);
-constexpr int kLive = kMisc + 16;
-constexpr int kAlloc = kLive + 4 * kTile + 1024;
+constexpr int kAlloc = kMisc + 16 + 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct Params {
     CUtensorMap latent;  // {512 latents, H heads, T tokens} BF16, 128-byte swizzle, boxes of 64 x 1 x 64
-    CUtensorMap w_uv;    // {128 values, 512 latents, H heads} BF16, 128-byte swizzle, boxes of 64 x 64 x 1
+    CUtensorMap w_uv;    // {64 values, 512 latents, 2 value halves, H heads} BF16, 128-byte swizzle, boxes of 64 x 64 x 2 x 1
     CUtensorMap gate;    // {H * 128, T} BF16, boxes of 128 x 64
     CUtensorMap out;     // {H * 128, T} BF16, boxes of 128 x 64
     const int32_t* lens; // [T] or null
@@ -79,6 +78,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// 1 / x by the approximate reciprocal (one MUFU operation, at most 1 ulp of
+// FP32 from the exact value; subnormal results kept, 1 / inf = 0): no
+// branches, so the compiler can overlap the 32 gates of a thread.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // kind::f16 instruction descriptor: BF16 A and B (format 1), FP32 D.
 constexpr uint32_t idesc_bf16(int m, int n, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
@@ -94,8 +102,27 @@ __device__ __forceinline__ void tma_store_2d(const void* map, int32_t x, int32_t
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_constant__ Params p) {
@@ -108,11 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_co
     uint64_t* mma_done = bars + kBlocks + 1;   // every product finished (commit)
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-    int32_t* live = reinterpret_cast<int32_t*>(smem + kLive);
-    __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + kG);  // gates in, values out
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x, t0 = blockIdx.y * kTile;
 
+    // thread 0 starts the copies as soon as its barriers exist; warp 1
+    // allocates TMEM meanwhile
     if (tid == 0) {
         for (int i = 0; i < kBlocks + 2; ++i) mbar_init(bars + i, 1);
         misc[1] = 0;
@@ -122,14 +149,19 @@ __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_co
         prefetch_tensor_map(&p.gate);
         prefetch_tensor_map(&p.out);
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(misc, kTile);  // D: 128 lanes (values) x 64 columns (tokens)
         tmem_relinquish();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (tid < kTile) {
-        const int t = t0 + tid;
-        live[tid] = t < p.tokens && (p.lens == nullptr || p.lens[t] > 0);
+    if (tid == 0) {
+        for (int kb = 0; kb < kBlocks; ++kb) {
+            mbar_arrive_expect_tx(block_full + kb, kLBlockBytes + kWBlockBytes);
+            tma_load_3d(sbase + kL + kb * kLBlockBytes, &p.latent, kb * 64, h, t0, block_full + kb);
+            tma_load_4d(sbase + kW + kb * kWBlockBytes, &p.w_uv, 0, kb * 64, 0, h, block_full + kb);
+        }
+        mbar_arrive_expect_tx(gate_full, kGateBytes);
+        tma_load_2d(sbase + kG, &p.gate, h * kV, t0, gate_full);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -138,15 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_co
 
     bool ok = true;
     if (tid == 0) {
-        for (int kb = 0; kb < kBlocks; ++kb) {
-            mbar_arrive_expect_tx(block_full + kb, kLBlockBytes + kWBlockBytes);
-            tma_load_3d(sbase + kL + kb * kLBlockBytes, &p.latent, kb * 64, h, t0, block_full + kb);
-            tma_load_3d(sbase + kW + kb * kWBlockBytes, &p.w_uv, 0, kb * 64, h, block_full + kb);
-            tma_load_3d(sbase + kW + kb * kWBlockBytes + kWBlockBytes / 2, &p.w_uv, 64, kb * 64, h, block_full + kb);
-        }
-        mbar_arrive_expect_tx(gate_full, kGateBytes);
-        tma_load_2d(sbase + kG, &p.gate, h * kV, t0, gate_full);
-
         // A = W_UV^T: MN-major, 64-value atoms 8 KB apart (LBO), 8-latent
         // groups 1 KB apart (SBO); B = latents: K-major, 8-token groups 1 KB
         // apart. A step of 16 latents moves A by 16 rows of 128 bytes and B by
@@ -168,26 +191,39 @@ __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_co
         mma_commit(mma_done);
     }
     __syncwarp();
+
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, so thread (w,
+    // lane) owns value v = 32 (w % 4) + lane of the 32 tokens tb .. tb + 31,
+    // tb = 32 (w / 4); bit t of `live` says whether token tb + t has keys
+    const int v = 32 * (warp & 3) + lane;
+    const int tb = 32 * (warp >> 2);
+    const int t_lane = t0 + tb + lane;
+    const uint32_t live =
+        __ballot_sync(~0u, t_lane < p.tokens && (p.lens == nullptr || p.lens[t_lane] > 0));
     ok &= mbar_wait_bounded(mma_done, 0, abort_flag, kWaitLimitNs);
     ok &= mbar_wait_bounded(gate_full, 0, abort_flag, kWaitLimitNs);
     __syncwarp();
     tc_fence_after_sync();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // epilogue: thread (warp w, lane) owns value v = 32 w + lane of every token
-    const int v = 32 * warp + lane;
-    float acc[kTile];
-    tmem_load16x4(tmem + (static_cast<uint32_t>(32 * warp) << 16), tmem + (static_cast<uint32_t>(32 * warp) << 16) + 16,
-                  tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32, tmem + (static_cast<uint32_t>(32 * warp) << 16) + 48,
-                  acc);
+    float acc[32];
+    const uint32_t col = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + tb;
+    tmem_load16x2(col, col + 16, acc);
+    const uint32_t slot = sbase + kG + static_cast<uint32_t>(tb * kV + v) * 2;  // gate / value of token tb
+    uint32_t bits[32];
 #pragma unroll
-    for (int t = 0; t < kTile; ++t) {
-        __nv_bfloat16* slot = tile + t * kV + v;
-        const float gate = __bfloat162float(*slot);
+    for (int t = 0; t < 32; ++t) bits[t] = lds_u16(slot + t * kV * 2);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+        const float gate = __uint_as_float(bits[t] << 16);
         const float rounded = __bfloat162float(__float2bfloat16_rn(acc[t]));
-        const float y = rounded * (1.0f / (1.0f + expf(-gate)));
-        *slot = live[t] ? __float2bfloat16_rn(y) : __float2bfloat16_rn(0.0f);
+        // sigmoid(g) = 1 / (1 + e^-g), in FP32 to a few ulp (the value is then
+        // rounded to BF16, 2^-8 relative)
+        const float y = rounded * rcp_approx(1.0f + __expf(-gate));
+        bits[t] = (live >> t) & 1u ? __bfloat16_as_ushort(__float2bfloat16_rn(y)) : 0u;
     }
+#pragma unroll
+    for (int t = 0; t < 32; ++t) sts_u16(slot + t * kV * 2, bits[t]);
     fence_proxy_async_smem();  // the values, written by threads, are read by the TMA store
     tc_fence_before_sync();
     __syncthreads();
@@ -198,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_co
         }
     }
     if (!ok && lane == 0) atomicOr(&g_value_error, SMLA_DEV_TIMEOUT);
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTile);
     }
@@ -208,7 +244,7 @@ bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims
             const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
     auto enc = smla::tensor_map_encoder();
     if (enc == nullptr) return false;
-    const cuuint32_t steps[3] = {1, 1, 1};
+    const cuuint32_t steps[4] = {1, 1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, steps,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -246,10 +282,13 @@ extern "C" int smla_value_gate(const smla_value_shape* shape, const void* latent
         if (!encode(&p.latent, latent, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
     }
     {
-        const cuuint64_t dims[3] = {kV, kJ, H};
-        const cuuint64_t strides[2] = {kV * 2, static_cast<cuuint64_t>(kJ) * kV * 2};
-        const cuuint32_t box[3] = {64, 64, 1};
-        if (!encode(&p.w_uv, w_uv, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
+        // W_UV[h][j][v] as {64 values, 512 latents, 2 value halves, H}: one
+        // box per 64-latent block lands as [value half][64 latents][64 values],
+        // the two MN atoms of A
+        const cuuint64_t dims[4] = {64, kJ, 2, H};
+        const cuuint64_t strides[3] = {kV * 2, 64 * 2, static_cast<cuuint64_t>(kJ) * kV * 2};
+        const cuuint32_t box[4] = {64, 64, 2, 1};
+        if (!encode(&p.w_uv, w_uv, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
     }
     {
         const cuuint64_t dims[2] = {H * kV, T};
