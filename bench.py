@@ -2,7 +2,7 @@
 """Benchmark: sparse MLA decode on GB300 (µs per call, achieved HBM GB/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config batch|tiny|verify|two_pool|merge|mxfp4|value]
+                    [--config batch|tiny|verify|two_pool|merge|mxfp4|value|merge_value]
 
 A step is one smla_decode call over one batch of seeded synthetic inputs. The
 default workload is the bandwidth-bound batch: 64 tokens x 128 heads x 2048
@@ -57,11 +57,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge", "mxfp4", "value"],
+    ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge", "mxfp4", "value",
+                                         "merge_value"],
                     default="batch",
                     help="merge: the LSE merge of 8 partial (out, lse) sets of the 64 x 128 batch shape; "
                          "mxfp4: the MXFP4 indexer-query quantisation of 16384 tokens x 32 heads; "
-                         "value: the value projection (W_UV) and sigmoid gate of the 64 x 128 batch shape")
+                         "value: the value projection (W_UV) and sigmoid gate of the 64 x 128 batch shape; "
+                         "merge_value: the merge of 8 partial sets fused with that projection")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
@@ -211,7 +213,8 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = {"value": ("smla_value.cu", "smla_ptx.cuh")}
+KERNEL_SOURCES = {"value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh"),
+                  "merge_value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh")}
 
 
 def kernel_sha(config: str = "batch") -> str:
@@ -912,6 +915,8 @@ def run_mxfp4_reference(args, rank, world):
 
 
 VALUE_METRIC = "µs/call and achieved HBM GB/s for the value projection (W_UV) and sigmoid gate"
+MERGE_VALUE_METRIC = ("µs/call and achieved HBM GB/s for the LSE merge of partial sets fused with the value "
+                      "projection (W_UV) and sigmoid gate")
 
 
 def value_bytes(T, H) -> int:
@@ -935,25 +940,38 @@ def value_sets(T, H, R, seed, device):
     return sets
 
 
-def run_value(args, rank, world, local_rank):
+def merge_value_bytes(S, T, H) -> int:
+    """The partial rows and LSEs, W_UV and the gates read; the values written."""
+    return S * T * H * (512 * 2 + 4) + H * 512 * 128 * 2 + 2 * T * H * 128 * 2 + 4 * T
+
+
+def run_value(args, rank, world, local_rank, fused=False):
     """--config value: smla_value_gate of the 64 x 128 batch shape (one W_UV
-    per input set, as for consecutive layers)."""
+    per input set, as for consecutive layers). --config merge_value:
+    smla_merge_value of 8 partial sets of that shape."""
     import torch
 
     import __graft_entry__
-    from sparse_mla_decode_gb300 import smla
+    from sparse_mla_decode_gb300 import smla, workloads
 
     __graft_entry__.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    T, H = 64, 128
-    per_call = value_bytes(T, H)
+    S, T, H = 8, 64, 128
+    per_call = merge_value_bytes(S, T, H) if fused else value_bytes(T, H)
     R = max(2, int(math.ceil(2.5 * L2_BYTES / per_call)))
     sets = value_sets(T, H, R, 5151 + rank, dev)
+    if fused:
+        merged = [workloads.merge_sets(1005 + 17 * r + 1000 * rank, S, T, H, device=dev) for r in range(R)]
+        sets = [(m[0], m[1], m[2], v[1], v[2]) for m, v in zip(merged, sets)]  # parts, lses, lens, w_uv, gate
     outs = [torch.empty((T, H * 128), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
     def call(i):
-        smla.smla_value_gate(*sets[i % R], outs[i % R])
+        if fused:
+            parts, lses, lens, w, gate = sets[i % R]
+            smla.smla_merge_value(parts, lses, lens, w, gate, outs[i % R])
+        else:
+            smla.smla_value_gate(*sets[i % R], outs[i % R])
 
     stream = torch.cuda.current_stream(dev)
     sampler = ClockSampler(local_rank)
@@ -989,18 +1007,29 @@ def run_value(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         # the weights stay resident (a layer's W_UV does not travel per call);
-        # the merged rows, gates and counts go up, the values come back
-        host = [(sets[k][0].cpu().pin_memory(), sets[k][2].cpu().pin_memory(), sets[k][3].cpu().pin_memory())
-                for k in range(R)]
-        dev_like = (sets[0][0], sets[0][2], sets[0][3])
+        # the rows (or partial sets), gates and counts go up, the values come back
+        if fused:
+            host = [(sets[k][0].cpu().pin_memory(), sets[k][1].cpu().pin_memory(), sets[k][2].cpu().pin_memory(),
+                     sets[k][4].cpu().pin_memory()) for k in range(R)]
+            dev_like = (sets[0][0], sets[0][1], sets[0][2], sets[0][4])
 
-        def e2e_run(inp, outp):
-            smla.smla_value_gate(inp[0], sets[0][1], inp[1], inp[2], outp[0])
+            def e2e_run(inp, outp):
+                smla.smla_merge_value(inp[0], inp[1], inp[2], sets[0][3], inp[3], outp[0])
 
+            h2d = S * T * H * (512 * 2 + 4) + T * H * 256 + 4 * T
+        else:
+            host = [(sets[k][0].cpu().pin_memory(), sets[k][2].cpu().pin_memory(), sets[k][3].cpu().pin_memory())
+                    for k in range(R)]
+            dev_like = (sets[0][0], sets[0][2], sets[0][3])
+
+            def e2e_run(inp, outp):
+                smla.smla_value_gate(inp[0], sets[0][1], inp[1], inp[2], outp[0])
+
+            h2d = T * H * 512 * 2 + T * H * 256 + 4 * T
         e_ms = pipelined_e2e(torch, host, dev_like, e2e_run, (outs[0],), min(args.steps, 100))
         e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(T * H * 512 * 2 + T * H * 256 + 4 * T),
+               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(T * H * 256),
                "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA "
                            "graph; W_UV resident"}
@@ -1008,59 +1037,86 @@ def run_value(args, rank, world, local_rank):
         return
     cpu = None
     if not args.no_cpu:
-        cpu = value_cpu_rate(sets[0], args.cpu_seconds)
+        cpu = value_cpu_rate(sets[0], args.cpu_seconds, fused)
     peak, peak_src = measured_hbm_peak()
+    config = "merge_value" if fused else "value"
+    if fused:
+        workload = (f"merge_value_s{S}_t{T}_h{H}: 8 partial sets (BF16 rows N(0, 1), base-2 LSEs with empty "
+                    f"sources), W_UV N(0, 1/512), gates N(0, 4)")
+        shape = {"sources": S, "tokens": T, "heads": H, "latent": 512, "values": 128}
+    else:
+        workload = f"value_gate_t{T}_h{H}: merged BF16 rows N(0, 1), W_UV N(0, 1/512), gates N(0, 4)"
+        shape = {"tokens": T, "heads": H, "latent": 512, "values": 128}
     line = {
-        "metric": VALUE_METRIC, "value": round(per_call * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "metric": MERGE_VALUE_METRIC if fused else VALUE_METRIC,
+        "value": round(per_call * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
         "us_per_call": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"value_gate_t{T}_h{H}: merged BF16 rows N(0, 1), W_UV N(0, 1/512), gates N(0, 4)",
-                   "tokens": T, "heads": H, "latent": 512, "values": 128, "input_sets": R,
+        "config": {"workload": workload, **shape, "input_sets": R,
                    "l2": "rotating %d input sets, W_UV included (%.1f MB per call)" % (R, per_call / 1e6),
                    "launch": "one CUDA graph of the %d timed library calls, replayed once" % args.steps},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic("value"),
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic(config),
                      "bytes_alg_per_launch": int(per_call)},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
 
 
-def value_cpu_rate(first_set, seconds: float):
-    """The oracle's projection and gate on the host (one thread) over a
-    bounded sample of tokens."""
+def value_cpu_rate(first_set, seconds: float, fused=False):
+    """The oracle's projection and gate (after its merge, when fused) on the
+    host over a bounded sample of tokens."""
     from oracle import oracle
 
     oracle.build()
-    latent, w, gate, lens = (x.cpu() for x in first_set)
-    T, H, _ = latent.shape
-    lat_b = latent.view(torch_int16()).numpy().view(np.uint16)
+    if fused:
+        parts, lses, lens, w, gate = (x.cpu() for x in first_set)
+        S, T, H, _ = parts.shape
+        p_b = parts.view(torch_int16()).numpy().view(np.uint16)
+    else:
+        latent, w, gate, lens = (x.cpu() for x in first_set)
+        T, H, _ = latent.shape
+        lat_b = latent.view(torch_int16()).numpy().view(np.uint16)
     w_b = w.view(torch_int16()).numpy().view(np.uint16)
     g_b = gate.view(torch_int16()).numpy().view(np.uint16)
     rng = np.random.default_rng(4)
     done, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < seconds and done < T:
         rows = rng.integers(0, T, 2)
-        oracle.value_gate(lat_b[rows], w_b, g_b[rows], lens.numpy()[rows])
+        if fused:
+            _, m_bits, _ = oracle.merge(oracle.MergeProblem(p_b[:, rows], lses.numpy()[:, rows],
+                                                            lens.numpy()[rows]), threads=oracle.max_threads())
+            oracle.value_gate(m_bits.reshape(2, H, 512), w_b, g_b[rows], lens.numpy()[rows])
+        else:
+            oracle.value_gate(lat_b[rows], w_b, g_b[rows], lens.numpy()[rows])
         done += 2
     per_call = (time.perf_counter() - t0) / done * T
-    return {"value": round(value_bytes(T, H) / per_call / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} of {T} tokens, all heads, in batches of 2", "us_per_call": round(per_call * 1e6, 1)}
+    total = merge_value_bytes(S, T, H) if fused else value_bytes(T, H)
+    return {"value": round(total / per_call / 1e9, 6), "unit": "GB/s", "cores": oracle.max_threads() if fused else 1,
+            "kind": "oracle", "sample": f"{done} of {T} tokens, all heads, in batches of 2",
+            "us_per_call": round(per_call * 1e6, 1)}
 
 
-def run_value_reference(args, rank, world):
+def run_value_reference(args, rank, world, fused=False):
     if rank != 0:
         return
-    T, H = 64, 128
+    from sparse_mla_decode_gb300 import workloads
+
+    S, T, H = 8, 64, 128
     first = value_sets(T, H, 1, 5151, "cpu")[0]
+    if fused:
+        m = workloads.merge_sets(1005, S, T, H)
+        first = (m[0], m[1], m[2], first[1], first[2])
     total = max(1, args.steps + args.warmup)
-    cpu = value_cpu_rate(first, min(60.0, 2.0 * total) / total * args.steps)
+    cpu = value_cpu_rate(first, min(60.0, 2.0 * total) / total * args.steps, fused)
+    name = f"merge_value_s{S}_t{T}_h{H}" if fused else f"value_gate_t{T}_h{H}"
     line = {
-        "metric": VALUE_METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "metric": MERGE_VALUE_METRIC if fused else VALUE_METRIC, "value": cpu["value"], "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(cpu["us_per_call"] / 1e3, 3), "us_per_call": cpu["us_per_call"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "impl": "reference", "config": {"workload": f"value_gate_t{T}_h{H}", "tokens": T, "heads": H},
+        "impl": "reference", "config": {"workload": name, "tokens": T, "heads": H, **({"sources": S} if fused else {})},
         "cpu_baseline": cpu,
         "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -1104,8 +1160,8 @@ def main():
             run_merge_reference(args, rank, world)
         elif args.config == "mxfp4":
             run_mxfp4_reference(args, rank, world)
-        elif args.config == "value":
-            run_value_reference(args, rank, world)
+        elif args.config in ("value", "merge_value"):
+            run_value_reference(args, rank, world, fused=args.config == "merge_value")
         else:
             run_reference(args, rank, world)
         return
@@ -1120,8 +1176,8 @@ def main():
             run_merge(args, rank, world, local_rank)
         elif args.config == "mxfp4":
             run_mxfp4(args, rank, world, local_rank)
-        elif args.config == "value":
-            run_value(args, rank, world, local_rank)
+        elif args.config in ("value", "merge_value"):
+            run_value(args, rank, world, local_rank, fused=args.config == "merge_value")
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -257,6 +257,43 @@ typedef struct smla_value_shape {
 int smla_value_gate(const smla_value_shape* shape, const void* latent, const void* w_uv, const void* gate,
                     const int32_t* lens, void* out, void* stream);
 
+/* The merge and the projection in one pass, as the page's owner runs them
+ * (DcpValue: the LSE merge of the partial sets into shared memory, then W_UV
+ * and the gate): for each (token, head) the row smla_merge would write, kept
+ * on chip, then the projection and gate of smla_value_gate. out equals
+ * smla_value_gate of smla_merge's out bit for bit. */
+typedef struct smla_merge_value_shape {
+    int32_t sources;  /* S partial sets (0: every row is empty) */
+    int32_t tokens;   /* T */
+    int32_t heads;    /* H */
+    int32_t reserved; /* 0 */
+    /* BF16 elements between consecutive sources / tokens / heads of `parts`
+     * (non-negative multiples of 8; the 512 latents of a row are contiguous) */
+    int64_t part_stride_source, part_stride_token, part_stride_head;
+    /* float elements between consecutive sources / tokens of `lses` (heads contiguous) */
+    int64_t lse_stride_source, lse_stride_token;
+    int64_t gate_stride_token; /* BF16 elements (multiple of 8, >= H*128); H*128 contiguous */
+    int64_t out_stride_token;  /* BF16 elements (multiple of 8, >= H*128); H*128 contiguous */
+} smla_merge_value_shape;
+
+/* Merges, projects and gates.
+ *   parts   device, BF16 [S, T, H, 512] at the shape's strides, 16-byte aligned.
+ *   lses    device, float [S, T, H] base-2 LSEs at the shape's strides.
+ *   lens    device, int32 [T] counts (<= 0: the token is empty), or NULL.
+ *   w_uv    device, BF16 [H, 512, 128], contiguous, 16-byte aligned.
+ *   gate    device, BF16 [T, H*128], 16-byte aligned.
+ *   out     device, BF16 [T, H*128], 16-byte aligned; must not overlap the inputs.
+ * Every buffer belongs to the caller; nothing is allocated. Launched with
+ * programmatic dependent launch; captureable in a CUDA graph. A bounded wait
+ * that gives up sets SMLA_DEV_TIMEOUT in the word smla_value_gate_error reads.
+ * Errors: SMLA_EINVAL (null buffers, negative sizes or strides, misaligned
+ * rows, gate or out token strides below H*128 or not multiples of 8),
+ * SMLA_EUNSUPPORTED (S above 64, T above 65535 * 64 or H above 65535, no
+ * tensor-map encoder) before any launch; SMLA_ECUDA when the launch fails.
+ * T = 0 or H = 0 launches nothing. */
+int smla_merge_value(const smla_merge_value_shape* shape, const void* parts, const float* lses,
+                     const int32_t* lens, const void* w_uv, const void* gate, void* out, void* stream);
+
 /* Reads and clears the value kernel's error word (SMLA_DEV_* bits) after
  * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
 int smla_value_gate_error(int32_t* bits);

@@ -11,10 +11,12 @@ from .smla import (  # noqa: F401
     load,
     make_shape,
     merge,
+    merge_value,
     mxfp4_q_quant,
     smla_decode,
     smla_device_error,
     smla_merge,
+    smla_merge_value,
     smla_mxfp4_q_quant,
     smla_plan_for,
     smla_value_gate,

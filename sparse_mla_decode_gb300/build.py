@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(BUILD_DIR, "libsmla.so")
 SOURCES = [os.path.join(CSRC, n) for n in ("smla_decode.cu", "smla_merge.cu", "smla_quant.cu", "smla_value.cu")]
-HEADERS = [os.path.join(CSRC, "smla_ptx.cuh"), os.path.join(INCLUDE, "smla.h")]
+HEADERS = [os.path.join(CSRC, n) for n in ("smla_ptx.cuh", "smla_merge_row.cuh")] + [os.path.join(INCLUDE, "smla.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

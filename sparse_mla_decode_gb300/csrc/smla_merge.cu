@@ -21,6 +21,7 @@
 #include <cstring>
 
 #include "smla.h"
+#include "smla_merge_row.cuh"
 
 namespace smla {
 void note_cuda_error(int code);  // the thread's last CUDA error, for smla_last_cuda_error
@@ -34,54 +35,14 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kGroup = 4;  // sources whose row loads are in flight together
 
 struct Params {
-    const __nv_bfloat16* parts;
-    int64_t part_stride_source, part_stride_token, part_stride_head;  // elements
-    const float* lses;
-    int64_t lse_stride_source, lse_stride_token;  // elements (heads contiguous)
-    const int32_t* lens;                           // [tokens] or null
+    smla::MergeInputs merge;  // the partial sets and their base-2 LSEs
+    const int32_t* lens;      // [tokens] or null
     __nv_bfloat16* out;
     int64_t out_stride_token, out_stride_head;  // elements
     float* lse_out;                             // or null
     int64_t lse_out_stride_token;
-    int32_t sources, tokens, heads;
+    int32_t tokens, heads;
 };
-
-__device__ __forceinline__ uint4 load_nc(const void* ptr) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr));
-    return v;
-}
-
-__device__ __forceinline__ float exp2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// acc[0..7] += w * the eight BF16 values of v
-__device__ __forceinline__ void add_weighted(float* acc, float w, const uint4& v) {
-    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 two;
-        memcpy(&two, &words[e], 4);
-        const float2 f = __bfloat1622float2(two);
-        acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
-    }
-}
-
-__device__ __forceinline__ uint4 pack_bf16(const float* x) {
-    uint32_t words[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 two = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-        memcpy(&words[e], &two, 4);
-    }
-    return make_uint4(words[0], words[1], words[2], words[3]);
-}
 
 __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_constant__ Params p) {
     const int lane = threadIdx.x & 31;
@@ -93,68 +54,12 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_consta
     for (int64_t row = first; row < rows; row += step) {
         const int t = static_cast<int>(row / p.heads), h = static_cast<int>(row % p.heads);
         const bool live = p.lens == nullptr || p.lens[t] > 0;
-        const float* lse_th = p.lses + static_cast<int64_t>(t) * p.lse_stride_token + h;
-
-        // the largest finite LSE and the sum of the weights (lanes stride the sources)
-        float top = -INFINITY;
-        if (live)
-            for (int s = lane; s < p.sources; s += 32) {
-                const float l = lse_th[s * p.lse_stride_source];
-                if (isfinite(l)) top = fmaxf(top, l);
-            }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) top = fmaxf(top, __shfl_xor_sync(0xFFFFFFFFu, top, o));
-        float total = 0.0f;
-        if (top != -INFINITY)
-            for (int s = lane; s < p.sources; s += 32) {
-                const float l = lse_th[s * p.lse_stride_source];
-                if (isfinite(l)) total += exp2_approx(l - top);
-            }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
-
-        float acc[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-        if (total > 0.0f) {
-            const float inverse = 1.0f / total;
-            const __nv_bfloat16* base = p.parts + static_cast<int64_t>(t) * p.part_stride_token +
-                                        static_cast<int64_t>(h) * p.part_stride_head + 16 * lane;
-            int s = 0;
-            for (; s + kGroup <= p.sources; s += kGroup) {  // kGroup sources' loads in flight
-                float w[kGroup];
-                uint4 v[2 * kGroup];
-#pragma unroll
-                for (int k = 0; k < kGroup; ++k) {
-                    const float l = lse_th[(s + k) * p.lse_stride_source];
-                    w[k] = isfinite(l) ? exp2_approx(l - top) * inverse : 0.0f;
-                    if (w[k] != 0.0f) {  // the same for every lane: an empty source's row is never read
-                        const __nv_bfloat16* src = base + (s + k) * p.part_stride_source;
-                        v[2 * k] = load_nc(src);
-                        v[2 * k + 1] = load_nc(src + 8);
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < kGroup; ++k)
-                    if (w[k] != 0.0f) {
-                        add_weighted(acc, w[k], v[2 * k]);
-                        add_weighted(acc + 8, w[k], v[2 * k + 1]);
-                    }
-            }
-            for (; s < p.sources; ++s) {
-                const float l = lse_th[s * p.lse_stride_source];
-                const float w = isfinite(l) ? exp2_approx(l - top) * inverse : 0.0f;
-                if (w != 0.0f) {
-                    const __nv_bfloat16* src = base + s * p.part_stride_source;
-                    add_weighted(acc, w, load_nc(src));
-                    add_weighted(acc + 8, w, load_nc(src + 8));
-                }
-            }
-        }
+        float top, acc[16];
+        const float total = smla::merge_row<kGroup>(p.merge, t, h, lane, live, top, acc);
         __nv_bfloat16* dst = p.out + static_cast<int64_t>(t) * p.out_stride_token +
                              static_cast<int64_t>(h) * p.out_stride_head + 16 * lane;
-        reinterpret_cast<uint4*>(dst)[0] = pack_bf16(acc);
-        reinterpret_cast<uint4*>(dst)[1] = pack_bf16(acc + 8);
+        reinterpret_cast<uint4*>(dst)[0] = smla::pack_bf16(acc);
+        reinterpret_cast<uint4*>(dst)[1] = smla::pack_bf16(acc + 8);
         if (p.lse_out != nullptr && lane == 0)
             p.lse_out[static_cast<int64_t>(t) * p.lse_out_stride_token + h] =
                 total > 0.0f ? top + log2f(total) : -INFINITY;
@@ -195,20 +100,14 @@ extern "C" int smla_merge(const smla_merge_shape* shape, const void* parts, cons
 
     Params p;
     std::memset(&p, 0, sizeof(p));
-    p.parts = static_cast<const __nv_bfloat16*>(parts);
-    p.part_stride_source = s.part_stride_source;
-    p.part_stride_token = s.part_stride_token;
-    p.part_stride_head = s.part_stride_head;
-    p.lses = lses;
-    p.lse_stride_source = s.lse_stride_source;
-    p.lse_stride_token = s.lse_stride_token;
+    p.merge = {static_cast<const __nv_bfloat16*>(parts), s.part_stride_source, s.part_stride_token,
+               s.part_stride_head, lses, s.lse_stride_source, s.lse_stride_token, s.sources};
     p.lens = lens;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.out_stride_token = s.out_stride_token;
     p.out_stride_head = s.out_stride_head;
     p.lse_out = lse_out;
     p.lse_out_stride_token = s.lse_out_stride_token;
-    p.sources = s.sources;
     p.tokens = s.tokens;
     p.heads = s.heads;
 

@@ -19,6 +19,13 @@
 // each per lane) round, gate and write the values into the gate tile in
 // place, and one TMA store writes the tile out (rows past the token count are
 // clipped).
+//
+// The fused entry point (smla_merge_value) takes the partial sets instead of
+// merged rows, as the page's owner does: its sixteen warps LSE-merge the 64
+// rows of the tile straight into the swizzled B tile (a warp per row, 16
+// latents per lane, the merge kernel's own row code, so the rows carry the
+// same bits as smla_merge's), while TMA brings W_UV and the gates; the product
+// and the epilogue are the same.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -30,6 +37,7 @@
 #include <cstring>
 
 #include "smla.h"
+#include "smla_merge_row.cuh"
 #include "smla_ptx.cuh"
 
 namespace smla {
@@ -45,7 +53,6 @@ constexpr int kTile = 64;   // tokens per CTA (N)
 constexpr int kJ = 512;     // latents (K)
 constexpr int kV = 128;     // values per head (M)
 constexpr int kBlocks = kJ / 64;              // 64-latent blocks, one swizzle atom wide
-constexpr int kThreads = 256;  // 8 warps: thread 0 issues TMA and MMA; all eight run the epilogue
 constexpr int kWBlockBytes = 64 * kV * 2;     // 64 latent rows x 128 values: two 8 KB MN atoms
 constexpr int kLBlockBytes = kTile * 128;     // 64 tokens x 64 latents
 constexpr int kGateBytes = kTile * kV * 2;    // 64 tokens x 128 values, unswizzled
@@ -55,14 +62,17 @@ constexpr int kG = kL + kBlocks * kLBlockBytes;
 constexpr int kBar = kG + kGateBytes;
 constexpr int kMisc = kBar + 8 * (kBlocks + 2);
 constexpr int kAlloc = kMisc + 16 + 1024;
+constexpr int kWarps = 8;  // thread 0 issues the copies and the products; all eight run the epilogue
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct Params {
     CUtensorMap latent;  // {512 latents, H heads, T tokens} BF16, 128-byte swizzle, boxes of 64 x 1 x 64
+                         // (fused: the partial sets, {512 latents, H, T, S sources}, boxes of 64 x 1 x 64 x 1)
     CUtensorMap w_uv;    // {64 values, 512 latents, 2 value halves, H heads} BF16, 128-byte swizzle, boxes of 64 x 64 x 2 x 1
     CUtensorMap gate;    // {H * 128, T} BF16, boxes of 128 x 64
     CUtensorMap out;     // {H * 128, T} BF16, boxes of 128 x 64
     const int32_t* lens; // [T] or null
+    MergeInputs merge;   // fused: the partial sets (for the weights; the rows come by TMA)
     int32_t tokens, heads;
 };
 
@@ -125,7 +135,55 @@ __device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_constant__ Params p) {
+// The epilogue of a CTA's tile: kEpiWarps warps (4 or 16) read D back from
+// TMEM, warp w reading lanes 32 (w % 4) .. + 31, so that thread (w, lane) owns
+// value v = 32 (w % 4) + lane of the kEpiWarps-dependent run of tokens from
+// tb; they round, gate and write the values into the gate tile in place.
+// Bit t of `live` says whether token tb + t has keys. Returns false if a
+// bounded wait gave up.
+template <int kEpiWarps>
+__device__ __forceinline__ bool gate_epilogue(const Params& p, uint32_t tile, uint32_t tmem, uint64_t* mma_done,
+                                              uint64_t* gate_full, volatile int* abort_flag, int t0, int warp,
+                                              int lane) {
+    constexpr int kTokensPerWarp = kTile * 4 / kEpiWarps;
+    const int v = 32 * (warp & 3) + lane;
+    const int tb = kTokensPerWarp * (warp >> 2);
+    const int t_lane = t0 + tb + (lane % kTokensPerWarp);
+    const uint32_t live =
+        __ballot_sync(~0u, t_lane < p.tokens && (p.lens == nullptr || p.lens[t_lane] > 0));
+    bool ok = mbar_wait_bounded(mma_done, 0, abort_flag, kWaitLimitNs);
+    ok &= mbar_wait_bounded(gate_full, 0, abort_flag, kWaitLimitNs);
+    __syncwarp();
+    tc_fence_after_sync();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    float acc[kTokensPerWarp];
+    const uint32_t col = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + tb;
+    if constexpr (kTokensPerWarp == 32) {
+        tmem_load16x2(col, col + 16, acc);
+    } else {
+        tmem_load16x1(col, acc);
+    }
+    const uint32_t slot = tile + static_cast<uint32_t>(tb * kV + v) * 2;  // gate / value of token tb
+    uint32_t bits[kTokensPerWarp];
+#pragma unroll
+    for (int t = 0; t < kTokensPerWarp; ++t) bits[t] = lds_u16(slot + t * kV * 2);
+#pragma unroll
+    for (int t = 0; t < kTokensPerWarp; ++t) {
+        const float gate = __uint_as_float(bits[t] << 16);
+        const float rounded = __bfloat162float(__float2bfloat16_rn(acc[t]));
+        // sigmoid(g) = 1 / (1 + e^-g), in FP32 to a few ulp (the value is then
+        // rounded to BF16, 2^-8 relative)
+        const float y = rounded * rcp_approx(1.0f + __expf(-gate));
+        bits[t] = (live >> t) & 1u ? __bfloat16_as_ushort(__float2bfloat16_rn(y)) : 0u;
+    }
+#pragma unroll
+    for (int t = 0; t < kTokensPerWarp; ++t) sts_u16(slot + t * kV * 2, bits[t]);
+    fence_proxy_async_smem();  // the values, written by threads, are read by the TMA store
+    return ok;
+}
+
+__global__ void __launch_bounds__(32 * kWarps, 1) value_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -191,40 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_co
         mma_commit(mma_done);
     }
     __syncwarp();
-
-    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, so thread (w,
-    // lane) owns value v = 32 (w % 4) + lane of the 32 tokens tb .. tb + 31,
-    // tb = 32 (w / 4); bit t of `live` says whether token tb + t has keys
-    const int v = 32 * (warp & 3) + lane;
-    const int tb = 32 * (warp >> 2);
-    const int t_lane = t0 + tb + lane;
-    const uint32_t live =
-        __ballot_sync(~0u, t_lane < p.tokens && (p.lens == nullptr || p.lens[t_lane] > 0));
-    ok &= mbar_wait_bounded(mma_done, 0, abort_flag, kWaitLimitNs);
-    ok &= mbar_wait_bounded(gate_full, 0, abort_flag, kWaitLimitNs);
-    __syncwarp();
-    tc_fence_after_sync();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    float acc[32];
-    const uint32_t col = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + tb;
-    tmem_load16x2(col, col + 16, acc);
-    const uint32_t slot = sbase + kG + static_cast<uint32_t>(tb * kV + v) * 2;  // gate / value of token tb
-    uint32_t bits[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) bits[t] = lds_u16(slot + t * kV * 2);
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-        const float gate = __uint_as_float(bits[t] << 16);
-        const float rounded = __bfloat162float(__float2bfloat16_rn(acc[t]));
-        // sigmoid(g) = 1 / (1 + e^-g), in FP32 to a few ulp (the value is then
-        // rounded to BF16, 2^-8 relative)
-        const float y = rounded * rcp_approx(1.0f + __expf(-gate));
-        bits[t] = (live >> t) & 1u ? __bfloat16_as_ushort(__float2bfloat16_rn(y)) : 0u;
-    }
-#pragma unroll
-    for (int t = 0; t < 32; ++t) sts_u16(slot + t * kV * 2, bits[t]);
-    fence_proxy_async_smem();  // the values, written by threads, are read by the TMA store
+    ok &= gate_epilogue<kWarps>(p, sbase + kG, tmem, mma_done, gate_full, abort_flag, t0, warp, lane);
     tc_fence_before_sync();
     __syncthreads();
     if (tid == 0) {
@@ -235,6 +260,230 @@ __global__ void __launch_bounds__(kThreads, 1) value_gate_kernel(const __grid_co
     }
     if (!ok && lane == 0) atomicOr(&g_value_error, SMLA_DEV_TIMEOUT);
     if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTile);
+    }
+}
+
+// ------------------------------------------------ fused merge + projection
+//
+// One CTA per (head, 64-token tile), 18 warps:
+//  - warps 0-15 (the consumers) first compute every row's merge weights into
+//    shared memory, then merge latent block by latent block: for block kb
+//    they take the S sources' 64-token boxes from a ring in chunks of four
+//    sources, thread c accumulating 8 latents (unit c % 8) of token c / 8 in
+//    FP32 with the merge's own operations in source order, and write the
+//    BF16 block into a 2-block B ring; at the end they run the epilogue;
+//  - warp 16 (the producer) streams the gate tile and then, block after
+//    block, the S boxes of partial rows into a ring of four 4-box chunks
+//    (128 KB in flight, what the HBM latency asks for at this SM's share of
+//    bandwidth), each chunk as soon as the consumers release it;
+//  - warp 17 (the MMA warp) owns TMEM, keeps W_UV's rows three blocks ahead
+//    in a 3-slot ring, and issues block kb's four products as soon as the
+//    block's B rows and W_UV rows are in; their completion frees both slots.
+namespace fz {
+constexpr int kConsumerWarps = 16;
+constexpr int kProducerWarp = 16, kMmaWarp = 17, kWarpsAll = 18;
+constexpr int kChunk = 4;                              // sources' boxes behind one barrier
+constexpr int kStages = 4, kWSlots = 3, kBSlots = 2;   // 4 chunks: 128 KB of partial rows in flight
+constexpr int kMaxSources = 64;
+constexpr int kW = 0;                                    // W_UV ring: 3 x 16 KB
+constexpr int kB = kW + kWSlots * kWBlockBytes;          // B ring: 2 x 8 KB
+constexpr int kP = kB + kBSlots * kLBlockBytes;          // partial-row ring: 4 chunks x 4 boxes x 8 KB
+constexpr int kG = kP + kStages * kChunk * kLBlockBytes; // gate / value tile: 16 KB
+constexpr int kWts = kG + kGateBytes;                    // weights: 64 tokens x S floats
+constexpr int kBar = kWts + kTile * kMaxSources * 4;
+constexpr int kNumBars = 2 * kStages + 2 * kWSlots + 2 * kBSlots + 2;
+constexpr int kMisc = kBar + 8 * kNumBars;
+constexpr int kAlloc = kMisc + 16 + 1024;
+}  // namespace fz
+
+__global__ void __launch_bounds__(32 * fz::kWarpsAll, 1) merge_value_kernel(const __grid_constant__ Params p) {
+    using namespace fz;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + fz::kBar);
+    uint64_t* full = bars;                          // [kStages] a chunk of partial rows landed (TMA bytes)
+    uint64_t* empty = full + kStages;               // [kStages] the consumers are done with it (16 warps)
+    uint64_t* w_full = empty + kStages;             // [kWSlots] W_UV rows landed (TMA bytes)
+    uint64_t* w_empty = w_full + kWSlots;           // [kWSlots] their products finished (commit)
+    uint64_t* b_ready = w_empty + kWSlots;          // [kBSlots] a B block written (16 warps)
+    uint64_t* b_empty = b_ready + kBSlots;          // [kBSlots] its products finished (commit)
+    uint64_t* gate_full = b_empty + kBSlots;        // the gate tile landed
+    uint64_t* mma_done = gate_full + 1;             // every product finished (commit)
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + fz::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    float* wts = reinterpret_cast<float*>(smem + kWts);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, t0 = blockIdx.y * kTile;
+    const int S = p.merge.sources;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, kConsumerWarps);
+        }
+        for (int i = 0; i < kWSlots; ++i) {
+            mbar_init(w_full + i, 1);
+            mbar_init(w_empty + i, 1);
+        }
+        for (int i = 0; i < kBSlots; ++i) {
+            mbar_init(b_ready + i, kConsumerWarps);
+            mbar_init(b_empty + i, 1);
+        }
+        mbar_init(gate_full, 1);
+        mbar_init(mma_done, 1);
+        misc[1] = 0;
+        mbar_init_fence();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        if (S > 0) prefetch_tensor_map(&p.latent);
+        prefetch_tensor_map(&p.w_uv);
+        prefetch_tensor_map(&p.gate);
+        prefetch_tensor_map(&p.out);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(misc, kTile);
+        tmem_relinquish();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    bool ok = true;
+    if (warp == kProducerWarp) {
+        // the consumers' count and LSE loads go out before the stream of rows
+        asm volatile("bar.sync 2, %0;" ::"r"(32 * (kConsumerWarps + 1)) : "memory");
+        if (lane == 0) {
+            mbar_arrive_expect_tx(gate_full, kGateBytes);
+            tma_load_2d(sbase + fz::kG, &p.gate, h * kV, t0, gate_full);
+            int n = 0;  // chunks of partial rows issued
+            for (int kb = 0; kb < kBlocks && ok; ++kb) {
+                for (int s0 = 0; s0 < S && ok; s0 += kChunk, ++n) {
+                    const int stage = n % kStages, boxes = min(kChunk, S - s0);
+                    if (n >= kStages)
+                        ok &= mbar_wait_bounded(empty + stage, (n / kStages - 1) & 1, abort_flag, kWaitLimitNs);
+                    mbar_arrive_expect_tx(full + stage, boxes * kLBlockBytes);
+                    for (int k = 0; k < boxes; ++k)
+                        tma_load_4d(sbase + kP + (stage * kChunk + k) * kLBlockBytes, &p.latent, kb * 64, h, t0,
+                                    s0 + k, full + stage);
+                }
+            }
+            if (!ok) *abort_flag = 1;
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            for (int kb = 0; kb < kWSlots; ++kb) {  // W_UV's first blocks
+                mbar_arrive_expect_tx(w_full + kb, kWBlockBytes);
+                tma_load_4d(sbase + fz::kW + kb * kWBlockBytes, &p.w_uv, 0, kb * 64, 0, h, w_full + kb);
+            }
+            constexpr uint32_t kIdesc = idesc_bf16(kV, kTile, 1, 0);
+            const uint64_t d_b = smem_desc(sbase + kB, 1024, 1024, kSwizzle128B);
+            for (int kb = 0; kb < kBlocks && ok; ++kb) {
+                const int slot = kb % kWSlots, bslot = kb % kBSlots;
+                ok &= mbar_wait_bounded(b_ready + bslot, (kb / kBSlots) & 1, abort_flag, kWaitLimitNs);
+                ok &= mbar_wait_bounded(w_full + slot, (kb / kWSlots) & 1, abort_flag, kWaitLimitNs);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint64_t d_a = smem_desc(sbase + fz::kW + slot * kWBlockBytes, kWBlockBytes / 2, 1024,
+                                               kSwizzle128B);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const uint32_t a_off = static_cast<uint32_t>(s4 * 16 * 128) >> 4;
+                    const uint32_t b_off = static_cast<uint32_t>(bslot * kLBlockBytes + s4 * 32) >> 4;
+                    mma_bf16(tmem, d_a + a_off, d_b + b_off, kIdesc, (kb | s4) != 0 ? 1u : 0u);
+                }
+                mma_commit(w_empty + slot);
+                mma_commit(b_empty + bslot);
+                if (kb + kWSlots < kBlocks) {  // refill the slot once these products have read it
+                    ok &= mbar_wait_bounded(w_empty + slot, (kb / kWSlots) & 1, abort_flag, kWaitLimitNs);
+                    mbar_arrive_expect_tx(w_full + slot, kWBlockBytes);
+                    tma_load_4d(sbase + fz::kW + slot * kWBlockBytes, &p.w_uv, 0, (kb + kWSlots) * 64, 0, h,
+                                w_full + slot);
+                }
+            }
+            mma_commit(mma_done);
+            if (!ok) *abort_flag = 1;
+        }
+        __syncwarp();
+    } else {
+        // the weights of the warp's rows warp, warp + 16, ... (one round of LSE loads)
+        constexpr int kRows = kTile / kConsumerWarps;
+        float l[kRows][2];
+        int count[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {  // the counts and the LSEs in one round of loads
+            const int tg = t0 + warp + kConsumerWarps * i;
+            const bool in = tg < p.tokens;
+            count[i] = in ? (p.lens == nullptr ? 1 : p.lens[tg]) : 0;
+            load_row_lses(p.merge, in ? tg : 0, h, lane, l[i]);
+        }
+        asm volatile("bar.arrive 2, %0;" ::"r"(32 * (kConsumerWarps + 1)) : "memory");
+#pragma unroll
+        for (int i = 0; i < kRows; ++i)
+            if (count[i] <= 0) empty_row_lses(l[i]);
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) merge_weights(l[i], S, lane, wts + (warp + kConsumerWarps * i) * S);
+        named_barrier(1, 32 * kConsumerWarps);
+
+        // then block by block, sources in order
+        const int t = tid >> 3, u = tid & 7;
+        const float* w_t = wts + t * S;
+        int n = 0;
+        for (int kb = 0; kb < kBlocks && ok; ++kb) {
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+            for (int s0 = 0; s0 < S; s0 += kChunk, ++n) {
+                const int stage = n % kStages, boxes = min(kChunk, S - s0);
+                ok &= mbar_wait_bounded(full + stage, (n / kStages) & 1, abort_flag, kWaitLimitNs);
+                if (!ok) break;
+                float w[kChunk];
+                uint4 x[kChunk];
+#pragma unroll
+                for (int k = 0; k < kChunk; ++k)
+                    if (k < boxes) {
+                        w[k] = w_t[s0 + k];
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(x[k].x), "=r"(x[k].y), "=r"(x[k].z), "=r"(x[k].w)
+                                     : "r"(sbase + kP + (stage * kChunk + k) * kLBlockBytes + t * 128 + u * 16));
+                    }
+#pragma unroll
+                for (int k = 0; k < kChunk; ++k)
+                    if (k < boxes && w[k] != 0.0f) add_weighted(acc, w[k], x[k]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + stage);
+            }
+            if (!ok) break;
+            const int bslot = kb % kBSlots;
+            if (kb >= kBSlots) {  // the products of block kb - 2 have read this slot
+                ok &= mbar_wait_bounded(b_empty + bslot, (kb / kBSlots - 1) & 1, abort_flag, kWaitLimitNs);
+                if (!ok) break;
+            }
+            const uint4 bf = pack_bf16(acc);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             sbase + kB + bslot * kLBlockBytes + t * 128 + ((u ^ (t & 7)) << 4)),
+                         "r"(bf.x), "r"(bf.y), "r"(bf.z), "r"(bf.w)
+                         : "memory");
+            fence_proxy_async_smem();  // the rows, written by threads, are read by the tensor cores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_ready + bslot);
+        }
+        if (!ok) *abort_flag = 1;
+        ok &= gate_epilogue<kConsumerWarps>(p, sbase + fz::kG, tmem, mma_done, gate_full, abort_flag, t0, warp, lane);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (tid == 0 && ok && *abort_flag == 0) {
+        tma_store_2d(&p.out, h * kV, t0, sbase + fz::kG);
+        tma_store_wait_read();
+    }
+    if (!ok && lane == 0) atomicOr(&g_value_error, SMLA_DEV_TIMEOUT);
+    if (warp == kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTile);
     }
@@ -252,35 +501,14 @@ bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims
 
 }  // namespace vgate
 
-extern "C" int smla_value_gate(const smla_value_shape* shape, const void* latent, const void* w_uv,
-                               const void* gate, const int32_t* lens, void* out, void* stream) {
-    using namespace vgate;
-    if (shape == nullptr) return SMLA_EINVAL;
-    const smla_value_shape& s = *shape;
-    if (s.tokens < 0 || s.heads < 0) return SMLA_EINVAL;
-    if (s.tokens == 0 || s.heads == 0) return SMLA_OK;
-    if (s.tokens > 65535 * kTile || s.heads > 65535) return SMLA_EUNSUPPORTED;
-    if (latent == nullptr || w_uv == nullptr || gate == nullptr || out == nullptr) return SMLA_EINVAL;
-    auto aligned16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
-    if (!aligned16(latent) || !aligned16(w_uv) || !aligned16(gate) || !aligned16(out)) return SMLA_EINVAL;
-    // latent rows may sit in any order (token- or head-major) as long as each
-    // row start is 16-byte aligned; output rows may not overlap
-    if (s.latent_stride_head <= 0 || s.latent_stride_token <= 0 || s.latent_stride_head >= (int64_t(1) << 36) ||
-        s.latent_stride_token >= (int64_t(1) << 36) || s.latent_stride_head % 8 || s.latent_stride_token % 8 ||
-        s.gate_stride_token < s.heads * kV ||
-        s.gate_stride_token % 8 || s.out_stride_token < s.heads * kV || s.out_stride_token % 8)
-        return SMLA_EINVAL;
+namespace vgate {
 
-    Params p;
-    std::memset(&p, 0, sizeof(p));
-    const cuuint64_t T = static_cast<cuuint64_t>(s.tokens), H = static_cast<cuuint64_t>(s.heads);
-    {
-        const cuuint64_t dims[3] = {kJ, H, T};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s.latent_stride_head) * 2,
-                                       static_cast<cuuint64_t>(s.latent_stride_token) * 2};
-        const cuuint32_t box[3] = {64, 1, kTile};
-        if (!encode(&p.latent, latent, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
-    }
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// The tensor maps of W_UV, the gates and the output.
+int encode_common(Params& p, const void* w_uv, const void* gate, int64_t gate_stride, void* out,
+                  int64_t out_stride, int tokens, int heads) {
+    const cuuint64_t T = static_cast<cuuint64_t>(tokens), H = static_cast<cuuint64_t>(heads);
     {
         // W_UV[h][j][v] as {64 values, 512 latents, 2 value halves, H}: one
         // box per 64-latent block lands as [value half][64 latents][64 values],
@@ -290,43 +518,123 @@ extern "C" int smla_value_gate(const smla_value_shape* shape, const void* latent
         const cuuint32_t box[4] = {64, 64, 2, 1};
         if (!encode(&p.w_uv, w_uv, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
     }
-    {
-        const cuuint64_t dims[2] = {H * kV, T};
-        const cuuint32_t box[2] = {kV, kTile};
-        const cuuint64_t gs[1] = {static_cast<cuuint64_t>(s.gate_stride_token) * 2};
-        const cuuint64_t os[1] = {static_cast<cuuint64_t>(s.out_stride_token) * 2};
-        if (!encode(&p.gate, gate, 2, dims, gs, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return SMLA_EUNSUPPORTED;
-        if (!encode(&p.out, out, 2, dims, os, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return SMLA_EUNSUPPORTED;
-    }
-    p.lens = lens;
-    p.tokens = s.tokens;
-    p.heads = s.heads;
+    const cuuint64_t dims[2] = {H * kV, T};
+    const cuuint32_t box[2] = {kV, kTile};
+    const cuuint64_t gs[1] = {static_cast<cuuint64_t>(gate_stride) * 2};
+    const cuuint64_t os[1] = {static_cast<cuuint64_t>(out_stride) * 2};
+    if (!encode(&p.gate, gate, 2, dims, gs, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return SMLA_EUNSUPPORTED;
+    if (!encode(&p.out, out, 2, dims, os, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return SMLA_EUNSUPPORTED;
+    p.tokens = tokens;
+    p.heads = heads;
+    return SMLA_OK;
+}
 
-    static bool configured[64] = {};
+// gate / out / W_UV checks shared by both entry points
+bool bad_projection_args(int heads, const void* w_uv, const void* gate, int64_t gate_stride, const void* out,
+                         int64_t out_stride) {
+    return w_uv == nullptr || gate == nullptr || out == nullptr || !aligned16(w_uv) || !aligned16(gate) ||
+           !aligned16(out) || gate_stride < static_cast<int64_t>(heads) * kV || gate_stride % 8 ||
+           out_stride < static_cast<int64_t>(heads) * kV || out_stride % 8;
+}
+
+template <typename Kernel>
+int launch(Kernel kernel, int threads, int smem_bytes, bool* configured, const Params& p, void* stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(value_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e == cudaSuccess) configured[dev] = true;
     }
     if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(s.heads), static_cast<unsigned>((s.tokens + kTile - 1) / kTile), 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kAlloc;
+        cfg.gridDim = dim3(static_cast<unsigned>(p.heads), static_cast<unsigned>((p.tokens + kTile - 1) / kTile), 1);
+        cfg.blockDim = dim3(threads, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes;
         cfg.stream = static_cast<cudaStream_t>(stream);
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, value_gate_kernel, p);
+        e = cudaLaunchKernelEx(&cfg, kernel, p);
     }
     if (e != cudaSuccess) {
         smla::note_cuda_error(static_cast<int>(e));
         return SMLA_ECUDA;
     }
     return SMLA_OK;
+}
+
+bool g_configured_value[64] = {}, g_configured_fused[64] = {};
+
+}  // namespace vgate
+
+extern "C" int smla_value_gate(const smla_value_shape* shape, const void* latent, const void* w_uv,
+                               const void* gate, const int32_t* lens, void* out, void* stream) {
+    using namespace vgate;
+    if (shape == nullptr) return SMLA_EINVAL;
+    const smla_value_shape& s = *shape;
+    if (s.tokens < 0 || s.heads < 0) return SMLA_EINVAL;
+    if (s.tokens == 0 || s.heads == 0) return SMLA_OK;
+    if (s.tokens > 65535 * kTile || s.heads > 65535) return SMLA_EUNSUPPORTED;
+    if (latent == nullptr || !aligned16(latent) ||
+        bad_projection_args(s.heads, w_uv, gate, s.gate_stride_token, out, s.out_stride_token))
+        return SMLA_EINVAL;
+    // latent rows may sit in any order (token- or head-major) as long as each
+    // row start is 16-byte aligned
+    if (s.latent_stride_head <= 0 || s.latent_stride_token <= 0 || s.latent_stride_head >= (int64_t(1) << 36) ||
+        s.latent_stride_token >= (int64_t(1) << 36) || s.latent_stride_head % 8 || s.latent_stride_token % 8)
+        return SMLA_EINVAL;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    {
+        const cuuint64_t dims[3] = {kJ, static_cast<cuuint64_t>(s.heads), static_cast<cuuint64_t>(s.tokens)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(s.latent_stride_head) * 2,
+                                       static_cast<cuuint64_t>(s.latent_stride_token) * 2};
+        const cuuint32_t box[3] = {64, 1, kTile};
+        if (!encode(&p.latent, latent, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return SMLA_EUNSUPPORTED;
+    }
+    const int rc = encode_common(p, w_uv, gate, s.gate_stride_token, out, s.out_stride_token, s.tokens, s.heads);
+    if (rc != SMLA_OK) return rc;
+    p.lens = lens;
+    return launch(value_kernel, 32 * kWarps, kAlloc, g_configured_value, p, stream);
+}
+
+extern "C" int smla_merge_value(const smla_merge_value_shape* shape, const void* parts, const float* lses,
+                                const int32_t* lens, const void* w_uv, const void* gate, void* out, void* stream) {
+    using namespace vgate;
+    if (shape == nullptr) return SMLA_EINVAL;
+    const smla_merge_value_shape& s = *shape;
+    if (s.sources < 0 || s.tokens < 0 || s.heads < 0) return SMLA_EINVAL;
+    if (s.tokens == 0 || s.heads == 0) return SMLA_OK;
+    if (s.tokens > 65535 * kTile || s.heads > 65535 || s.sources > fz::kMaxSources) return SMLA_EUNSUPPORTED;
+    if (bad_projection_args(s.heads, w_uv, gate, s.gate_stride_token, out, s.out_stride_token)) return SMLA_EINVAL;
+    if (s.sources > 0 && (parts == nullptr || lses == nullptr || !aligned16(parts))) return SMLA_EINVAL;
+    if (s.part_stride_source < 0 || s.part_stride_token < 0 || s.part_stride_head < 0 || s.lse_stride_source < 0 ||
+        s.lse_stride_token < 0 || s.part_stride_source % 8 || s.part_stride_token % 8 || s.part_stride_head % 8 ||
+        (s.heads > 1 && s.sources > 0 && s.part_stride_head < kJ))
+        return SMLA_EINVAL;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    const int rc = encode_common(p, w_uv, gate, s.gate_stride_token, out, s.out_stride_token, s.tokens, s.heads);
+    if (rc != SMLA_OK) return rc;
+    p.lens = lens;
+    p.merge = {static_cast<const __nv_bfloat16*>(parts), s.part_stride_source, s.part_stride_token,
+               s.part_stride_head, lses, s.lse_stride_source, s.lse_stride_token, s.sources};
+    if (s.sources > 0) {
+        // the partial rows as {512 latents, H, T, S}: a box is 64 latents of
+        // the tile's 64 tokens of one head and source, unswizzled
+        const cuuint64_t dims[4] = {kJ, static_cast<cuuint64_t>(s.heads), static_cast<cuuint64_t>(s.tokens),
+                                    static_cast<cuuint64_t>(s.sources)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.part_stride_head) * 2,
+                                       static_cast<cuuint64_t>(s.part_stride_token) * 2,
+                                       static_cast<cuuint64_t>(s.part_stride_source) * 2};
+        const cuuint32_t box[4] = {64, 1, kTile, 1};
+        if (!encode(&p.latent, parts, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return SMLA_EUNSUPPORTED;
+    }
+    return launch(merge_value_kernel, 32 * fz::kWarpsAll, fz::kAlloc, g_configured_fused, p, stream);
 }
 
 extern "C" int smla_value_gate_error(int32_t* bits) {

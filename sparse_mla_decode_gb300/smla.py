@@ -75,6 +75,17 @@ class SmlaValueShape(ctypes.Structure):
     ]
 
 
+class SmlaMergeValueShape(ctypes.Structure):
+    _fields_ = [
+        ("sources", ctypes.c_int32), ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("part_stride_source", ctypes.c_int64), ("part_stride_token", ctypes.c_int64),
+        ("part_stride_head", ctypes.c_int64),
+        ("lse_stride_source", ctypes.c_int64), ("lse_stride_token", ctypes.c_int64),
+        ("gate_stride_token", ctypes.c_int64), ("out_stride_token", ctypes.c_int64),
+    ]
+
+
 DTYPE_BF16 = 1
 DTYPE_F32 = 2
 VALUE_DIM = 128
@@ -123,6 +134,8 @@ def load(path: str | None = None):
         lib.smla_mxfp4_q_quant.restype = i32
         lib.smla_value_gate.argtypes = [ctypes.POINTER(SmlaValueShape), vp, vp, vp, vp, vp, vp]
         lib.smla_value_gate.restype = i32
+        lib.smla_merge_value.argtypes = [ctypes.POINTER(SmlaMergeValueShape), vp, vp, vp, vp, vp, vp, vp]
+        lib.smla_merge_value.restype = i32
         lib.smla_value_gate_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
         lib.smla_value_gate_error.restype = i32
         _lib = lib
@@ -351,3 +364,47 @@ def smla_value_gate_error() -> int:
     if rc != OK:
         raise SmlaError(rc, "smla_value_gate_error")
     return int(bits.value)
+
+
+def smla_merge_value(parts: torch.Tensor, lses: torch.Tensor, lens: torch.Tensor | None, w_uv: torch.Tensor,
+                     gate: torch.Tensor, out: torch.Tensor, stream=None):
+    """The LSE merge, the W_UV projection and the gate in one pass through the
+    C ABI (see ``smla_merge_value`` in smla.h). parts: bfloat16 [S, T, H, 512],
+    latents contiguous; lses: float32 [S, T, H], heads contiguous; lens: int32
+    [T] or None; w_uv: bfloat16 [H, 512, 128] contiguous; gate and out:
+    bfloat16 [T, H*128], rows contiguous."""
+    lib = load()
+    S, T, H, J = parts.shape
+    if J != LATENT or tuple(lses.shape) != (S, T, H):
+        raise ValueError("merge_value: parts [S, T, H, 512], lses [S, T, H]")
+    if parts.dtype != torch.bfloat16 or lses.dtype != torch.float32 or w_uv.dtype != torch.bfloat16 \
+            or gate.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("merge_value: dtypes")
+    if tuple(w_uv.shape) != (H, LATENT, VALUE_DIM) or tuple(gate.shape) != (T, H * VALUE_DIM) \
+            or tuple(out.shape) != (T, H * VALUE_DIM):
+        raise ValueError("merge_value: shapes")
+    if parts.stride(3) != 1 or (H > 1 and lses.stride(2) != 1) or not w_uv.is_contiguous() \
+            or gate.stride(1) != 1 or out.stride(1) != 1:
+        raise ValueError("merge_value: inner dimensions must be contiguous")
+    if lens is not None and (lens.dtype != torch.int32 or tuple(lens.shape) != (T,) or lens.stride(0) != 1):
+        raise ValueError("merge_value: lens must be contiguous int32 [T]")
+    shape = SmlaMergeValueShape()
+    shape.sources, shape.tokens, shape.heads, shape.reserved = S, T, H, 0
+    shape.part_stride_source, shape.part_stride_token, shape.part_stride_head = parts.stride()[:3]
+    shape.lse_stride_source, shape.lse_stride_token = lses.stride()[:2]
+    shape.gate_stride_token, shape.out_stride_token = gate.stride(0), out.stride(0)
+    if stream is None:
+        stream = torch.cuda.current_stream(out.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib.smla_merge_value(ctypes.byref(shape), _ptr(parts), _ptr(lses), _ptr(lens), _ptr(w_uv), _ptr(gate),
+                              _ptr(out), ctypes.c_void_p(handle))
+    if rc != OK:
+        raise SmlaError(rc, "smla_merge_value")
+    return out
+
+
+def merge_value(parts, lses, w_uv, gate, lens=None, stream=None):
+    """Allocates the output on parts' device and calls :func:`smla_merge_value`."""
+    _, T, H, _ = parts.shape
+    out = torch.empty((T, H * VALUE_DIM), dtype=torch.bfloat16, device=parts.device)
+    return smla_merge_value(parts, lses, lens, w_uv, gate, out, stream=stream)

@@ -196,3 +196,36 @@ def test_value_gate_rejects_bad_arguments_before_any_launch(lib, kw, ptrs):
 def test_value_gate_of_nothing_is_ok_without_a_device(lib):
     assert lib.smla_value_gate(ctypes.byref(_value_shape(tokens=0)), None, None, None, None, None, None) == smla.OK
     assert lib.smla_value_gate(ctypes.byref(_value_shape(heads=0)), None, None, None, None, None, None) == smla.OK
+
+
+def _merge_value_shape(**kw):
+    s = smla.SmlaMergeValueShape()
+    base = dict(sources=2, tokens=3, heads=4, part_stride_source=3 * 4 * 512, part_stride_token=4 * 512,
+                part_stride_head=512, lse_stride_source=12, lse_stride_token=4, gate_stride_token=4 * 128,
+                out_stride_token=4 * 128)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(s, k, v)
+    return s
+
+
+@pytest.mark.parametrize("kw,ptrs", [
+    (dict(sources=-1), (16, 16, 16, 16, 16)),
+    (dict(part_stride_head=500), (16, 16, 16, 16, 16)),   # rows not 16-byte aligned
+    (dict(lse_stride_token=-4), (16, 16, 16, 16, 16)),
+    (dict(out_stride_token=4 * 128 - 8), (16, 16, 16, 16, 16)),
+    (dict(), (0, 16, 16, 16, 16)),                         # no parts
+    (dict(), (16, 0, 16, 16, 16)),                         # no lses
+    (dict(), (8, 16, 16, 16, 16)),                         # parts misaligned
+    (dict(), (16, 16, 16, 16, 0)),                         # no out
+    (dict(), (16, 16, 8, 16, 16)),                         # w_uv misaligned
+])
+def test_merge_value_rejects_bad_arguments_before_any_launch(lib, kw, ptrs):
+    parts, lses, w, gate, out = (ctypes.c_void_p(p) if p else None for p in ptrs)
+    rc = lib.smla_merge_value(ctypes.byref(_merge_value_shape(**kw)), parts, lses, None, w, gate, out, None)
+    assert rc == smla.EINVAL
+
+
+def test_merge_value_of_nothing_is_ok_without_a_device(lib):
+    assert lib.smla_merge_value(ctypes.byref(_merge_value_shape(tokens=0)), None, None, None, None, None, None,
+                                None) == smla.OK

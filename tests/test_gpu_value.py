@@ -141,3 +141,106 @@ def test_value_gate_batch_size_sampled():
     torch.cuda.synchronize()
     rows = np.arange(0, T, 37).tolist() + [T - 1]
     check(latent[rows], w, gate[rows], lens[rows], out[rows])
+
+
+# ------------------------------------------------- fused merge + projection
+
+def partial_sets(seed, S, T, H, invalid=0.1):
+    """BF16 partial rows N(0, 1), base-2 LSEs U(-6, 6), a fraction of empty
+    sources (-inf, NaN or +inf LSE)."""
+    rng = np.random.default_rng(seed)
+    parts = torch.from_numpy(rng.standard_normal((S, T, H, 512)).astype(np.float32)).to(torch.bfloat16)
+    lses = rng.uniform(-6.0, 6.0, (S, T, H)).astype(np.float32)
+    kinds = rng.random((S, T, H))
+    lses[kinds < invalid] = -np.inf
+    lses[(kinds >= invalid) & (kinds < invalid * 1.3)] = np.nan
+    lses[(kinds >= invalid * 1.3) & (kinds < invalid * 1.5)] = np.inf
+    return parts, torch.from_numpy(lses)
+
+
+def fused_and_composed(parts, lses, lens, w, gate):
+    d = [x.cuda() if x is not None else None for x in (parts, lses, lens, w, gate)]
+    fused = smla.merge_value(d[0], d[1], d[3], d[4], d[2])
+    merged, _ = smla.merge(d[0], d[1], d[2], with_lse=False)
+    composed = smla.value_gate(merged, d[3], d[4], d[2])
+    torch.cuda.synchronize()
+    assert smla.smla_value_gate_error() == 0
+    return fused, composed, merged
+
+
+def check_against_oracle(parts, lses, lens, w, gate, got, rows=None):
+    """The oracle's merge then its projection. The GPU's merged rows may each
+    differ from the oracle's by one BF16 step (plus 1e-6 of the largest source
+    magnitude), which moves the product by at most sum_j |W[h, j, v]| times
+    that; the projection's own bound comes on top."""
+    S, T, H, _ = parts.shape
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    bits = parts.view(torch.int16).numpy().view(np.uint16)[:, rows]
+    lens_np = None if lens is None else lens.numpy()[rows]
+    value_m, m_bits, _ = oracle.merge(oracle.MergeProblem(bits, lses.numpy()[:, rows], lens_np))
+    m_bits = m_bits.reshape(len(rows), H, 512)
+    value, _ = oracle.value_gate(m_bits, bits_of(w), bits_of(gate[rows]), lens_np)
+    m = value_m.reshape(len(rows), H, 512)
+    scale = np.abs(parts.float().numpy()[:, rows]).max(axis=(0, 3))  # [rows, H]
+    slack = bf16_ulp(m) + 1e-6 * scale[:, :, None]
+    wd = np.abs(w.double().numpy())
+    prop = np.matmul(slack.transpose(1, 0, 2), wd).transpose(1, 0, 2).reshape(len(rows), H * 128)
+    mag = np.matmul(np.abs(m).transpose(1, 0, 2), wd).transpose(1, 0, 2).reshape(len(rows), H * 128)
+    acc = np.matmul(m.transpose(1, 0, 2), w.double().numpy()).transpose(1, 0, 2).reshape(len(rows), H * 128)
+    sig = 1.0 / (1.0 + np.exp(-gate[rows].double().numpy()))
+    bound = sig * (bf16_ulp(acc) + 2.0 ** -16 * mag + prop) + bf16_ulp(value)
+    g = got.float().cpu().numpy()[rows]
+    worst = float((np.abs(g - value) / bound).max())
+    print(f"merge + value vs the oracle: worst {worst:.3f} of the bound")
+    assert worst <= 1.0
+
+
+@pytest.mark.parametrize("S,T,H", [(1, 3, 2), (3, 5, 4), (8, 64, 8), (13, 70, 3), (37, 2, 2)])
+def test_merge_value_equals_merge_then_value_gate(S, T, H):
+    parts, lses = partial_sets(500 + S, S, T, H)
+    _, w, gate, lens = inputs(600 + S, T, H, lens_zero=(1,) if T > 2 else ())
+    fused, composed, _ = fused_and_composed(parts, lses, lens, w, gate)
+    assert torch.equal(fused.view(torch.int16), composed.view(torch.int16))
+    check_against_oracle(parts, lses, lens, w, gate, fused)
+
+
+def test_merge_value_of_no_sources_is_zero():
+    T, H = 5, 2
+    parts = torch.empty((0, T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lses = torch.empty((0, T, H), dtype=torch.float32, device="cuda")
+    _, w, gate, _ = inputs(7, T, H)
+    out = smla.merge_value(parts, lses, w.cuda(), gate.cuda())
+    torch.cuda.synchronize()
+    assert torch.all(out.view(torch.int16) == 0)
+
+
+def test_merge_value_strided_layouts_match_contiguous():
+    """Sources interleaved per token ([T, S, H, 512] storage) with padded
+    heads, LSEs inside a wider buffer, output rows inside a wider buffer."""
+    S, T, H = 4, 67, 3
+    parts, lses = partial_sets(31, S, T, H)
+    _, w, gate, lens = inputs(32, T, H, lens_zero=(2,))
+    d_parts, d_lses, d_w, d_gate, d_lens = (x.cuda() for x in (parts, lses, w, gate, lens))
+    ref = smla.merge_value(d_parts, d_lses, d_w, d_gate, d_lens)
+    big = torch.zeros((T, S, H + 2, 520), dtype=torch.bfloat16, device="cuda")
+    big[:, :, :H, :512] = d_parts.permute(1, 0, 2, 3)
+    sparts = big[:, :, :H, :512].permute(1, 0, 2, 3)
+    lbig = torch.zeros((T, S, H + 5), dtype=torch.float32, device="cuda")
+    lbig[:, :, :H] = d_lses.permute(1, 0, 2)
+    slses = lbig[:, :, :H].permute(1, 0, 2)
+    obig = torch.full((T, H * 128 + 16), 5.0, dtype=torch.bfloat16, device="cuda")
+    smla.smla_merge_value(sparts, slses, d_lens, d_w, d_gate, obig[:, :H * 128])
+    torch.cuda.synchronize()
+    assert torch.equal(obig[:, :H * 128].view(torch.int16), ref.view(torch.int16))
+    assert torch.all(obig[:, H * 128:] == 5.0)
+
+
+def test_merge_value_batch_size():
+    """8 partial sets of the 64 x 128 batch shape: bit for bit the composition
+    of the two steps, every 5th token against the oracle."""
+    S, T, H = 8, 64, 128
+    parts, lses = partial_sets(2027, S, T, H, invalid=0.05)
+    _, w, gate, lens = inputs(2028, T, H, lens_zero=(3, 60))
+    fused, composed, _ = fused_and_composed(parts, lses, lens, w, gate)
+    assert torch.equal(fused.view(torch.int16), composed.view(torch.int16))
+    check_against_oracle(parts, lses, lens, w, gate, fused, rows=np.arange(0, T, 5))
