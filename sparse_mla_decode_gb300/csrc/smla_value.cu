@@ -141,10 +141,28 @@ __device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v) {
 // tb; they round, gate and write the values into the gate tile in place.
 // Bit t of `live` says whether token tb + t has keys. Returns false if a
 // bounded wait gave up.
+// sigmoid(g) = 1 / (1 + e^-g), in FP32 to a few ulp (the value is then
+// rounded to BF16, 2^-8 relative)
+__device__ __forceinline__ float sigmoid_of_bf16(uint32_t bits) {
+    return rcp_approx(1.0f + __expf(-__uint_as_float(bits << 16)));
+}
+
+// The gates of the epilogue thread (warp, lane) of a kEpiWarps-warp epilogue,
+// as sigmoids.
 template <int kEpiWarps>
+__device__ __forceinline__ void epilogue_sigmoids(uint32_t tile, int warp, int lane,
+                                                  float (&sig)[kTile * 4 / kEpiWarps]) {
+    constexpr int kTokensPerWarp = kTile * 4 / kEpiWarps;
+    const int v = 32 * (warp & 3) + lane, tb = kTokensPerWarp * (warp >> 2);
+    const uint32_t slot = tile + static_cast<uint32_t>(tb * kV + v) * 2;
+#pragma unroll
+    for (int t = 0; t < kTokensPerWarp; ++t) sig[t] = sigmoid_of_bf16(lds_u16(slot + t * kV * 2));
+}
+
+template <int kEpiWarps, bool kHaveSigmoids = false>
 __device__ __forceinline__ bool gate_epilogue(const Params& p, uint32_t tile, uint32_t tmem, uint64_t* mma_done,
                                               uint64_t* gate_full, volatile int* abort_flag, int t0, int warp,
-                                              int lane) {
+                                              int lane, const float* sig = nullptr) {
     constexpr int kTokensPerWarp = kTile * 4 / kEpiWarps;
     const int v = 32 * (warp & 3) + lane;
     const int tb = kTokensPerWarp * (warp >> 2);
@@ -152,7 +170,7 @@ __device__ __forceinline__ bool gate_epilogue(const Params& p, uint32_t tile, ui
     const uint32_t live =
         __ballot_sync(~0u, t_lane < p.tokens && (p.lens == nullptr || p.lens[t_lane] > 0));
     bool ok = mbar_wait_bounded(mma_done, 0, abort_flag, kWaitLimitNs);
-    ok &= mbar_wait_bounded(gate_full, 0, abort_flag, kWaitLimitNs);
+    if (!kHaveSigmoids) ok &= mbar_wait_bounded(gate_full, 0, abort_flag, kWaitLimitNs);
     __syncwarp();
     tc_fence_after_sync();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -166,15 +184,14 @@ __device__ __forceinline__ bool gate_epilogue(const Params& p, uint32_t tile, ui
     }
     const uint32_t slot = tile + static_cast<uint32_t>(tb * kV + v) * 2;  // gate / value of token tb
     uint32_t bits[kTokensPerWarp];
+    if (!kHaveSigmoids) {
 #pragma unroll
-    for (int t = 0; t < kTokensPerWarp; ++t) bits[t] = lds_u16(slot + t * kV * 2);
+        for (int t = 0; t < kTokensPerWarp; ++t) bits[t] = lds_u16(slot + t * kV * 2);
+    }
 #pragma unroll
     for (int t = 0; t < kTokensPerWarp; ++t) {
-        const float gate = __uint_as_float(bits[t] << 16);
         const float rounded = __bfloat162float(__float2bfloat16_rn(acc[t]));
-        // sigmoid(g) = 1 / (1 + e^-g), in FP32 to a few ulp (the value is then
-        // rounded to BF16, 2^-8 relative)
-        const float y = rounded * rcp_approx(1.0f + __expf(-gate));
+        const float y = rounded * (kHaveSigmoids ? sig[t] : sigmoid_of_bf16(bits[t]));
         bits[t] = (live >> t) & 1u ? __bfloat16_as_ushort(__float2bfloat16_rn(y)) : 0u;
     }
 #pragma unroll
@@ -430,6 +447,12 @@ __global__ void __launch_bounds__(32 * fz::kWarpsAll, 1) merge_value_kernel(cons
         for (int i = 0; i < kRows; ++i) merge_weights(l[i], S, lane, wts + (warp + kConsumerWarps * i) * S);
         named_barrier(1, 32 * kConsumerWarps);
 
+        // the epilogue's sigmoids while the first rows are in flight (the
+        // gate tile is the producer's first copy)
+        float sig[kTile * 4 / kConsumerWarps];
+        ok &= mbar_wait_bounded(gate_full, 0, abort_flag, kWaitLimitNs);
+        epilogue_sigmoids<kConsumerWarps>(sbase + fz::kG, warp, lane, sig);
+
         // then block by block, sources in order
         const int t = tid >> 3, u = tid & 7;
         const float* w_t = wts + t * S;
@@ -474,7 +497,8 @@ __global__ void __launch_bounds__(32 * fz::kWarpsAll, 1) merge_value_kernel(cons
             if (lane == 0) mbar_arrive(b_ready + bslot);
         }
         if (!ok) *abort_flag = 1;
-        ok &= gate_epilogue<kConsumerWarps>(p, sbase + fz::kG, tmem, mma_done, gate_full, abort_flag, t0, warp, lane);
+        ok &= gate_epilogue<kConsumerWarps, true>(p, sbase + fz::kG, tmem, mma_done, gate_full, abort_flag, t0, warp,
+                                                  lane, sig);
     }
     tc_fence_before_sync();
     __syncthreads();
