@@ -98,6 +98,14 @@ struct Params {
     float scale_log2, out_scale;
 };
 
+// The split merge's inbox holds splits x ceil(16 / splits) latent slices of
+// 32; the most over 1..kMaxSplits splits (30, at 15).
+constexpr int max_inbox_slices() {
+    int most = 0;
+    for (int s = 1; s <= kMaxSplits; ++s) most = most > s * ((16 + s - 1) / s) ? most : s * ((16 + s - 1) / s);
+    return most;
+}
+
 // Shared-memory map of one CTA for N heads and D-byte rows (offsets from a
 // 1024-byte aligned base; every MMA operand tile starts on 1024 bytes).
 template <int N, int D>
@@ -116,7 +124,14 @@ struct Layout {
     static constexpr int kHead = kRed + 4 * N * 4;      // float [4][N]: m_run, bias, alpha, l
     static constexpr int kBar = kHead + 4 * N * 4;      // 16 mbarriers
     static constexpr int kMisc = kBar + 16 * 8;         // tmem base, abort flag
-    static constexpr int kBytes = kMisc + 64;
+    // 16-head tiles: the split merge's inbox, stats and weights in their own
+    // area (the KV tiles stay untouched), so that a CTA may receive its
+    // partners' partials without first waiting for the cluster to leave the
+    // main loop. Larger tiles reuse the KV tiles and wait.
+    static constexpr bool kOwnInbox = N == 16;
+    static constexpr int kInboxBytes = max_inbox_slices() * N * 32 * 4 + kMaxSplits * 2 * N * 4 + kMaxSplits * N * 4;
+    static constexpr int kInbox = (kMisc + 64 + 1023) / 1024 * 1024;
+    static constexpr int kBytes = kOwnInbox ? kInbox + kInboxBytes : kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;
     // TMEM columns: S^T chain 0 of buffers 0/1 at [0, 2N), O^T blocks at
     // [2N, 6N), S^T chain 1 of buffers 0/1 at [6N, 8N).
@@ -749,12 +764,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         // owning their latent slice: slice s (latent 32 s .. 32 s + 31, s < 16)
         // belongs to rank s % splits. The areas reuse the KV and Q tiles.
         const int slots = (16 + splits - 1) / splits;
-        const uint32_t inbox = sbase;                                   // float [S][slots][N][32]
+        constexpr int kInboxAt = L::kOwnInbox ? L::kInbox : 0;
+        const uint32_t inbox = sbase + kInboxAt;                        // float [S][slots][N][32]
         const uint32_t stats = inbox + splits * slots * N * 32 * 4;     // float [S][2][N]
-        float* stats_f = reinterpret_cast<float*>(smem + splits * slots * N * 32 * 4);
+        float* stats_f = reinterpret_cast<float*>(smem + kInboxAt + splits * slots * N * 32 * 4);
         float* weight_f = stats_f + splits * 2 * N;                     // float [S][N]
-        const float* inbox_f = reinterpret_cast<const float*>(smem);
-        cluster_sync_relaxed();  // every CTA of the cluster is past its main loop
+        const float* inbox_f = reinterpret_cast<const float*>(smem + kInboxAt);
+        if (!L::kOwnInbox) cluster_sync_relaxed();  // every CTA of the cluster is past its main loop
         if (tid < N) {
             for (int r = 0; r < splits; ++r) {
                 st_cluster_f32(map_to_rank(stats + ((split * 2 + 0) * N + tid) * 4, half * splits + r), m_run_s[tid]);
@@ -780,29 +796,40 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         }
         cluster_sync_all();  // every partial has landed
         if (tid < N) {
+            // the splits' loops unrolled to the maximum split count, so that
+            // their loads and exponentials issue together
             const int h = head0 + tid;
+            const float sink2 = p.sinks != nullptr ? p.sinks[h] * kLog2e : -INFINITY;
+            float m[kMaxSplits], l[kMaxSplits];
+#pragma unroll
+            for (int s = 0; s < kMaxSplits; ++s) {
+                m[s] = s < splits ? stats_f[(s * 2) * N + tid] : -INFINITY;
+                l[s] = s < splits ? stats_f[(s * 2 + 1) * N + tid] : 0.0f;
+            }
             float top = -INFINITY;
-            for (int s = 0; s < splits; ++s) top = fmaxf(top, stats_f[(s * 2) * N + tid]);
+#pragma unroll
+            for (int s = 0; s < kMaxSplits; ++s) top = fmaxf(top, m[s]);
             float lse2 = -INFINITY;
             if (top == -INFINITY) {
                 for (int s = 0; s < splits; ++s) weight_f[s * N + tid] = 0.0f;
             } else {
                 float extra = 0.0f;
                 if (p.sinks != nullptr) {
-                    const float s2 = p.sinks[h] * kLog2e;
-                    top = fmaxf(top, s2);
-                    extra = 448.0f * fast_exp2(s2 - top);
+                    top = fmaxf(top, sink2);
+                    extra = 448.0f * fast_exp2(sink2 - top);
                 }
+                float w[kMaxSplits];
                 float total = 0.0f;
-                for (int s = 0; s < splits; ++s) {
-                    const float m = stats_f[(s * 2) * N + tid];
-                    const float w = (m == -INFINITY) ? 0.0f : fast_exp2(m - top);
-                    weight_f[s * N + tid] = w;
-                    total += w * stats_f[(s * 2 + 1) * N + tid];
+#pragma unroll
+                for (int s = 0; s < kMaxSplits; ++s) {
+                    w[s] = (m[s] == -INFINITY) ? 0.0f : fast_exp2(m[s] - top);
+                    total += w[s] * l[s];
                 }
                 total += extra;
                 const float inverse = p.out_scale / total;
-                for (int s = 0; s < splits; ++s) weight_f[s * N + tid] *= inverse;
+#pragma unroll
+                for (int s = 0; s < kMaxSplits; ++s)
+                    if (s < splits) weight_f[s * N + tid] = w[s] * inverse;
                 lse2 = top - kLog2P + log2f(total);
             }
             if (split == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(token) * p.lse_stride_token + h] = lse2;
