@@ -298,13 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             tma_load_3d(sbase + L::kQ + kb * N * 128, &p.q_latent, kb * 128, head0, token, q_full);
         if constexpr (L::kRope) tma_load_3d(sbase + L::kQ + 4 * N * 128, &p.q_rope, 512, head0, token, q_full);
     }
-    if (warp == kProducerWarp && lane < 4 && p.width > 0) {
-        // The first chunk's indices, pulled into L2 while the count loads
-        // (assuming the full width; a shorter count only leaves them unused).
-        const int chunks_w = (p.width + kChunk - 1) / kChunk;
-        const int col = split * ((chunks_w + splits - 1) / splits) * kChunk + 32 * lane;
-        if (col < p.width) prefetch_l2_line(p.indices + static_cast<int64_t>(token) * p.idx_stride + col);
-    }
+    // The first chunk's raw indices, loaded while the count loads: the
+    // chunk this split starts with when the count fills the width (always
+    // for split 0). Thread k of the chunk's resolvers (the softmax range
+    // unpaired, the producers paired) takes column k; the count masks them
+    // later, and a split whose first chunk turns out elsewhere reloads.
+    const int chunks_w = (p.width + kChunk - 1) / kChunk;
+    const int col_guess = split * ((chunks_w + splits - 1) / splits) * kChunk;
+    const int resolver = paired ? tid - kProducerWarp * 32 : tid;
+    int32_t raw_guess = -1;
+    if (resolver >= 0 && resolver < kChunk && col_guess + resolver < p.width)
+        raw_guess = p.indices[static_cast<int64_t>(token) * p.idx_stride + col_guess + resolver];
     const int count = min(max(p.lens[token], 0), p.width);
     // This split's chunks of the token: ceil(chunks / splits) consecutive
     // chunks each, dealt over the token's own count (later splits may be empty).
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             const int col = col0 + tid;
             int32_t id = -1;
             if (col < count) {
-                const int32_t raw = idx_row[col];
+                const int32_t raw = col0 == col_guess ? raw_guess : idx_row[col];
                 const bool second = p.num_pools == 2 && col >= p.pool_split;
                 if (raw >= 0) {
                     if (raw < (second ? p.rows1 : p.rows0))
@@ -381,7 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
             const int col0 = (c_first + c) * kChunk;
-            const int32_t raw = (g < kChunk && col0 + g < count) ? idx_row[col0 + g] : -1;
+            const int32_t raw = (g < kChunk && col0 + g < count)
+                                    ? ((c == 0 && col0 == col_guess) ? raw_guess : idx_row[col0 + g])
+                                    : -1;
             if (c >= 2) ok &= mbar_wait_bounded(&stage_free[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             if (g < kChunk) {
                 int32_t id = -1;
