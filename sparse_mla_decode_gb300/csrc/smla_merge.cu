@@ -33,6 +33,7 @@ constexpr int kLatent = 512;
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kGroup = 4;  // sources whose row loads are in flight together
+constexpr int kMaxPipelinedSources = 64;  // up to here a warp loads its next row's LSEs ahead
 
 struct Params {
     smla::MergeInputs merge;  // the partial sets and their base-2 LSEs
@@ -45,24 +46,106 @@ struct Params {
 };
 
 __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_constant__ Params p) {
-    const int lane = threadIdx.x & 31;
+    __shared__ float wts[kWarps][kMaxPipelinedSources];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t rows = static_cast<int64_t>(p.tokens) * p.heads;
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     const int64_t step = static_cast<int64_t>(gridDim.x) * kWarps;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the partial sets are read only after this point
 
-    for (int64_t row = first; row < rows; row += step) {
-        const int t = static_cast<int>(row / p.heads), h = static_cast<int>(row % p.heads);
-        const bool live = p.lens == nullptr || p.lens[t] > 0;
-        float top, acc[16];
-        const float total = smla::merge_row<kGroup>(p.merge, t, h, lane, live, top, acc);
-        __nv_bfloat16* dst = p.out + static_cast<int64_t>(t) * p.out_stride_token +
-                             static_cast<int64_t>(h) * p.out_stride_head + 16 * lane;
-        reinterpret_cast<uint4*>(dst)[0] = smla::pack_bf16(acc);
-        reinterpret_cast<uint4*>(dst)[1] = smla::pack_bf16(acc + 8);
-        if (p.lse_out != nullptr && lane == 0)
-            p.lse_out[static_cast<int64_t>(t) * p.lse_out_stride_token + h] =
-                total > 0.0f ? top + log2f(total) : -INFINITY;
+    if (p.merge.sources <= kMaxPipelinedSources) {
+        // The next row's counts and LSEs load while this row's partial rows
+        // are in flight, so that a row costs one round trip to memory. The
+        // weights come from the same operations as merge_row's.
+        float* w_row = wts[warp];
+        float l_next[2];
+        int count_next = 0;
+        auto load_row = [&](int64_t row, float (&l)[2], int& count) {
+            const int t = static_cast<int>(row / p.heads), h = static_cast<int>(row % p.heads);
+            count = p.lens == nullptr ? 1 : p.lens[t];
+            smla::load_row_lses(p.merge, t, h, lane, l);
+        };
+        if (first < rows) load_row(first, l_next, count_next);
+        for (int64_t row = first; row < rows; row += step) {
+            const int t = static_cast<int>(row / p.heads), h = static_cast<int>(row % p.heads);
+            float l[2] = {l_next[0], l_next[1]};
+            if (count_next <= 0) smla::empty_row_lses(l);
+            if (row + step < rows) load_row(row + step, l_next, count_next);
+            smla::merge_weights(l, p.merge.sources, lane, w_row);
+            __syncwarp();
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            const __nv_bfloat16* base = p.merge.parts + static_cast<int64_t>(t) * p.merge.part_stride_token +
+                                        static_cast<int64_t>(h) * p.merge.part_stride_head + 16 * lane;
+            int s = 0;
+            for (; s + kGroup <= p.merge.sources; s += kGroup) {
+                float w[kGroup];
+                uint4 v[2 * kGroup];
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k) {
+                    w[k] = w_row[s + k];
+                    if (w[k] != 0.0f) {  // the same for every lane: an empty source's row is never read
+                        const __nv_bfloat16* src = base + (s + k) * p.merge.part_stride_source;
+                        v[2 * k] = smla::load_nc(src);
+                        v[2 * k + 1] = smla::load_nc(src + 8);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kGroup; ++k)
+                    if (w[k] != 0.0f) {
+                        smla::add_weighted(acc, w[k], v[2 * k]);
+                        smla::add_weighted(acc + 8, w[k], v[2 * k + 1]);
+                    }
+            }
+            for (; s < p.merge.sources; ++s) {
+                const float w = w_row[s];
+                if (w != 0.0f) {
+                    const __nv_bfloat16* src = base + s * p.merge.part_stride_source;
+                    smla::add_weighted(acc, w, smla::load_nc(src));
+                    smla::add_weighted(acc + 8, w, smla::load_nc(src + 8));
+                }
+            }
+            __nv_bfloat16* dst = p.out + static_cast<int64_t>(t) * p.out_stride_token +
+                                 static_cast<int64_t>(h) * p.out_stride_head + 16 * lane;
+            reinterpret_cast<uint4*>(dst)[0] = smla::pack_bf16(acc);
+            reinterpret_cast<uint4*>(dst)[1] = smla::pack_bf16(acc + 8);
+            if (p.lse_out != nullptr) {
+                // the row's largest finite LSE and the weights' sum, again by
+                // merge_row's operations (cheap next to the row's bytes)
+                float top = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (isfinite(l[k])) top = fmaxf(top, l[k]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) top = fmaxf(top, __shfl_xor_sync(0xFFFFFFFFu, top, o));
+                float total = 0.0f;
+                if (top != -INFINITY)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        if (isfinite(l[k])) total += smla::exp2_approx(l[k] - top);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+                if (lane == 0)
+                    p.lse_out[static_cast<int64_t>(t) * p.lse_out_stride_token + h] =
+                        total > 0.0f ? top + log2f(total) : -INFINITY;
+            }
+            __syncwarp();  // w_row is rewritten for the next row
+        }
+    } else {
+        for (int64_t row = first; row < rows; row += step) {
+            const int t = static_cast<int>(row / p.heads), h = static_cast<int>(row % p.heads);
+            const bool live = p.lens == nullptr || p.lens[t] > 0;
+            float top, acc[16];
+            const float total = smla::merge_row<kGroup>(p.merge, t, h, lane, live, top, acc);
+            __nv_bfloat16* dst = p.out + static_cast<int64_t>(t) * p.out_stride_token +
+                                 static_cast<int64_t>(h) * p.out_stride_head + 16 * lane;
+            reinterpret_cast<uint4*>(dst)[0] = smla::pack_bf16(acc);
+            reinterpret_cast<uint4*>(dst)[1] = smla::pack_bf16(acc + 8);
+            if (p.lse_out != nullptr && lane == 0)
+                p.lse_out[static_cast<int64_t>(t) * p.lse_out_stride_token + h] =
+                    total > 0.0f ? top + log2f(total) : -INFINITY;
+        }
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
