@@ -36,7 +36,7 @@
  *                        that the online/merge algebra can be checked against
  *                        the plain definition.
  *
- * Readings where the pages are silent (each listed in the design doc):
+ * Readings where the pages are silent:
  *   - logits use bmm1_scale only; the output multiplier is bmm2_scale*k_scale;
  *   - the LSE is base 2 and includes the sink term of the denominator;
  *   - sinks are in score units (already scaled), base 2 = sink * log2(e);
