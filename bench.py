@@ -214,7 +214,9 @@ def measured_hbm_peak():
 
 
 KERNEL_SOURCES = {"value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh"),
-                  "merge_value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh")}
+                  "merge_value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh"),
+                  "merge": ("smla_merge.cu", "smla_merge_row.cuh"),
+                  "mxfp4": ("smla_quant.cu",)}
 
 
 def kernel_sha(config: str = "batch") -> str:
@@ -742,7 +744,7 @@ def run_merge(args, rank, world, local_rank):
                              if graph is not None else "%d library calls from Python" % args.steps,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic("merge"),
                      "bytes_alg_per_launch": int(per_call)},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
     }
@@ -864,7 +866,7 @@ def run_mxfp4(args, rank, world, local_rank):
                    "launch": "one CUDA graph of the %d timed library calls, replayed once" % args.steps,
                    "pages_context": "the pages' Triton kernel: ~35 us at 16K tokens x 32 heads on GB300"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic("mxfp4"),
                      "bytes_alg_per_launch": int(per_call)},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
     }
