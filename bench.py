@@ -634,9 +634,21 @@ MERGE_METRIC = "µs/call and achieved HBM GB/s for the LSE merge of partial (out
 
 
 def merge_bytes(S, T, H) -> int:
-    """Algorithmic bytes of one merge: every source row and LSE read once, the
-    merged row and LSE written once."""
+    """Bytes of one merge that reads every source row: every source row and LSE
+    read once, the merged row and LSE written once (an upper bound, used to
+    size the input rotation)."""
     return S * T * H * (512 * 2 + 4) + T * H * (512 * 2 + 4) + T * 4
+
+
+def merge_bytes_live(lses, lens) -> int:
+    """Algorithmic bytes of one merge of these sets: the rows of the sources
+    that carry weight (finite LSE, token count > 0) and every LSE read once,
+    the merged row and LSE written once. A source without weight needs no row."""
+    import torch
+
+    S, T, H = lses.shape
+    live = torch.isfinite(lses) & (lens > 0).view(1, T, 1)
+    return int(live.sum().item()) * 512 * 2 + S * T * H * 4 + T * H * (512 * 2 + 4) + T * 4
 
 
 def run_merge(args, rank, world, local_rank):
@@ -651,9 +663,9 @@ def run_merge(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     S, T, H = 8, 64, 128
-    per_call = merge_bytes(S, T, H)
-    R = int(math.ceil(2.5 * L2_BYTES / per_call))
+    R = int(math.ceil(2.5 * L2_BYTES / merge_bytes(S, T, H)))
     sets = [workloads.merge_sets(1005 + 17 * r + 1000 * rank, S, T, H, device=dev) for r in range(R)]
+    per_call = sum(merge_bytes_live(l, n) for _, l, n in sets) / R  # the sets' mean
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
 
@@ -770,7 +782,7 @@ def merge_cpu_rate(first_set, seconds: float):
         done += n
     elapsed = time.perf_counter() - t0
     per_call = elapsed / done * T * H
-    return {"value": round(merge_bytes(S, T, H) / per_call / 1e9, 4), "unit": "GB/s", "cores": cores,
+    return {"value": round(merge_bytes_live(lses, lens) / per_call / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle", "sample": f"{done} merged rows in batches of {n} drawn from the {T * H} rows of one call",
             "us_per_call": round(per_call * 1e6, 1)}
 
