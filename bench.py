@@ -955,8 +955,19 @@ def value_sets(T, H, R, seed, device):
 
 
 def merge_value_bytes(S, T, H) -> int:
-    """The partial rows and LSEs, W_UV and the gates read; the values written."""
+    """Every partial row and LSE, W_UV and the gates read; the values written
+    (an upper bound, used to size the input rotation)."""
     return S * T * H * (512 * 2 + 4) + H * 512 * 128 * 2 + 2 * T * H * 128 * 2 + 4 * T
+
+
+def merge_value_bytes_live(lses, lens) -> int:
+    """Algorithmic bytes of one fused merge + projection: the rows of the
+    sources that carry weight and every LSE, W_UV and the gates read; the
+    values written. (The kernel's TMA boxes also read the rows of empty
+    sources, which shows in its DRAM traffic.)"""
+    S, T, H = lses.shape
+    rows = merge_bytes_live(lses, lens) - S * T * H * 4 - T * H * (512 * 2 + 4) - T * 4
+    return rows + S * T * H * 4 + H * 512 * 128 * 2 + 2 * T * H * 128 * 2 + 4 * T
 
 
 def run_value(args, rank, world, local_rank, fused=False):
@@ -978,6 +989,7 @@ def run_value(args, rank, world, local_rank, fused=False):
     if fused:
         merged = [workloads.merge_sets(1005 + 17 * r + 1000 * rank, S, T, H, device=dev) for r in range(R)]
         sets = [(m[0], m[1], m[2], v[1], v[2]) for m, v in zip(merged, sets)]  # parts, lses, lens, w_uv, gate
+        per_call = sum(merge_value_bytes_live(m[1], m[2]) for m in merged) / R  # the sets' mean
     outs = [torch.empty((T, H * 128), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
     def call(i):
@@ -1106,7 +1118,7 @@ def value_cpu_rate(first_set, seconds: float, fused=False):
             oracle.value_gate(lat_b[rows], w_b, g_b[rows], lens.numpy()[rows])
         done += 2
     per_call = (time.perf_counter() - t0) / done * T
-    total = merge_value_bytes(S, T, H) if fused else value_bytes(T, H)
+    total = merge_value_bytes_live(lses, lens) if fused else value_bytes(T, H)
     return {"value": round(total / per_call / 1e9, 6), "unit": "GB/s", "cores": oracle.max_threads() if fused else 1,
             "kind": "oracle", "sample": f"{done} of {T} tokens, all heads, in batches of 2",
             "us_per_call": round(per_call * 1e6, 1)}
