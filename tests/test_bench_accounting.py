@@ -1,0 +1,73 @@
+"""Host-side accounting of bench.py: algorithmic bytes per call, the source
+hashes that tie a committed DRAM-traffic figure to the kernel it was taken on,
+and the lookup that reports it. No GPU."""
+
+import json
+import os
+
+import pytest
+import torch
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_merge_bytes_live_counts_only_rows_with_weight():
+    S, T, H = 3, 4, 2
+    lses = torch.zeros((S, T, H))
+    lens = torch.full((T,), 5, dtype=torch.int32)
+    full = bench.merge_bytes_live(lses, lens)
+    assert full == bench.merge_bytes(S, T, H)  # every row live: the upper bound
+    lses[0, 1, 1] = float("-inf")
+    lses[2, 3, 0] = float("nan")
+    assert bench.merge_bytes_live(lses, lens) == full - 2 * 1024
+    lens[2] = 0  # a token without keys: none of its S * H rows is read
+    assert bench.merge_bytes_live(lses, lens) == full - 2 * 1024 - S * H * 1024
+
+
+def test_merge_value_bytes_live_adds_the_projection_operands():
+    S, T, H = 2, 3, 4
+    lses = torch.zeros((S, T, H))
+    lens = torch.full((T,), 1, dtype=torch.int32)
+    assert bench.merge_value_bytes_live(lses, lens) == bench.merge_value_bytes(S, T, H)
+    lses[1, 0, 2] = float("-inf")
+    assert bench.merge_value_bytes_live(lses, lens) == bench.merge_value_bytes(S, T, H) - 1024
+
+
+def test_value_bytes_formula():
+    T, H = 64, 128
+    # merged rows, W_UV, gates in, values out, counts
+    assert bench.value_bytes(T, H) == T * H * 1024 + H * 512 * 128 * 2 + 2 * T * H * 256 + 4 * T
+
+
+@pytest.mark.parametrize("config", ["batch", "value", "merge_value", "merge", "mxfp4"])
+def test_kernel_sha_is_stable_and_tracks_the_sources(config):
+    a, b = bench.kernel_sha(config), bench.kernel_sha(config)
+    assert a == b and len(a) == 16
+    names = bench.KERNEL_SOURCES.get(config, ("smla_decode.cu", "smla_ptx.cuh"))
+    for n in names:
+        assert os.path.exists(os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc", n))
+
+
+def test_configs_with_distinct_kernels_hash_differently():
+    shas = {c: bench.kernel_sha(c) for c in ("batch", "value", "merge", "mxfp4")}
+    assert len(set(shas.values())) == 4
+
+
+def test_traffic_is_reported_only_for_the_source_it_was_taken_on(tmp_path, monkeypatch):
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        recorded = json.load(f)
+    for config, entry in recorded.items():
+        expected = entry["dram_bytes_per_launch"] if entry["kernel_sha"] == bench.kernel_sha(config) else None
+        assert bench.ncu_traffic(config) == expected
+    # a record taken on another source is not reported
+    fake_root = tmp_path
+    (fake_root / "profiles").mkdir()
+    stale = {"batch": dict(recorded.get("batch", {}), kernel_sha="0" * 16, dram_bytes_per_launch=1)}
+    (fake_root / "profiles" / "dram_traffic.json").write_text(json.dumps(stale))
+    real = {c: bench.kernel_sha(c) for c in ("batch", "value")}
+    monkeypatch.setattr(bench, "kernel_sha", lambda config="batch": real[config])
+    monkeypatch.setattr(bench, "ROOT", str(fake_root))
+    assert bench.ncu_traffic("batch") is None
+    assert bench.ncu_traffic("value") is None  # no record at all
