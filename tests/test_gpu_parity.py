@@ -11,7 +11,6 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import oracle
 from sparse_mla_decode_gb300 import smla, workloads
 from tests.gpu_helpers import compare, plan_of, run_gpu, to_device
 
