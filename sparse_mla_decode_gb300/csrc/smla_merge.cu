@@ -11,7 +11,7 @@
 // The pass streams every source row once and writes the merged row once, so
 // it is bound by HBM bandwidth: one warp per (token, head) row, each lane 16
 // consecutive latents (two 16-byte loads per source, four sources in flight),
-// up to eight CTAs per SM, a grid-stride loop beyond that.
+// one resident wave of CTAs over a grid-stride loop of rows.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -196,11 +196,12 @@ extern "C" int smla_merge(const smla_merge_shape* shape, const void* parts, cons
 
     const int sms = device_sms();
     if (sms <= 0) return SMLA_ECUDA;
-    // One row per warp up to eight CTAs per SM (the CTA scheduler keeps the SMs
-    // busy as rows finish); beyond that, a grid-stride loop.
+    // One resident wave (three CTAs per SM at the kernel's registers) with a
+    // grid-stride loop, so that each warp has rows after the current one and
+    // can load their LSEs ahead.
     const int64_t rows = static_cast<int64_t>(s.tokens) * s.heads;
     const int64_t want = (rows + kWarps - 1) / kWarps;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    const int64_t cap = static_cast<int64_t>(sms) * 3;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
