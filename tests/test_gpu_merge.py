@@ -54,8 +54,10 @@ def check(parts, lses, lens, got, got_lse):
         print(f"merge: worst {worst:.3f} of the bound, {same:.5f} of the bits equal")
 
 
-@pytest.mark.parametrize("S,T,H", [(1, 3, 16), (2, 2, 32), (3, 5, 16), (5, 4, 64), (8, 3, 128), (37, 2, 16)])
+@pytest.mark.parametrize("S,T,H", [(1, 3, 16), (2, 2, 32), (3, 5, 16), (5, 4, 64), (8, 3, 128), (37, 2, 16), (70, 3, 16)])
 def test_merge_matches_the_oracle(S, T, H):
+    """Up to 64 sources a warp loads its next row's LSEs ahead; beyond, the
+    kernel takes each row's LSEs with it (70 here)."""
     parts, lses, lens = random_sets(100 + S, S, T, H, lens_zero=(1,) if T > 2 else ())
     d = parts.cuda()
     out, lse = smla.merge(d, torch.from_numpy(lses).cuda(), torch.from_numpy(lens).cuda())
