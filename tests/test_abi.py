@@ -229,3 +229,10 @@ def test_merge_value_rejects_bad_arguments_before_any_launch(lib, kw, ptrs):
 def test_merge_value_of_nothing_is_ok_without_a_device(lib):
     assert lib.smla_merge_value(ctypes.byref(_merge_value_shape(tokens=0)), None, None, None, None, None, None,
                                 None) == smla.OK
+
+
+def test_merge_value_beyond_64_sources_is_unsupported_before_any_launch(lib):
+    s = _merge_value_shape(sources=65, part_stride_token=65 * 4 * 512 // 65)
+    p16 = ctypes.c_void_p(16)
+    rc = lib.smla_merge_value(ctypes.byref(s), p16, p16, None, p16, p16, p16, None)
+    assert rc == smla.EUNSUPPORTED
