@@ -21,11 +21,12 @@
 // clipped).
 //
 // The fused entry point (smla_merge_value) takes the partial sets instead of
-// merged rows, as the page's owner does: its sixteen warps LSE-merge the 64
-// rows of the tile straight into the swizzled B tile (a warp per row, 16
-// latents per lane, the merge kernel's own row code, so the rows carry the
-// same bits as smla_merge's), while TMA brings W_UV and the gates; the product
-// and the epilogue are the same.
+// merged rows, as the page's owner does. A producer warp streams the sources'
+// 64-token boxes of partial rows by TMA, sixteen consumer warps merge them
+// block by block into a swizzled B ring with the merge kernel's own weights
+// and operation order (so the rows carry the same bits as smla_merge's), and
+// an MMA warp runs each block's products as soon as it is merged; the epilogue
+// is the same.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
