@@ -2,7 +2,8 @@
 
     python -m sparse_mla_decode_gb300.build [--force]
 
-The library lands in ``sparse_mla_decode_gb300/_build/libsmla.so`` (git-ignored).
+The library lands in ``sparse_mla_decode_gb300/_build/libsmla.so`` (git-ignored), beside
+``libsmla_peak.so``, the FP8 tensor-core microbenchmark.
 It links the CUDA runtime dynamically, so a process that already loaded
 PyTorch's runtime shares it.
 """
@@ -20,8 +21,12 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(BUILD_DIR, "libsmla.so")
+PEAK_LIBRARY = os.path.join(BUILD_DIR, "libsmla_peak.so")
 SOURCES = [os.path.join(CSRC, n) for n in ("smla_decode.cu", "smla_merge.cu", "smla_quant.cu", "smla_value.cu")]
 HEADERS = [os.path.join(CSRC, n) for n in ("smla_ptx.cuh", "smla_merge_row.cuh")] + [os.path.join(INCLUDE, "smla.h")]
+# the FP8 tensor-core microbenchmark, a library of its own
+PEAK_SOURCES = [os.path.join(CSRC, "smla_peak.cu")]
+TARGETS = {LIBRARY: (SOURCES, HEADERS), PEAK_LIBRARY: (PEAK_SOURCES, [])}
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -32,32 +37,53 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libsmla.so")
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIBRARY):
+def _fresh(library: str) -> bool:
+    if not os.path.exists(library):
         return False
-    t = os.path.getmtime(LIBRARY)
-    return all(os.path.getmtime(f) <= t for f in SOURCES + HEADERS)
+    t = os.path.getmtime(library)
+    sources, headers = TARGETS[library]
+    return all(os.path.getmtime(f) <= t for f in sources + headers)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIBRARY
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIBRARY + f".{os.getpid()}.tmp"
+def up_to_date() -> bool:
+    return all(_fresh(lib) for lib in TARGETS)
+
+
+def _command(library: str, tmp: str, verbose: bool):
     cmd = [
         nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
         "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared",
         "-Xlinker", "-rpath=" + os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64"),
-        "-I", INCLUDE, "-o", tmp, *SOURCES,
+        "-I", INCLUDE, "-o", tmp, *TARGETS[library][0],
     ]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
-    if verbose:
-        sys.stderr.write(res.stderr)
-    os.replace(tmp, LIBRARY)
+    return cmd
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles every stale library (in parallel) and returns libsmla.so's path."""
+    todo = [lib for lib in TARGETS if force or not _fresh(lib)]
+    if not todo:
+        return LIBRARY
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    jobs = []
+    for lib in todo:
+        tmp = lib + f".{os.getpid()}.tmp"
+        cmd = _command(lib, tmp, verbose)
+        jobs.append((lib, tmp, cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                                      text=True)))
+    failed = []
+    for lib, tmp, cmd, proc in jobs:
+        out, err = proc.communicate()
+        if proc.returncode != 0:
+            failed.append("nvcc failed:\n" + " ".join(cmd) + "\n" + out + err)
+            continue
+        if verbose:
+            sys.stderr.write(err)
+        os.replace(tmp, lib)
+    if failed:
+        raise RuntimeError("\n".join(failed))
     return LIBRARY
 
 

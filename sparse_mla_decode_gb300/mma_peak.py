@@ -1,0 +1,119 @@
+"""FP8 tensor-core rates of this GPU, measured with the library's own tcgen05
+microbenchmark (``libsmla_peak.so``, built from ``csrc/smla_peak.cu``).
+
+    python -m sparse_mla_decode_gb300.mma_peak [--json PATH]
+
+For each MMA shape the decode uses or could use (cta_group::1 at M = 128 and
+cta_group::2 at M = 256 over a CTA pair; N = 64 / 128 / 256; operands K-major
+or MN-major as the decode reads them), two numbers:
+
+* ``cycles_per_mma``: one CTA (or pair) issues 4000 K = 32 MMAs into one
+  accumulator; the clock64 span from the first issue to the commit's arrival,
+  divided by the MMA count. An ideal dense FP8 tensor core does M_cta x N x 32
+  multiply-adds in M_cta x N x 32 / 8192 cycles (128 x N x 32 / 8192 = N / 2).
+* ``tflops``: every SM does the same; FLOPs of the launch / its CUDA-event time.
+
+The largest ``tflops`` is the measured dense FP8 peak that ``bench.py`` quotes
+the decode's tensor fraction against. With ``--json`` the table is written as
+JSON (the summary committed under ``profiles/``).
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+# (cta_group, N, A MN-major, B MN-major, what the decode uses it for)
+SHAPES = [
+    (1, 64, 0, 0, "QK of a 64-head tile (S^T = KV.Q^T)"),
+    (1, 64, 1, 1, "PV of a 64-head tile (O^T = V^T.P^T)"),
+    (1, 64, 1, 0, "PV with P^T K-major"),
+    (1, 128, 0, 0, "K-major, N = 128"),
+    (1, 128, 1, 1, "MN-major, N = 128"),
+    (1, 256, 0, 0, "K-major, N = 256"),
+    (2, 128, 0, 0, "QK of 128 heads over a CTA pair"),
+    (2, 128, 1, 1, "PV of 128 heads over a CTA pair"),
+    (2, 128, 1, 0, "pair PV with P^T K-major"),
+    (2, 256, 0, 0, "K-major, N = 256, pair"),
+    (2, 256, 1, 1, "MN-major, N = 256, pair"),
+]
+
+
+def _lib():
+    from sparse_mla_decode_gb300 import build
+
+    build.build()
+    lib = ctypes.CDLL(build.PEAK_LIBRARY)
+    lib.smla_peak_mma.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_longlong),
+                                                       ctypes.POINTER(ctypes.c_float)]
+    lib.smla_peak_mma.restype = ctypes.c_int
+    return lib
+
+
+def measure(sms: int, iters_one: int = 1000, iters_all: int = 4000):
+    lib = _lib()
+    rows = []
+    for cg, n, amn, bmn, use in SHAPES:
+        cyc = ctypes.c_longlong(0)
+        ms = ctypes.c_float(0.0)
+        rc = lib.smla_peak_mma(cg, n, amn, bmn, iters_one, cg, ctypes.byref(cyc), ctypes.byref(ms))
+        if rc != 0:
+            raise RuntimeError(f"smla_peak_mma({cg}, {n}, {amn}, {bmn}) one CTA: {rc}")
+        per_mma = cyc.value / (4 * iters_one)
+        ctas = (sms // cg) * cg
+        rc = lib.smla_peak_mma(cg, n, amn, bmn, iters_all, ctas, ctypes.byref(cyc), ctypes.byref(ms))
+        if rc != 0:
+            raise RuntimeError(f"smla_peak_mma({cg}, {n}, {amn}, {bmn}) all SMs: {rc}")
+        flops = ctas * 128 * n * 32 * 2 * 4 * iters_all
+        rows.append({
+            "cta_group": cg, "n": n, "a_mn_major": bool(amn), "b_mn_major": bool(bmn), "use": use,
+            "cycles_per_mma": round(per_mma, 2), "ideal_cycles": n / 2,
+            "tflops": round(flops / (ms.value * 1e-3) / 1e12, 1), "ctas": ctas,
+        })
+    return rows
+
+
+def clocks():
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().splitlines()[0]
+        cur, mx = (float(x) for x in out.split(","))
+        return {"sm_mhz_after": cur, "sm_max_mhz": mx}
+    except Exception:  # noqa: BLE001 - informational only
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--json", default=None, help="write the table as JSON here")
+    args = ap.parse_args()
+    import torch
+
+    props = torch.cuda.get_device_properties(0)
+    rows = measure(props.multi_processor_count)
+    peak = max(r["tflops"] for r in rows)
+    result = {"gpu": props.name, "sms": props.multi_processor_count, "fp8_dense_peak_tflops": peak,
+              "how": "libsmla_peak.so: every SM issues 16000 tcgen05.mma kind::f8f6f4 (K = 32) into one TMEM "
+                     "accumulator; FLOPs / CUDA-event time of the launch",
+              "clocks": clocks(), "shapes": rows}
+    print("| cta_group | N | A | B | cycles/MMA | ideal | TFLOP/s (all SMs) | use |")
+    print("|---|---|---|---|---|---|---|---|")
+    for r in rows:
+        print(f"| {r['cta_group']} | {r['n']} | {'MN' if r['a_mn_major'] else 'K'} | "
+              f"{'MN' if r['b_mn_major'] else 'K'} | {r['cycles_per_mma']} | {r['ideal_cycles']:.0f} | "
+              f"{r['tflops']} | {r['use']} |")
+    print(json.dumps({"fp8_dense_peak_tflops": peak}))
+    if args.json:
+        with open(args.json, "w") as f:
+            json.dump(result, f, indent=1)
+            f.write("\n")
+
+
+if __name__ == "__main__":
+    sys.exit(main())
