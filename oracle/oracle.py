@@ -35,6 +35,8 @@ LIBRARY = os.path.join(HERE, "_build", "libsmla_oracle.so")
 
 NO_P_ROUNDING = 1
 EXACT = 2
+P_UP = 4
+P_DOWN = 8
 LATENT = 512
 
 _lock = threading.Lock()
@@ -112,7 +114,7 @@ def _load():
             lib.smla_oracle_bf16_from_float.argtypes = [ctypes.c_float]
             lib.smla_oracle_bf16_from_float.restype = ctypes.c_uint16
             lib.smla_oracle_fp64_pairs.argtypes = [P, vp, vp, i32, vp, vp, i32]
-            lib.smla_oracle_emulate_pairs.argtypes = [P, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
+            lib.smla_oracle_emulate_pairs.argtypes = [P, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, i32]
             lib.smla_oracle_max_threads.restype = i32
             lib.smla_oracle_merge_f64.argtypes = [i32, vp, vp, vp, vp]
             lib.smla_oracle_e2m1_from_float.argtypes = [ctypes.c_float]
@@ -211,21 +213,27 @@ def fp64(problem: Problem, pairs=None, threads: int = 0):
 
 
 def emulate(problem: Problem, splits: int, chunk: int, pairs=None, flags: int = 0,
-            threads: int = 0):
+            threads: int = 0, ties: bool = False):
     """E4M3-P datapath on the given partition. Returns (value [n, 512] float64 --
-    the pre-BF16 result, bf16 [n, 512] uint16 bits, lse2 [n] float64)."""
+    the pre-BF16 result, bf16 [n, 512] uint16 bits, lse2 [n] float64), and with
+    ``ties`` a fourth array [n, 512]: the most each value moves when every P
+    within a relative 2^-16 of an E4M3 rounding midpoint takes its other code
+    (a rounding the FP32 datapath leaves open)."""
     lib = _load()
     tok, head = _pairs(problem, pairs)
     n = tok.size
     value = np.zeros((n, LATENT), np.float64)
     bits = np.zeros((n, LATENT), np.uint16)
     lse = np.zeros(n, np.float64)
+    tie = np.zeros((n, LATENT), np.float64)
     rc = lib.smla_oracle_emulate_pairs(ctypes.byref(problem.struct), tok.ctypes.data,
                                        head.ctypes.data, n, int(splits), int(chunk), int(flags),
                                        value.ctypes.data, bits.ctypes.data, lse.ctypes.data,
-                                       threads)
+                                       tie.ctypes.data, threads)
     if rc != 0:
         raise ValueError("oracle emulate: bad partition")
+    if ties:
+        return value, bits, lse, tie
     return value, bits, lse
 
 

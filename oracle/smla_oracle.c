@@ -198,10 +198,28 @@ int smla_oracle_fp64(const smla_oracle_problem* p, int t, int h, double* out, do
 /* One rounding to binary32, or none when the caller asked for exact math. */
 static double r32(double x, int exact) { return exact ? x : (double)(float)x; }
 
+/* The E4M3 code of P is a rounding decision that the datapath takes on an
+ * FP32 value whose last bits the pages leave open: the logits come from FP8
+ * products summed in FP32 in an order they do not fix, and exp2 is a fast
+ * approximation (Kimi K3.1 attn_sparse page, "Precision"). A P within a
+ * relative 2^-16 of a rounding midpoint may therefore take either neighbouring
+ * code. The emulation keeps the round-to-nearest code and reports, per output
+ * element, the most that taking the other code at every such P can move it. */
+#define TIE_WINDOW (1.0 / 65536.0)
+
+static double code_value(double x) {
+    return smla_oracle_e4m3_to_double(smla_oracle_e4m3_from_float((float)x));
+}
+
 int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, int chunk,
-                        int flags, double* out_value, uint16_t* out_bf16, double* lse2_out) {
+                        int flags, double* out_value, uint16_t* out_bf16, double* lse2_out,
+                        double* tie_out) {
     const int exact = (flags & SMLA_ORACLE_EXACT) != 0;
     const int keep_p = (flags & SMLA_ORACLE_NO_P_ROUNDING) != 0;
+    /* P moved to either edge of the tie window before its rounding (the two
+     * codes a tie-ambiguous P may take; the sums keep the unmoved P) */
+    const double nudge = (flags & SMLA_ORACLE_P_UP) ? 1.0 + TIE_WINDOW
+                       : (flags & SMLA_ORACLE_P_DOWN) ? 1.0 - TIE_WINDOW : 1.0;
     const double log2_448 = log2(448.0);
     if (splits < 1 || chunk < 1) return -1;
 
@@ -221,12 +239,15 @@ int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, 
     double* m_split = (double*)malloc(sizeof(double) * splits);
     double* l_split = (double*)malloc(sizeof(double) * splits);
     double* acc = (double*)calloc((size_t)splits * LATENT, sizeof(double));
+    double* tie_acc = (double*)calloc((size_t)splits * LATENT, sizeof(double));
     double* s2 = (double*)malloc(sizeof(double) * chunk);
     double* prob = (double*)malloc(sizeof(double) * chunk);
+    double* spread = (double*)malloc(sizeof(double) * chunk);
 
     for (int s = 0; s < splits; ++s) {
         double m_run = -INFINITY, l_run = 0.0;
         double* a = acc + (size_t)s * LATENT;
+        double* ta = tie_acc + (size_t)s * LATENT;
         int c_first = s * per_split;
         int c_last = c_first + per_split < chunks ? c_first + per_split : chunks;
         for (int ck = c_first; ck < c_last; ++ck) {
@@ -255,8 +276,9 @@ int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, 
                 double x = 0.0;
                 if (s2[i] != -INFINITY) x = r32(exp2(r32(s2[i] - bias, exact)), exact);
                 chunk_sum = r32(chunk_sum + x, exact); /* sums of the unquantised P */
-                prob[i] = keep_p ? x
-                                 : smla_oracle_e4m3_to_double(smla_oracle_e4m3_from_float((float)x));
+                prob[i] = keep_p ? x : code_value(x * nudge);
+                /* the two codes P may take within the tie window */
+                spread[i] = keep_p ? 0.0 : code_value(x * (1.0 + TIE_WINDOW)) - code_value(x * (1.0 - TIE_WINDOW));
             }
             l_run = r32(r32(l_run * alpha, exact) + chunk_sum, exact);
             m_run = m_new;
@@ -269,6 +291,12 @@ int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, 
                     pv += prob[i] * smla_oracle_e4m3_to_double(row[j]);
                 }
                 a[j] = r32(r32(a[j] * alpha, exact) + pv, exact);
+                double tie = 0.0;
+                for (int i = 0; i < n; ++i) {
+                    if (spread[i] == 0.0) continue;
+                    tie += spread[i] * fabs(smla_oracle_e4m3_to_double(column_row(p, t, base + i)[j]));
+                }
+                ta[j] = ta[j] * alpha + tie;
             }
         }
         m_split[s] = m_run;
@@ -286,13 +314,16 @@ int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, 
     }
     double total = 0.0;
     double* merged = (double*)calloc(LATENT, sizeof(double));
+    double* tie_merged = (double*)calloc(LATENT, sizeof(double));
     if (!empty) {
         for (int s = 0; s < splits; ++s) {
             if (m_split[s] == -INFINITY) continue;
             double w = r32(exp2(m_split[s] - top), exact);
             total = r32(total + r32(w * l_split[s], exact), exact);
-            for (int j = 0; j < LATENT; ++j)
+            for (int j = 0; j < LATENT; ++j) {
                 merged[j] = r32(merged[j] + r32(w * acc[(size_t)s * LATENT + j], exact), exact);
+                tie_merged[j] += w * tie_acc[(size_t)s * LATENT + j];
+            }
         }
         if (p->sinks) {
             double sink2 = r32((double)p->sinks[h] * log2e, exact);
@@ -304,6 +335,7 @@ int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, 
         for (int j = 0; j < LATENT; ++j) {
             if (out_value) out_value[j] = 0.0;
             if (out_bf16) out_bf16[j] = 0;
+            if (tie_out) tie_out[j] = 0.0;
         }
         if (lse2_out) *lse2_out = -INFINITY;
     } else {
@@ -313,12 +345,16 @@ int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, 
             double value = exact ? merged[j] * out_scale / total : r32(merged[j] * inverse, 0);
             if (out_value) out_value[j] = value;
             if (out_bf16) out_bf16[j] = smla_oracle_bf16_from_float((float)value);
+            if (tie_out) tie_out[j] = tie_merged[j] * fabs(out_scale) / total;
         }
         if (lse2_out) *lse2_out = top - log2_448 + log2(total);
     }
+    free(tie_merged);
     free(merged);
+    free(spread);
     free(prob);
     free(s2);
+    free(tie_acc);
     free(acc);
     free(l_split);
     free(m_split);
@@ -554,7 +590,8 @@ int smla_oracle_fp64_pairs(const smla_oracle_problem* p, const int32_t* tokens,
 /* Emulating datapath over a list of (token, head) pairs. */
 int smla_oracle_emulate_pairs(const smla_oracle_problem* p, const int32_t* tokens,
                               const int32_t* heads, int n, int splits, int chunk, int flags,
-                              double* out_value, uint16_t* out_bf16, double* lse2, int threads) {
+                              double* out_value, uint16_t* out_bf16, double* lse2, double* tie,
+                              int threads) {
     int bad = 0;
 #ifdef _OPENMP
     if (threads > 0) omp_set_num_threads(threads);
@@ -564,7 +601,8 @@ int smla_oracle_emulate_pairs(const smla_oracle_problem* p, const int32_t* token
         bad |= smla_oracle_emulate(p, tokens[i], heads[i], splits, chunk, flags,
                                    out_value ? out_value + (size_t)i * LATENT : NULL,
                                    out_bf16 ? out_bf16 + (size_t)i * LATENT : NULL,
-                                   lse2 ? lse2 + i : NULL) != 0;
+                                   lse2 ? lse2 + i : NULL,
+                                   tie ? tie + (size_t)i * LATENT : NULL) != 0;
     (void)threads;
     return bad ? -1 : 0;
 }

@@ -36,7 +36,9 @@ typedef struct smla_oracle_problem {
 
 enum {
     SMLA_ORACLE_NO_P_ROUNDING = 1, /* keep P unrounded (no E4M3 step) */
-    SMLA_ORACLE_EXACT = 2          /* no FP32 roundings anywhere */
+    SMLA_ORACLE_EXACT = 2,         /* no FP32 roundings anywhere */
+    SMLA_ORACLE_P_UP = 4,          /* round P * (1 + 2^-16) to E4M3 (the upper code of the tie window) */
+    SMLA_ORACLE_P_DOWN = 8         /* round P * (1 - 2^-16) to E4M3 (the lower code) */
 };
 
 double smla_oracle_e4m3_to_double(uint8_t byte);
@@ -48,16 +50,20 @@ float smla_oracle_bf16_to_float(uint16_t bits);
 int smla_oracle_fp64(const smla_oracle_problem* p, int t, int h, double* out, double* lse2);
 
 /* The E4M3-P datapath on `splits` splits of `chunk`-column chunks: out_value
- * (pre-BF16 value, double), out_bf16 (bits) and the base-2 LSE; any may be NULL. */
+ * (pre-BF16 value, double), out_bf16 (bits), the base-2 LSE and tie_out[512],
+ * the most that P codes within a relative 2^-16 of a rounding midpoint can
+ * move each output value by taking their other code; any may be NULL. */
 int smla_oracle_emulate(const smla_oracle_problem* p, int t, int h, int splits, int chunk,
-                        int flags, double* out_value, uint16_t* out_bf16, double* lse2_out);
+                        int flags, double* out_value, uint16_t* out_bf16, double* lse2_out,
+                        double* tie_out);
 
 int smla_oracle_fp64_all(const smla_oracle_problem* p, double* out, double* lse2, int threads);
 int smla_oracle_fp64_pairs(const smla_oracle_problem* p, const int32_t* tokens,
                            const int32_t* heads, int n, double* out, double* lse2, int threads);
 int smla_oracle_emulate_pairs(const smla_oracle_problem* p, const int32_t* tokens,
                               const int32_t* heads, int n, int splits, int chunk, int flags,
-                              double* out_value, uint16_t* out_bf16, double* lse2, int threads);
+                              double* out_value, uint16_t* out_bf16, double* lse2, double* tie,
+                              int threads);
 int smla_oracle_max_threads(void);
 
 /* LSE merge of partial sets (the DCP owner's merge).

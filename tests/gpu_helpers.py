@@ -23,6 +23,10 @@ from sparse_mla_decode_gb300 import smla
 #    pages' own random workloads that already moves elements by up to ~3.7% of
 #    the row maximum, past a flat 2% -- the emulated datapath, which has no
 #    other error source, shows it;
+#  vs the emulated datapath, plus for each element the most that P values
+#    within a relative 2^-16 of an E4M3 rounding midpoint can move it by taking
+#    their other code (the oracle's tie bound): the GPU's FP32 logits and fast
+#    exp2 may put such a P on either side of the midpoint;
 #  |lse - lse_ref| <= 1e-3 (base 2).
 TOL_FP64 = 0.02
 TOL_EMU = 2e-3
@@ -137,13 +141,13 @@ def compare(w, got, got_bits, got_lse, pairs=None, emulate=True):
             failures.append(f"lse error {lerr.max()}")
     if emulate:
         plan = plan_of(w)
-        val, bits, emu_lse = oracle.emulate(prob, plan["splits"], plan["chunk"], pairs)
+        val, bits, emu_lse, ties = oracle.emulate(prob, plan["splits"], plan["chunk"], pairs, ties=True)
         if not np.array_equal(np.isneginf(emu_lse), empty):
             failures.append("emulated empty rows differ")
         if live.any():
             rowmax = np.abs(val[live]).max(axis=1, keepdims=True)
             err = np.abs(g[live] - val[live])
-            bound = TOL_EMU * rowmax + bf16_ulp(val[live])
+            bound = TOL_EMU * rowmax + bf16_ulp(val[live]) + ties[live]
             worst = (err / bound).max()
             report["emu_worst_frac_of_bound"] = round(float(worst), 4)
             report["emu_max_rel_err"] = round(float((err / rowmax).max()), 6)

@@ -273,6 +273,52 @@ def test_p_anchors_at_the_running_max():
     assert np.abs(val1[0] - exact).max() > 1e-3 * np.abs(exact).max()
 
 
+def test_tie_window_bound_covers_both_codes_of_a_midpoint_p():
+    """A P that lands on a rounding midpoint of E4M3 (46, between the codes 44
+    and 48) may take either code under the datapath's FP32 arithmetic (Kimi
+    K3.1 attn_sparse page, "Precision": FP32 logits of FP8 products in an
+    unspecified order, a fast exp2). Two keys: the first scores the maximum (P
+    = 448), the second is placed by bmm1_scale at P = 448 * 2^log2(46/448). The
+    two codes move the output by 4 * V_2 * out_scale / l in closed form, and
+    the emulation's tie bound is exactly that spread."""
+    w = workloads.small("tie", seed=31, tokens=1, heads=16, width=2, head_dim=576, pool_rows=64, lens=[2])
+    w["indices"][0] = [3, 9]
+    q, k1, k2 = dec(w["q"][0, 0]), dec(w["pools"][0][3]), dec(w["pools"][0][9])
+    s1, s2 = q @ k1, q @ k2
+    if s1 < s2:
+        w["indices"][0] = [9, 3]
+        s1, s2, k1, k2 = s2, s1, k2, k1
+    w["bmm1_scale"] = math.log2(46.0 / 448.0) / ((s2 - s1) * LOG2E)
+    w["bmm2_scale"], w["k_scale"] = 0.5, 1.0
+    prob = oracle.Problem.from_workload(w)
+    val, _, _, tie = oracle.emulate(prob, 1, 128, pairs=[(0, 0)], ties=True)
+    up, _, _ = oracle.emulate(prob, 1, 128, pairs=[(0, 0)], flags=oracle.P_UP)
+    down, _, _ = oracle.emulate(prob, 1, 128, pairs=[(0, 0)], flags=oracle.P_DOWN)
+    l = 448.0 + 46.0
+    spread = 4.0 * k2[:512] * 0.5 / l
+    # the outputs carry FP32 roundings of values up to ~0.5 (2^-24 each)
+    assert np.allclose(up[0] - down[0], spread, rtol=0, atol=2e-7)
+    assert np.allclose(tie[0], np.abs(spread), rtol=1e-6, atol=0)
+    assert np.all((val[0] == up[0]) | (val[0] == down[0]))
+
+
+@pytest.mark.parametrize("splits,chunk", [(1, 256), (3, 128), (2, 64)])
+def test_tie_bound_is_zero_without_midpoints_and_covers_the_other_codes(splits, chunk):
+    """On random workloads the codes of the window's two edges differ only
+    where the tie bound is positive, and never by more than it."""
+    w = workloads.small("ties", seed=32 + splits, tokens=3, heads=32, width=700, head_dim=576, pool_rows=4096,
+                        holes=0.05, sinks=True, lens=[700, 333, 9])
+    prob = oracle.Problem.from_workload(w)
+    val, _, _, tie = oracle.emulate(prob, splits, chunk, ties=True)
+    up, _, _ = oracle.emulate(prob, splits, chunk, flags=oracle.P_UP)
+    down, _, _ = oracle.emulate(prob, splits, chunk, flags=oracle.P_DOWN)
+    gap = np.maximum(np.abs(up - val), np.abs(down - val))
+    assert np.all(gap <= tie * (1 + 1e-6) + 1e-7 * np.abs(val).max())
+    quiet = tie.max(axis=1) == 0
+    assert quiet.mean() > 0.5  # most rows have no P near a midpoint
+    assert np.array_equal(up[quiet], val[quiet]) and np.array_equal(down[quiet], val[quiet])
+
+
 def test_one_chunk_matches_a_float32_library_evaluation():
     """One split, one chunk: the datapath is P = E4M3(2^(s2 - m + log2 448))
     with FP32 logits, sums of the unrounded P, FP32 PV, one BF16 rounding --
