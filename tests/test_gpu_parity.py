@@ -101,30 +101,67 @@ def env():
             os.environ[name] = value
 
 
-PAIRED = [
-    # heads, head_dim, width, forced head tile, forced splits, lens
-    (128, 576, 2048, None, None, [2048, 1000, 5]),
-    (128, 576, 700, None, 3, [700, 699, 300]),
-    (64, 512, 1300, 16, 2, [1300, 640, 641]),
-    (32, 576, 257, 16, 1, [257, 0, 128]),
-    (128, 576, 900, 32, 8, [900, 129, 850]),
+PAIR_KERNEL = [
+    # tokens, heads, head_dim, width, lens, holes, sinks, two pools (split column)
+    (3, 128, 576, 2048, [2048, 1000, 5], 0.07, True, None),
+    (3, 128, 576, 700, [700, 699, 300], 0.0, False, None),
+    (3, 128, 512, 1300, [1300, 640, 641], 0.07, True, None),
+    (3, 256, 576, 257, [257, 0, 128], 0.05, True, None),
+    (4, 128, 512, 640, [640, 300, 129, 0], 0.05, True, 128),
+    (2, 128, 576, 256, [256, 255], 0.0, False, None),
 ]
 
 
-@pytest.mark.parametrize("case", PAIRED, ids=[f"h{c[0]}_d{c[1]}_w{c[2]}_t{c[3]}_s{c[4]}" for c in PAIRED])
-def test_paired_head_groups(env, case):
-    """Head-group pairs sharing each chunk's gather (tile::gather4 multicast),
-    with and without split merges across the pair's cluster."""
-    heads, dim, width, tile, splits, lens = case
-    env("SMLA_PAIR", 1)
-    env("SMLA_HEAD_TILE", tile)
-    env("SMLA_SPLITS", splits)
-    w = workloads.small("paired", seed=heads + width, tokens=3, heads=heads, width=width, head_dim=dim,
-                        pool_rows=6000, holes=0.07, sinks=True, lens=lens)
+@pytest.mark.parametrize("case", PAIR_KERNEL,
+                         ids=[f"t{c[0]}_h{c[1]}_d{c[2]}_w{c[3]}{'_pools' if c[7] else ''}" for c in PAIR_KERNEL])
+def test_pair_kernel(env, case):
+    """The 128-head CTA-pair kernel (cta_group::2 products, the softmax over
+    256-key chunks split across the pair) on ragged counts, holes, sinks, two
+    pools, 512-byte rows, two head groups and an empty token."""
+    tokens, heads, dim, width, lens, holes, sinks, split = case
+    env("SMLA_KERNEL", "pair")
+    w = workloads.small("pair", seed=heads + width + tokens, tokens=tokens, heads=heads, width=width,
+                        head_dim=dim, pool_rows=6000, holes=holes, sinks=sinks, lens=lens,
+                        two_pools=split is not None, pool_split=split or 0)
     plan = plan_of(w)
-    assert plan["pair"] == 2
+    assert (plan["pair"], plan["head_tile"], plan["chunk"], plan["splits"]) == (2, 128, 256, 1)
     got, bits, lse = run_gpu(w)
     print(case, plan, compare(w, got, bits, lse))
+
+
+@pytest.mark.parametrize("kernel", ["tile", "pair"])
+def test_128_heads_both_kernels(env, kernel):
+    """The same 128-head workload through either kernel, each against the
+    oracle's emulation of its own partition (128- or 256-column chunks)."""
+    env("SMLA_KERNEL", kernel)
+    w = workloads.small("both", seed=404, tokens=5, heads=128, width=600, head_dim=576, pool_rows=8192,
+                        holes=0.1, sinks=True, lens=[600, 599, 1, 256, 300])
+    got, bits, lse = run_gpu(w)
+    print(kernel, plan_of(w), compare(w, got, bits, lse))
+
+
+# Launches of more CTAs than the GPU holds at once (several waves), sampled
+# against both oracle modes: the sweep's 256-token points at 128 and 16 heads,
+# and its recipe of 10% holes with counts uniform in [k/2, k].
+MULTI_WAVE = [
+    # tokens, heads, width, holes, counts in [k/2, k]
+    (256, 128, 2048, 0.0, False),
+    (256, 16, 256, 0.0, False),
+    (128, 64, 1024, 0.1, True),
+]
+
+
+@pytest.mark.parametrize("case", MULTI_WAVE, ids=[f"t{c[0]}_h{c[1]}_k{c[2]}" for c in MULTI_WAVE])
+def test_multi_wave_launches_sampled(case):
+    tokens, heads, width, holes, ragged = case
+    w = workloads.sweep_point(tokens, heads, width, seed=tokens * 7 + heads + width, pool_rows=1 << 18) if ragged else \
+        workloads.small("waves", seed=tokens + heads + width, tokens=tokens, heads=heads, width=width, head_dim=576,
+                        pool_rows=1 << 18, holes=holes)
+    plan = plan_of(w)
+    got, bits, lse = run_gpu(w)
+    rng = np.random.default_rng(tokens + heads)
+    pairs = np.stack([rng.integers(0, tokens, 64), rng.integers(0, heads, 64)], axis=1)
+    print(case, plan, compare(w, got, bits, lse, pairs=pairs))
 
 
 def test_two_pools_ragged_split_boundary():
