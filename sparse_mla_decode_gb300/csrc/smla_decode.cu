@@ -979,6 +979,19 @@ bool encode_q_map(CUtensorMap* map, const void* q, const smla_shape* s, int n, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pool rows of `d` bytes, read by tile::gather4 in boxes of `box` bytes x 1 row.
+bool encode_kv_map(CUtensorMap* map, const void* pool, int64_t rows, int d, int box, CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr || rows <= 0) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d)};
+    const cuuint32_t boxes[2] = {static_cast<cuuint32_t>(box), 1};
+    const cuuint32_t steps[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, boxes, steps,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int device_sms() {
     static std::mutex mu;
     static int cache[64] = {0};
@@ -1230,6 +1243,11 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
         pp.num_pools = shape->num_pools;
         pp.scale_log2 = scale_log2;
         pp.out_scale = out_scale;
+        pp.peer_tma = encode_kv_map(&pp.kv0, kv_pools[0].data, kv_pools[0].rows, shape->head_dim, 128,
+                                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+                      (shape->num_pools == 1 ||
+                       encode_kv_map(&pp.kv1, second.data, second.rows, shape->head_dim, 128,
+                                     CU_TENSOR_MAP_SWIZZLE_128B));
         e = launch_pair(pp, shape->head_dim, plan.head_groups, shape->tokens, dependent_launch(), st);
         if (e != cudaSuccess) {
             t_last_cuda_error = static_cast<int>(e);

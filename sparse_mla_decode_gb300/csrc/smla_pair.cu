@@ -40,10 +40,13 @@
 //         128 (TMEM lane t of S^T) and latent row t of each O^T block;
 //   8     allocates TMEM (both CTAs together); in CTA 0 one thread issues the
 //         pair's MMAs, in CTA 1 one thread relays that its copies landed;
-//   9-15  producers: the chunk's 256 indices, 16-byte cp.async copies of
-//         the CTA's own rows into 128B-swizzled K-major tiles (a latent row
-//         per warp instruction, masked keys zero-filled), then, once QK is
-//         done, the peer keys' latent half.
+//   9-14  producers of the CTA's own rows: the chunk's indices (loaded a
+//         chunk ahead), 16-byte cp.async copies into 128B-swizzled K-major
+//         tiles (a latent row per warp instruction, masked keys zero-filled),
+//         and an L2 prefetch of the next chunk's rows;
+//   15    producer of the peer keys' latent half, once QK is done: TMA
+//         tile::gather4 (four rows of 128 bytes per instruction, on the SM's
+//         TMA unit beside the warps' cp.async; rows past a pool read as zeros).
 // Every wait is bounded; a timeout sets an error bit, tells the peer, and
 // the kernel still passes every barrier and frees its TMEM.
 
@@ -65,9 +68,10 @@ namespace pair {
 constexpr int kKeys = 128;   // keys of one CTA per chunk (its 128 MMA rows)
 constexpr int kHalf = 64;    // heads whose Q and P^T one CTA holds
 constexpr int kMmaWarp = 8;
-constexpr int kProducerWarp = 9;
-constexpr int kProducerThreads = 224;
-constexpr int kProducerWarps = kProducerThreads / 32;
+constexpr int kProducerWarp = 9;  // first of the own-row producers
+constexpr int kProducerWarps = 6;
+constexpr int kProducerThreads = kProducerWarps * 32;
+constexpr int kPeerWarp = kProducerWarp + kProducerWarps;  // 15
 constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
@@ -83,8 +87,13 @@ struct Layout {
     static constexpr int kQBytes = 4 * kHalf * 128 + (kRope ? kHalf * 64 : 0);
     static constexpr int kPBytes = kPairChunk * kHalf;  // P^T [256 keys][64 heads]
     static constexpr int kP = kQ + kQBytes;             // 2 buffers
-    static constexpr int kIdx = kP + 2 * kPBytes;       // int32 [2][256] row of each key, -1 masked
-    static constexpr int kRed = kIdx + 2 * kPairChunk * 4;  // float [2 warpgroups][4 warps][64]
+    // P^T of this CTA's keys for the peer's heads, staged for one bulk copy
+    // into the peer (8 KB): the rope block of the chunk's stage, which only QK
+    // reads; rows of 512 bytes have no rope block and get two of their own.
+    static constexpr int kPStageBytes = kKeys * kHalf;
+    static constexpr int kPStage = kP + 2 * kPBytes;
+    static constexpr int kIdx = kPStage + (kRope ? 0 : 2 * kPStageBytes);  // int32 [2][128] own keys' rows, -1 masked
+    static constexpr int kRed = kIdx + 2 * kKeys * 4;  // float [2 warpgroups][4 warps][64]
     static constexpr int kHead = kRed + 2 * 4 * kHalf * 4;  // float [4][128]: m_run, bias, alpha, l
     static constexpr int kPeer = kHead + 4 * kPairHeads * 4;  // float [2][128] peer maxima, [128] peer sums
     static constexpr int kBar = kPeer + 3 * kPairHeads * 4;
@@ -94,23 +103,28 @@ struct Layout {
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kAlloc <= 227 * 1024, "shared memory");
     static_assert(2 * kStage >= kPairHeads * 256 * 2, "the output tile reuses the stages");
+    // where chunk c's staged P^T goes: stage b's rope block, or its own area
+    static constexpr int p_stage(int b) { return kRope ? kKv + b * kStage + 4 * kBlock : kPStage + b * kPStageBytes; }
 };
 
 // Barriers (indices into the CTA's array).
 enum : int {
     kOwnFull = 0,    // [2] this CTA's rows of a stage landed (producer cp.async arrivals + index release)
-    kPeerFull = 2,   // [2] the peer keys' latent half landed (producer cp.async arrivals)
+    kPeerFull = 2,   // [2] the peer keys' latent half landed (TMA bytes + the peer warp's cp.async arrivals)
     kSFull = 4,      // [2] QK of the stage's chunk done (commit of the pair's MMAs)
     kPvDone = 6,     // [2] PV of the stage's chunk done (commit)
     kQFull = 8,      // this CTA's Q half landed (TMA bytes)
-    kPmaxFull = 9,   // [2 buffers][2 warpgroups] the peer's chunk maxima arrived
+    kPmaxFull = 9,   // [2 buffers][2 warpgroups] the peer's chunk maxima arrived (st.async bytes + local arm)
     kLFull = 13,     // the peer's per-head sums arrived
     kDrain = 14,     // CTA 0: every MMA done
     kRelayOwn = 15,  // CTA 0: [2] CTA 1's rows of a stage landed
     kRelayPeer = 17, // CTA 0: [2] CTA 1's peer half of a stage landed
     kRelayQ = 19,    // CTA 0: CTA 1's Q half landed
-    kPFull = 20,     // CTA 0: P^T of a chunk written and O^T rescaled in both CTAs (16 warp arrivals)
+    kPLocal = 20,    // P^T written here and O^T rescaled (the CTA's eight softmax warps), per chunk
+    kPRemote = 21,   // [2] the peer's part of this CTA's P^T landed (bulk-copy bytes + local arm)
+    kRelayP = 23,    // CTA 0: CTA 1's P^T complete and O^T rescaled, per chunk
 };
+static_assert(kRelayP < Layout<576>::kNumBars, "barriers");
 
 __device__ __forceinline__ const uint8_t* row_of(const PairParams& p, int col, int32_t id, int d) {
     const bool second = p.num_pools == 2 && col >= p.pool_split;
@@ -162,8 +176,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
     if (tid == 0) {
         mbar_init(&bars[kOwnFull + 0], kProducerThreads + 1);
         mbar_init(&bars[kOwnFull + 1], kProducerThreads + 1);
-        mbar_init(&bars[kPeerFull + 0], kProducerThreads);
-        mbar_init(&bars[kPeerFull + 1], kProducerThreads);
+        mbar_init(&bars[kPeerFull + 0], 32 + 1);  // the peer warp's cp.async arrivals + its expect-tx arrival
+        mbar_init(&bars[kPeerFull + 1], 32 + 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[kSFull + i], 1);
             mbar_init(&bars[kPvDone + i], 1);
@@ -171,11 +185,14 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
             mbar_init(&bars[kRelayPeer + i], 1);
         }
         mbar_init(&bars[kQFull], 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[kPmaxFull + i], 2);  // two warps of the peer's warpgroup
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[kPmaxFull + i], 1);  // the local arm; the bytes come by st.async
         mbar_init(&bars[kLFull], 4);                                      // the peer's four head warps
         mbar_init(&bars[kDrain], 1);
         mbar_init(&bars[kRelayQ], 1);
-        mbar_init(&bars[kPFull], 16);  // eight softmax warps in each CTA
+        mbar_init(&bars[kPLocal], 8);  // the CTA's eight softmax warps
+        mbar_init(&bars[kPRemote + 0], 1);
+        mbar_init(&bars[kPRemote + 1], 1);
+        mbar_init(&bars[kRelayP], 1);
         misc[1] = 0;
         mbar_init_fence();
     }
@@ -192,6 +209,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensor_map(&p.q_latent);
         if constexpr (L::kRope) prefetch_tensor_map(&p.q_rope);
+    }
+    if (warp == kPeerWarp && lane == 0 && p.peer_tma) {
+        prefetch_tensor_map(&p.kv0);
+        if (p.num_pools == 2) prefetch_tensor_map(&p.kv1);
     }
     tc_fence_before_sync();
     cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
@@ -212,38 +233,32 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
     grid_launch_dependents();
 
     bool ok = true;
-    if (warp >= kProducerWarp) {
-        // ================================================== producers
-        // Thread g < 128 resolves columns g and 128 + g of the chunk; warp w
-        // then copies the CTA's keys w, w + 7, ... (one 512-byte latent row
-        // per instruction, lane l: bytes 16 l .. 16 l + 15; the 64-byte
-        // ropes of eight keys per instruction), and after QK the peer keys'
-        // 256 latent bytes this CTA multiplies, two keys per instruction.
+    if (warp >= kProducerWarp && warp < kPeerWarp) {
+        // ========================================= own-row producers
+        // Thread g < 128 loads and resolves column g of the CTA's half of a
+        // chunk (the load a chunk ahead); warp w copies the CTA's keys w,
+        // w + 6, ... (one 512-byte latent row per instruction, lane l: bytes
+        // 16 l .. 16 l + 15) and the 64-byte ropes of eight keys per
+        // instruction, then asks L2 for the next chunk's rows.
         const int g = tid - kProducerWarp * 32;
         const int pw = g >> 5;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
-        const int own0 = kKeys * static_cast<int>(rank), other0 = kKeys * static_cast<int>(peer);
-        const int src_blk = rank == 0 ? 0 : 2;  // the peer-key blocks this CTA's PV reads
-        const int dst_blk = rank == 0 ? 2 : 0;  // this CTA's blocks its own PV never reads
+        const int own0 = kKeys * static_cast<int>(rank);
+        int32_t raw = -1;
+        if (g < kKeys && own0 + g < count) raw = idx_row[own0 + g];
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
             const int col0 = c * kPairChunk;
-            // the chunk's indices load before the wait for its stage
-            int32_t raw0 = -1, raw1 = -1;
-            if (g < kKeys) {
-                if (col0 + g < count) raw0 = idx_row[col0 + g];
-                if (col0 + kKeys + g < count) raw1 = idx_row[col0 + kKeys + g];
-            }
+            const int next_col = col0 + kPairChunk + own0 + g;
+            int32_t raw_next = -1;
+            if (g < kKeys && next_col < count) raw_next = idx_row[next_col];
             if (c >= 2) ok &= mbar_wait_bounded(&bars[kPvDone + b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
-            if (g < kKeys) {
-                idx_s[b * kPairChunk + g] = resolve(p, col0 + g, raw0);
-                idx_s[b * kPairChunk + kKeys + g] = resolve(p, col0 + kKeys + g, raw1);
-            }
+            if (g < kKeys) idx_s[b * kKeys + g] = resolve(p, col0 + own0 + g, raw);
             named_barrier(3, kProducerThreads);
             if (g == 0) mbar_arrive(&bars[kOwnFull + b]);  // also releases idx_s to the softmax
             const uint32_t stage = sbase + L::kKv + b * L::kStage;
             for (int k = pw; k < kKeys; k += kProducerWarps) {
-                const int32_t id = idx_s[b * kPairChunk + own0 + k];
+                const int32_t id = idx_s[b * kKeys + k];
                 const uint8_t* src = row_of(p, col0 + own0 + k, id, D) + lane * 16;
                 const uint32_t dst =
                     stage + (lane >> 3) * L::kBlock + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
@@ -252,7 +267,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
             if constexpr (L::kRope) {
                 for (int j = pw; j < kKeys / 8; j += kProducerWarps) {
                     const int k = j * 8 + (lane >> 2), u = lane & 3;
-                    const int32_t id = idx_s[b * kPairChunk + own0 + k];
+                    const int32_t id = idx_s[b * kKeys + k];
                     const uint8_t* src = row_of(p, col0 + own0 + k, id, D) + 512 + u * 16;
                     const uint32_t dst =
                         stage + 4 * L::kBlock + (k >> 3) * 512 + (k & 7) * 64 + ((u ^ ((k >> 1) & 3)) << 4);
@@ -260,18 +275,81 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                 }
             }
             cp_async_arrive_noinc(&bars[kOwnFull + b]);
-            // the dead blocks are free once QK of this chunk has read them
+            // the next chunk's rows start their way from HBM into L2 now
+            if (g < kKeys && raw_next >= 0) {
+                const bool second = p.num_pools == 2 && next_col >= p.pool_split;
+                if (raw_next < (second ? p.rows1 : p.rows0)) prefetch_l2(row_of(p, next_col, raw_next, D), D);
+            }
+            raw = raw_next;
+        }
+        cp_async_wait_all();
+    } else if (warp == kPeerWarp) {
+        // =========================================== peer-half producer
+        // Lane l takes keys 4 l .. 4 l + 3 of the peer's half of a chunk. Once
+        // QK of the chunk has read this CTA's dead blocks, the lane's four
+        // rows' 256 latent bytes this CTA multiplies in PV (CTA 0: bytes
+        // 0..255 into its blocks 2, 3; CTA 1: 256..511 into its blocks 0, 1)
+        // come by two tile::gather4 copies; a masked key names a row past its
+        // pool (zero fill). Four keys that straddle the pools' boundary, or a
+        // pool without a tensor map, are copied by cp.async instead.
+        const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
+        const int other0 = kKeys * static_cast<int>(peer);
+        const int src_x = rank == 0 ? 0 : 256;
+        const int dst_blk = rank == 0 ? 2 : 0;
+        int32_t raw[4], raw_next[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int col = other0 + 4 * lane + i;
+            raw[i] = col < count ? idx_row[col] : -1;
+        }
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            const int col0 = c * kPairChunk + other0 + 4 * lane;  // this lane's first column
+            int32_t id[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                // out-of-pool indices are flagged by the CTA that owns the column
+                const bool second = p.num_pools == 2 && col0 + i >= p.pool_split;
+                id[i] = (raw[i] >= 0 && raw[i] < (second ? p.rows1 : p.rows0)) ? raw[i] : -1;
+                const int col = col0 + kPairChunk + i;
+                raw_next[i] = col < count ? idx_row[col] : -1;
+            }
+            const bool first_second = p.num_pools == 2 && col0 >= p.pool_split;
+            const bool last_second = p.num_pools == 2 && col0 + 3 >= p.pool_split;
+            const bool by_tma = p.peer_tma && first_second == last_second;
+            const uint32_t tma_lanes = __ballot_sync(0xFFFFFFFFu, by_tma);
             ok &= mbar_wait_bounded(&bars[kSFull + b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
-            for (int k2 = pw; k2 < kKeys / 2; k2 += kProducerWarps) {
-                const int k = 2 * k2 + (lane >> 4), v = lane & 15;  // v: 16-byte unit of the 256 bytes
-                const int32_t id = idx_s[b * kPairChunk + other0 + k];
-                const uint8_t* src = row_of(p, col0 + other0 + k, id, D) + src_blk * 128 + v * 16;
-                const int u = v & 7;
-                const uint32_t dst = stage + (dst_blk + (v >> 3)) * L::kBlock + (k >> 3) * 1024 + (k & 7) * 128 +
-                                     ((u ^ (k & 7)) << 4);
-                cp_async_16(dst, src, id >= 0 ? 16u : 0u);
+            const uint32_t stage = sbase + L::kKv + b * L::kStage;
+            const int k = 4 * lane;  // first of the lane's four keys in the tile
+            if (lane == 0) mbar_arrive_expect_tx(&bars[kPeerFull + b], __popc(tma_lanes) * 4 * 256);
+            __syncwarp();
+            if (by_tma) {
+                const void* map = first_second ? static_cast<const void*>(&p.kv1) : static_cast<const void*>(&p.kv0);
+                const int32_t past_end = static_cast<int32_t>(first_second ? p.rows1 : p.rows0);
+                int32_t r[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) r[i] = id[i] >= 0 ? id[i] : past_end;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tma_gather4(stage + (dst_blk + h) * L::kBlock + (k >> 3) * 1024 + (k & 7) * 128, map,
+                                src_x + 128 * h, r[0], r[1], r[2], r[3], &bars[kPeerFull + b]);
+            } else {
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+                    const uint8_t* row = row_of(p, col0 + i, id[i], D) + src_x;
+                    const int kk = k + i;
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) {
+                        const int u = v & 7;
+                        const uint32_t dst = stage + (dst_blk + (v >> 3)) * L::kBlock + (kk >> 3) * 1024 +
+                                             (kk & 7) * 128 + ((u ^ (kk & 7)) << 4);
+                        cp_async_16(dst, row + v * 16, id[i] >= 0 ? 16u : 0u);
+                    }
+                }
             }
             cp_async_arrive_noinc(&bars[kPeerFull + b]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) raw[i] = raw_next[i];
         }
         cp_async_wait_all();
     } else if (warp == kMmaWarp) {
@@ -292,7 +370,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
             const uint64_t d_p = smem_desc(sbase + L::kP, 512, 512, kSwizzle64B);
             const uint32_t s_full_peer = peer_addr(&bars[kSFull]);
             const uint32_t pv_done_peer = peer_addr(&bars[kPvDone]);
-            int next_qk = 0, next_pv = 0;
+            int next_qk = 0, next_pv = 0, armed = 0;  // armed: chunks whose P^T bytes this thread expects
             bool q_ready = false;
             uint64_t idle_since = 0;
             while (next_pv < nch) {
@@ -327,7 +405,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                 if (next_pv < next_qk) {
                     const int c = next_pv, b = c & 1;
                     const uint32_t par = (c >> 1) & 1;
-                    if (mbar_test_wait_cluster(&bars[kPFull], c & 1) && mbar_test_wait(&bars[kPeerFull + b], par) &&
+                    if (armed == c) {  // the peer's bulk copy of this chunk's P^T part
+                        mbar_arrive_expect_tx(&bars[kPRemote + b], L::kPStageBytes);
+                        ++armed;
+                    }
+                    if (mbar_test_wait(&bars[kPLocal], c & 1) && mbar_test_wait_cluster(&bars[kPRemote + b], par) &&
+                        mbar_test_wait_cluster(&bars[kRelayP], c & 1) && mbar_test_wait(&bars[kPeerFull + b], par) &&
                         mbar_test_wait_cluster(&bars[kRelayPeer + b], par)) {
                         fence_proxy_async_all();
                         tc_fence_after_sync();
@@ -372,10 +455,26 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
             ok &= mbar_wait_bounded(&bars[kQFull], 0, abort_flag, kWaitLimitNs);
             fence_proxy_async_all();
             mbar_arrive_cluster(leader_addr(&bars[kRelayQ]));
-            int next_own = 0, next_peer = 0;
+            int next_own = 0, next_peer = 0, next_p = 0, armed = 0;
             uint64_t idle_since = 0;
-            while (next_peer < nch) {
+            while (next_peer < nch || next_p < nch) {
                 bool progressed = false;
+                if (next_p < next_own) {
+                    const int b = next_p & 1;
+                    if (armed == next_p) {
+                        mbar_arrive_expect_tx(&bars[kPRemote + b], L::kPStageBytes);
+                        ++armed;
+                    }
+                    if (mbar_test_wait(&bars[kPLocal], next_p & 1) &&
+                        mbar_test_wait_cluster(&bars[kPRemote + b], (next_p >> 1) & 1)) {
+                        tc_fence_after_sync();
+                        fence_proxy_async_all();
+                        tc_fence_before_sync();
+                        mbar_arrive_cluster(leader_addr(&bars[kRelayP]));
+                        ++next_p;
+                        progressed = true;
+                    }
+                }
                 if (next_own < nch && mbar_test_wait(&bars[kOwnFull + (next_own & 1)], (next_own >> 1) & 1)) {
                     fence_proxy_async_all();
                     mbar_arrive_cluster(leader_addr(&bars[kRelayOwn + (next_own & 1)]));
@@ -409,7 +508,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
         const int wg = warp >> 2, quarter = warp & 3, t = tid & 127, hw = kHalf * wg;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const float scale_log2 = p.scale_log2;
-        // P^T of these heads lives in CTA wg: its own buffer or the peer's
+        // P^T of these heads lives in CTA wg: written straight into its own
+        // buffer, or staged here and sent to the peer by one bulk copy
         const bool p_local = static_cast<uint32_t>(wg) == rank;
         const uint32_t p_row = kKeys * rank + t;  // this key's row of the chunk's P^T
         float lsum[kHalf];
@@ -422,33 +522,42 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
             ok &= mbar_wait_bounded(&bars[kOwnFull + b], par, abort_flag, kWaitLimitNs);
             ok &= mbar_wait_bounded(&bars[kSFull + b], par, abort_flag, kWaitLimitNs);
             tc_fence_after_sync();
-            const bool active = idx_s[b * kPairChunk + kKeys * rank + t] >= 0;
+            const bool active = idx_s[b * kKeys + t] >= 0;
             const uint32_t s_col = tmem + lane_base + b * kPairHeads + hw;
 
             // chunk maxima per head over this CTA's keys (raw logits;
-            // bmm1_scale > 0 keeps the order, masked keys are -inf)
+            // bmm1_scale > 0 keeps the order, masked keys are -inf), 32 heads
+            // at a time: a transposing butterfly, each step hands half of a
+            // lane's heads to its partner, so that lane l ends with head l
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float s[32];
-                tmem_load32x1(s_col + 32 * half, s);
-                float mine = -INFINITY;
+                float v[32];
+                tmem_load32x1(s_col + 32 * half, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float m = warp_max(active ? s[j] : -INFINITY);
-                    mine = (lane == j) ? m : mine;
+                for (int j = 0; j < 32; ++j) v[j] = active ? v[j] : -INFINITY;
+#pragma unroll
+                for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+                    const bool up = (lane & o) != 0;
+#pragma unroll
+                    for (int i = 0; i < n / 2; ++i) {
+                        const float send = up ? v[i] : v[i + n / 2];
+                        const float keep = up ? v[i + n / 2] : v[i];
+                        v[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+                    }
                 }
-                red[(wg * 4 + quarter) * kHalf + 32 * half + lane] = mine;
+                red[(wg * 4 + quarter) * kHalf + 32 * half + lane] = v[0];
             }
             named_barrier(1 + wg, 128);
             if (t < kHalf) {
-                // head hw + t: the CTA's maximum to the peer, the peer's back,
-                // and the same running maximum in both CTAs
+                // head hw + t: the CTA's maximum to the peer (st.async, the
+                // bytes counted on the peer's barrier), the peer's back, and
+                // the same running maximum in both CTAs
                 const float* r = red + wg * 4 * kHalf + t;
                 const float cm = fmaxf(fmaxf(r[0], r[kHalf]), fmaxf(r[2 * kHalf], r[3 * kHalf]));
-                st_cluster_f32(peer_addr(&pmax_s[b * kPairHeads + hw + t]), cm);
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(peer_addr(&bars[kPmaxFull + 2 * b + wg]));
-                ok &= mbar_wait_cluster_bounded(&bars[kPmaxFull + 2 * b + wg], par, abort_flag, kWaitLimitNs);
+                uint64_t* pmax_bar = &bars[kPmaxFull + 2 * b + wg];
+                st_async_f32(peer_addr(&pmax_s[b * kPairHeads + hw + t]), cm, peer_addr(pmax_bar));
+                if (t == 0) mbar_arrive_expect_tx(pmax_bar, kHalf * 4);
+                ok &= mbar_wait_cluster_bounded(pmax_bar, par, abort_flag, kWaitLimitNs);
                 const float both = fmaxf(cm, pmax_s[b * kPairHeads + hw + t]);
                 const int h = hw + t;
                 const float mo = m_run_s[h];
@@ -459,17 +568,18 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
             }
             named_barrier(1 + wg, 128);
 
-            // P = 2^(s * scale_log2 - m + log2 448) as E4M3 into P^T[b] of the
-            // CTA holding these heads (PV of chunk c - 2 has finished reading
-            // it in both CTAs); FP32 sums of the unrounded P
+            // P = 2^(s * scale_log2 - m + log2 448) as E4M3 (PV of chunk c - 2
+            // has finished reading P^T[b] in both CTAs); FP32 sums of the
+            // unrounded P. Rows of 64 heads (64 bytes), 16-byte units swizzled
+            // (64B) as the PV's B operand reads them.
             if (c >= 2) ok &= mbar_wait_bounded(&bars[kPvDone + b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             {
-                const uint32_t pbuf = sbase + L::kP + b * L::kPBytes;
-                const uint32_t pdst = p_local ? pbuf : map_to_rank(pbuf, peer);
+                uint8_t* prow = p_local ? smem + L::kP + b * L::kPBytes + p_row * 64
+                                        : smem + L::p_stage(b) + t * 64;
 #pragma unroll
                 for (int gq = 0; gq < 4; ++gq) {
-                    float s[16];
-                    tmem_load16x1(s_col + 16 * gq, s);
+                    float sv[16];
+                    tmem_load16x1(s_col + 16 * gq, sv);
                     uint32_t words[4];
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
@@ -478,10 +588,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                         const float4 al = reinterpret_cast<const float4*>(alpha_s + hw)[j / 4];
                         float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                         if (active) {
-                            pr[0] = fast_exp2(fmaf(s[4 * q4 + 0], scale_log2, -bi.x));
-                            pr[1] = fast_exp2(fmaf(s[4 * q4 + 1], scale_log2, -bi.y));
-                            pr[2] = fast_exp2(fmaf(s[4 * q4 + 2], scale_log2, -bi.z));
-                            pr[3] = fast_exp2(fmaf(s[4 * q4 + 3], scale_log2, -bi.w));
+                            pr[0] = fast_exp2(fmaf(sv[4 * q4 + 0], scale_log2, -bi.x));
+                            pr[1] = fast_exp2(fmaf(sv[4 * q4 + 1], scale_log2, -bi.y));
+                            pr[2] = fast_exp2(fmaf(sv[4 * q4 + 2], scale_log2, -bi.z));
+                            pr[3] = fast_exp2(fmaf(sv[4 * q4 + 3], scale_log2, -bi.w));
                         }
                         lsum[j + 0] = fmaf(lsum[j + 0], al.x, pr[0]);
                         lsum[j + 1] = fmaf(lsum[j + 1], al.y, pr[1]);
@@ -489,13 +599,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                         lsum[j + 3] = fmaf(lsum[j + 3], al.w, pr[3]);
                         words[q4] = e4m3x2(pr[0], pr[1]) | (e4m3x2(pr[2], pr[3]) << 16);
                     }
-                    // P^T rows of 64 heads (64 bytes), 16-byte units swizzled (64B)
-                    const uint32_t off = p_row * 64 + ((gq ^ ((p_row >> 1) & 3)) << 4);
-                    if (p_local)
-                        *reinterpret_cast<uint4*>(smem + L::kP + b * L::kPBytes + off) =
-                            make_uint4(words[0], words[1], words[2], words[3]);
-                    else
-                        st_cluster_v4(pdst + off, words[0], words[1], words[2], words[3]);
+                    // the swizzle of row p_row; the staged rows (p_row - 128 r)
+                    // share it, 128 r being a multiple of 8
+                    *reinterpret_cast<uint4*>(prow + ((gq ^ ((p_row >> 1) & 3)) << 4)) =
+                        make_uint4(words[0], words[1], words[2], words[3]);
+                }
+                fence_proxy_async_cta();  // for the tensor cores, or the bulk copy
+                if (!p_local) {
+                    named_barrier(1 + wg, 128);
+                    if (t == 0)
+                        bulk_copy_to_cluster(map_to_rank(sbase + L::kP + b * L::kPBytes + kKeys * rank * 64, peer),
+                                             sbase + L::p_stage(b), L::kPStageBytes, peer_addr(&bars[kPRemote + b]));
                 }
             }
 
@@ -518,22 +632,19 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                         rescale |= (v4.x != 1.0f) | (v4.y != 1.0f) | (v4.z != 1.0f) | (v4.w != 1.0f);
                     }
                     if (rescale) {
+                        const uint32_t col = tmem + lane_base + 2 * kPairHeads + hw + 16 * gq;
+                        float v[32];
+                        tmem_load16x2(col, col + kPairHeads, v);
 #pragma unroll
-                        for (int grp = 0; grp < 2; ++grp) {
-                            const uint32_t col = tmem + lane_base + 2 * kPairHeads + grp * kPairHeads + hw + 16 * gq;
-                            float v[16];
-                            tmem_load16x1(col, v);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] *= a[i];
-                            tmem_store16(col, v);
-                        }
+                        for (int i = 0; i < 32; ++i) v[i] *= a[i & 15];
+                        tmem_store16x2(col, col + kPairHeads, v);
                     }
                 }
+                tmem_wait_st();
             }
-            fence_proxy_async_all();  // the P^T writes (local and remote), for the tensor cores
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(leader_addr(&bars[kPFull]));
+            if (lane == 0) mbar_arrive(&bars[kPLocal]);
         }
         if (nch > 0)
             ok &= mbar_wait_bounded(&bars[kPvDone + ((nch - 1) & 1)], ((nch - 1) >> 1) & 1, abort_flag, kWaitLimitNs);

@@ -17,6 +17,10 @@ struct PairParams {
     // the 64-byte rope box (64B swizzle).
     CUtensorMap q_latent;
     CUtensorMap q_rope;
+    // Row gathers of each pool (tile::gather4, boxes of 128 bytes x 1 row,
+    // 128B swizzle), used when peer_tma is set.
+    CUtensorMap kv0;
+    CUtensorMap kv1;
     const uint8_t* pool0;
     const uint8_t* pool1;
     int64_t rows0, rows1;
@@ -30,7 +34,8 @@ struct PairParams {
     int64_t lse_stride_token;
     int32_t width, pool_split, num_pools;
     float scale_log2, out_scale;
-    int32_t* error;  // the library's device error word
+    int32_t peer_tma;  // both pools have row-gather maps
+    int32_t* error;    // the library's device error word
 };
 
 // Keys of one chunk of the pair (128 per CTA), heads per pair.

@@ -464,6 +464,31 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
     }
 }
 
+// Stores 4 bytes into another CTA's shared memory (shared::cluster address
+// `addr`) and completes 4 bytes of transaction count on that CTA's mbarrier at
+// `bar`; the receiver arms the barrier with the bytes it expects.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(v)), "r"(bar)
+                 : "memory");
+}
+
+// Copies `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory to another CTA's (shared::cluster `dst`) on the TMA
+// engine, completing the bytes on that CTA's mbarrier at `bar`.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Generic-proxy writes of this thread to its own CTA's shared memory, made
+// visible to the async proxy (TMA engine and tensor cores).
+__device__ __forceinline__ void fence_proxy_async_cta() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Makes this thread's generic-proxy writes to shared memory (its own CTA's or
 // another's of the cluster) visible to the async proxy that the tensor cores
 // read through.
