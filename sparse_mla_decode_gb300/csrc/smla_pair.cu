@@ -40,13 +40,15 @@
 //         128 (TMEM lane t of S^T) and latent row t of each O^T block;
 //   8     allocates TMEM (both CTAs together); in CTA 0 one thread issues the
 //         pair's MMAs, in CTA 1 one thread relays that its copies landed;
-//   9-14  producers of the CTA's own rows: the chunk's indices (loaded a
+//   9-13  producers of the CTA's own rows: the chunk's indices (loaded a
 //         chunk ahead), 16-byte cp.async copies into 128B-swizzled K-major
 //         tiles (a latent row per warp instruction, masked keys zero-filled),
 //         and an L2 prefetch of the next chunk's rows;
-//   15    producer of the peer keys' latent half, once QK is done: TMA
+//   14-15 producers of the peer keys' latent half, once QK is done: TMA
 //         tile::gather4 (four rows of 128 bytes per instruction, on the SM's
 //         TMA unit beside the warps' cp.async; rows past a pool read as zeros).
+//         A warp's TMA instructions issue one after another, about 55 ns
+//         each, so two warps share them.
 // Every wait is bounded; a timeout sets an error bit, tells the peer, and
 // the kernel still passes every barrier and frees its TMEM.
 
@@ -69,9 +71,12 @@ constexpr int kKeys = 128;   // keys of one CTA per chunk (its 128 MMA rows)
 constexpr int kHalf = 64;    // heads whose Q and P^T one CTA holds
 constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp = 9;  // first of the own-row producers
-constexpr int kProducerWarps = 6;
+constexpr int kProducerWarps = 5;
 constexpr int kProducerThreads = kProducerWarps * 32;
-constexpr int kPeerWarp = kProducerWarp + kProducerWarps;  // 15
+constexpr int kPeerWarp = kProducerWarp + kProducerWarps;  // 14
+constexpr int kPeerWarps = 2;
+constexpr int kPeerGroups = kKeys / 4 / kPeerWarps;  // groups of four peer keys per peer warp
+static_assert(kPeerWarp + kPeerWarps == kPairThreads / 32, "warps");
 constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait, then give up
@@ -176,8 +181,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
     if (tid == 0) {
         mbar_init(&bars[kOwnFull + 0], kProducerThreads + 1);
         mbar_init(&bars[kOwnFull + 1], kProducerThreads + 1);
-        mbar_init(&bars[kPeerFull + 0], 32 + 1);  // the peer warp's cp.async arrivals + its expect-tx arrival
-        mbar_init(&bars[kPeerFull + 1], 32 + 1);
+        // the peer warps' cp.async arrivals + one expect-tx arrival each
+        mbar_init(&bars[kPeerFull + 0], kPeerWarps * 33);
+        mbar_init(&bars[kPeerFull + 1], kPeerWarps * 33);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[kSFull + i], 1);
             mbar_init(&bars[kPvDone + i], 1);
@@ -283,9 +289,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
             raw = raw_next;
         }
         cp_async_wait_all();
-    } else if (warp == kPeerWarp) {
-        // =========================================== peer-half producer
-        // Lane l takes keys 4 l .. 4 l + 3 of the peer's half of a chunk. Once
+    } else if (warp >= kPeerWarp) {
+        // ========================================== peer-half producers
+        // Lane l < 16 of peer warp v takes keys 4 q .. 4 q + 3 of the peer's
+        // half of a chunk, q = 16 v + l. Once
         // QK of the chunk has read this CTA's dead blocks, the lane's four
         // rows' 256 latent bytes this CTA multiplies in PV (CTA 0: bytes
         // 0..255 into its blocks 2, 3; CTA 1: 256..511 into its blocks 0, 1)
@@ -296,15 +303,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
         const int other0 = kKeys * static_cast<int>(peer);
         const int src_x = rank == 0 ? 0 : 256;
         const int dst_blk = rank == 0 ? 2 : 0;
+        const bool has_group = lane < kPeerGroups;
+        const int q = (warp - kPeerWarp) * kPeerGroups + lane;  // this lane's group (when it has one)
         int32_t raw[4], raw_next[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int col = other0 + 4 * lane + i;
-            raw[i] = col < count ? idx_row[col] : -1;
+            const int col = other0 + 4 * q + i;
+            raw[i] = (has_group && col < count) ? idx_row[col] : -1;
         }
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1;
-            const int col0 = c * kPairChunk + other0 + 4 * lane;  // this lane's first column
+            const int col0 = c * kPairChunk + other0 + 4 * q;  // this lane's first column
             int32_t id[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -312,15 +321,15 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                 const bool second = p.num_pools == 2 && col0 + i >= p.pool_split;
                 id[i] = (raw[i] >= 0 && raw[i] < (second ? p.rows1 : p.rows0)) ? raw[i] : -1;
                 const int col = col0 + kPairChunk + i;
-                raw_next[i] = col < count ? idx_row[col] : -1;
+                raw_next[i] = (has_group && col < count) ? idx_row[col] : -1;
             }
             const bool first_second = p.num_pools == 2 && col0 >= p.pool_split;
             const bool last_second = p.num_pools == 2 && col0 + 3 >= p.pool_split;
-            const bool by_tma = p.peer_tma && first_second == last_second;
+            const bool by_tma = has_group && p.peer_tma && first_second == last_second;
             const uint32_t tma_lanes = __ballot_sync(0xFFFFFFFFu, by_tma);
             ok &= mbar_wait_bounded(&bars[kSFull + b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             const uint32_t stage = sbase + L::kKv + b * L::kStage;
-            const int k = 4 * lane;  // first of the lane's four keys in the tile
+            const int k = 4 * q;  // first of the lane's four keys in the tile
             if (lane == 0) mbar_arrive_expect_tx(&bars[kPeerFull + b], __popc(tma_lanes) * 4 * 256);
             __syncwarp();
             if (by_tma) {
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                 for (int h = 0; h < 2; ++h)
                     tma_gather4(stage + (dst_blk + h) * L::kBlock + (k >> 3) * 1024 + (k & 7) * 128, map,
                                 src_x + 128 * h, r[0], r[1], r[2], r[3], &bars[kPeerFull + b]);
-            } else {
+            } else if (has_group) {
 #pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
                     const uint8_t* row = row_of(p, col0 + i, id[i], D) + src_x;
