@@ -418,8 +418,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) sparse_mla_decode_pair_kernel
                         mbar_arrive_expect_tx(&bars[kPRemote + b], L::kPStageBytes);
                         ++armed;
                     }
-                    if (mbar_test_wait(&bars[kPLocal], c & 1) && mbar_test_wait_cluster(&bars[kPRemote + b], par) &&
-                        mbar_test_wait_cluster(&bars[kRelayP], c & 1) && mbar_test_wait(&bars[kPeerFull + b], par) &&
+                    // this CTA's barriers first (CTA-scope tests are cheap), the
+                    // ones the peer completes after
+                    if (mbar_test_wait(&bars[kPLocal], c & 1) && mbar_test_wait(&bars[kPeerFull + b], par) &&
+                        mbar_test_wait_cluster(&bars[kPRemote + b], par) && mbar_test_wait_cluster(&bars[kRelayP], c & 1) &&
                         mbar_test_wait_cluster(&bars[kRelayPeer + b], par)) {
                         fence_proxy_async_all();
                         tc_fence_after_sync();
