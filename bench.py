@@ -21,8 +21,10 @@ One JSON line on rank 0:
               pipelined over three streams)
   cpu_baseline the CPU oracle (fp64 definition) on a bounded sample, all cores
 With --impl reference the same line is produced by the CPU oracle alone.
-Under torchrun (--gpus N > 1) every rank runs an independent replica on its
-own GPU (the path has no exchange step); value sums the ranks' bytes.
+The library is built for runs on one GPU (its paired gathers use cluster
+multicast, which only a one-GPU run may use): with --gpus N > 1 or under a
+torchrun of several processes, this arm prints one line saying so and runs
+nothing. The reference arm (the CPU oracle) runs on rank 0 alone.
 """
 
 from __future__ import annotations
@@ -43,7 +45,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from sparse_mla_decode_gb300.replicas import job_rate, reduce_over_ranks  # noqa: E402
 
 METRIC = "µs/call and achieved HBM GB/s (% of 8 TB/s) for sparse MLA decode"
 NOMINAL_HBM_GBS = 8000.0
@@ -85,16 +86,14 @@ def parse():
 def make_sets(config: str, rank: int, sets: int):
     from sparse_mla_decode_gb300 import workloads
 
-    from sparse_mla_decode_gb300.replicas import rank_seed
-
     if config == "batch":
-        rng = np.random.default_rng(rank_seed(5000, rank))
+        rng = np.random.default_rng(5000)
         pool = workloads.e4m3_normal(rng, (1 << 20, 576))
-        return [workloads.bandwidth_batch(seed=rank_seed(1003, rank, r), pool=pool) for r in range(sets)]
+        return [workloads.bandwidth_batch(seed=1003 + r, pool=pool) for r in range(sets)]
     make = {"tiny": workloads.tiny, "verify": workloads.verify_rows,
             "two_pool": workloads.two_pool_sinks}[config]
     base = {"tiny": 1000, "verify": 1001, "two_pool": 1002}[config]
-    return [make(seed=rank_seed(base, rank, r)) for r in range(sets)]
+    return [make(seed=base + r) for r in range(sets)]
 
 
 def bytes_alg(w) -> int:
@@ -419,14 +418,8 @@ def run_ours(args, rank, world, local_rank):
                          w["bmm2_scale"], w["k_scale"], d["out"], d["lse"], stream=None,
                          pool_split=w.get("pool_split", 0))
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
 
     def barrier():
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
         torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank)
@@ -495,7 +488,9 @@ def run_ours(args, rank, world, local_rank):
 
     step_bytes = float(np.mean([byts[i % len(byts)] for i in range(args.steps)]))
     step_flops = float(np.mean([flops[i % len(flops)] for i in range(args.steps)]))
-    ms, total_bytes, value = job_rate(dist, elapsed_ms, step_bytes, args.steps, device=dev)
+    ms = elapsed_ms / args.steps
+    total_bytes = step_bytes
+    value = total_bytes / (ms * 1e-3) / 1e9
 
     # end to end through the public API, host buffers in pinned memory
     e2e = None
@@ -515,7 +510,6 @@ def run_ours(args, rank, world, local_rank):
         steps = min(args.steps, 500)
         e_ms = pipelined_e2e(torch, host, (dsets[0]["q"], dsets[0]["indices"], dsets[0]["lens"]), e2e_run,
                              (dsets[0]["out"], dsets[0]["lse"]), steps)
-        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
@@ -562,7 +556,7 @@ def run_ours(args, rank, world, local_rank):
             "launch": ("one CUDA graph of the %d timed library calls, replayed once" % args.steps)
                       if graph is not None else "%d library calls from Python" % args.steps,
             "plan": plan,
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "parallelism": "single GPU",
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -673,14 +667,8 @@ def run_merge(args, rank, world, local_rank):
         parts, lses, lens = sets[i % R]
         smla.smla_merge(parts, lses, lens, out, lse)
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
 
     def barrier():
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
         torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream(dev)
@@ -719,7 +707,9 @@ def run_merge(args, rank, world, local_rank):
                 call(i)
         torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, max(t_wall1, soak_until))
-    ms, total_bytes, value = job_rate(dist, elapsed_ms, per_call, args.steps, device=dev)
+    ms = elapsed_ms / args.steps
+    total_bytes = per_call
+    value = total_bytes / (ms * 1e-3) / 1e9
 
     e2e = None
     if not args.no_e2e:
@@ -730,7 +720,6 @@ def run_merge(args, rank, world, local_rank):
             smla.smla_merge(inp[0], inp[1], sets[0][2], outp[0], outp[1])
 
         e_ms = pipelined_e2e(torch, host, (sets[0][0], sets[0][1]), e2e_run, (out, lse), min(args.steps, 200))
-        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(T * H * (512 * 2 + 4)),
@@ -754,7 +743,7 @@ def run_merge(args, rank, world, local_rank):
                          % (R, per_call / 1e6, R * per_call / 1e6),
                    "launch": ("one CUDA graph of the %d timed library calls, replayed once" % args.steps)
                              if graph is not None else "%d library calls from Python" % args.steps,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic("merge"),
                      "bytes_alg_per_launch": int(per_call)},
@@ -843,10 +832,7 @@ def run_mxfp4(args, rank, world, local_rank):
         graph.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, max(t_wall1, t_wall0 + args.soak))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-    ms, _, _ = job_rate(dist, start.elapsed_time(end), per_call, args.steps, device=dev)
+    ms = start.elapsed_time(end) / args.steps
     achieved = per_call / (ms * 1e-3) / 1e9
     e2e = None
     if not args.no_e2e:
@@ -856,7 +842,6 @@ def run_mxfp4(args, rank, world, local_rank):
             smla.smla_mxfp4_q_quant(inp[0], inp[1], 0.0625, *outp)
 
         e_ms = pipelined_e2e(torch, host, sets[0], e2e_run, outs[0], min(args.steps, 100))
-        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(T * H * (256 + 4)),
                "d2h_bytes_per_step": int(T * H * 72),
@@ -1025,10 +1010,7 @@ def run_value(args, rank, world, local_rank, fused=False):
     clocks = sampler.stop(t_wall0, max(t_wall1, t_wall0 + args.soak))
     if smla.smla_value_gate_error() != 0:
         raise RuntimeError("value kernel reported a device error")
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-    ms, _, _ = job_rate(dist, start.elapsed_time(end), per_call, args.steps, device=dev)
+    ms = start.elapsed_time(end) / args.steps
     achieved = per_call / (ms * 1e-3) / 1e9
     e2e = None
     if not args.no_e2e:
@@ -1053,7 +1035,6 @@ def run_value(args, rank, world, local_rank, fused=False):
 
             h2d = T * H * 512 * 2 + T * H * 256 + 4 * T
         e_ms = pipelined_e2e(torch, host, dev_like, e2e_run, (outs[0],), min(args.steps, 100))
-        e_ms = reduce_over_ranks(dist, e_ms, "max", device=dev)
         e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(T * H * 256),
@@ -1179,7 +1160,7 @@ def run_merge_reference(args, rank, world):
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         if args.config == "merge":
@@ -1191,27 +1172,23 @@ def main():
         else:
             run_reference(args, rank, world)
         return
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    try:
-        if args.config == "merge":
-            run_merge(args, rank, world, local_rank)
-        elif args.config == "mxfp4":
-            run_mxfp4(args, rank, world, local_rank)
-        elif args.config in ("value", "merge_value"):
-            run_value(args, rank, world, local_rank, fused=args.config == "merge_value")
-        else:
-            run_ours(args, rank, world, local_rank)
-    finally:
-        if world > 1:
-            import torch.distributed as dist
-
-            dist.barrier()
-            dist.destroy_process_group()
+    n_gpus = max(world, args.gpus)
+    if n_gpus > 1:
+        # one GPU per run: the paired gathers use cluster multicast, which only
+        # a run on one GPU may use, so this build has no multi-GPU path
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "impl": "ours", "n_gpus": n_gpus,
+                              "unavailable": "single-GPU build: its paired gathers use cluster multicast, which "
+                                             "only a one-GPU run may use; run with --gpus 1"}), flush=True)
+        return
+    if args.config == "merge":
+        run_merge(args, rank, world, local_rank)
+    elif args.config == "mxfp4":
+        run_mxfp4(args, rank, world, local_rank)
+    elif args.config in ("value", "merge_value"):
+        run_value(args, rank, world, local_rank, fused=args.config == "merge_value")
+    else:
+        run_ours(args, rank, world, local_rank)
 
 
 if __name__ == "__main__":

@@ -27,8 +27,6 @@
 //              tile comes by TMA tile loads. (Random 576-byte rows stream
 //              fastest this way: TMA tile::gather4 reaches only about 60% of
 //              the cp.async rate on L2 hits and needs as many issuing warps.)
-// Head groups of 128 heads go to the CTA-pair kernel of smla_pair.cu instead,
-// whose products run at the full FP8 rate.
 // Both products put the long side on the MMA's M = 128 and the heads on N, as
 // the DeepSeek page sketches:
 //   S^T[key, head]   = KV[key, :] . Q[head, :]      (A = KV K-major, B = Q K-major)
@@ -39,6 +37,8 @@
 // Key splits of one (token, head tile) form a cluster and merge over DSMEM.
 // Every wait is bounded; a timeout sets an error bit and the kernel still
 // returns (and frees its TMEM).
+// Head groups of 128 heads may also run on the CTA-pair kernel of
+// smla_pair.cu, whose products run at the tensor core's full FP8 rate.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -79,6 +79,10 @@ struct Params {
     // 64-byte rope box (64B swizzle).
     CUtensorMap q_latent;
     CUtensorMap q_rope;
+    // Row gathers of pool 0 for paired CTAs (tile::gather4, one row high):
+    // 128-byte latent boxes (128B swizzle) and the 64-byte rope box.
+    CUtensorMap kv_latent;
+    CUtensorMap kv_rope;
     const uint8_t* q;
     int64_t q_stride_token, q_stride_head;
     const uint8_t* pool0;
@@ -93,6 +97,7 @@ struct Params {
     float* lse;
     int64_t lse_stride_token;
     int32_t width, pool_split, num_pools, splits;
+    int32_t pair;  // head groups sharing each gathered chunk (1 or 2; 2 needs one pool)
     float scale_log2, out_scale;
 };
 
@@ -216,6 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     uint64_t* drain = bars + 8;     // every MMA done (commit)
     uint64_t* q_full = bars + 9;    // the Q tile landed (TMA transaction bytes)
     uint64_t* kv_first = bars + 10; // chunk 0 landed (256 cp.async arrivals + 1); later chunks use kv_full
+    // stage_free[b] (paired): PV of the chunk in stage b finished in both CTAs
+    // of the pair (one multicast commit from each), so either may refill the
+    // stage in both.
+    uint64_t* stage_free = bars + 11;  // [2]
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::kIdx);
@@ -227,16 +236,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int splits = p.splits;
-    // The cluster holds the splits of one (token, head group).
-    const int split = static_cast<int>(blockIdx.x) % splits;
+    const bool paired = p.pair == 2;
+    // The cluster holds the splits of `pair` consecutive head groups of one
+    // token: rank = half * splits + split.
+    const int rank = static_cast<int>(blockIdx.x) % (splits * p.pair);
+    const int split = rank % splits;
+    const int half = rank / splits;
     const int head0 = (static_cast<int>(blockIdx.x) / splits) * N;
+    // the CTA of the same split in the other head group of the pair, and both
+    const uint16_t pair_mask = static_cast<uint16_t>((1u << split) | (1u << (splits + split)));
     const int token = blockIdx.y;
 
     // ---- set-up (reads no input, so it overlaps the previous kernel) -------
     if (tid == 0) {
-        // every producer thread's cp.async arrival and one index-release arrival
-        mbar_init(&kv_full[0], kProducerThreads + 1);
-        mbar_init(&kv_full[1], kProducerThreads + 1);
+        // paired: the producer's expect-tx arrival; else every producer
+        // thread's cp.async arrival and one index-release arrival
+        mbar_init(&kv_full[0], paired ? 1 : kProducerThreads + 1);
+        mbar_init(&kv_full[1], paired ? 1 : kProducerThreads + 1);
+        mbar_init(&stage_free[0], 2);
+        mbar_init(&stage_free[1], 2);
         mbar_init(q_full, 1);
         mbar_init(&pv_done[0], 1);
         mbar_init(&pv_done[1], 1);
@@ -261,9 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensor_map(&p.q_latent);
         if constexpr (L::kRope) prefetch_tensor_map(&p.q_rope);
+        if (paired) {
+            prefetch_tensor_map(&p.kv_latent);
+            if constexpr (L::kRope) prefetch_tensor_map(&p.kv_rope);
+        }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if (paired)
+        cluster_sync_all();  // the partner's barriers are initialised before anything reaches them
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = misc[0];
 
@@ -278,14 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     }
     // The first chunk's raw indices, loaded while the count loads: the
     // chunk this split starts with when the count fills the width (always
-    // for split 0). Thread k of the softmax range takes column k; the count
-    // masks them later, and a split whose first chunk turns out elsewhere
-    // reloads.
+    // for split 0). Thread k of the chunk's resolvers (the softmax range
+    // unpaired, the producers paired) takes column k; the count masks them
+    // later, and a split whose first chunk turns out elsewhere reloads.
     const int chunks_w = (p.width + kChunk - 1) / kChunk;
     const int col_guess = split * ((chunks_w + splits - 1) / splits) * kChunk;
+    const int resolver = paired ? tid - kProducerWarp * 32 : tid;
     int32_t raw_guess = -1;
-    if (tid < kChunk && col_guess + tid < p.width)
-        raw_guess = p.indices[static_cast<int64_t>(token) * p.idx_stride + col_guess + tid];
+    if (resolver >= 0 && resolver < kChunk && col_guess + resolver < p.width)
+        raw_guess = p.indices[static_cast<int64_t>(token) * p.idx_stride + col_guess + resolver];
     const int count = min(max(p.lens[token], 0), p.width);
     // This split's chunks of the token: ceil(chunks / splits) consecutive
     // chunks each, dealt over the token's own count (later splits may be empty).
@@ -296,13 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     grid_launch_dependents();
     // Chunk c's stage barrier and the parity of its phase: chunk 0 has its own
     // barrier; stage 1 serves chunks 1, 3, 5, ..., stage 0 chunks 2, 4, ...
-    auto kv_bar = [&](int c) -> uint64_t* { return c == 0 ? kv_first : &kv_full[c & 1]; };
+    // Paired CTAs use the two stage barriers from chunk 0 on.
+    auto kv_bar = [&](int c) -> uint64_t* { return (c == 0 && !paired) ? kv_first : &kv_full[c & 1]; };
     auto kv_parity = [&](int c) -> uint32_t {
+        if (paired) return static_cast<uint32_t>((c >> 1) & 1);
         return c == 0 ? 0u : static_cast<uint32_t>(((c >> 1) - ((c & 1) ? 0 : 1)) & 1);
     };
 
     bool ok = true;
-    if (warp < kSoftmaxRange / 32 && nch > 0) {
+    if (warp < kSoftmaxRange / 32 && nch > 0 && !paired) {
         // ============================= chunk 0 by the softmax-range warps
         // (idle until the first QK): the first gather is on every CTA's
         // critical path, and more issuing warps stream it faster.
@@ -347,7 +375,63 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         }
         cp_async_arrive_noinc(kv_first);
     }
-    if (warp >= kProducerWarp) {
+    if (warp >= kProducerWarp && paired) {
+        // =========================================== paired producers
+        // Both CTAs of the pair hold the same token and split, so the same
+        // chunks. Each resolves all 128 indices (the softmax masks by them)
+        // and gathers its half of the rows with tile::gather4, multicast into
+        // the stage of both CTAs; a stage is refilled once PV has released it
+        // in both. Masked keys get a row past the pool's end (zero fill).
+        const int g = tid - kProducerWarp * 32;
+        const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
+        const int32_t past_end = static_cast<int32_t>(p.rows0);
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            const int col0 = (c_first + c) * kChunk;
+            const int32_t raw = (g < kChunk && col0 + g < count)
+                                    ? ((c == 0 && col0 == col_guess) ? raw_guess : idx_row[col0 + g])
+                                    : -1;
+            if (c >= 2) ok &= mbar_wait_bounded(&stage_free[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
+            if (g < kChunk) {
+                int32_t id = -1;
+                if (raw >= 0) {
+                    if (raw < p.rows0)
+                        id = raw;
+                    else
+                        atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
+                }
+                idx_s[b * kChunk + g] = id;
+            }
+            named_barrier(3, kProducerThreads);
+            if (g == 0) mbar_arrive_expect_tx(&kv_full[b], L::kStage);  // both halves; also releases idx_s
+            if (lane == 0) {
+                // one lane per producer warp: the TMA instructions of one
+                // thread issue one after another, several threads overlap
+                const uint32_t stage = sbase + L::kKv + b * L::kStage;
+                for (int k = half * (kChunk / 2) + 4 * (g >> 5); k < (half + 1) * (kChunk / 2);
+                     k += 4 * (kProducerThreads / 32)) {
+                    int32_t r[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int32_t id = idx_s[b * kChunk + k + i];
+                        r[i] = id >= 0 ? id : past_end;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tma_gather4_multicast(stage + j * kChunk * 128 + (k >> 3) * 1024 + (k & 7) * 128, &p.kv_latent,
+                                              j * 128, r[0], r[1], r[2], r[3], &kv_full[b], pair_mask);
+                    if constexpr (L::kRope)
+                        tma_gather4_multicast(stage + 4 * kChunk * 128 + (k >> 3) * 512 + (k & 7) * 64, &p.kv_rope,
+                                              512, r[0], r[1], r[2], r[3], &kv_full[b], pair_mask);
+                }
+            }
+        }
+        // The partner's commits for the last chunks have reached this CTA's
+        // stage barriers before either CTA moves on to its exit.
+        if (g == 0)
+            for (int c = max(0, nch - 2); c < nch; ++c)
+                ok &= mbar_wait_bounded(&stage_free[c & 1], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+    } else if (warp >= kProducerWarp) {
         // ================================================== producers
         // Thread g < 128 resolves key g's row; warp w then copies keys w,
         // w + 7, ..., one 512-byte latent row per instruction (lane l: bytes
@@ -471,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                         }
                     }
                     mma_commit(&pv_done[c & 1]);
+                    if (paired) mma_commit_multicast(&stage_free[c & 1], pair_mask);
                     ++next_pv;
                     progressed = true;
                 }
@@ -697,8 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         if (!L::kOwnInbox) cluster_sync_relaxed();  // every CTA of the cluster is past its main loop
         if (tid < N) {
             for (int r = 0; r < splits; ++r) {
-                st_cluster_f32(map_to_rank(stats + ((split * 2 + 0) * N + tid) * 4, r), m_run_s[tid]);
-                st_cluster_f32(map_to_rank(stats + ((split * 2 + 1) * N + tid) * 4, r), l_s[tid]);
+                st_cluster_f32(map_to_rank(stats + ((split * 2 + 0) * N + tid) * 4, half * splits + r), m_run_s[tid]);
+                st_cluster_f32(map_to_rank(stats + ((split * 2 + 1) * N + tid) * 4, half * splits + r), l_s[tid]);
             }
         }
         if (has_heads && !split_empty) {
@@ -707,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 const int slice = blk * 4 + (warp & 3);
                 const int owner = slice % splits, slot = slice / splits;
                 const uint32_t dst =
-                    map_to_rank(inbox + (((split * slots + slot) * N + hb) * 32 + lane) * 4, owner);
+                    map_to_rank(inbox + (((split * slots + slot) * N + hb) * 32 + lane) * 4, half * splits + owner);
                 float v[HW];
                 const uint32_t col = tmem + lane_base + 2 * N + blk * N + hb;
                 if constexpr (HW == 32)
@@ -807,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         __syncwarp();
         tmem_dealloc(tmem, L::kTmemCols);
     }
+    if (paired) cluster_sync_all();  // neither CTA of a pair leaves while the other may still signal it
 }
 
 // ============================================================== host side
@@ -1079,23 +1165,27 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     }
     if (const char* env = std::getenv("SMLA_SPLITS")) forced_splits = std::max(0, std::atoi(env));
 
-    // Head groups of 128 heads: the CTA-pair kernel (smla_pair.cu), unless a
-    // tile or split count of the tile kernel is forced, SMLA_KERNEL=tile asks
-    // for the tile kernel, or the estimate favours it. The pair kernel runs
-    // a (token, head group) on two SMs without splitting its keys; its
-    // estimate is a fixed cost plus its 256-key chunks per wave of pairs.
-    int kernel_mode = -1;  // -1: by estimate; 0: tile kernel; 1: pair kernel
-    if (const char* env = std::getenv("SMLA_KERNEL")) {
-        if (std::strcmp(env, "pair") == 0) kernel_mode = 1;
-        if (std::strcmp(env, "tile") == 0) kernel_mode = 0;
-    }
-    const bool pair_shape = shape->heads % kPairHeads == 0 && forced_tile == 0 && forced_splits == 0;
+    // Head groups of 128 heads may run on the CTA-pair kernel (smla_pair.cu)
+    // when SMLA_KERNEL=pair asks for it and no tile or split count of the
+    // tile kernel is forced. On GB300 the tile kernel with paired gathers
+    // measured faster at the 128-head shapes of the sweep (the pair kernel's
+    // three cross-SM handoffs per chunk cost about a microsecond each), so it
+    // stays the default.
+    const bool use_pair = shape->heads % kPairHeads == 0 && forced_tile == 0 && forced_splits == 0 && [] {
+        const char* env = std::getenv("SMLA_KERNEL");
+        return env != nullptr && std::strcmp(env, "pair") == 0;
+    }();
     const int pair_chunks = (shape->width + kPairChunk - 1) / kPairChunk;
     const long pair_units = static_cast<long>(shape->tokens) * (shape->heads / kPairHeads);
-    int pair_resident = query_device ? pair_resident_on_device(shape->head_dim) : 0;
-    if (pair_resident <= 0) pair_resident = num_sms / 2;
-    const long pair_waves = pair_units > 0 ? (pair_units + pair_resident - 1) / pair_resident : 0;
-    const double pair_cost = 6.0 + 1.6 * static_cast<double>(pair_waves * pair_chunks);
+    // Pairing (two head groups share each gathered chunk) pays once a CTA
+    // streams at least four chunks, where the gather bounds the pipeline
+    // (up to 12% at 128-256 tokens x 128 heads on GB300); at one or two
+    // chunks per CTA its multicast latency costs up to 8%.
+    int pair_mode = -1;  // -1: by chunks per CTA; 0: never; 1: whenever the shape allows
+    if (const char* env = std::getenv("SMLA_PAIR")) pair_mode = std::atoi(env) != 0 ? 1 : 0;
+    auto can_pair = [&](int tile) {
+        return pair_mode != 0 && shape->num_pools == 1 && (shape->heads / tile) % 2 == 0;
+    };
     auto resident = [&](int tile, int s) {
         const int r = query_device ? resident_ctas_on_device(tile, shape->head_dim, s) : 0;
         return r > 0 ? r : (num_sms / s) * s;
@@ -1120,14 +1210,16 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         for (int tile = 64; tile >= 16; tile /= 2) {
             if (shape->heads % tile != 0 || (forced_tile > 0 && tile != forced_tile)) continue;
             const long units = static_cast<long>(shape->tokens) * (shape->heads / tile);
+            const int pair = 1;  // pairing is decided for the chosen tile and splits
             const double a = tile == 64 ? 8.05 : tile == 32 ? 6.34 : 5.13;
             const double b = tile == 64 ? 2.82 : tile == 32 ? 2.28 : 2.24;
             for (int s = 1; s <= max_splits; ++s) {
                 if (s > 1 && !merge_fits(tile, shape->head_dim, s)) continue;
                 const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
                 if (per > 0 && (chunks + per - 1) / per != s) continue;  // same chunks per CTA as fewer splits
+                if (pair * s > kMaxSplits) continue;
                 const long ctas = units * s;
-                if (ctas > resident(tile, s)) continue;
+                if (ctas > resident(tile, pair * s)) continue;
                 const double cost = a + 0.71 * std::log2(static_cast<double>(s)) +
                                     per * (b + 0.62 * static_cast<double>(ctas) / num_sms);
                 if (cost < best_cost - 1e-9) {
@@ -1142,10 +1234,13 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         const int cap = chunks < kMaxSplits ? (chunks < 1 ? 1 : chunks) : kMaxSplits;
         if (s > cap) s = cap;
         while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
+        if (can_pair(n) && pair_mode == 1 && 2 * s > kMaxSplits) s = kMaxSplits / 2;
         const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
         best = per > 0 ? (chunks + per - 1) / per : 1;
     }
-    if (pair_shape && kernel_mode != 0 && (kernel_mode == 1 || pair_cost < best_cost)) {
+    if (use_pair) {
+        int pair_resident = query_device ? pair_resident_on_device(shape->head_dim) : 0;
+        if (pair_resident <= 0) pair_resident = num_sms / 2;
         plan->head_tile = kPairHeads;
         plan->head_groups = shape->heads / kPairHeads;
         plan->chunk = kPairChunk;
@@ -1163,7 +1258,12 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     }
     const int groups = shape->heads / n;
     const long units = static_cast<long>(shape->tokens) * groups;
-    const int best_resident = resident(n, best);
+    const int per_cta = chunks > 0 ? (chunks + best - 1) / best : 0;
+    int pair = 1;
+    if (can_pair(n) && (pair_mode == 1 || per_cta >= 4) && 2 * best <= kMaxSplits &&
+        (units * best <= resident(n, best) ? units * best <= resident(n, 2 * best) : true))
+        pair = 2;
+    const int best_resident = resident(n, pair * best);
     plan->head_tile = n;
     plan->head_groups = groups;
     plan->chunk = kChunk;
@@ -1176,7 +1276,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     plan->tmem_columns = tmem_for(n);
     plan->num_sms = num_sms;
     plan->resident_ctas = best_resident;
-    plan->pair = 1;
+    plan->pair = pair;
     return SMLA_OK;
 }
 
@@ -1284,19 +1384,29 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
     p.pool_split = shape->num_pools == 2 ? shape->pool_split : 0;
     p.num_pools = shape->num_pools;
     p.splits = plan.splits;
+    p.pair = plan.pair;
+    if (plan.pair == 2) {
+        const bool rope = shape->head_dim == 576;
+        if (!encode_kv_map(&p.kv_latent, kv_pools[0].data, kv_pools[0].rows, shape->head_dim, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+            (rope && !encode_kv_map(&p.kv_rope, kv_pools[0].data, kv_pools[0].rows, shape->head_dim, 64,
+                                    CU_TENSOR_MAP_SWIZZLE_64B)))
+            p.pair = 1;  // an empty pool (nothing to gather): unpaired
+    }
     p.scale_log2 = scale_log2;
     p.out_scale = out_scale;
 
     const dim3 grid(static_cast<unsigned>(plan.head_groups * plan.splits), static_cast<unsigned>(shape->tokens), 1);
+    const int cluster = plan.splits * p.pair;
     const int n = plan.head_tile;
     if (shape->head_dim == 576) {
-        e = n == 64 ? launch<64, 576>(p, grid, plan.splits, st)
-          : n == 32 ? launch<32, 576>(p, grid, plan.splits, st)
-                    : launch<16, 576>(p, grid, plan.splits, st);
+        e = n == 64 ? launch<64, 576>(p, grid, cluster, st)
+          : n == 32 ? launch<32, 576>(p, grid, cluster, st)
+                    : launch<16, 576>(p, grid, cluster, st);
     } else {
-        e = n == 64 ? launch<64, 512>(p, grid, plan.splits, st)
-          : n == 32 ? launch<32, 512>(p, grid, plan.splits, st)
-                    : launch<16, 512>(p, grid, plan.splits, st);
+        e = n == 64 ? launch<64, 512>(p, grid, cluster, st)
+          : n == 32 ? launch<32, 512>(p, grid, cluster, st)
+                    : launch<16, 512>(p, grid, cluster, st);
     }
     if (e != cudaSuccess) {
         t_last_cuda_error = static_cast<int>(e);

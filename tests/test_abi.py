@@ -40,18 +40,11 @@ def shape(**kw):
 
 
 def test_plan_bandwidth_batch(lib):
-    """128 heads: one CTA pair per (token, 128-head group), 256-key chunks."""
     p = smla.smla_plan_for(shape(), num_sms=152)
-    assert p["head_tile"] == 128 and p["head_groups"] == 1 and p["chunk"] == 256 and p["pair"] == 2
-    assert p["chunks"] == 8 and p["splits"] == 1 and p["chunks_per_split"] == 8
-    assert p["ctas"] == 64 * 2 and p["threads"] == 512
+    assert p["head_tile"] == 64 and p["head_groups"] == 2 and p["chunk"] == 128
+    assert p["chunks"] == 16 and p["splits"] * p["chunks_per_split"] >= 16
+    assert p["ctas"] == 64 * 2 * p["splits"]
     assert p["smem_bytes"] <= 232448 and p["tmem_columns"] == 512
-
-
-@pytest.fixture
-def tile_kernel(monkeypatch):
-    """The planner of the tile kernel (16 / 32 / 64 heads per CTA)."""
-    monkeypatch.setenv("SMLA_KERNEL", "tile")
 
 
 @pytest.mark.parametrize("tokens,heads,width,dim,groups,chunks", [(64, 128, 2048, 576, 1, 8), (5, 256, 256, 576, 2, 1),
@@ -61,6 +54,7 @@ def test_plan_pair_kernel(lib, monkeypatch, tokens, heads, width, dim, groups, c
     p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width, head_dim=dim), num_sms=152)
     assert (p["head_tile"], p["head_groups"], p["chunk"], p["chunks"], p["splits"]) == (128, groups, 256, chunks, 1)
     assert p["ctas"] == 2 * tokens * groups and p["resident_ctas"] == 152 and p["pair"] == 2
+    assert p["threads"] == 512 and p["tmem_columns"] == 512
 
 
 def test_plan_pair_kernel_needs_128_head_groups(lib, monkeypatch):
@@ -73,7 +67,7 @@ def test_plan_pair_kernel_needs_128_head_groups(lib, monkeypatch):
 
 @pytest.mark.parametrize("tokens,heads,width,dim", [(1, 16, 256, 576), (5, 128, 256, 576),
                                                     (12, 16, 640, 512), (256, 64, 1024, 576)])
-def test_plan_fills_the_machine_without_empty_splits(lib, tile_kernel, tokens, heads, width, dim):
+def test_plan_fills_the_machine_without_empty_splits(lib, tokens, heads, width, dim):
     p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width, head_dim=dim), num_sms=152)
     assert 1 <= p["splits"] <= 16
     assert (p["splits"] - 1) * p["chunks_per_split"] < p["chunks"]  # the last split has work
@@ -82,7 +76,7 @@ def test_plan_fills_the_machine_without_empty_splits(lib, tile_kernel, tokens, h
 
 @pytest.mark.parametrize("tokens,heads,width,want", [(1, 16, 2048, 8), (1, 128, 256, 2), (64, 128, 2048, 1),
                                                      (128, 128, 2048, 1), (256, 16, 2048, 1), (32, 16, 1024, 4)])
-def test_plan_splits_only_while_resident(lib, tile_kernel, tokens, heads, width, want):
+def test_plan_splits_only_while_resident(lib, tokens, heads, width, want):
     p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width), num_sms=152)
     assert p["splits"] == want
     assert p["resident_ctas"] == (152 // p["splits"]) * p["splits"]
@@ -91,24 +85,22 @@ def test_plan_splits_only_while_resident(lib, tile_kernel, tokens, heads, width,
 
 @pytest.mark.parametrize("tokens,heads,width,tile,splits", [(1, 128, 256, 16, 2), (64, 128, 2048, 64, 1),
                                                             (32, 128, 256, 32, 1), (256, 64, 1024, 64, 1)])
-def test_plan_head_tile(lib, tile_kernel, tokens, heads, width, tile, splits):
+def test_plan_head_tile(lib, tokens, heads, width, tile, splits):
     p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width), num_sms=152)
     assert (p["head_tile"], p["splits"]) == (tile, splits)
     assert p["head_groups"] * p["head_tile"] == heads
 
 
-@pytest.mark.parametrize("heads,pools,pair", [(128, 1, 2), (64, 1, 1), (128, 2, 2), (16, 1, 1), (256, 1, 2)])
-def test_plan_kernel_by_heads(lib, heads, pools, pair):
-    """At the batch's width, 128-head groups take the pair kernel (either pool
-    count); other head counts the tile kernel (one CTA per tile)."""
+@pytest.mark.parametrize("heads,pools,pair", [(128, 1, 2), (64, 1, 1), (128, 2, 1), (16, 1, 1), (32, 1, 1)])
+def test_plan_pairs_head_groups(lib, heads, pools, pair):
     kw = dict(tokens=64, heads=heads, width=2048)
     p = smla.smla_plan_for(smla.make_shape(kw["tokens"], heads, kw["width"], 576, pools, 1024 if pools == 2 else 0),
                            num_sms=152)
     assert p["pair"] == pair
-    assert p["head_tile"] == (128 if pair == 2 else p["head_tile"])
+    assert p["head_groups"] % p["pair"] == 0
 
 
-def test_forced_head_tile(lib, tile_kernel, monkeypatch):
+def test_forced_head_tile(lib, monkeypatch):
     monkeypatch.setenv("SMLA_HEAD_TILE", "32")
     assert smla.smla_plan_for(shape(), num_sms=152)["head_tile"] == 32
     monkeypatch.setenv("SMLA_HEAD_TILE", "64")
@@ -120,7 +112,11 @@ def test_forced_splits(lib, monkeypatch):
     assert smla.smla_plan_for(shape(), num_sms=152)["splits"] == 4  # 16 chunks: 4 x 4 ... no empty split
     monkeypatch.setenv("SMLA_SPLITS", "16")
     p = smla.smla_plan_for(shape(), num_sms=152)
-    assert (p["splits"], p["pair"], p["head_tile"]) == (16, 1, 64)  # a forced split count: the tile kernel
+    assert (p["splits"], p["pair"]) == (16, 1)  # one chunk per CTA: unpaired
+    monkeypatch.setenv("SMLA_PAIR", "1")
+    p = smla.smla_plan_for(shape(), num_sms=152)
+    assert (p["splits"], p["pair"]) == (8, 2)  # forced pairing: clusters of 2 x 8 at most
+    monkeypatch.delenv("SMLA_PAIR")
     monkeypatch.setenv("SMLA_SPLITS", "99")
     assert smla.smla_plan_for(shape(width=300), num_sms=152)["splits"] == 3
 

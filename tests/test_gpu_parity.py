@@ -101,6 +101,32 @@ def env():
             os.environ[name] = value
 
 
+PAIRED = [
+    # heads, head_dim, width, forced head tile, forced splits, lens
+    (128, 576, 2048, None, None, [2048, 1000, 5]),
+    (128, 576, 700, None, 3, [700, 699, 300]),
+    (64, 512, 1300, 16, 2, [1300, 640, 641]),
+    (32, 576, 257, 16, 1, [257, 0, 128]),
+    (128, 576, 900, 32, 8, [900, 129, 850]),
+]
+
+
+@pytest.mark.parametrize("case", PAIRED, ids=[f"h{c[0]}_d{c[1]}_w{c[2]}_t{c[3]}_s{c[4]}" for c in PAIRED])
+def test_paired_head_groups(env, case):
+    """Head-group pairs sharing each chunk's gather (tile::gather4 multicast),
+    with and without split merges across the pair's cluster."""
+    heads, dim, width, tile, splits, lens = case
+    env("SMLA_PAIR", 1)
+    env("SMLA_HEAD_TILE", tile)
+    env("SMLA_SPLITS", splits)
+    w = workloads.small("paired", seed=heads + width, tokens=3, heads=heads, width=width, head_dim=dim,
+                        pool_rows=6000, holes=0.07, sinks=True, lens=lens)
+    plan = plan_of(w)
+    assert plan["pair"] == 2
+    got, bits, lse = run_gpu(w)
+    print(case, plan, compare(w, got, bits, lse))
+
+
 PAIR_KERNEL = [
     # tokens, heads, head_dim, width, lens, holes, sinks, two pools (split column)
     (3, 128, 576, 2048, [2048, 1000, 5], 0.07, True, None),
