@@ -597,15 +597,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             // chunk maxima per head, in logit units (bmm1_scale > 0 keeps the
             // order; masked keys are -inf)
             {
+                // a transposing butterfly: each step hands half of a lane's
+                // heads to its partner; with 32 heads lane l ends with head l,
+                // with 16 lanes 2 h and 2 h + 1 share head h
                 float s[HW];
                 load_logits<HW>(chain0, chain1, s);
-                float mine = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < HW; ++j) {
-                    const float m = warp_max(active ? s[j] : -INFINITY);
-                    mine = (lane == j) ? m : mine;
+                for (int j = 0; j < HW; ++j) s[j] = active ? s[j] : -INFINITY;
+#pragma unroll
+                for (int o = 16, n = HW; n > 1; o >>= 1, n >>= 1) {
+                    const bool up = (lane & o) != 0;
+#pragma unroll
+                    for (int i = 0; i < n / 2; ++i) {
+                        const float send = up ? s[i] : s[i + n / 2];
+                        const float keep = up ? s[i + n / 2] : s[i];
+                        s[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+                    }
                 }
-                if (lane < HW) red[(warp & 3) * N + hb + lane] = mine;
+                if constexpr (HW == 16) {
+                    s[0] = fmaxf(s[0], __shfl_xor_sync(0xFFFFFFFFu, s[0], 1));
+                    if ((lane & 1) == 0) red[(warp & 3) * N + hb + (lane >> 1)] = s[0];
+                } else {
+                    red[(warp & 3) * N + hb + lane] = s[0];
+                }
             }
             named_barrier(1 + wg, 128);
             if (t < HW) {
