@@ -39,7 +39,17 @@ extern "C" {
 #define SMLA_ECUDA (-3)        /* a CUDA runtime call failed (see smla_last_cuda_error) */
 #define SMLA_EDEVICE (-4)      /* the device reported an error (smla_device_error) */
 
-/* Device error bits, set by the kernels in the library's device error word. */
+/* Device error bits, set by the kernels in the library's device error word.
+ *
+ * The error word: one 32-bit word per device, shared by every kernel of this
+ * library on that device (decode, merge-and-project, project-and-gate) and by
+ * every stream and host thread that launches them. Kernels OR bits into it;
+ * nothing clears it but a read (smla_read_device_error, smla_device_error),
+ * which takes every bit present at that moment and leaves zero. So bits cannot
+ * be attributed to one stream when other streams run the library's kernels at
+ * the same time: a stream-ordered read sees every bit that work queued before
+ * it on its stream set, plus whatever concurrent work on other streams had set
+ * when the read ran, and two reads never report the same bit twice. */
 #define SMLA_DEV_INDEX_RANGE 1 /* an index >= pool rows (that column was masked) */
 #define SMLA_DEV_TIMEOUT 2     /* a bounded wait gave up; outputs are invalid */
 
@@ -248,7 +258,7 @@ typedef struct smla_value_shape {
  *   out     device, BF16 [T, H*128], 16-byte aligned.
  * Every buffer belongs to the caller; nothing is allocated. Launched with
  * programmatic dependent launch; captureable in a CUDA graph. A bounded wait
- * that gives up sets SMLA_DEV_TIMEOUT in the word smla_value_gate_error reads.
+ * that gives up sets SMLA_DEV_TIMEOUT in the device error word.
  * Errors: SMLA_EINVAL (null buffers, negative sizes, latent strides not
  * positive multiples of 8, gate or out token strides below H*128 or not
  * multiples of 8, misalignment), SMLA_EUNSUPPORTED (T above
@@ -285,7 +295,7 @@ typedef struct smla_merge_value_shape {
  *   out     device, BF16 [T, H*128], 16-byte aligned; must not overlap the inputs.
  * Every buffer belongs to the caller; nothing is allocated. Launched with
  * programmatic dependent launch; captureable in a CUDA graph. A bounded wait
- * that gives up sets SMLA_DEV_TIMEOUT in the word smla_value_gate_error reads.
+ * that gives up sets SMLA_DEV_TIMEOUT in the device error word.
  * Errors: SMLA_EINVAL (null buffers, negative sizes or strides, misaligned
  * rows, gate or out token strides below H*128 or not multiples of 8),
  * SMLA_EUNSUPPORTED (S above 64, T above 65535 * 64 or H above 65535, no
@@ -294,13 +304,32 @@ typedef struct smla_merge_value_shape {
 int smla_merge_value(const smla_merge_value_shape* shape, const void* parts, const float* lses,
                      const int32_t* lens, const void* w_uv, const void* gate, void* out, void* stream);
 
-/* Reads and clears the value kernel's error word (SMLA_DEV_* bits) after
- * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
-int smla_value_gate_error(int32_t* bits);
+/* Reads and clears the current device's error word (SMLA_DEV_* bits) in
+ * stream order, without synchronising the device: a one-thread kernel on
+ * `stream` (a cudaStream_t, NULL: the legacy default stream) exchanges the
+ * word for zero once the work queued before it on that stream has finished,
+ * its value is copied to `bits` (host) and only `stream` is waited for.
+ * Concurrent reads from several host threads are serialised on the host (one
+ * staging word per device). Not captureable: SMLA_EINVAL on a stream that is
+ * capturing, or for a NULL `bits`; SMLA_ECUDA when a launch, the copy or the
+ * wait fails. This library has no counterpart on the pages; it replaces a
+ * device-wide synchronisation in callers that keep other streams busy. */
+int smla_read_device_error(void* stream, int32_t* bits);
 
-/* Reads and clears the current device's error word (SMLA_DEV_* bits) after
- * synchronising the device. Returns SMLA_OK or SMLA_ECUDA. */
+/* Reads and clears the current device's error word after synchronising the
+ * whole device (every stream). Returns SMLA_OK, SMLA_EINVAL (NULL `bits`) or
+ * SMLA_ECUDA. */
 int smla_device_error(int32_t* bits);
+
+/* Self-test of the bounded waits every kernel of this library uses: launches
+ * one warp on `stream` that waits on an mbarrier expecting one arrival, with
+ * the waits' own code and a limit of `limit_ns` nanoseconds. With `arrive`
+ * set, the warp arrives itself and the wait succeeds; with `arrive` zero
+ * nothing arrives, the wait gives up after about `limit_ns` and the kernel
+ * sets SMLA_DEV_TIMEOUT in the error word and returns, leaving the context
+ * usable. No counterpart on the pages. Errors: SMLA_EINVAL for `limit_ns`
+ * outside [1000, 1e9]; SMLA_ECUDA when the launch fails. */
+int smla_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream);
 
 /* A static string for a return code. */
 const char* smla_error_string(int code);

@@ -15,12 +15,13 @@ from .smla import (  # noqa: F401
     mxfp4_q_quant,
     smla_decode,
     smla_device_error,
+    smla_read_device_error,
+    smla_selftest_bounded_wait,
     smla_merge,
     smla_merge_value,
     smla_mxfp4_q_quant,
     smla_plan_for,
     smla_value_gate,
-    smla_value_gate_error,
     smla_version,
     value_gate,
 )

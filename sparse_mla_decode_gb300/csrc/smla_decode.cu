@@ -1429,6 +1429,72 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
     return SMLA_OK;
 }
 
+namespace smla {
+
+// Where the stream-ordered read of the error word leaves the bits it took, for
+// the copy back to the host.
+__device__ int32_t g_error_taken;
+
+// Takes the error word's bits and clears it in one atomic step, in stream
+// order after the kernels queued before it.
+__global__ void take_error_kernel() { g_error_taken = atomicExch(&g_device_error, 0); }
+
+// One warp: thread 0 sets up an mbarrier that expects one arrival and, with
+// `arrive` set, arrives on it; every lane then waits with the library's
+// bounded wait and `limit_ns`. A wait that gives up records SMLA_DEV_TIMEOUT.
+__global__ void bounded_wait_selftest_kernel(int arrive, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && arrive) mbar_arrive(&bar);
+    const bool ok = mbar_wait_bounded(&bar, 0, &abort_flag, limit_ns);
+    if (!ok && threadIdx.x == 0) atomicOr(&g_device_error, SMLA_DEV_TIMEOUT);
+}
+
+}  // namespace smla
+
+extern "C" int smla_read_device_error(void* stream, int32_t* bits) {
+    if (bits == nullptr) return SMLA_EINVAL;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &capture);
+    if (e == cudaSuccess && capture != cudaStreamCaptureStatusNone) return SMLA_EINVAL;
+    // one staging word per device: the launch, the copy and the wait of one
+    // read finish before another thread's read starts
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int32_t v = 0;
+    if (e == cudaSuccess) {
+        smla::take_error_kernel<<<1, 1, 0, st>>>();
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&v, smla::g_error_taken, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return SMLA_ECUDA;
+    }
+    *bits = v;
+    return SMLA_OK;
+}
+
+extern "C" int smla_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream) {
+    if (limit_ns < 1000 || limit_ns > 1000000000) return SMLA_EINVAL;
+    smla::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        arrive != 0, static_cast<uint64_t>(limit_ns));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return SMLA_ECUDA;
+    }
+    return SMLA_OK;
+}
+
 extern "C" int smla_device_error(int32_t* bits) {
     if (bits == nullptr) return SMLA_EINVAL;
     cudaError_t e = cudaDeviceSynchronize();

@@ -44,6 +44,7 @@
 namespace smla {
 void note_cuda_error(int code);
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+int32_t* device_error_word();
 }  // namespace smla
 
 namespace vgate {
@@ -75,9 +76,8 @@ struct Params {
     const int32_t* lens; // [T] or null
     MergeInputs merge;   // fused: the partial sets (for the weights; the rows come by TMA)
     int32_t tokens, heads;
+    int32_t* error;      // the library's device error word
 };
-
-__device__ int32_t g_value_error;
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(32 * kWarps, 1) value_kernel(const __grid_cons
             tma_store_wait_read();
         }
     }
-    if (!ok && lane == 0) atomicOr(&g_value_error, SMLA_DEV_TIMEOUT);
+    if (!ok && lane == 0) atomicOr(p.error, SMLA_DEV_TIMEOUT);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTile);
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(32 * fz::kWarpsAll, 1) merge_value_kernel(cons
         tma_store_2d(&p.out, h * kV, t0, sbase + fz::kG);
         tma_store_wait_read();
     }
-    if (!ok && lane == 0) atomicOr(&g_value_error, SMLA_DEV_TIMEOUT);
+    if (!ok && lane == 0) atomicOr(p.error, SMLA_DEV_TIMEOUT);
     if (warp == kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTile);
@@ -566,6 +566,7 @@ template <typename Kernel>
 int launch(Kernel kernel, int threads, int smem_bytes, bool* configured, const Params& p, void* stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && p.error == nullptr) e = cudaErrorInvalidSymbol;  // the error word has no address here
     if (e == cudaSuccess && dev < 64 && !configured[dev]) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e == cudaSuccess) configured[dev] = true;
@@ -623,6 +624,7 @@ extern "C" int smla_value_gate(const smla_value_shape* shape, const void* latent
     const int rc = encode_common(p, w_uv, gate, s.gate_stride_token, out, s.out_stride_token, s.tokens, s.heads);
     if (rc != SMLA_OK) return rc;
     p.lens = lens;
+    p.error = smla::device_error_word();
     return launch(value_kernel, 32 * kWarps, kAlloc, g_configured_value, p, stream);
 }
 
@@ -646,6 +648,7 @@ extern "C" int smla_merge_value(const smla_merge_value_shape* shape, const void*
     const int rc = encode_common(p, w_uv, gate, s.gate_stride_token, out, s.out_stride_token, s.tokens, s.heads);
     if (rc != SMLA_OK) return rc;
     p.lens = lens;
+    p.error = smla::device_error_word();
     p.merge = {static_cast<const __nv_bfloat16*>(parts), s.part_stride_source, s.part_stride_token,
                s.part_stride_head, lses, s.lse_stride_source, s.lse_stride_token, s.sources};
     if (s.sources > 0) {
@@ -660,19 +663,4 @@ extern "C" int smla_merge_value(const smla_merge_value_shape* shape, const void*
         if (!encode(&p.latent, parts, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return SMLA_EUNSUPPORTED;
     }
     return launch(merge_value_kernel, 32 * fz::kWarpsAll, fz::kAlloc, g_configured_fused, p, stream);
-}
-
-extern "C" int smla_value_gate_error(int32_t* bits) {
-    if (bits == nullptr) return SMLA_EINVAL;
-    cudaError_t e = cudaDeviceSynchronize();
-    int32_t v = 0;
-    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, vgate::g_value_error, sizeof(v));
-    const int32_t zero = 0;
-    if (e == cudaSuccess) e = cudaMemcpyToSymbol(vgate::g_value_error, &zero, sizeof(zero));
-    if (e != cudaSuccess) {
-        smla::note_cuda_error(static_cast<int>(e));
-        return SMLA_ECUDA;
-    }
-    *bits = v;
-    return SMLA_OK;
 }

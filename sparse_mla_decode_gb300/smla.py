@@ -136,8 +136,10 @@ def load(path: str | None = None):
         lib.smla_value_gate.restype = i32
         lib.smla_merge_value.argtypes = [ctypes.POINTER(SmlaMergeValueShape), vp, vp, vp, vp, vp, vp, vp]
         lib.smla_merge_value.restype = i32
-        lib.smla_value_gate_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
-        lib.smla_value_gate_error.restype = i32
+        lib.smla_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.smla_read_device_error.restype = i32
+        lib.smla_selftest_bounded_wait.argtypes = [i32, ctypes.c_int64, vp]
+        lib.smla_selftest_bounded_wait.restype = i32
         _lib = lib
         return lib
 
@@ -215,6 +217,32 @@ def smla_device_error() -> int:
     if rc != OK:
         raise SmlaError(rc, "smla_device_error")
     return int(bits.value)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def smla_read_device_error(stream=None) -> int:
+    """Reads and clears the device error word in ``stream``'s order (the
+    current stream by default) and waits for that stream alone."""
+    lib = load()
+    bits = ctypes.c_int32(0)
+    rc = lib.smla_read_device_error(ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(bits))
+    if rc != OK:
+        raise SmlaError(rc, "smla_read_device_error")
+    return int(bits.value)
+
+
+def smla_selftest_bounded_wait(arrive: bool, limit_ns: int, stream=None) -> None:
+    """Launches the bounded-wait self-test (one warp waits on an mbarrier that
+    only it may arrive on) on ``stream``."""
+    rc = load().smla_selftest_bounded_wait(int(bool(arrive)), int(limit_ns),
+                                           ctypes.c_void_p(_stream_handle(stream)))
+    if rc != OK:
+        raise SmlaError(rc, "smla_selftest_bounded_wait")
 
 
 def smla_version() -> int:
@@ -354,16 +382,6 @@ def value_gate(latent, w_uv, gate, lens=None, stream=None):
     T, H, _ = latent.shape
     out = torch.empty((T, H * VALUE_DIM), dtype=torch.bfloat16, device=latent.device)
     return smla_value_gate(latent, w_uv, gate, lens, out, stream=stream)
-
-
-def smla_value_gate_error() -> int:
-    """Reads and clears the value kernel's error word (after a device sync)."""
-    lib = load()
-    bits = ctypes.c_int32(0)
-    rc = lib.smla_value_gate_error(ctypes.byref(bits))
-    if rc != OK:
-        raise SmlaError(rc, "smla_value_gate_error")
-    return int(bits.value)
 
 
 def smla_merge_value(parts: torch.Tensor, lses: torch.Tensor, lens: torch.Tensor | None, w_uv: torch.Tensor,

@@ -250,7 +250,23 @@ def test_merge_value_of_nothing_is_ok_without_a_device(lib):
 
 
 def test_merge_value_beyond_64_sources_is_unsupported_before_any_launch(lib):
-    s = _merge_value_shape(sources=65, part_stride_token=65 * 4 * 512 // 65)
+    # every other argument valid: the parts of 65 sources x 3 tokens x 4 heads
+    # x 512 latents, 16-byte aligned pointers, so the source limit alone refuses
+    s = _merge_value_shape(sources=65, part_stride_source=3 * 4 * 512, part_stride_token=4 * 512,
+                           part_stride_head=512)
     p16 = ctypes.c_void_p(16)
     rc = lib.smla_merge_value(ctypes.byref(s), p16, p16, None, p16, p16, p16, None)
     assert rc == smla.EUNSUPPORTED
+    # with no tokens there is nothing to launch, whatever the source count
+    s.tokens = 0
+    assert lib.smla_merge_value(ctypes.byref(s), p16, p16, None, p16, p16, p16, None) == smla.OK
+
+
+def test_read_device_error_needs_somewhere_to_put_the_bits(lib):
+    assert lib.smla_read_device_error(None, None) == smla.EINVAL
+    assert lib.smla_device_error(None) == smla.EINVAL
+
+
+@pytest.mark.parametrize("limit", [0, 999, 1000000001, -5])
+def test_bounded_wait_selftest_rejects_limits_outside_a_microsecond_to_a_second(lib, limit):
+    assert lib.smla_selftest_bounded_wait(0, limit, None) == smla.EINVAL

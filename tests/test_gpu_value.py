@@ -66,7 +66,7 @@ def check(latent, w, gate, lens, got):
         print(f"value gate: worst {worst:.3f} of the bound, {same:.5f} of the bits equal the oracle's")
         assert worst <= 1.0, f"value gate error at {worst:.3f} of the bound"
         assert same >= 0.99
-    assert smla.smla_value_gate_error() == 0
+    assert smla.smla_device_error() == 0
 
 
 @pytest.mark.parametrize("T,H", [(1, 1), (3, 4), (128, 2), (129, 3), (300, 5), (64, 16)])
@@ -164,7 +164,7 @@ def fused_and_composed(parts, lses, lens, w, gate):
     merged, _ = smla.merge(d[0], d[1], d[2], with_lse=False)
     composed = smla.value_gate(merged, d[3], d[4], d[2])
     torch.cuda.synchronize()
-    assert smla.smla_value_gate_error() == 0
+    assert smla.smla_device_error() == 0
     return fused, composed, merged
 
 
