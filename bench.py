@@ -246,10 +246,28 @@ def ncu_traffic(config: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def _median_rate(run, n_of, seconds: float, reps: int = 3):
+    """Wall-clock median of ``reps`` runs of ``run(n)`` on ``n`` (token, head)
+    pairs, ``n`` sized from a probe so that each run takes about ``seconds``.
+    Returns (median seconds per pair, n, the runs' seconds)."""
+    probe = n_of(None)
+    t0 = time.perf_counter()
+    run(probe)
+    per_pair = (time.perf_counter() - t0) / probe
+    n = n_of(int(seconds / max(per_pair, 1e-9)))
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        run(n)
+        times.append(time.perf_counter() - t0)
+    return float(np.median(times)) / n, n, times
+
+
 def cpu_oracle_rate(sets, seconds: float):
-    """Times the fp64 oracle on a bounded sample of (token, head) pairs of the
-    first input set, on all host cores. Returns (GB/s-equivalent, seconds per
-    full call, cores, sample description)."""
+    """Times the fp64 oracle on bounded samples of (token, head) pairs of the
+    first input set: on all host cores and on one core, each the wall-clock
+    median of 3 runs. ``seconds`` is the whole CPU budget. Returns the
+    cpu_baseline entry (its value: the all-cores rate, GB/s-equivalent)."""
     from oracle import oracle
 
     w = sets[0]
@@ -257,19 +275,44 @@ def cpu_oracle_rate(sets, seconds: float):
     prob = oracle.Problem.from_workload(w)
     cores = oracle.max_threads()
     rng = np.random.default_rng(11)
-    n = min(T * H, max(cores, 16))
-    pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
-    t0 = time.perf_counter()
-    oracle.fp64(prob, pairs, threads=cores)
-    per_pair = (time.perf_counter() - t0) / n
-    n = int(min(T * H, max(n, seconds / max(per_pair, 1e-9))))
-    pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
-    t0 = time.perf_counter()
-    oracle.fp64(prob, pairs, threads=cores)
-    elapsed = time.perf_counter() - t0
-    per_call = elapsed / n * T * H
-    rate = bytes_alg(w) / per_call / 1e9
-    return rate, per_call, cores, f"{n} of {T * H} (token, head) pairs of one call, {elapsed:.1f} s"
+
+    def leg(threads, budget):
+        def n_of(n):
+            return min(T * H, max(threads, 4) if n is None else max(n, threads, 4))
+
+        def run(n):
+            pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
+            oracle.fp64(prob, pairs, threads=threads)
+
+        per_pair, n, times = _median_rate(run, n_of, budget / 3.0)
+        per_call = per_pair * T * H
+        return {"value": round(bytes_alg(w) / per_call / 1e9, 6), "cores": threads,
+                "us_per_call": round(per_call * 1e6, 1),
+                "sample": f"{n} of {T * H} (token, head) pairs of one call per run, median of 3 runs "
+                          f"({', '.join(f'{t:.2f}' for t in times)} s)"}
+
+    everything = leg(cores, 0.6 * seconds)
+    one = leg(1, 0.4 * seconds)
+    return {"value": everything["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": everything["sample"], "us_per_call": everything["us_per_call"],
+            "statistic": "wall-clock median of 3 runs, scaled from the sampled pairs to the whole call",
+            "one_core": one}
+
+
+def fp8_peak():
+    """The dense FP8 tensor peak measured by this library's own tcgen05
+    microbenchmark (profiles/fp8_mma_peak.json), else twice the measured BF16
+    burst peak."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "fp8_mma_peak.json")) as f:
+            return float(json.load(f)["fp8_dense_peak_tflops"]), "measured (profiles/fp8_mma_peak.json, tcgen05 kind::f8f6f4)"
+    except (OSError, KeyError, ValueError):
+        pass
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "2x the measured BF16 burst peak"
+    except (OSError, KeyError, ValueError):
+        return 2.0 * 1900.0, "2x the fallback BF16 peak"
 
 
 # --------------------------------------------------------------- our arm
@@ -346,6 +389,22 @@ def pipelined_e2e(torch, host_inputs, dev_like, run, out_like, steps, warmup=3, 
         t1.record(comp)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / steps
+
+
+def e2e_entry(torch, step_bytes, host, dev_like, run, out_like, steps, h2d, d2h):
+    """The e2e entry: the steps issued eagerly from Python (every step pays the
+    API's host work: validation, planning, tensor-map encoding, the ctypes
+    call) as the value, and the same steps replayed from one CUDA graph
+    beside it."""
+    eager = pipelined_e2e(torch, host, dev_like, run, out_like, steps, graph=False)
+    graph = pipelined_e2e(torch, host, dev_like, run, out_like, steps, graph=True)
+    return {"value": round(step_bytes / (eager * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "us_per_call": round(eager * 1e3, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipeline": "per step: H2D of the inputs from pinned memory, the library call, D2H of the outputs to "
+                        "pinned memory, on three streams over three slots, issued eagerly from Python",
+            "graph": {"value": round(step_bytes / (graph * 1e-3) / 1e9, 2), "unit": "GB/s",
+                      "us_per_call": round(graph * 1e3, 3),
+                      "pipeline": "the same steps (copies included) captured once in a CUDA graph and replayed"}}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -508,28 +567,16 @@ def run_ours(args, rank, world, local_rank):
                              w0["bmm2_scale"], w0["k_scale"], outp[0], outp[1], pool_split=w0.get("pool_split", 0))
 
         steps = min(args.steps, 500)
-        e_ms = pipelined_e2e(torch, host, (dsets[0]["q"], dsets[0]["indices"], dsets[0]["lens"]), e2e_run,
-                             (dsets[0]["out"], dsets[0]["lse"]), steps)
-        e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
+        like = ((dsets[0]["q"], dsets[0]["indices"], dsets[0]["lens"]), (dsets[0]["out"], dsets[0]["lse"]))
+        e2e = e2e_entry(torch, total_bytes, host, like[0], e2e_run, like[1], steps, h2d, d2h)
 
     if rank != 0:
         return
     peak, peak_src = measured_hbm_peak()
     achieved = step_bytes / (ms * 1e-3) / 1e9  # this rank's kernel
     traffic = ncu_traffic(args.config)
-    cpu = None
-    if not args.no_cpu:
-        rate, per_call, cores, sample = cpu_oracle_rate(sets, args.cpu_seconds)
-        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": sample, "us_per_call": round(per_call * 1e6, 1)}
-    fp8_peak_tflops = None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            fp8_peak_tflops = 2.0 * float(json.load(f)["bf16_tflops"])
-    except (OSError, KeyError, ValueError):
-        fp8_peak_tflops = 2.0 * 1900.0
+    cpu = None if args.no_cpu else cpu_oracle_rate(sets, args.cpu_seconds)
+    fp8_peak_tflops, fp8_peak_src = fp8_peak()
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -564,6 +611,7 @@ def run_ours(args, rank, world, local_rank):
             "traffic": traffic, "bytes_alg_per_launch": int(step_bytes),
             "tensor_tflops": round(step_flops / (ms * 1e-3) / 1e12, 2),
             "tensor_frac_of_fp8_peak": round(step_flops / (ms * 1e-3) / 1e12 / fp8_peak_tflops, 4),
+            "fp8_peak_tflops": fp8_peak_tflops, "fp8_peak_source": fp8_peak_src,
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -578,7 +626,12 @@ def run_ours(args, rank, world, local_rank):
 
 def run_reference(args, rank, world):
     """The CPU oracle (fp64 definition) as the reference implementation; rank 0
-    alone runs it, on a bounded sample of each step's workload."""
+    alone runs it. Each step is the oracle over a bounded sample of the call's
+    (token, head) pairs (the whole call when it fits), sized so that the
+    warm-up and timed steps take about two minutes in all: ``ms_per_step`` is
+    the measured time of such a step, and ``value`` the sample's bytes over
+    that time (the rate scaled to a whole call, which is what
+    ``us_per_call_extrapolated`` states)."""
     if rank != 0:
         return
     from oracle import oracle
@@ -598,26 +651,37 @@ def run_reference(args, rank, world):
     total_steps = max(1, args.steps + args.warmup)
     budget = 120.0  # seconds for the whole run
     n = int(max(1, min(T * H, budget / total_steps / max(per_pair, 1e-9))))
+    whole = n == T * H
+    every = np.stack([np.repeat(np.arange(T), H), np.tile(np.arange(H), T)], axis=1)
+
+    def sample():
+        if whole:
+            return every
+        return np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
+
     for _ in range(args.warmup):
-        pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
-        oracle.fp64(prob, pairs, threads=cores)
+        oracle.fp64(prob, sample(), threads=cores)
     elapsed = 0.0
     for _ in range(args.steps):
-        pairs = np.stack([rng.integers(0, T, n), rng.integers(0, H, n)], axis=1)
+        pairs = sample()
         t0 = time.perf_counter()
         oracle.fp64(prob, pairs, threads=cores)
         elapsed += time.perf_counter() - t0
-    per_call = elapsed / args.steps / n * T * H
-    value = bytes_alg(w) / per_call / 1e9
+    step_s = elapsed / args.steps
+    per_call = step_s / n * T * H
+    value = bytes_alg(w) * (n / (T * H)) / step_s / 1e9
+    desc = (f"the whole call ({T * H} (token, head) pairs) per step" if whole else
+            f"{n} of {T * H} (token, head) pairs per step, drawn at random")
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_call * 1e3, 3),
-        "us_per_call": round(per_call * 1e6, 1), "higher_is_better": True, "scaling": "weak",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+        "us_per_call_extrapolated": round(per_call * 1e6, 1), "extrapolated": not whole,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
         "config": {"workload": workload_name(args.config, w), "tokens": int(T), "heads": int(H),
-                   "width": int(w["indices"].shape[1]), "head_dim": int(D)},
+                   "width": int(w["indices"].shape[1]), "head_dim": int(D), "step": desc},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n} of {T * H} (token, head) pairs per step"},
+                         "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -719,11 +783,8 @@ def run_merge(args, rank, world, local_rank):
         def e2e_run(inp, outp):
             smla.smla_merge(inp[0], inp[1], sets[0][2], outp[0], outp[1])
 
-        e_ms = pipelined_e2e(torch, host, (sets[0][0], sets[0][1]), e2e_run, (out, lse), min(args.steps, 200))
-        e2e = {"value": round(total_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(T * H * (512 * 2 + 4)),
-               "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
+        e2e = e2e_entry(torch, total_bytes, host, (sets[0][0], sets[0][1]), e2e_run, (out, lse),
+                        min(args.steps, 200), h2d, T * H * (512 * 2 + 4))
     if rank != 0:
         return
     cpu = None
@@ -841,11 +902,8 @@ def run_mxfp4(args, rank, world, local_rank):
         def e2e_run(inp, outp):
             smla.smla_mxfp4_q_quant(inp[0], inp[1], 0.0625, *outp)
 
-        e_ms = pipelined_e2e(torch, host, sets[0], e2e_run, outs[0], min(args.steps, 100))
-        e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(T * H * (256 + 4)),
-               "d2h_bytes_per_step": int(T * H * 72),
-               "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA graph"}
+        e2e = e2e_entry(torch, per_call, host, sets[0], e2e_run, outs[0], min(args.steps, 100),
+                        T * H * (256 + 4), T * H * 72)
     if rank != 0:
         return
     cpu = None
@@ -1008,7 +1066,7 @@ def run_value(args, rank, world, local_rank, fused=False):
         graph.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, max(t_wall1, t_wall0 + args.soak))
-    if smla.smla_value_gate_error() != 0:
+    if smla.smla_device_error() != 0:
         raise RuntimeError("value kernel reported a device error")
     ms = start.elapsed_time(end) / args.steps
     achieved = per_call / (ms * 1e-3) / 1e9
@@ -1034,12 +1092,9 @@ def run_value(args, rank, world, local_rank, fused=False):
                 smla.smla_value_gate(inp[0], sets[0][1], inp[1], inp[2], outp[0])
 
             h2d = T * H * 512 * 2 + T * H * 256 + 4 * T
-        e_ms = pipelined_e2e(torch, host, dev_like, e2e_run, (outs[0],), min(args.steps, 100))
-        e2e = {"value": round(per_call * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "us_per_call": round(e_ms * 1e3, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(T * H * 256),
-               "pipeline": "H2D, call and D2H on three streams over three slots, the steps replayed from one CUDA "
-                           "graph; W_UV resident"}
+        e2e = e2e_entry(torch, per_call, host, dev_like, e2e_run, (outs[0],), min(args.steps, 100), h2d,
+                        T * H * 256)
+        e2e["resident"] = "W_UV (a layer's weights do not travel per call)"
     if rank != 0:
         return
     cpu = None

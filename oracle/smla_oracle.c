@@ -434,8 +434,8 @@ int smla_oracle_merge_pairs(const smla_oracle_merge_problem* m, const int32_t* t
                             double* lse2, int threads) {
     int bad = 0;
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+    const int team = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel for num_threads(team) schedule(dynamic, 4) reduction(| : bad)
 #endif
     for (int i = 0; i < n; ++i)
         bad |= smla_oracle_merge(m, tokens[i], heads[i], out_value ? out_value + (size_t)i * LATENT : NULL,
@@ -565,8 +565,8 @@ int smla_oracle_value_gate(int tokens, int heads, const uint16_t* latent, const 
 int smla_oracle_fp64_all(const smla_oracle_problem* p, double* out, double* lse2, int threads) {
     int pairs = p->tokens * p->heads;
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(dynamic, 1)
+    const int team = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel for num_threads(team) schedule(dynamic, 1)
 #endif
     for (int i = 0; i < pairs; ++i)
         smla_oracle_fp64(p, i / p->heads, i % p->heads, out + (size_t)i * LATENT, lse2 + i);
@@ -578,8 +578,8 @@ int smla_oracle_fp64_all(const smla_oracle_problem* p, double* out, double* lse2
 int smla_oracle_fp64_pairs(const smla_oracle_problem* p, const int32_t* tokens,
                            const int32_t* heads, int n, double* out, double* lse2, int threads) {
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(dynamic, 1)
+    const int team = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel for num_threads(team) schedule(dynamic, 1)
 #endif
     for (int i = 0; i < n; ++i)
         smla_oracle_fp64(p, tokens[i], heads[i], out + (size_t)i * LATENT, lse2 + i);
@@ -594,8 +594,8 @@ int smla_oracle_emulate_pairs(const smla_oracle_problem* p, const int32_t* token
                               int threads) {
     int bad = 0;
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    const int team = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel for num_threads(team) schedule(dynamic, 1) reduction(| : bad)
 #endif
     for (int i = 0; i < n; ++i)
         bad |= smla_oracle_emulate(p, tokens[i], heads[i], splits, chunk, flags,
