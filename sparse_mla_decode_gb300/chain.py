@@ -33,16 +33,17 @@ if ROOT not in sys.path:
 L2_BYTES = 129 * 1024 * 1024
 
 
-def measure(shape: str, layers: int, steps: int) -> dict:
+def make_sets(shape: str, layers: int, sets: int | None, dev):
+    """The chain's inputs: ``sets`` input sets (None: enough that one pass over
+    them reads more than 2.5x the L2) of ``layers`` calls each, and the shared
+    pool they read. Each call is a dict of device tensors (``q``, ``pools``,
+    ``indices``, ``lens``, ``sinks``, ``out``, ``lse``) plus ``w``, its
+    workload with the indices renumbered into the shared pool."""
     import numpy as np
     import torch
 
-    import __graft_entry__
-    from sparse_mla_decode_gb300 import smla, workloads
+    from sparse_mla_decode_gb300 import workloads
 
-    __graft_entry__.build()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
     make = {"verify": workloads.verify_rows, "tiny": workloads.tiny}[shape]
     ws = [make(seed=5000 + 97 * l) for l in range(layers)]
     # Each (set r, layer l) reads its own block of `block` rows of one pool:
@@ -53,7 +54,7 @@ def measure(shape: str, layers: int, steps: int) -> dict:
     assert all(u.size <= block for u in uniq)
     D = ws[0]["q"].shape[2]
     per_step = sum(u.size for u in uniq) * D
-    R = int(min(256, max(4, math.ceil(2.5 * L2_BYTES / per_step))))
+    R = sets or int(min(256, max(4, math.ceil(2.5 * L2_BYTES / per_step))))
     gen = torch.Generator(device=dev)
     gen.manual_seed(77)
     pool = torch.randn((R * layers * block, D), generator=gen, device=dev).to(torch.float8_e4m3fn).view(torch.uint8)
@@ -71,15 +72,37 @@ def measure(shape: str, layers: int, steps: int) -> dict:
                 "lens": torch.from_numpy(w["lens"]).to(dev),
                 "sinks": None if w["sinks"] is None else torch.from_numpy(w["sinks"]).to(dev),
                 "out": torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
-                "lse": torch.empty((T, H), dtype=torch.float32, device=dev), "w": w,
+                "lse": torch.empty((T, H), dtype=torch.float32, device=dev),
+                "w": dict(w, indices=idx.astype(np.int32)),
             })
         steps_sets.append(calls)
+    return pool, steps_sets
+
+
+def run_layers(calls) -> None:
+    """One step: the layers' decode calls, back to back on the current stream."""
+    from sparse_mla_decode_gb300 import smla
+
+    for c in calls:
+        w = c["w"]
+        smla.smla_decode(c["q"], c["pools"], c["indices"], c["lens"], c["sinks"], w["bmm1_scale"],
+                         w["bmm2_scale"], w["k_scale"], c["out"], c["lse"], pool_split=w.get("pool_split", 0))
+
+
+def measure(shape: str, layers: int, steps: int) -> dict:
+    import torch
+
+    import __graft_entry__
+    from sparse_mla_decode_gb300 import smla
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _, steps_sets = make_sets(shape, layers, None, dev)
+    R = len(steps_sets)
 
     def step(i):
-        for c in steps_sets[i % R]:
-            w = c["w"]
-            smla.smla_decode(c["q"], c["pools"], c["indices"], c["lens"], c["sinks"], w["bmm1_scale"],
-                             w["bmm2_scale"], w["k_scale"], c["out"], c["lse"], pool_split=w.get("pool_split", 0))
+        run_layers(steps_sets[i % R])
 
     for i in range(3):
         step(i)
