@@ -19,6 +19,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "smla.h"
 #include "smla_merge_row.cuh"
@@ -157,6 +158,22 @@ int device_sms() {
     return sms;
 }
 
+// CTAs of the merge kernel one SM holds at once (occupancy query at its
+// launch shape), cached per device; -1 when the query fails.
+int resident_merge_ctas() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, lse_merge_kernel, kThreads, 0) != cudaSuccess)
+        return -1;
+    if (dev < 64) cache[dev] = blocks;
+    return blocks;
+}
+
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 }  // namespace lse_merge
@@ -195,13 +212,14 @@ extern "C" int smla_merge(const smla_merge_shape* shape, const void* parts, cons
     p.heads = s.heads;
 
     const int sms = device_sms();
-    if (sms <= 0) return SMLA_ECUDA;
-    // One resident wave (three CTAs per SM at the kernel's registers) with a
-    // grid-stride loop, so that each warp has rows after the current one and
-    // can load their LSEs ahead.
+    const int per_sm = resident_merge_ctas();
+    if (sms <= 0 || per_sm <= 0) return SMLA_ECUDA;
+    // One resident wave (the CTAs an SM holds at the kernel's registers, from
+    // the occupancy query) with a grid-stride loop, so that each warp has rows
+    // after the current one and can load their LSEs ahead.
     const int64_t rows = static_cast<int64_t>(s.tokens) * s.heads;
     const int64_t want = (rows + kWarps - 1) / kWarps;
-    const int64_t cap = static_cast<int64_t>(sms) * 3;
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
