@@ -32,8 +32,8 @@
 //   S^T[key, head]   = KV[key, :] . Q[head, :]      (A = KV K-major, B = Q K-major)
 //   O^T[lat, head]  += V^T[lat, key] . P^T[key, head] (A = the same KV tile read
 //                      MN-major, B = P^T K-major), four 128-latent blocks.
-// TMEM holds two S^T buffers, each as two partial sums over halves of the
-// row (independent accumulator chains keep the tensor pipe busy), and O^T.
+// TMEM holds two S^T buffers (one accumulator over the whole row: a single
+// chain runs at the same smem-bound rate as two) and O^T.
 // Key splits of one (token, head tile) form a cluster and merge over DSMEM.
 // Every wait is bounded; a timeout sets an error bit and the kernel still
 // returns (and frees its TMEM).
@@ -136,8 +136,8 @@ struct Layout {
     static constexpr int kInbox = (kMisc + 64 + 1023) / 1024 * 1024;
     static constexpr int kBytes = kOwnInbox ? kInbox + kInboxBytes : kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;
-    // TMEM columns: S^T chain 0 of buffers 0/1 at [0, 2N), O^T blocks at
-    // [2N, 6N), S^T chain 1 of buffers 0/1 at [6N, 8N).
+    // TMEM columns: S^T of buffers 0/1 at [0, 2N), O^T blocks at [2N, 6N)
+    // (the allocation is a power of two).
     static constexpr int kTmemCols = 8 * N;
 };
 
@@ -181,24 +181,14 @@ __device__ __forceinline__ void store_rows(const Params& p, const __nv_bfloat16*
     }
 }
 
-// Logits of the H heads at two TMEM chain addresses (H = 16 or 32): the sum of
-// the two partial-sum chains of S^T, one TMEM round trip.
+// Logits of the H heads (H = 16 or 32) of this thread's key, from the S^T
+// accumulator at TMEM address `col` (one round trip).
 template <int H>
-__device__ __forceinline__ void load_logits(uint32_t chain0, uint32_t chain1, float (&s)[H]) {
-    if constexpr (H == 16) {
-        float v[32];
-        tmem_load16x2(chain0, chain1, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) s[j] = v[j] + v[16 + j];
-    } else {
-        float v[64];
-        tmem_load16x4(chain0, chain1, chain0 + 16, chain1 + 16, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            s[j] = v[j] + v[16 + j];
-            s[16 + j] = v[32 + j] + v[48 + j];
-        }
-    }
+__device__ __forceinline__ void load_logits(uint32_t col, float (&s)[H]) {
+    if constexpr (H == 16)
+        tmem_load16x1(col, s);
+    else
+        tmem_load16x2(col, col + 16, s);
 }
 
 template <int N, int D>
@@ -515,24 +505,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
                     tc_fence_after_sync();
                     const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
-                    // chain 0: latent bytes 0..255; chain 1: 256..511 and the
-                    // rope; their MMAs alternate
-                    const uint32_t d_s0 = tmem + (c & 1) * N;
-                    const uint32_t d_s1 = tmem + 6 * N + (c & 1) * N;
+                    // one accumulator: the 16 latent K steps, then the rope's two
+                    const uint32_t d_s = tmem + (c & 1) * N;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         const int kb = i >> 2, ks = i & 3;
-                        const uint32_t a0 = stage16 + ((kb * kChunk * 128 + ks * 32) >> 4);
-                        const uint32_t b0 = (kb * N * 128 + ks * 32) >> 4;
-                        mma_f8(d_s0, d_kv + a0, d_q + b0, kIdescQK, i != 0 ? 1u : 0u);
-                        const uint32_t a1 = stage16 + (((kb + 2) * kChunk * 128 + ks * 32) >> 4);
-                        const uint32_t b1 = ((kb + 2) * N * 128 + ks * 32) >> 4;
-                        mma_f8(d_s1, d_kv + a1, d_q + b1, kIdescQK, i != 0 ? 1u : 0u);
+                        const uint32_t a = stage16 + ((kb * kChunk * 128 + ks * 32) >> 4);
+                        const uint32_t bq = (kb * N * 128 + ks * 32) >> 4;
+                        mma_f8(d_s, d_kv + a, d_q + bq, kIdescQK, i != 0 ? 1u : 0u);
                     }
                     if constexpr (L::kRope) {
 #pragma unroll
                         for (int ks = 0; ks < 2; ++ks)
-                            mma_f8(d_s1, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
+                            mma_f8(d_s, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
                                    kIdescQK, 1u);
                     }
                     mma_commit(&s_full[c & 1]);
@@ -592,33 +577,41 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             ok &= mbar_wait_bounded(&s_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             tc_fence_after_sync();
             const bool active = idx_s[b * kChunk + t] >= 0;
-            const uint32_t chain0 = tmem + lane_base + b * N + hb, chain1 = tmem + lane_base + 6 * N + b * N + hb;
+            // this key's logits of the warpgroup's heads, kept for the P pass
+            float s[HW];
+            load_logits<HW>(tmem + lane_base + b * N + hb, s);
 
             // chunk maxima per head, in logit units (bmm1_scale > 0 keeps the
             // order; masked keys are -inf)
             {
                 // a transposing butterfly: each step hands half of a lane's
                 // heads to its partner; with 32 heads lane l ends with head l,
-                // with 16 lanes 2 h and 2 h + 1 share head h
-                float s[HW];
-                load_logits<HW>(chain0, chain1, s);
+                // with 16 lanes 2 h and 2 h + 1 share head h. The first step
+                // reads the logits and leaves them in place.
+                float m[HW / 2];
+                {
+                    const bool up = (lane & 16) != 0;
 #pragma unroll
-                for (int j = 0; j < HW; ++j) s[j] = active ? s[j] : -INFINITY;
+                    for (int i = 0; i < HW / 2; ++i) {
+                        const float lo = active ? s[i] : -INFINITY, hi = active ? s[i + HW / 2] : -INFINITY;
+                        m[i] = fmaxf(up ? hi : lo, __shfl_xor_sync(0xFFFFFFFFu, up ? lo : hi, 16));
+                    }
+                }
 #pragma unroll
-                for (int o = 16, n = HW; n > 1; o >>= 1, n >>= 1) {
+                for (int o = 8, n = HW / 2; n > 1; o >>= 1, n >>= 1) {
                     const bool up = (lane & o) != 0;
 #pragma unroll
                     for (int i = 0; i < n / 2; ++i) {
-                        const float send = up ? s[i] : s[i + n / 2];
-                        const float keep = up ? s[i + n / 2] : s[i];
-                        s[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+                        const float send = up ? m[i] : m[i + n / 2];
+                        const float keep = up ? m[i + n / 2] : m[i];
+                        m[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
                     }
                 }
                 if constexpr (HW == 16) {
-                    s[0] = fmaxf(s[0], __shfl_xor_sync(0xFFFFFFFFu, s[0], 1));
-                    if ((lane & 1) == 0) red[(warp & 3) * N + hb + (lane >> 1)] = s[0];
+                    m[0] = fmaxf(m[0], __shfl_xor_sync(0xFFFFFFFFu, m[0], 1));
+                    if ((lane & 1) == 0) red[(warp & 3) * N + hb + (lane >> 1)] = m[0];
                 } else {
-                    red[(warp & 3) * N + hb + lane] = s[0];
+                    red[(warp & 3) * N + hb + lane] = m[0];
                 }
             }
             named_barrier(1 + wg, 128);
@@ -637,8 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             // chunk c-2 has finished reading it); FP32 sums of the unrounded P
             if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
             {
-                float s[HW];
-                load_logits<HW>(chain0, chain1, s);
                 uint8_t* pbuf = smem + L::kP + b * kChunk * N;
 #pragma unroll
                 for (int g = 0; g < HW / 16; ++g) {
