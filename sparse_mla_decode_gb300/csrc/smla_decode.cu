@@ -59,7 +59,7 @@
 
 namespace smla {
 
-constexpr int kChunk = 128;  // keys per chunk = the MMA's M
+constexpr int kRows = 128;  // the MMA's M: rows of S^T, latents of an O^T block
 constexpr int kLatent = 512;
 constexpr int kThreads = 512;
 constexpr int kSoftmaxRange = 256;  // warps 0-7: one or two softmax warpgroups
@@ -111,19 +111,24 @@ constexpr int max_inbox_slices() {
 
 // Shared-memory map of one CTA for N heads and D-byte rows (offsets from a
 // 1024-byte aligned base; every MMA operand tile starts on 1024 bytes).
-template <int N, int D>
+template <int N, int D, int C>
 struct Layout {
     // A tile of R rows: four 128-byte latent K blocks (128B swizzle, 8-row
     // atoms of 1 KB) then, for 576-byte rows, the 64-byte rope block (64B
     // swizzle, 8-row atoms of 512 bytes).
+    // C keys per chunk: 128 in two stages, or 96 in three (the MMAs still
+    // read 128 rows; the 32 past a 96-key block are the next block's or the
+    // next area's bytes, and their S^T rows are masked, their P^T rows never
+    // read).
     static constexpr bool kRope = D == 576;
-    static constexpr int kStage = 4 * kChunk * 128 + (kRope ? kChunk * 64 : 0);
-    static constexpr int kKv = 0;                                 // 2 stages of KV rows
-    static constexpr int kQ = 2 * kStage;                         // the Q tile
+    static constexpr int kStages = C == 128 ? 2 : 3;
+    static constexpr int kStage = 4 * C * 128 + (kRope ? C * 64 : 0);
+    static constexpr int kKv = 0;                                 // kStages stages of KV rows
+    static constexpr int kQ = kStages * kStage;                   // the Q tile
     static constexpr int kQBytes = 4 * N * 128 + (kRope ? N * 64 : 0);
-    static constexpr int kP = kQ + kQBytes;                       // 2 buffers of P^T (kChunk x N bytes)
-    static constexpr int kIdx = kP + 2 * kChunk * N;    // int32 [2][128] row of each key, -1 masked
-    static constexpr int kRed = kIdx + 2 * kChunk * 4;  // float [4][N] per-warp partials
+    static constexpr int kP = kQ + kQBytes;                       // 2 buffers of P^T (C x N bytes)
+    static constexpr int kIdx = kP + 2 * C * N;            // int32 [kStages][C] row of each key, -1 masked
+    static constexpr int kRed = kIdx + kStages * C * 4;    // float [4][N] per-warp partials
     static constexpr int kHead = kRed + 4 * N * 4;      // float [4][N]: m_run, bias, alpha, l
     static constexpr int kBar = kHead + 4 * N * 4;      // 16 mbarriers
     static constexpr int kMisc = kBar + 16 * 8;         // tmem base, abort flag
@@ -136,6 +141,9 @@ struct Layout {
     static constexpr int kInbox = (kMisc + 64 + 1023) / 1024 * 1024;
     static constexpr int kBytes = kOwnInbox ? kInbox + kInboxBytes : kMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;
+    static_assert(C == 128 || C == 96, "chunks of 128 or 96 keys");
+    static_assert(kAlloc <= 227 * 1024, "one CTA's shared memory");
+    static_assert(kStage % 1024 == 0 && kQ % 1024 == 0 && kP % 512 == 0, "operand tiles stay aligned");
     // TMEM columns: S^T of buffers 0/1 at [0, 2N), O^T blocks at [2N, 6N)
     // (the allocation is a power of two).
     static constexpr int kTmemCols = 8 * N;
@@ -191,9 +199,10 @@ __device__ __forceinline__ void load_logits(uint32_t col, float (&s)[H]) {
         tmem_load16x2(col, col + 16, s);
 }
 
-template <int N, int D>
+template <int N, int D, int C>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __grid_constant__ Params p) {
-    using L = Layout<N, D>;
+    using L = Layout<N, D, C>;
+    constexpr int NS = L::kStages;
     constexpr int NG = N == 64 ? 2 : 1;  // softmax warpgroups
     constexpr int HW = N / NG;           // heads per softmax warpgroup (16 or 32)
     extern __shared__ uint8_t smem_raw[];
@@ -201,20 +210,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     const uint32_t sbase = smem_u32(smem);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint64_t* kv_full = bars + 0;   // [2] a stage's rows landed (224 cp.async arrivals + 1)
-    // pv_done[b]: PV of the chunk in stage b finished (its KV stage and P^T
-    // buffer are free, O^T holds it). One barrier per stage, so that no waiter
-    // is ever more than one phase behind the barrier it waits on.
-    uint64_t* pv_done = bars + 2;   // [2] commit
-    uint64_t* s_full = bars + 4;    // [2] QK of a chunk done (commit)
-    uint64_t* p_full = bars + 6;    // P^T written, O^T rescaled (softmax arrivals)
-    uint64_t* drain = bars + 8;     // every MMA done (commit)
-    uint64_t* q_full = bars + 9;    // the Q tile landed (TMA transaction bytes)
-    uint64_t* kv_first = bars + 10; // chunk 0 landed (256 cp.async arrivals + 1); later chunks use kv_full
-    // stage_free[b] (paired): PV of the chunk in stage b finished in both CTAs
-    // of the pair (one multicast commit from each), so either may refill the
-    // stage in both.
-    uint64_t* stage_free = bars + 11;  // [2]
+    uint64_t* kv_full = bars + 0;   // [NS] a stage's rows landed (224 cp.async arrivals + 1)
+    // pv_done[st]: PV of the chunk in stage st finished (its KV stage is free,
+    // O^T holds it). One barrier per stage, so that no waiter is ever more
+    // than one phase behind the barrier it waits on.
+    uint64_t* pv_done = bars + 3;   // [NS] commit
+    uint64_t* s_full = bars + 6;    // [2] QK of a chunk done (commit)
+    uint64_t* p_full = bars + 8;    // P^T written, O^T rescaled (softmax arrivals)
+    uint64_t* drain = bars + 9;     // every MMA done (commit)
+    uint64_t* q_full = bars + 10;   // the Q tile landed (TMA transaction bytes)
+    uint64_t* kv_first = bars + 11; // chunk 0 landed (256 cp.async arrivals + 1); later chunks use kv_full
+    // stage_free[st] (paired): PV of the chunk in stage st finished in both
+    // CTAs of the pair (one multicast commit from each), so either may refill
+    // the stage in both.
+    uint64_t* stage_free = bars + 12;  // [NS]
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::kIdx);
@@ -241,13 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     if (tid == 0) {
         // paired: the producer's expect-tx arrival; else every producer
         // thread's cp.async arrival and one index-release arrival
-        mbar_init(&kv_full[0], paired ? 1 : kProducerThreads + 1);
-        mbar_init(&kv_full[1], paired ? 1 : kProducerThreads + 1);
-        mbar_init(&stage_free[0], 2);
-        mbar_init(&stage_free[1], 2);
+        for (int st = 0; st < NS; ++st) {
+            mbar_init(&kv_full[st], paired ? 1 : kProducerThreads + 1);
+            mbar_init(&stage_free[st], 2);
+            mbar_init(&pv_done[st], 1);
+        }
         mbar_init(q_full, 1);
-        mbar_init(&pv_done[0], 1);
-        mbar_init(&pv_done[1], 1);
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
         mbar_init(p_full, NG * 128);
@@ -296,37 +304,42 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     // for split 0). Thread k of the chunk's resolvers (the softmax range
     // unpaired, the producers paired) takes column k; the count masks them
     // later, and a split whose first chunk turns out elsewhere reloads.
-    const int chunks_w = (p.width + kChunk - 1) / kChunk;
-    const int col_guess = split * ((chunks_w + splits - 1) / splits) * kChunk;
+    const int chunks_w = (p.width + C - 1) / C;
+    const int col_guess = split * ((chunks_w + splits - 1) / splits) * C;
     const int resolver = paired ? tid - kProducerWarp * 32 : tid;
     int32_t raw_guess = -1;
-    if (resolver >= 0 && resolver < kChunk && col_guess + resolver < p.width)
+    if (resolver >= 0 && resolver < C && col_guess + resolver < p.width)
         raw_guess = p.indices[static_cast<int64_t>(token) * p.idx_stride + col_guess + resolver];
     const int count = min(max(p.lens[token], 0), p.width);
     // This split's chunks of the token: ceil(chunks / splits) consecutive
     // chunks each, dealt over the token's own count (later splits may be empty).
-    const int chunks_total = (count + kChunk - 1) / kChunk;
+    const int chunks_total = (count + C - 1) / C;
     const int per_split = (chunks_total + splits - 1) / splits;
     const int c_first = split * per_split;
     const int nch = max(0, min(per_split, chunks_total - c_first));
     grid_launch_dependents();
-    // Chunk c's stage barrier and the parity of its phase: chunk 0 has its own
-    // barrier; stage 1 serves chunks 1, 3, 5, ..., stage 0 chunks 2, 4, ...
-    // Paired CTAs use the two stage barriers from chunk 0 on.
-    auto kv_bar = [&](int c) -> uint64_t* { return (c == 0 && !paired) ? kv_first : &kv_full[c & 1]; };
+    // Chunk c lives in stage c % NS. Its stage barrier and the parity of its
+    // phase: unpaired, chunk 0 has its own barrier and stage 0's barrier
+    // serves chunks NS, 2 NS, ... from its first phase; paired CTAs use the
+    // stage barriers from chunk 0 on. A phase of pv_done / stage_free
+    // completes per chunk of its stage, chunk c's being phase c / NS.
+    bool ok = true;
+    auto kv_bar = [&](int c) -> uint64_t* { return (c == 0 && !paired) ? kv_first : &kv_full[c % NS]; };
     auto kv_parity = [&](int c) -> uint32_t {
-        if (paired) return static_cast<uint32_t>((c >> 1) & 1);
-        return c == 0 ? 0u : static_cast<uint32_t>(((c >> 1) - ((c & 1) ? 0 : 1)) & 1);
+        if (paired) return static_cast<uint32_t>((c / NS) & 1);
+        return c == 0 ? 0u : static_cast<uint32_t>(((c / NS) - (c % NS == 0 ? 1 : 0)) & 1);
+    };
+    auto pv_wait = [&](int c) {  // PV of chunk c has finished
+        ok &= mbar_wait_bounded(&pv_done[c % NS], static_cast<uint32_t>((c / NS) & 1), abort_flag, kWaitLimitNs);
     };
 
-    bool ok = true;
     if (warp < kSoftmaxRange / 32 && nch > 0 && !paired) {
         // ============================= chunk 0 by the softmax-range warps
         // (idle until the first QK): the first gather is on every CTA's
         // critical path, and more issuing warps stream it faster.
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
-        const int col0 = c_first * kChunk;
-        if (tid < kChunk) {
+        const int col0 = c_first * C;
+        if (tid < C) {
             const int col = col0 + tid;
             int32_t id = -1;
             if (col < count) {
@@ -344,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         named_barrier(5, kSoftmaxRange);
         if (tid == 0) mbar_arrive(kv_first);  // every idx_s entry (release)
         const uint32_t stage = sbase + L::kKv;
-        const uint32_t lane_part = stage + (lane >> 3) * kChunk * 128;
-        for (int k = warp; k < kChunk; k += kSoftmaxRange / 32) {
+        const uint32_t lane_part = stage + (lane >> 3) * C * 128;
+        for (int k = warp; k < C; k += kSoftmaxRange / 32) {
             const int32_t id = idx_s[k];
             const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
             const uint8_t* src = (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + lane * 16;
@@ -353,13 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             cp_async_16(dst, src, id >= 0 ? 16u : 0u);
         }
         if constexpr (L::kRope) {
-            for (int j = warp; j < kChunk / 8; j += kSoftmaxRange / 32) {
+            for (int j = warp; j < C / 8; j += kSoftmaxRange / 32) {
                 const int k = j * 8 + (lane >> 2), u = lane & 3;
                 const int32_t id = idx_s[k];
                 const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
                 const uint8_t* src =
                     (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + 512 + u * 16;
-                const uint32_t dst = stage + 4 * kChunk * 128 + (k >> 3) * 512 + (k & 7) * 64 + ((u ^ ((k >> 1) & 3)) << 4);
+                const uint32_t dst = stage + 4 * C * 128 + (k >> 3) * 512 + (k & 7) * 64 + ((u ^ ((k >> 1) & 3)) << 4);
                 cp_async_16(dst, src, id >= 0 ? 16u : 0u);
             }
         }
@@ -376,13 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
         const int32_t past_end = static_cast<int32_t>(p.rows0);
         for (int c = 0; c < nch; ++c) {
-            const int b = c & 1;
-            const int col0 = (c_first + c) * kChunk;
-            const int32_t raw = (g < kChunk && col0 + g < count)
+            const int b = c % NS;
+            const int col0 = (c_first + c) * C;
+            const int32_t raw = (g < C && col0 + g < count)
                                     ? ((c == 0 && col0 == col_guess) ? raw_guess : idx_row[col0 + g])
                                     : -1;
-            if (c >= 2) ok &= mbar_wait_bounded(&stage_free[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
-            if (g < kChunk) {
+            if (c >= NS)
+                ok &= mbar_wait_bounded(&stage_free[b], ((c - NS) / NS) & 1, abort_flag, kWaitLimitNs);
+            if (g < C) {
                 int32_t id = -1;
                 if (raw >= 0) {
                     if (raw < p.rows0)
@@ -390,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     else
                         atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
                 }
-                idx_s[b * kChunk + g] = id;
+                idx_s[b * C + g] = id;
             }
             named_barrier(3, kProducerThreads);
             if (g == 0) mbar_arrive_expect_tx(&kv_full[b], L::kStage);  // both halves; also releases idx_s
@@ -398,20 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 // one lane per producer warp: the TMA instructions of one
                 // thread issue one after another, several threads overlap
                 const uint32_t stage = sbase + L::kKv + b * L::kStage;
-                for (int k = half * (kChunk / 2) + 4 * (g >> 5); k < (half + 1) * (kChunk / 2);
+                for (int k = half * (C / 2) + 4 * (g >> 5); k < (half + 1) * (C / 2);
                      k += 4 * (kProducerThreads / 32)) {
                     int32_t r[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int32_t id = idx_s[b * kChunk + k + i];
+                        const int32_t id = idx_s[b * C + k + i];
                         r[i] = id >= 0 ? id : past_end;
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        tma_gather4_multicast(stage + j * kChunk * 128 + (k >> 3) * 1024 + (k & 7) * 128, &p.kv_latent,
+                        tma_gather4_multicast(stage + j * C * 128 + (k >> 3) * 1024 + (k & 7) * 128, &p.kv_latent,
                                               j * 128, r[0], r[1], r[2], r[3], &kv_full[b], pair_mask);
                     if constexpr (L::kRope)
-                        tma_gather4_multicast(stage + 4 * kChunk * 128 + (k >> 3) * 512 + (k & 7) * 64, &p.kv_rope,
+                        tma_gather4_multicast(stage + 4 * C * 128 + (k >> 3) * 512 + (k & 7) * 64, &p.kv_rope,
                                               512, r[0], r[1], r[2], r[3], &kv_full[b], pair_mask);
                 }
             }
@@ -419,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         // The partner's commits for the last chunks have reached this CTA's
         // stage barriers before either CTA moves on to its exit.
         if (g == 0)
-            for (int c = max(0, nch - 2); c < nch; ++c)
-                ok &= mbar_wait_bounded(&stage_free[c & 1], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+            for (int c = max(0, nch - NS); c < nch; ++c)
+                ok &= mbar_wait_bounded(&stage_free[c % NS], (c / NS) & 1, abort_flag, kWaitLimitNs);
     } else if (warp >= kProducerWarp) {
         // ================================================== producers
         // Thread g < 128 resolves key g's row; warp w then copies keys w,
@@ -432,13 +446,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         const int pw = g >> 5;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
         for (int c = 1; c < nch; ++c) {  // chunk 0 is gathered by the softmax-range warps
-            const int b = c & 1;
-            const int col0 = (c_first + c) * kChunk;
+            const int b = c % NS;
+            const int col0 = (c_first + c) * C;
             // This chunk's index is loaded before the wait for its stage, so
             // that its latency overlaps the wait.
-            const int32_t raw = (g < kChunk && col0 + g < count) ? idx_row[col0 + g] : -1;
-            if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
-            if (g < kChunk) {
+            const int32_t raw = (g < C && col0 + g < count) ? idx_row[col0 + g] : -1;
+            if (c >= NS) pv_wait(c - NS);
+            if (g < C) {
                 const int col = col0 + g;
                 int32_t id = -1;
                 if (col < count) {
@@ -450,27 +464,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                             atomicOr(&g_device_error, SMLA_DEV_INDEX_RANGE);
                     }
                 }
-                idx_s[b * kChunk + g] = id;
+                idx_s[b * C + g] = id;
             }
             named_barrier(3, kProducerThreads);
             if (g == 0) mbar_arrive(&kv_full[b]);
             const uint32_t stage = sbase + L::kKv + b * L::kStage;
-            const uint32_t lane_part = stage + (lane >> 3) * kChunk * 128;
-            for (int k = pw; k < kChunk; k += kProducerThreads / 32) {
-                const int32_t id = idx_s[b * kChunk + k];
+            const uint32_t lane_part = stage + (lane >> 3) * C * 128;
+            for (int k = pw; k < C; k += kProducerThreads / 32) {
+                const int32_t id = idx_s[b * C + k];
                 const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
                 const uint8_t* src = (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + lane * 16;
                 const uint32_t dst = lane_part + (k >> 3) * 1024 + (k & 7) * 128 + (((lane & 7) ^ (k & 7)) << 4);
                 cp_async_16(dst, src, id >= 0 ? 16u : 0u);
             }
             if constexpr (L::kRope) {
-                for (int j = pw; j < kChunk / 8; j += kProducerThreads / 32) {
+                for (int j = pw; j < C / 8; j += kProducerThreads / 32) {
                     const int k = j * 8 + (lane >> 2), u = lane & 3;
-                    const int32_t id = idx_s[b * kChunk + k];
+                    const int32_t id = idx_s[b * C + k];
                     const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
                     const uint8_t* src =
                         (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + 512 + u * 16;
-                    const uint32_t dst = stage + 4 * kChunk * 128 + (k >> 3) * 512 + (k & 7) * 64 + ((u ^ ((k >> 1) & 3)) << 4);
+                    const uint32_t dst = stage + 4 * C * 128 + (k >> 3) * 512 + (k & 7) * 64 + ((u ^ ((k >> 1) & 3)) << 4);
                     cp_async_16(dst, src, id >= 0 ? 16u : 0u);
                 }
             }
@@ -483,15 +497,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         // softmax of chunk c - 2 is done, i.e. PV(c - 2) was issued); PV(c) as
         // soon as P(c) is ready. Whichever is due goes first.
         if (lane == 0) {
-            constexpr uint32_t kIdescQK = idesc_e4m3(128, N, 0, 0);
-            constexpr uint32_t kIdescPV = idesc_e4m3(128, N, 1, 1);
+            constexpr uint32_t kIdescQK = idesc_e4m3(kRows, N, 0, 0);
+            constexpr uint32_t kIdescPV = idesc_e4m3(kRows, N, 1, 1);
             // Descriptors of every operand tile; moving a descriptor by b
             // bytes adds b >> 4 to its start field (no carry: shared
             // addresses stay below 256 KB).
             const uint64_t d_q = smem_desc(sbase + L::kQ, 1024, 1024, kSwizzle128B);
             const uint64_t d_q_rope = smem_desc(sbase + L::kQ + 4 * N * 128, 512, 512, kSwizzle64B);
             const uint64_t d_kv = smem_desc(sbase + L::kKv, 1024, 1024, kSwizzle128B);
-            const uint64_t d_kv_rope = smem_desc(sbase + L::kKv + 4 * kChunk * 128, 512, 512, kSwizzle64B);
+            const uint64_t d_kv_rope = smem_desc(sbase + L::kKv + 4 * C * 128, 512, 512, kSwizzle64B);
             const uint64_t d_p = smem_desc(sbase + L::kP, 8 * N, 8 * N, p_swizzle<N>());
             int next_qk = 0, next_pv = 0;
             bool q_ready = false;
@@ -504,13 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                     const int c = next_qk;
                     fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
                     tc_fence_after_sync();
-                    const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
+                    const uint32_t stage16 = static_cast<uint32_t>((c % NS) * L::kStage) >> 4;
                     // one accumulator: the 16 latent K steps, then the rope's two
                     const uint32_t d_s = tmem + (c & 1) * N;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int kb = i >> 2, ks = i & 3;
-                        const uint32_t a = stage16 + ((kb * kChunk * 128 + ks * 32) >> 4);
+                        const uint32_t a = stage16 + ((kb * C * 128 + ks * 32) >> 4);
                         const uint32_t bq = (kb * N * 128 + ks * 32) >> 4;
                         mma_f8(d_s, d_kv + a, d_q + bq, kIdescQK, i != 0 ? 1u : 0u);
                     }
@@ -527,20 +541,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                 if (next_pv < next_qk && mbar_test_wait(p_full, next_pv & 1)) {
                     const int c = next_pv;
                     tc_fence_after_sync();
-                    const uint32_t stage16 = static_cast<uint32_t>((c & 1) * L::kStage) >> 4;
-                    const uint32_t p16 = static_cast<uint32_t>((c & 1) * kChunk * N) >> 4;
+                    const uint32_t stage16 = static_cast<uint32_t>((c % NS) * L::kStage) >> 4;
+                    const uint32_t p16 = static_cast<uint32_t>((c & 1) * C * N) >> 4;
 #pragma unroll
-                    for (int kk = 0; kk < kChunk / 32; ++kk) {  // the four latent blocks are independent chains
+                    for (int kk = 0; kk < C / 32; ++kk) {  // the four latent blocks are independent chains
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint32_t a_off = stage16 + ((j * kChunk * 128 + kk * 32 * 128) >> 4);
+                            const uint32_t a_off = stage16 + ((j * C * 128 + kk * 32 * 128) >> 4);
                             const uint32_t b_off = p16 + ((kk * 32 * N) >> 4);
                             mma_f8(tmem + 2 * N + j * N, d_kv + a_off, d_p + b_off, kIdescPV,
                                    (c > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
-                    mma_commit(&pv_done[c & 1]);
-                    if (paired) mma_commit_multicast(&stage_free[c & 1], pair_mask);
+                    mma_commit(&pv_done[c % NS]);
+                    if (paired) mma_commit_multicast(&stage_free[c % NS], pair_mask);
                     ++next_pv;
                     progressed = true;
                 }
@@ -576,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             ok &= mbar_wait_bounded(kv_bar(c), kv_parity(c), abort_flag, kWaitLimitNs);
             ok &= mbar_wait_bounded(&s_full[b], (c >> 1) & 1, abort_flag, kWaitLimitNs);
             tc_fence_after_sync();
-            const bool active = idx_s[b * kChunk + t] >= 0;
+            const bool active = t < C && idx_s[(c % NS) * C + t] >= 0;
             // this key's logits of the warpgroup's heads, kept for the P pass
             float s[HW];
             load_logits<HW>(tmem + lane_base + b * N + hb, s);
@@ -628,9 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
 
             // P = 2^(s * scale_log2 - m + log2 448) as E4M3 into P^T[b] (PV of
             // chunk c-2 has finished reading it); FP32 sums of the unrounded P
-            if (c >= 2) ok &= mbar_wait_bounded(&pv_done[b], ((c - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
+            if (c >= 2) pv_wait(c - 2);  // its P^T buffer is free
             {
-                uint8_t* pbuf = smem + L::kP + b * kChunk * N;
+                uint8_t* pbuf = smem + L::kP + b * C * N;
 #pragma unroll
                 for (int g = 0; g < HW / 16; ++g) {
                     uint32_t words[4];
@@ -652,14 +666,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
                         lsum[j + 3] = fmaf(lsum[j + 3], al.w, pr[3]);
                         words[q4] = e4m3x2(pr[0], pr[1]) | (e4m3x2(pr[2], pr[3]) << 16);
                     }
-                    *reinterpret_cast<uint4*>(pbuf + p_unit<N>(t, hb / 16 + g)) =
-                        make_uint4(words[0], words[1], words[2], words[3]);
+                    if (t < C)
+                        *reinterpret_cast<uint4*>(pbuf + p_unit<N>(t, hb / 16 + g)) =
+                            make_uint4(words[0], words[1], words[2], words[3]);
                 }
             }
 
             // O^T *= alpha where a head's running maximum rose (PV of chunk c-1 is done)
             if (c >= 1) {
-                ok &= mbar_wait_bounded(&pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+                pv_wait(c - 1);
                 tc_fence_after_sync();
 #pragma unroll
                 for (int g = 0; g < HW / 16; ++g) {
@@ -689,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             tc_fence_before_sync();
             mbar_arrive(p_full);
         }
-        if (nch > 0) ok &= mbar_wait_bounded(&pv_done[(nch - 1) & 1], ((nch - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+        if (nch > 0) pv_wait(nch - 1);
         tc_fence_after_sync();
 
         // per-head totals of the per-thread partial sums
@@ -912,22 +927,18 @@ int head_tile_for(int heads) {
     return 16;
 }
 
-template <int N, int D>
-constexpr int smem_bytes() {
-    return Layout<N, D>::kAlloc;
-}
-
-int smem_for(int n, int d) {
-    if (d == 576) return n == 64 ? smem_bytes<64, 576>() : n == 32 ? smem_bytes<32, 576>() : smem_bytes<16, 576>();
-    return n == 64 ? smem_bytes<64, 512>() : n == 32 ? smem_bytes<32, 512>() : smem_bytes<16, 512>();
+template <int N, int D, int C>
+int smem_bytes() {
+    return Layout<N, D, C>::kAlloc;
 }
 
 int tmem_for(int n) { return 8 * n; }
 
-// Largest split count whose merge area fits the KV + Q tiles it reuses.
-bool merge_fits(int n, int d, int splits) {
-    const int stage = 4 * kChunk * 128 + (d == 576 ? kChunk * 64 : 0);
-    const int limit = 2 * stage + 4 * n * 128 + (d == 576 ? n * 64 : 0);  // KV stages + Q tile
+// Whether the merge area of `splits` splits fits the KV + Q tiles it reuses
+// (chunks of c keys).
+bool merge_fits(int n, int d, int c, int splits) {
+    const int stage = 4 * c * 128 + (d == 576 ? c * 64 : 0);
+    const int limit = (c == 128 ? 2 : 3) * stage + 4 * n * 128 + (d == 576 ? n * 64 : 0);  // KV stages + Q tile
     const int slots = (16 + splits - 1) / splits;
     return splits * slots * n * 32 * 4 + splits * 3 * n * 4 <= limit;
 }
@@ -945,10 +956,10 @@ bool dependent_launch() {
 
 // Opts the kernel into its shared-memory size and non-portable clusters, once
 // per device.
-template <int N, int D>
+template <int N, int D, int C>
 cudaError_t configure() {
-    auto kernel = sparse_mla_decode_kernel<N, D>;
-    constexpr int kSmem = Layout<N, D>::kAlloc;
+    auto kernel = sparse_mla_decode_kernel<N, D, C>;
+    constexpr int kSmem = Layout<N, D, C>::kAlloc;
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -966,13 +977,13 @@ cudaError_t configure() {
 // CTAs in clusters of `splits` that the current device holds at once (the
 // occupancy API's cluster count x splits; GPC boundaries make it smaller than
 // the SM count for wide clusters). 0 when the query fails.
-template <int N, int D>
+template <int N, int D, int C>
 int resident_ctas_query(int splits) {
-    if (configure<N, D>() != cudaSuccess) return 0;
+    if (configure<N, D, C>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(splits), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Layout<N, D>::kAlloc;
+    cfg.dynamicSmemBytes = Layout<N, D, C>::kAlloc;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = static_cast<unsigned>(splits);
@@ -981,43 +992,65 @@ int resident_ctas_query(int splits) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, sparse_mla_decode_kernel<N, D>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, sparse_mla_decode_kernel<N, D, C>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return clusters * splits;
 }
 
-int resident_ctas_on_device(int n, int d, int splits) {
+// The kernel's variants, by head tile n, row bytes d and chunk keys c.
+struct Variant {
+    int (*smem)();
+    int (*resident)(int splits);
+    cudaError_t (*launch)(const Params& p, dim3 grid, int cluster, cudaStream_t stream);
+};
+
+template <int N, int D, int C>
+cudaError_t launch(const Params& p, dim3 grid, int cluster, cudaStream_t stream);
+
+template <int N, int D, int C>
+Variant variant() {
+    return {smem_bytes<N, D, C>, resident_ctas_query<N, D, C>, launch<N, D, C>};
+}
+
+const Variant& variant_for(int n, int d, int c) {
+    static const Variant table[3][2][2] = {
+        {{variant<64, 576, 128>(), variant<64, 576, 96>()}, {variant<64, 512, 128>(), variant<64, 512, 96>()}},
+        {{variant<32, 576, 128>(), variant<32, 576, 96>()}, {variant<32, 512, 128>(), variant<32, 512, 96>()}},
+        // 16-head tiles keep 128-key chunks: their own merge inbox leaves no room for a third stage
+        {{variant<16, 576, 128>(), variant<16, 576, 128>()}, {variant<16, 512, 128>(), variant<16, 512, 128>()}},
+    };
+    return table[n == 64 ? 0 : n == 32 ? 1 : 2][d == 576 ? 0 : 1][c == 128 ? 0 : 1];
+}
+
+int smem_for(int n, int d, int c) { return variant_for(n, d, c).smem(); }
+
+int resident_ctas_on_device(int n, int d, int c, int splits) {
     static std::mutex mu;
-    static int cache[64][3][2][kMaxSplits + 1] = {};
+    static int cache[64][3][2][2][kMaxSplits + 1] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || splits < 1 || splits > kMaxSplits) return 0;
     const int ni = n == 64 ? 0 : n == 32 ? 1 : 2;
     const int di = d == 576 ? 0 : 1;
+    const int ci = c == 128 ? 0 : 1;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (cache[dev][ni][di][splits] != 0) return cache[dev][ni][di][splits];
+        if (cache[dev][ni][di][ci][splits] != 0) return cache[dev][ni][di][ci][splits];
     }
-    int r = 0;
-    if (d == 576)
-        r = n == 64 ? resident_ctas_query<64, 576>(splits) : n == 32 ? resident_ctas_query<32, 576>(splits)
-                                                                    : resident_ctas_query<16, 576>(splits);
-    else
-        r = n == 64 ? resident_ctas_query<64, 512>(splits) : n == 32 ? resident_ctas_query<32, 512>(splits)
-                                                                    : resident_ctas_query<16, 512>(splits);
+    const int r = variant_for(n, d, c).resident(splits);
     if (r > 0) {
         std::lock_guard<std::mutex> lock(mu);
-        cache[dev][ni][di][splits] = r;
+        cache[dev][ni][di][ci][splits] = r;
     }
     return r;
 }
 
-template <int N, int D>
+template <int N, int D, int C>
 cudaError_t launch(const Params& p, dim3 grid, int cluster, cudaStream_t stream) {
-    auto kernel = sparse_mla_decode_kernel<N, D>;
-    constexpr int kSmem = Layout<N, D>::kAlloc;
-    cudaError_t e = configure<N, D>();
+    auto kernel = sparse_mla_decode_kernel<N, D, C>;
+    constexpr int kSmem = Layout<N, D, C>::kAlloc;
+    cudaError_t e = configure<N, D, C>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -1161,7 +1194,15 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         num_sms = device_sms();
         if (num_sms <= 0) return SMLA_ECUDA;
     }
-    const int chunks = (shape->width + kChunk - 1) / kChunk;
+    // Keys per chunk: tiles and splits are chosen for chunks of 128 keys in
+    // two stages; SMLA_CHUNK=96 or 128 forces the chunk (96 keys in three
+    // stages needs a 32- or 64-head tile).
+    const int forced_chunk = [] {
+        const char* env = std::getenv("SMLA_CHUNK");
+        const int v = env != nullptr ? std::atoi(env) : 0;
+        return v == 96 || v == 128 ? v : 0;
+    }();
+    auto chunk_for = [&](int tile) { return forced_chunk == 96 && tile >= 32 ? 96 : 128; };
     const int max_tile = head_tile_for(shape->heads);
     int forced_tile = 0, forced_splits = 0;
     if (const char* env = std::getenv("SMLA_HEAD_TILE")) {
@@ -1192,7 +1233,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         return pair_mode != 0 && shape->num_pools == 1 && (shape->heads / tile) % 2 == 0;
     };
     auto resident = [&](int tile, int s) {
-        const int r = query_device ? resident_ctas_on_device(tile, shape->head_dim, s) : 0;
+        const int r = query_device ? resident_ctas_on_device(tile, shape->head_dim, chunk_for(tile), s) : 0;
         return r > 0 ? r : (num_sms / s) * s;
     };
 
@@ -1210,16 +1251,18 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     int n = forced_tile > 0 ? forced_tile : max_tile;
     int best = 1;
     double best_cost = 1e300;
-    const int max_splits = chunks < 8 ? (chunks < 1 ? 1 : chunks) : 8;
+    auto chunks_for = [&](int tile) { return (shape->width + chunk_for(tile) - 1) / chunk_for(tile); };
     if (forced_splits == 0) {
         for (int tile = 64; tile >= 16; tile /= 2) {
             if (shape->heads % tile != 0 || (forced_tile > 0 && tile != forced_tile)) continue;
+            const int chunks = chunks_for(tile);
+            const int max_splits = chunks < 8 ? (chunks < 1 ? 1 : chunks) : 8;
             const long units = static_cast<long>(shape->tokens) * (shape->heads / tile);
             const int pair = 1;  // pairing is decided for the chosen tile and splits
             const double a = tile == 64 ? 8.05 : tile == 32 ? 6.34 : 5.13;
             const double b = tile == 64 ? 2.82 : tile == 32 ? 2.28 : 2.24;
             for (int s = 1; s <= max_splits; ++s) {
-                if (s > 1 && !merge_fits(tile, shape->head_dim, s)) continue;
+                if (s > 1 && !merge_fits(tile, shape->head_dim, chunk_for(tile), s)) continue;
                 const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
                 if (per > 0 && (chunks + per - 1) / per != s) continue;  // same chunks per CTA as fewer splits
                 if (pair * s > kMaxSplits) continue;
@@ -1236,9 +1279,10 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         }
     } else {
         int s = forced_splits;
+        const int chunks = chunks_for(n);
         const int cap = chunks < kMaxSplits ? (chunks < 1 ? 1 : chunks) : kMaxSplits;
         if (s > cap) s = cap;
-        while (s > 1 && !merge_fits(n, shape->head_dim, s)) --s;
+        while (s > 1 && !merge_fits(n, shape->head_dim, chunk_for(n), s)) --s;
         if (can_pair(n) && pair_mode == 1 && 2 * s > kMaxSplits) s = kMaxSplits / 2;
         const int per = chunks > 0 ? (chunks + s - 1) / s : 0;
         best = per > 0 ? (chunks + per - 1) / per : 1;
@@ -1263,21 +1307,35 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     }
     const int groups = shape->heads / n;
     const long units = static_cast<long>(shape->tokens) * groups;
+    int chunk = chunk_for(n);
+    int chunks = chunks_for(n);
     const int per_cta = chunks > 0 ? (chunks + best - 1) / best : 0;
     int pair = 1;
     if (can_pair(n) && (pair_mode == 1 || per_cta >= 4) && 2 * best <= kMaxSplits &&
         (units * best <= resident(n, best) ? units * best <= resident(n, 2 * best) : true))
         pair = 2;
-    const int best_resident = resident(n, pair * best);
+    // An unpaired CTA of a 32- or 64-head tile that streams eight or more
+    // chunks of 128 keys (its cp.async gathers bound the two-stage pipeline)
+    // takes chunks of 96 keys in three stages instead: 4-7% faster at 128 x
+    // 64 x 2048 and 256 x 64 x 1024 on GB300; paired CTAs and short streams
+    // measured within 4% either way, slower more often than not.
+    if (forced_chunk == 0 && pair == 1 && n >= 32 && per_cta >= 8 && (best == 1 || merge_fits(n, shape->head_dim, 96, best))) {
+        chunk = 96;
+        chunks = (shape->width + chunk - 1) / chunk;
+    }
+    const int best_resident = [&] {
+        const int r = query_device ? resident_ctas_on_device(n, shape->head_dim, chunk, pair * best) : 0;
+        return r > 0 ? r : (num_sms / (pair * best)) * (pair * best);
+    }();
     plan->head_tile = n;
     plan->head_groups = groups;
-    plan->chunk = kChunk;
+    plan->chunk = chunk;
     plan->chunks = chunks;
     plan->splits = best;
     plan->chunks_per_split = chunks > 0 ? (chunks + best - 1) / best : 0;
     plan->ctas = static_cast<int32_t>(units * best);
     plan->threads = kThreads;
-    plan->smem_bytes = smem_for(n, shape->head_dim);
+    plan->smem_bytes = smem_for(n, shape->head_dim, chunk);
     plan->tmem_columns = tmem_for(n);
     plan->num_sms = num_sms;
     plan->resident_ctas = best_resident;
@@ -1403,16 +1461,7 @@ extern "C" int smla_decode(const smla_shape* shape, const void* q, const smla_po
 
     const dim3 grid(static_cast<unsigned>(plan.head_groups * plan.splits), static_cast<unsigned>(shape->tokens), 1);
     const int cluster = plan.splits * p.pair;
-    const int n = plan.head_tile;
-    if (shape->head_dim == 576) {
-        e = n == 64 ? launch<64, 576>(p, grid, cluster, st)
-          : n == 32 ? launch<32, 576>(p, grid, cluster, st)
-                    : launch<16, 576>(p, grid, cluster, st);
-    } else {
-        e = n == 64 ? launch<64, 512>(p, grid, cluster, st)
-          : n == 32 ? launch<32, 512>(p, grid, cluster, st)
-                    : launch<16, 512>(p, grid, cluster, st);
-    }
+    e = variant_for(plan.head_tile, shape->head_dim, plan.chunk).launch(p, grid, cluster, st);
     if (e != cudaSuccess) {
         t_last_cuda_error = static_cast<int>(e);
         return SMLA_ECUDA;

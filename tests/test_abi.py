@@ -47,6 +47,32 @@ def test_plan_bandwidth_batch(lib):
     assert p["smem_bytes"] <= 232448 and p["tmem_columns"] == 512
 
 
+@pytest.mark.parametrize("tokens,heads,width,chunk,chunks,pair", [
+    (128, 64, 2048, 96, 22, 1),   # unpaired, 16 chunks of 128 per CTA: three stages of 96
+    (256, 64, 1024, 96, 11, 1),   # unpaired, 8 chunks of 128 per CTA
+    (64, 128, 2048, 128, 16, 2),  # paired head groups keep chunks of 128
+    (32, 64, 2048, 128, 16, 1),   # split four ways: 4 chunks per CTA
+    (12, 16, 2048, 128, 16, 1),   # 16-head tiles have no room for a third stage
+])
+def test_plan_chunk_keys(lib, tokens, heads, width, chunk, chunks, pair):
+    p = smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width), num_sms=152)
+    assert (p["chunk"], p["chunks"], p["pair"]) == (chunk, chunks, pair), p
+    if chunk == 96:
+        assert p["smem_bytes"] > smla.smla_plan_for(shape(tokens=tokens, heads=heads, width=width, head_dim=512),
+                                                    num_sms=152)["smem_bytes"]
+
+
+def test_forced_chunk_keys(lib, monkeypatch):
+    monkeypatch.setenv("SMLA_CHUNK", "128")
+    assert smla.smla_plan_for(shape(tokens=128, heads=64), num_sms=152)["chunk"] == 128
+    monkeypatch.setenv("SMLA_CHUNK", "96")
+    p = smla.smla_plan_for(shape(tokens=32, heads=64), num_sms=152)
+    assert p["chunk"] == 96 and p["chunks"] == 22 and p["smem_bytes"] <= 232448
+    assert smla.smla_plan_for(shape(tokens=64, heads=128), num_sms=152)["chunk"] == 96  # paired, forced
+    monkeypatch.setenv("SMLA_HEAD_TILE", "16")
+    assert smla.smla_plan_for(shape(tokens=4, heads=64), num_sms=152)["chunk"] == 128
+
+
 @pytest.mark.parametrize("tokens,heads,width,dim,groups,chunks", [(64, 128, 2048, 576, 1, 8), (5, 256, 256, 576, 2, 1),
                                                                    (12, 128, 640, 512, 1, 3), (256, 128, 2048, 576, 1, 8)])
 def test_plan_pair_kernel(lib, monkeypatch, tokens, heads, width, dim, groups, chunks):

@@ -75,8 +75,9 @@ def test_forced_split_counts(forced_splits, splits):
     w = workloads.small("splits", seed=77, tokens=2, heads=64, width=2048, head_dim=576,
                         pool_rows=8192, holes=0.05, sinks=True, lens=[2048, 1000])
     plan = plan_of(w)
-    per = -(-16 // splits)
-    assert plan["splits"] == -(-16 // per)  # no split without chunks at full width
+    chunks = plan["chunks"]
+    per = -(-chunks // splits)
+    assert plan["splits"] == -(-chunks // per)  # no split without chunks at full width
     got, bits, lse = run_gpu(w)
     print(splits, plan, compare(w, got, bits, lse))
 
@@ -123,6 +124,33 @@ def test_paired_head_groups(env, case):
                         pool_rows=6000, holes=0.07, sinks=True, lens=lens)
     plan = plan_of(w)
     assert plan["pair"] == 2
+    got, bits, lse = run_gpu(w)
+    print(case, plan, compare(w, got, bits, lse))
+
+
+CHUNK96 = [
+    # tokens, heads, head_dim, width, forced head tile, forced splits, pair, lens
+    (3, 64, 576, 300, 64, None, 0, [300, 97, 0]),      # ragged tail: 96 + 96 + 96 + 12
+    (2, 64, 512, 2048, 32, None, 0, [2048, 1111]),
+    (3, 128, 576, 1000, 64, None, 1, [1000, 96, 950]),  # paired, gather4 multicast
+    (4, 64, 576, 2048, 64, 3, 0, [2048, 2000, 1500, 193]),  # split merge over three CTAs
+    (2, 128, 576, 777, 64, 2, 1, [777, 500]),          # paired and split
+]
+
+
+@pytest.mark.parametrize("case", CHUNK96, ids=[f"t{c[0]}_h{c[1]}_d{c[2]}_w{c[3]}_s{c[5]}_p{c[6]}" for c in CHUNK96])
+def test_chunks_of_96_keys_in_three_stages(env, case):
+    """The three-stage pipeline of 96-key chunks (the MMAs read 128 rows; the
+    32 past each chunk are masked in S^T and never read by PV)."""
+    tokens, heads, dim, width, tile, splits, pair, lens = case
+    env("SMLA_CHUNK", 96)
+    env("SMLA_HEAD_TILE", tile)
+    env("SMLA_SPLITS", splits)
+    env("SMLA_PAIR", pair)
+    w = workloads.small("chunk96", seed=tokens * 1000 + width, tokens=tokens, heads=heads, width=width,
+                        head_dim=dim, pool_rows=5000, holes=0.08, sinks=True, lens=lens)
+    plan = plan_of(w)
+    assert plan["chunk"] == 96 and plan["pair"] == (2 if pair else 1), plan
     got, bits, lse = run_gpu(w)
     print(case, plan, compare(w, got, bits, lse))
 
