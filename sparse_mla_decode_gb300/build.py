@@ -26,8 +26,8 @@ SOURCES = [os.path.join(CSRC, n) for n in ("smla_decode.cu", "smla_pair.cu", "sm
                                           "smla_value.cu")]
 HEADERS = [os.path.join(CSRC, n) for n in ("smla_ptx.cuh", "smla_merge_row.cuh", "smla_pair.cuh")] + [os.path.join(INCLUDE, "smla.h")]
 # the FP8 tensor-core microbenchmark, a library of its own
-PEAK_SOURCES = [os.path.join(CSRC, "smla_peak.cu")]
-TARGETS = {LIBRARY: (SOURCES, HEADERS), PEAK_LIBRARY: (PEAK_SOURCES, [])}
+PEAK_SOURCES = [os.path.join(CSRC, "smla_peak.cu"), os.path.join(CSRC, "smla_peak_gather.cu")]
+TARGETS = {LIBRARY: (SOURCES, HEADERS), PEAK_LIBRARY: (PEAK_SOURCES, [os.path.join(CSRC, "smla_ptx.cuh")])}
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -296,3 +296,19 @@ def test_read_device_error_needs_somewhere_to_put_the_bits(lib):
 @pytest.mark.parametrize("limit", [0, 999, 1000000001, -5])
 def test_bounded_wait_selftest_rejects_limits_outside_a_microsecond_to_a_second(lib, limit):
     assert lib.smla_selftest_bounded_wait(0, limit, None) == smla.EINVAL
+
+
+def test_peak_library_exports_its_benchmarks_and_rejects_bad_arguments_without_a_device():
+    path = build.build() and build.PEAK_LIBRARY
+    peak = ctypes.CDLL(path)
+    peak.smla_peak_mma.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_void_p]
+    peak.smla_peak_gather.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_longlong,
+                                      ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    out = ctypes.c_float(0.0)
+    cycles = ctypes.c_longlong(0)
+    assert peak.smla_peak_mma(1, 64, 0, 0, 0, 1, ctypes.byref(cycles), ctypes.byref(out)) == -1  # no iterations
+    assert peak.smla_peak_mma(2, 128, 0, 0, 10, 3, ctypes.byref(cycles), ctypes.byref(out)) == -1  # odd pair count
+    p16 = ctypes.c_void_p(16)
+    assert peak.smla_peak_gather(0, 7, None, 100, p16, 2, 1, p16, ctypes.byref(out)) == -2  # no pool
+    assert peak.smla_peak_gather(2, 7, p16, 100, p16, 3, 1, p16, ctypes.byref(out)) == -2  # pairs need even CTAs
+    assert peak.smla_peak_gather(0, 7, ctypes.c_void_p(24), 100, p16, 2, 1, p16, ctypes.byref(out)) == -2  # unaligned
