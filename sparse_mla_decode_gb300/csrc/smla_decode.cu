@@ -66,6 +66,9 @@ constexpr int kSoftmaxRange = 256;  // warps 0-7: one or two softmax warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp = 9;  // first of seven
 constexpr int kProducerThreads = 224;
+// Unpaired chunk 0 is gathered by every warp but the MMA warp: the softmax
+// range and the producers.
+constexpr int kFirstGatherThreads = kSoftmaxRange + kProducerThreads;
 constexpr int kMaxSplits = 16;
 constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     uint64_t* p_full = bars + 8;    // P^T written, O^T rescaled (softmax arrivals)
     uint64_t* drain = bars + 9;     // every MMA done (commit)
     uint64_t* q_full = bars + 10;   // the Q tile landed (TMA transaction bytes)
-    uint64_t* kv_first = bars + 11; // chunk 0 landed (256 cp.async arrivals + 1); later chunks use kv_full
+    uint64_t* kv_first = bars + 11; // chunk 0 landed (480 cp.async arrivals + 1); later chunks use kv_full
     // stage_free[st] (paired): PV of the chunk in stage st finished in both
     // CTAs of the pair (one multicast commit from each), so either may refill
     // the stage in both.
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         mbar_init(&s_full[1], 1);
         mbar_init(p_full, NG * 128);
         mbar_init(drain, 1);
-        mbar_init(kv_first, kSoftmaxRange + 1);
+        mbar_init(kv_first, kFirstGatherThreads + 1);
         misc[1] = 0;
         mbar_init_fence();
     }
@@ -333,10 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         ok &= mbar_wait_bounded(&pv_done[c % NS], static_cast<uint32_t>((c / NS) & 1), abort_flag, kWaitLimitNs);
     };
 
-    if (warp < kSoftmaxRange / 32 && nch > 0 && !paired) {
-        // ============================= chunk 0 by the softmax-range warps
-        // (idle until the first QK): the first gather is on every CTA's
-        // critical path, and more issuing warps stream it faster.
+    if (warp != kMmaWarp && nch > 0 && !paired) {
+        // ======================= chunk 0 by the softmax-range and producer
+        // warps (the softmax is idle until the first QK, the producers until
+        // chunk 1): the first gather is on every CTA's critical path, and
+        // more issuing warps stream it faster.
+        const int gw = warp < kMmaWarp ? warp : warp - 1;  // 0 .. 14
+        constexpr int kGatherWarps = kFirstGatherThreads / 32;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
         const int col0 = c_first * C;
         if (tid < C) {
@@ -354,11 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             }
             idx_s[tid] = id;
         }
-        named_barrier(5, kSoftmaxRange);
+        named_barrier(5, kFirstGatherThreads);
         if (tid == 0) mbar_arrive(kv_first);  // every idx_s entry (release)
         const uint32_t stage = sbase + L::kKv;
         const uint32_t lane_part = stage + (lane >> 3) * C * 128;
-        for (int k = warp; k < C; k += kSoftmaxRange / 32) {
+        for (int k = gw; k < C; k += kGatherWarps) {
             const int32_t id = idx_s[k];
             const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
             const uint8_t* src = (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + lane * 16;
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             cp_async_16(dst, src, id >= 0 ? 16u : 0u);
         }
         if constexpr (L::kRope) {
-            for (int j = warp; j < C / 8; j += kSoftmaxRange / 32) {
+            for (int j = gw; j < C / 8; j += kGatherWarps) {
                 const int k = j * 8 + (lane >> 2), u = lane & 3;
                 const int32_t id = idx_s[k];
                 const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
