@@ -314,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     if (resolver >= 0 && resolver < C && col_guess + resolver < p.width)
         raw_guess = p.indices[static_cast<int64_t>(token) * p.idx_stride + col_guess + resolver];
     const int count = min(max(p.lens[token], 0), p.width);
+    // this thread's head's sink (threads < N), read now so that the epilogue
+    // does not wait for it
+    const float sink_of_head = (tid < N && p.sinks != nullptr) ? p.sinks[head0 + tid] * kLog2e : -INFINITY;
     // This split's chunks of the token: ceil(chunks / splits) consecutive
     // chunks each, dealt over the token's own count (later splits may be empty).
     const int chunks_total = (count + C - 1) / C;
@@ -750,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             if (m != -INFINITY) {
                 float top = m, extra = 0.0f;
                 if (p.sinks != nullptr) {
-                    const float s2 = p.sinks[h] * kLog2e;
+                    const float s2 = sink_of_head;
                     top = fmaxf(m, s2);
                     extra = 448.0f * fast_exp2(s2 - top);
                 }
@@ -834,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             // the splits' loops unrolled to the maximum split count, so that
             // their loads and exponentials issue together
             const int h = head0 + tid;
-            const float sink2 = p.sinks != nullptr ? p.sinks[h] * kLog2e : -INFINITY;
+            const float sink2 = sink_of_head;
             float m[kMaxSplits], l[kMaxSplits];
 #pragma unroll
             for (int s = 0; s < kMaxSplits; ++s) {
