@@ -1035,11 +1035,11 @@ const Variant& variant_for(int n, int d, int c) {
 
 int smem_for(int n, int d, int c) { return variant_for(n, d, c).smem(); }
 
-int resident_ctas_on_device(int n, int d, int c, int splits) {
+// `dev` is the current device (the query runs on it).
+int resident_ctas_on_device(int dev, int n, int d, int c, int splits) {
     static std::mutex mu;
     static int cache[64][3][2][2][kMaxSplits + 1] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || splits < 1 || splits > kMaxSplits) return 0;
+    if (dev < 0 || dev >= 64 || splits < 1 || splits > kMaxSplits) return 0;
     const int ni = n == 64 ? 0 : n == 32 ? 1 : 2;
     const int di = d == 576 ? 0 : 1;
     const int ci = c == 128 ? 0 : 1;
@@ -1094,35 +1094,89 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// Every argument of one tiled tensor-map encode of bytes; the cache below
+// compares them whole (the struct is zeroed before it is filled).
+struct MapKey {
+    const void* base;
+    uint32_t rank;
+    int32_t swizzle, promotion;
+    cuuint64_t dims[3];
+    cuuint64_t strides[2];
+    cuuint32_t box[3];
+};
+
+// cuTensorMapEncodeTiled through a small cache of recent encodes: a decode's
+// Q and pool maps repeat from call to call (fixed buffers, or a few rotating
+// ones), and an encode costs microseconds of host time. Sixteen entries,
+// replaced round robin; a map is a plain 128-byte value, so a hit copies it.
+bool encode_cached(CUtensorMap* map, const MapKey& k) {
+    constexpr int kEntries = 16;
+    static std::mutex mu;
+    static MapKey keys[kEntries];
+    static CUtensorMap maps[kEntries];
+    static bool used[kEntries] = {};
+    static int next = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < kEntries; ++i)
+            if (used[i] && std::memcmp(&keys[i], &k, sizeof(MapKey)) == 0) {
+                *map = maps[i];
+                return true;
+            }
+    }
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint32_t steps[3] = {1, 1, 1};
+    if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, k.rank, const_cast<void*>(k.base), k.dims, k.strides, k.box, steps,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(k.swizzle),
+            static_cast<CUtensorMapL2promotion>(k.promotion), CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    keys[next] = k;
+    maps[next] = *map;
+    used[next] = true;
+    next = (next + 1) % kEntries;
+    return true;
+}
+
 // Q as [T][H][D] bytes with the caller's strides, read in boxes of `box`
 // bytes x n heads of one token.
 bool encode_q_map(CUtensorMap* map, const void* q, const smla_shape* s, int n, int box, CUtensorMapSwizzle swizzle) {
-    auto enc = tensor_map_encoder();
-    if (enc == nullptr) return false;
     const int64_t head_stride = s->q_stride_head;
     int64_t token_stride = s->q_stride_token;
     if (s->tokens == 1 && token_stride < head_stride * s->heads) token_stride = head_stride * s->heads;  // unused
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(s->head_dim), static_cast<cuuint64_t>(s->heads),
-                                static_cast<cuuint64_t>(s->tokens)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_stride), static_cast<cuuint64_t>(token_stride)};
-    const cuuint32_t boxes[3] = {static_cast<cuuint32_t>(box), static_cast<cuuint32_t>(n), 1};
-    const cuuint32_t steps[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q), dims, strides, boxes, steps,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = q;
+    k.rank = 3;
+    k.swizzle = swizzle;
+    k.promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+    k.dims[0] = static_cast<cuuint64_t>(s->head_dim);
+    k.dims[1] = static_cast<cuuint64_t>(s->heads);
+    k.dims[2] = static_cast<cuuint64_t>(s->tokens);
+    k.strides[0] = static_cast<cuuint64_t>(head_stride);
+    k.strides[1] = static_cast<cuuint64_t>(token_stride);
+    k.box[0] = static_cast<cuuint32_t>(box);
+    k.box[1] = static_cast<cuuint32_t>(n);
+    k.box[2] = 1;
+    return encode_cached(map, k);
 }
 
 // Pool rows of `d` bytes, read by tile::gather4 in boxes of `box` bytes x 1 row.
 bool encode_kv_map(CUtensorMap* map, const void* pool, int64_t rows, int d, int box, CUtensorMapSwizzle swizzle) {
-    auto enc = tensor_map_encoder();
-    if (enc == nullptr || rows <= 0) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d)};
-    const cuuint32_t boxes[2] = {static_cast<cuuint32_t>(box), 1};
-    const cuuint32_t steps[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, boxes, steps,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (rows <= 0) return false;
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = pool;
+    k.rank = 2;
+    k.swizzle = swizzle;
+    k.promotion = CU_TENSOR_MAP_L2_PROMOTION_NONE;
+    k.dims[0] = static_cast<cuuint64_t>(d);
+    k.dims[1] = static_cast<cuuint64_t>(rows);
+    k.strides[0] = static_cast<cuuint64_t>(d);
+    k.box[0] = static_cast<cuuint32_t>(box);
+    k.box[1] = 1;
+    return encode_cached(map, k);
 }
 
 int device_sms() {
@@ -1199,9 +1253,10 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     const int rc = validate(shape);
     if (rc != SMLA_OK) return rc;
     const bool query_device = num_sms <= 0;
+    int dev = -1;
     if (query_device) {
         num_sms = device_sms();
-        if (num_sms <= 0) return SMLA_ECUDA;
+        if (num_sms <= 0 || cudaGetDevice(&dev) != cudaSuccess) return SMLA_ECUDA;
     }
     // Keys per chunk: tiles and splits are chosen for chunks of 128 keys in
     // two stages; SMLA_CHUNK=96 or 128 forces the chunk (96 keys in three
@@ -1242,7 +1297,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         return pair_mode != 0 && shape->num_pools == 1 && (shape->heads / tile) % 2 == 0;
     };
     auto resident = [&](int tile, int s) {
-        const int r = query_device ? resident_ctas_on_device(tile, shape->head_dim, chunk_for(tile), s) : 0;
+        const int r = query_device ? resident_ctas_on_device(dev, tile, shape->head_dim, chunk_for(tile), s) : 0;
         return r > 0 ? r : (num_sms / s) * s;
     };
 
@@ -1333,7 +1388,7 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
         chunks = (shape->width + chunk - 1) / chunk;
     }
     const int best_resident = [&] {
-        const int r = query_device ? resident_ctas_on_device(n, shape->head_dim, chunk, pair * best) : 0;
+        const int r = query_device ? resident_ctas_on_device(dev, n, shape->head_dim, chunk, pair * best) : 0;
         return r > 0 ? r : (num_sms / (pair * best)) * (pair * best);
     }();
     plan->head_tile = n;

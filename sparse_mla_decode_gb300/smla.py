@@ -169,6 +169,38 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# Shape structs and pool descriptor arrays of recent calls, by the tuples
+# that define them: a decode step repeats the same few, and building them
+# anew costs more host time than the C call.
+_shapes: dict = {}
+_pool_arrays: dict = {}
+
+
+def _cached(cache: dict, key, build):
+    v = cache.get(key)
+    if v is None:
+        if len(cache) >= 256:
+            cache.clear()
+        v = cache[key] = build()
+    return v
+
+
+def _pool_array(kv_pools, D):
+    def build():
+        pools = (SmlaPool * len(kv_pools))()
+        for i, pool in enumerate(kv_pools):
+            if pool.shape[0] > 1 and (pool.stride(1) != 1 or pool.stride(0) != D):
+                raise ValueError("pool rows must be contiguous")
+            pools[i].data = pool.data_ptr()
+            pools[i].rows = pool.shape[0]
+            pools[i].row_bytes = pool.shape[1]
+            pools[i].reserved = 0
+        return pools
+
+    key = tuple((p.data_ptr(), p.shape[0], p.shape[1], p.stride(0), p.stride(1)) for p in kv_pools)
+    return _cached(_pool_arrays, (D, key), build)
+
+
 def smla_decode(q: torch.Tensor, kv_pools, indices: torch.Tensor, lens: torch.Tensor,
                 sinks: torch.Tensor | None, bmm1_scale: float, bmm2_scale: float, k_scale: float,
                 out: torch.Tensor, lse: torch.Tensor | None, stream=None, pool_split: int = 0):
@@ -180,30 +212,25 @@ def smla_decode(q: torch.Tensor, kv_pools, indices: torch.Tensor, lens: torch.Te
     sinks float32 [H] or None; out bf16 [T, H, 512]; lse float32 [T, H] or None.
     Runs on ``stream`` (default: torch's current stream) without synchronising.
     """
-    lib = load()
+    lib = _lib if _lib is not None else load()
     T, H, D = q.shape
     W = indices.shape[1]
-    for name, t, dim in (("q", q, 2), ("out", out, 2), ("indices", indices, 1)):
-        if t.shape[dim] > 1 and t.stride(dim) != 1:
-            raise ValueError(f"{name}: innermost dimension must be contiguous")
-    pools = (SmlaPool * len(kv_pools))()
-    for i, pool in enumerate(kv_pools):
-        if pool.shape[0] > 1 and (pool.stride(1) != 1 or pool.stride(0) != D):
-            raise ValueError("pool rows must be contiguous")
-        pools[i].data = pool.data_ptr()
-        pools[i].rows = pool.shape[0]
-        pools[i].row_bytes = pool.shape[1]
-        pools[i].reserved = 0
-    shape = make_shape(T, H, W, D, len(kv_pools), pool_split,
-                       q_strides=(q.stride(0) * q.element_size(), q.stride(1) * q.element_size()),
-                       idx_stride=indices.stride(0), out_strides=(out.stride(0), out.stride(1)),
-                       lse_stride=None if lse is None else lse.stride(0))
+    qst, ost, ist = q.stride(), out.stride(), indices.stride()
+    if (D > 1 and qst[2] != 1) or (out.shape[2] > 1 and ost[2] != 1) or (W > 1 and ist[1] != 1):
+        raise ValueError("q, out and indices: innermost dimension must be contiguous")
+    esz = q.element_size()
+    lse_stride = None if lse is None else lse.stride(0)
+    key = (T, H, W, D, len(kv_pools), pool_split, qst[0] * esz, qst[1] * esz, ist[0], ost[0], ost[1], lse_stride)
+    shape = _cached(_shapes, key, lambda: make_shape(
+        T, H, W, D, len(kv_pools), pool_split, q_strides=(qst[0] * esz, qst[1] * esz), idx_stride=ist[0],
+        out_strides=(ost[0], ost[1]), lse_stride=lse_stride))
+    pools = _pool_array(kv_pools, D)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    rc = lib.smla_decode(ctypes.byref(shape), _ptr(q), pools, _ptr(indices), _ptr(lens), _ptr(sinks),
-                         float(bmm1_scale), float(bmm2_scale), float(k_scale), _ptr(out), _ptr(lse),
-                         ctypes.c_void_p(handle))
+    rc = lib.smla_decode(shape, q.data_ptr(), pools, indices.data_ptr(), lens.data_ptr(),
+                         None if sinks is None else sinks.data_ptr(), bmm1_scale, bmm2_scale, k_scale,
+                         out.data_ptr(), None if lse is None else lse.data_ptr(), handle)
     if rc != OK:
         raise SmlaError(rc, "smla_decode")
     return out, lse
