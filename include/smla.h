@@ -304,6 +304,48 @@ typedef struct smla_merge_value_shape {
 int smla_merge_value(const smla_merge_value_shape* shape, const void* parts, const float* lses,
                      const int32_t* lens, const void* w_uv, const void* gate, void* out, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Decode over fp8_ds_mla cache rows (Kimi K3.1 dsa_indexer_mxfp4 page,
+ * mxfp4_fused_prologue: mla_cache [num_blocks, block_size, 656] bytes, filled
+ * with [kv_c_normed | k_pe] and viewed as FP8, float32 and BF16). The page
+ * prints no row layout; this library reads a 656-byte row as bytes 0..511 the
+ * E4M3 codes of the 512 latents, bytes 512..527 four little-endian FP32
+ * scales (scale b covers latents 128 b .. 128 b + 127), bytes 528..655 the 64
+ * rope values as little-endian BF16. Latent j is dec(code_j) * s_(j / 128).
+ * The attention is smla_decode's with K the 576 values of a row and V its 512
+ * latents; the row scales take the place of k_scale. */
+typedef struct smla_ds_mla_shape {
+    int32_t tokens;     /* T >= 0 */
+    int32_t heads;      /* H: a positive multiple of 32, <= 1024 */
+    int32_t width;      /* W >= 0 */
+    int32_t num_pools;  /* 1 or 2 */
+    int32_t pool_split; /* columns < pool_split read pool 0 (num_pools == 2) */
+    int32_t reserved;   /* 0 */
+    int64_t q_stride_token, q_stride_head;       /* q_latent: bytes, multiples of 16; head stride >= 512 */
+    int64_t rope_stride_token, rope_stride_head; /* q_rope: BF16 elements, multiples of 8; head stride >= 64 */
+    int64_t idx_stride_token;                    /* int32 elements, >= W */
+    int64_t out_stride_token, out_stride_head;   /* BF16 elements, even; head stride >= 512 */
+    int64_t lse_stride_token;                    /* float elements */
+} smla_ds_mla_shape;
+
+/* Sparse MLA decode over fp8_ds_mla rows.
+ *   q_latent  device, E4M3 [T, H, 512] at the shape's byte strides, 16-byte aligned.
+ *   q_rope    device, BF16 [T, H, 64] at the shape's element strides, 16-byte aligned.
+ *   kv_pools  host array of num_pools descriptors: rows of row_bytes = 656,
+ *             data 16-byte aligned in device memory.
+ *   indices, lens, sinks, lse, stream: as for smla_decode.
+ *   bmm1_scale  multiplies the dot products (> 0); bmm2_scale multiplies the
+ *             output (the row scales replace k_scale).
+ *   out       device, BF16 [T, H, 512].
+ * One CTA per (token, 32 heads), no key split; launched with programmatic
+ * dependent launch; captureable in a CUDA graph (no allocation, no
+ * synchronisation). Errors: SMLA_EINVAL / SMLA_EUNSUPPORTED before anything is
+ * launched, SMLA_ECUDA when the launch fails; an index beyond its pool and a
+ * wait that timed out set bits in the device error word. */
+int smla_decode_ds_mla(const smla_ds_mla_shape* shape, const void* q_latent, const void* q_rope,
+                       const smla_pool* kv_pools, const int32_t* indices, const int32_t* lens, const float* sinks,
+                       float bmm1_scale, float bmm2_scale, void* out, float* lse, void* stream);
+
 /* Reads and clears the current device's error word (SMLA_DEV_* bits) in
  * stream order, without synchronising the device: a one-thread kernel on
  * `stream` (a cudaStream_t, NULL: the legacy default stream) exchanges the

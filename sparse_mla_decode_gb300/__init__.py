@@ -8,12 +8,14 @@ binding and :mod:`sparse_mla_decode_gb300.workloads` draws seeded inputs.
 from .smla import (  # noqa: F401
     SmlaError,
     decode,
+    decode_ds_mla,
     load,
     make_shape,
     merge,
     merge_value,
     mxfp4_q_quant,
     smla_decode,
+    smla_decode_ds_mla,
     smla_device_error,
     smla_read_device_error,
     smla_selftest_bounded_wait,

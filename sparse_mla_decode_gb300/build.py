@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(BUILD_DIR, "libsmla.so")
 PEAK_LIBRARY = os.path.join(BUILD_DIR, "libsmla_peak.so")
-SOURCES = [os.path.join(CSRC, n) for n in ("smla_decode.cu", "smla_pair.cu", "smla_merge.cu", "smla_quant.cu",
+SOURCES = [os.path.join(CSRC, n) for n in ("smla_decode.cu", "smla_pair.cu", "smla_ds_mla.cu", "smla_merge.cu", "smla_quant.cu",
                                           "smla_value.cu")]
 HEADERS = [os.path.join(CSRC, n) for n in ("smla_ptx.cuh", "smla_merge_row.cuh", "smla_pair.cuh")] + [os.path.join(INCLUDE, "smla.h")]
 # the FP8 tensor-core microbenchmark, a library of its own

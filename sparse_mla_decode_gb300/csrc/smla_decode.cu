@@ -1139,6 +1139,26 @@ bool encode_cached(CUtensorMap* map, const MapKey& k) {
     return true;
 }
 
+// A tiled map of bytes of rank 2 or 3 (dims[0] innermost, strides of the
+// outer dimensions in bytes), through the cache; for the library's other
+// translation units.
+bool encode_bytes_map(CUtensorMap* map, const void* base, uint32_t rank, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box, int swizzle, int promotion) {
+    if (rank < 2 || rank > 3) return false;
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = base;
+    k.rank = rank;
+    k.swizzle = swizzle;
+    k.promotion = promotion;
+    for (uint32_t i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank) k.strides[i] = strides[i];
+    }
+    return encode_cached(map, k);
+}
+
 // Q as [T][H][D] bytes with the caller's strides, read in boxes of `box`
 // bytes x n heads of one token.
 bool encode_q_map(CUtensorMap* map, const void* q, const smla_shape* s, int n, int box, CUtensorMapSwizzle swizzle) {

@@ -28,6 +28,18 @@ class SmlaPool(ctypes.Structure):
                 ("row_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class SmlaDsMlaShape(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("width", ctypes.c_int32),
+        ("num_pools", ctypes.c_int32), ("pool_split", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("q_stride_token", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
+        ("rope_stride_token", ctypes.c_int64), ("rope_stride_head", ctypes.c_int64),
+        ("idx_stride_token", ctypes.c_int64),
+        ("out_stride_token", ctypes.c_int64), ("out_stride_head", ctypes.c_int64),
+        ("lse_stride_token", ctypes.c_int64),
+    ]
+
+
 class SmlaShape(ctypes.Structure):
     _fields_ = [
         ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("width", ctypes.c_int32),
@@ -136,6 +148,9 @@ def load(path: str | None = None):
         lib.smla_value_gate.restype = i32
         lib.smla_merge_value.argtypes = [ctypes.POINTER(SmlaMergeValueShape), vp, vp, vp, vp, vp, vp, vp]
         lib.smla_merge_value.restype = i32
+        lib.smla_decode_ds_mla.argtypes = [ctypes.POINTER(SmlaDsMlaShape), vp, vp, ctypes.POINTER(SmlaPool), vp, vp,
+                                           vp, ctypes.c_float, ctypes.c_float, vp, vp, vp]
+        lib.smla_decode_ds_mla.restype = i32
         lib.smla_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.smla_read_device_error.restype = i32
         lib.smla_selftest_bounded_wait.argtypes = [i32, ctypes.c_int64, vp]
@@ -234,6 +249,63 @@ def smla_decode(q: torch.Tensor, kv_pools, indices: torch.Tensor, lens: torch.Te
     if rc != OK:
         raise SmlaError(rc, "smla_decode")
     return out, lse
+
+
+DS_MLA_ROW_BYTES = 656
+
+
+def smla_decode_ds_mla(q_latent: torch.Tensor, q_rope: torch.Tensor, kv_pools, indices: torch.Tensor,
+                       lens: torch.Tensor, sinks: torch.Tensor | None, bmm1_scale: float, bmm2_scale: float,
+                       out: torch.Tensor, lse: torch.Tensor | None, stream=None, pool_split: int = 0):
+    """Sparse MLA decode over fp8_ds_mla rows through the C ABI.
+
+    q_latent: uint8 (E4M3 bytes) or float8_e4m3fn [T, H, 512]; q_rope: bfloat16
+    [T, H, 64]; kv_pools: list of 1 or 2 uint8 [rows, 656] tensors, rows
+    contiguous; indices int32 [T, >= W]; lens int32 [T]; sinks float32 [H] or
+    None; out bf16 [T, H, 512]; lse float32 [T, H] or None. H a multiple of 32.
+    """
+    lib = _lib if _lib is not None else load()
+    T, H, _ = q_latent.shape
+    W = indices.shape[1]
+    qst, rst, ost, ist = q_latent.stride(), q_rope.stride(), out.stride(), indices.stride()
+    if qst[2] != 1 or rst[2] != 1 or ost[2] != 1 or (W > 1 and ist[1] != 1):
+        raise ValueError("q_latent, q_rope, out and indices: innermost dimension must be contiguous")
+    esz = q_latent.element_size()
+    lse_stride = None if lse is None else lse.stride(0)
+    key = ("ds", T, H, W, len(kv_pools), pool_split, qst[0] * esz, qst[1] * esz, rst[0], rst[1], ist[0], ost[0],
+           ost[1], lse_stride)
+
+    def build():
+        sh = SmlaDsMlaShape()
+        sh.tokens, sh.heads, sh.width, sh.num_pools, sh.pool_split = T, H, W, len(kv_pools), pool_split
+        sh.q_stride_token, sh.q_stride_head = qst[0] * esz, qst[1] * esz
+        sh.rope_stride_token, sh.rope_stride_head = rst[0], rst[1]
+        sh.idx_stride_token = ist[0]
+        sh.out_stride_token, sh.out_stride_head = ost[0], ost[1]
+        sh.lse_stride_token = lse_stride if lse_stride is not None else H
+        return sh
+
+    shape = _cached(_shapes, key, build)
+    pools = _pool_array(kv_pools, DS_MLA_ROW_BYTES)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_latent.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib.smla_decode_ds_mla(shape, q_latent.data_ptr(), q_rope.data_ptr(), pools, indices.data_ptr(),
+                                lens.data_ptr(), None if sinks is None else sinks.data_ptr(), bmm1_scale,
+                                bmm2_scale, out.data_ptr(), None if lse is None else lse.data_ptr(), handle)
+    if rc != OK:
+        raise SmlaError(rc, "smla_decode_ds_mla")
+    return out, lse
+
+
+def decode_ds_mla(q_latent, q_rope, kv_pools, indices, lens, sinks=None, bmm1_scale=1.0, bmm2_scale=1.0,
+                  pool_split=0, stream=None, with_lse=True):
+    """Allocates out (and lse) on q_latent's device and calls :func:`smla_decode_ds_mla`."""
+    T, H, _ = q_latent.shape
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q_latent.device)
+    lse = torch.empty((T, H), dtype=torch.float32, device=q_latent.device) if with_lse else None
+    return smla_decode_ds_mla(q_latent, q_rope, kv_pools, indices, lens, sinks, bmm1_scale, bmm2_scale, out, lse,
+                              stream=stream, pool_split=pool_split)
 
 
 def smla_device_error() -> int:

@@ -273,3 +273,66 @@ def merge_sets(seed: int = 1005, sources: int = 8, tokens: int = 64, heads: int 
     if tokens > 5:
         lens[5] = 0
     return parts, lses, lens
+
+
+# ------------------------------------------------------------ fp8_ds_mla rows
+# A 656-byte cache row (Kimi K3.1 dsa_indexer_mxfp4 page: mla_cache of
+# [num_blocks, block_size, 656] bytes, viewed as FP8, float32 and BF16), laid
+# out as this library reads it: 512 E4M3 latent codes, four little-endian FP32
+# scales, 64 little-endian BF16 rope values.
+DS_MLA_ROW = 656
+
+
+def bf16_normal(rng: np.random.Generator, shape) -> np.ndarray:
+    """uint16 BF16 bits of N(0, 1) draws (torch's round-to-nearest cast)."""
+    x = rng.standard_normal(int(np.prod(shape)), dtype=np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(shape)
+
+
+def ds_mla_rows(rng: np.random.Generator, rows: int, block: int = 1 << 16) -> np.ndarray:
+    """uint8 [rows, 656]: N(0, 1) E4M3 codes, four scales 2^u * v (u uniform in
+    [-6, 2], v uniform in [0.5, 1)), N(0, 1) BF16 rope values."""
+    out = np.empty((rows, DS_MLA_ROW), np.uint8)
+    for start in range(0, rows, block):
+        n = min(block, rows - start)
+        out[start:start + n, :512] = e4m3_normal(rng, (n, 512))
+        scales = (2.0 ** rng.integers(-6, 3, (n, 4)) * rng.uniform(0.5, 1.0, (n, 4))).astype("<f4")
+        out[start:start + n, 512:528] = scales.view(np.uint8).reshape(n, 16)
+        out[start:start + n, 528:] = bf16_normal(rng, (n, 64)).astype("<u2").view(np.uint8).reshape(n, 128)
+    return out
+
+
+def ds_mla_small(name: str, seed: int, tokens: int, heads: int, width: int, pool_rows: int = 512,
+                 holes: float = 0.0, lens=None, sinks: bool = False, two_pools: bool = False,
+                 pool_split: int = 0, bmm2_scale: float = 1.0) -> dict:
+    """A small random problem over fp8_ds_mla rows. Keys of the dict as for the
+    576-byte workloads, except: q_latent uint8 [T, H, 512] E4M3 bytes and
+    q_rope uint16 [T, H, 64] BF16 bits instead of q; pools of [R, 656] rows; no
+    k_scale."""
+    rng = np.random.default_rng(seed)
+    w = {
+        "name": name,
+        "q_latent": e4m3_normal(rng, (tokens, heads, 512)),
+        "q_rope": bf16_normal(rng, (tokens, heads, 64)),
+        "pools": [ds_mla_rows(rng, pool_rows)],
+        "pool_split": 0,
+        "sinks": rng.standard_normal(heads, dtype=np.float32) if sinks else None,
+        "bmm1_scale": 1.0 / math.sqrt(192.0),
+        "bmm2_scale": bmm2_scale,
+    }
+    if two_pools:
+        w["pools"].append(ds_mla_rows(rng, pool_rows * 2))
+        w["pool_split"] = pool_split
+    idx = np.empty((tokens, width), np.int32)
+    for t in range(tokens):
+        if two_pools:
+            idx[t, :pool_split] = rng.integers(0, pool_rows, size=min(pool_split, width))
+            idx[t, pool_split:] = rng.integers(0, 2 * pool_rows, size=max(0, width - pool_split))
+        else:
+            idx[t] = unique_rows(rng, pool_rows, width) if width <= pool_rows else \
+                rng.integers(0, pool_rows, size=width)
+    if holes > 0:
+        idx[rng.random((tokens, width)) < holes] = -1
+    w["indices"] = idx
+    w["lens"] = np.full(tokens, width, np.int32) if lens is None else np.asarray(lens, np.int32).reshape(tokens)
+    return w

@@ -312,3 +312,46 @@ def test_peak_library_exports_its_benchmarks_and_rejects_bad_arguments_without_a
     assert peak.smla_peak_gather(0, 7, None, 100, p16, 2, 1, p16, ctypes.byref(out)) == -2  # no pool
     assert peak.smla_peak_gather(2, 7, p16, 100, p16, 3, 1, p16, ctypes.byref(out)) == -2  # pairs need even CTAs
     assert peak.smla_peak_gather(0, 7, ctypes.c_void_p(24), 100, p16, 2, 1, p16, ctypes.byref(out)) == -2  # unaligned
+
+
+def _ds_shape(**kw):
+    s = smla.SmlaDsMlaShape()
+    base = dict(tokens=2, heads=64, width=100, num_pools=1, pool_split=0, q_stride_token=64 * 512, q_stride_head=512,
+                rope_stride_token=64 * 64, rope_stride_head=64, idx_stride_token=100, out_stride_token=64 * 512,
+                out_stride_head=512, lse_stride_token=64)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(s, k, v)
+    return s
+
+
+@pytest.mark.parametrize("kw,row_bytes,ptr", [
+    (dict(heads=48), 656, 16),               # heads not a multiple of 32
+    (dict(q_stride_head=520), 656, 16),      # q rows not 16-byte aligned
+    (dict(rope_stride_head=60), 656, 16),    # rope rows below 64 values
+    (dict(idx_stride_token=99), 656, 16),    # index rows shorter than the width
+    (dict(num_pools=2, pool_split=101), 656, 16),
+    (dict(), 576, 16),                       # a 576-byte pool
+    (dict(), 656, 8),                        # misaligned q
+])
+def test_ds_mla_decode_rejects_bad_arguments_before_any_launch(lib, kw, row_bytes, ptr):
+    pools = (smla.SmlaPool * 2)()
+    for i in range(2):
+        pools[i].data, pools[i].rows, pools[i].row_bytes = 16, 10, row_bytes
+    p = ctypes.c_void_p(ptr)
+    p16 = ctypes.c_void_p(16)
+    rc = lib.smla_decode_ds_mla(ctypes.byref(_ds_shape(**kw)), p, p16, pools, p16, p16, None, 0.1, 1.0, p16, None,
+                                None)
+    assert rc == smla.EINVAL
+
+
+def test_ds_mla_decode_limits_and_empty_calls(lib):
+    pools = (smla.SmlaPool * 1)()
+    pools[0].data, pools[0].rows, pools[0].row_bytes = 16, 10, 656
+    p16 = ctypes.c_void_p(16)
+    args = (p16, p16, pools, p16, p16, None, 0.1, 1.0, p16, None, None)
+    assert lib.smla_decode_ds_mla(ctypes.byref(_ds_shape(heads=1056)), *args) == smla.EUNSUPPORTED
+    assert lib.smla_decode_ds_mla(ctypes.byref(_ds_shape(num_pools=3)), *args) == smla.EUNSUPPORTED
+    assert lib.smla_decode_ds_mla(ctypes.byref(_ds_shape(tokens=0)), *args) == smla.OK  # nothing to launch
+    bad_scale = (p16, p16, pools, p16, p16, None, -0.1, 1.0, p16, None, None)
+    assert lib.smla_decode_ds_mla(ctypes.byref(_ds_shape()), *bad_scale) == smla.EINVAL
