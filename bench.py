@@ -59,12 +59,13 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=["batch", "tiny", "verify", "two_pool", "merge", "mxfp4", "value",
-                                         "merge_value"],
+                                         "merge_value", "ds_mla"],
                     default="batch",
                     help="merge: the LSE merge of 8 partial (out, lse) sets of the 64 x 128 batch shape; "
                          "mxfp4: the MXFP4 indexer-query quantisation of 16384 tokens x 32 heads; "
                          "value: the value projection (W_UV) and sigmoid gate of the 64 x 128 batch shape; "
-                         "merge_value: the merge of 8 partial sets fused with that projection")
+                         "merge_value: the merge of 8 partial sets fused with that projection; "
+                         "ds_mla: the 64 x 128 x 2048 batch over 656-byte fp8_ds_mla rows")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
@@ -215,7 +216,8 @@ def measured_hbm_peak():
 KERNEL_SOURCES = {"value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh"),
                   "merge_value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh"),
                   "merge": ("smla_merge.cu", "smla_merge_row.cuh"),
-                  "mxfp4": ("smla_quant.cu",)}
+                  "mxfp4": ("smla_quant.cu",),
+                  "ds_mla": ("smla_ds_mla.cu", "smla_ptx.cuh")}
 
 
 def kernel_sha(config: str = "batch") -> str:
@@ -684,6 +686,188 @@ def run_reference(args, rank, world):
                          "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+DS_MLA_METRIC = "µs/call and achieved HBM GB/s for sparse MLA decode over 656-byte fp8_ds_mla rows"
+
+
+def ds_mla_bytes(w) -> int:
+    """Unique gathered rows x 656 + Q (512 E4M3 + 64 BF16 per head) + BF16 out."""
+    from sparse_mla_decode_gb300 import workloads
+
+    T, H, _ = w["q_latent"].shape
+    return workloads.unique_active_rows(w) * 656 + T * H * (512 + 128) + T * H * 512 * 2
+
+
+def ds_mla_sets(rank: int, sets: int):
+    from sparse_mla_decode_gb300 import workloads
+
+    rng = np.random.default_rng(7000 + rank)
+    pool = workloads.ds_mla_rows(rng, 1 << 20)
+    return [workloads.ds_mla_batch(seed=1007 + r + 100 * rank, pool=pool) for r in range(sets)]
+
+
+def ds_mla_cpu_rate(w, seconds: float, reps: int = 3):
+    """The FP64 definition over fp8_ds_mla rows (numpy) on a bounded sample of
+    tokens (all heads each), median of ``reps`` runs; scaled to a whole call."""
+    from oracle import ds_mla
+
+    T, H, _ = w["q_latent"].shape
+    import torch
+
+    q = torch.cat([torch.from_numpy(w["q_latent"]).view(torch.float8_e4m3fn).to(torch.float64),
+                   torch.from_numpy(w["q_rope"].view(np.int16)).view(torch.bfloat16).to(torch.float64)], -1).numpy()
+    pool = w["pools"][0]
+
+    def run(n):
+        ds_mla.fp64(q[:n], pool, w["indices"][:n], w["lens"][:n], None, w["bmm1_scale"], w["bmm2_scale"])
+
+    t0 = time.perf_counter()
+    run(1)
+    per_token = time.perf_counter() - t0
+    n = int(max(1, min(T, seconds / reps / max(per_token, 1e-9))))
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        run(n)
+        times.append(time.perf_counter() - t0)
+    per_call = float(np.median(times)) / n * T
+    return {"value": round(ds_mla_bytes(w) / per_call / 1e9, 6), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "us_per_call": round(per_call * 1e6, 1), "extrapolated": n < T,
+            "sample": f"{n} of {T} tokens (all {H} heads) per run, median of {reps} runs "
+                      f"({', '.join(f'{t:.2f}' for t in times)} s); numpy's BLAS threads",
+            "statistic": "wall-clock median, scaled from the sampled tokens to the whole call"}
+
+
+def run_ds_mla(args, rank, world, local_rank):
+    """--config ds_mla: smla_decode_ds_mla over the 64 x 128 x 2048 batch of
+    656-byte rows, rotating over 6 input sets (distinct rows > 2x L2)."""
+    import torch
+
+    import __graft_entry__
+    from sparse_mla_decode_gb300 import smla
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    R = 6
+    sets = ds_mla_sets(rank, R)
+    pool = torch.from_numpy(sets[0]["pools"][0]).to(dev)
+    T, H, _ = sets[0]["q_latent"].shape
+    dsets = [{"ql": torch.from_numpy(w["q_latent"]).to(dev),
+              "qr": torch.from_numpy(w["q_rope"].view(np.int16)).view(torch.bfloat16).to(dev),
+              "idx": torch.from_numpy(w["indices"]).to(dev), "lens": torch.from_numpy(w["lens"]).to(dev),
+              "out": torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
+              "lse": torch.empty((T, H), dtype=torch.float32, device=dev)} for w in sets]
+    byts = [ds_mla_bytes(w) for w in sets]
+    w0 = sets[0]
+
+    def call(i):
+        d = dsets[i % R]
+        smla.smla_decode_ds_mla(d["ql"], d["qr"], [pool], d["idx"], d["lens"], None, w0["bmm1_scale"],
+                                w0["bmm2_scale"], d["out"], d["lse"])
+
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(max(3, args.warmup)):
+        call(i)
+    torch.cuda.synchronize()
+    if smla.smla_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    graph = None
+    if args.launch == "graph":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                call(i)
+        graph.replay()
+        torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            call(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    elapsed_ms = start.elapsed_time(end)
+    t_wall1 = time.time()
+    soak_until = t_wall1 + max(0.0, args.soak - (t_wall1 - t_wall0)) if args.soak > 0 else t_wall1
+    while time.time() < soak_until:
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(200):
+                call(i)
+        torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, max(t_wall1, soak_until))
+    if smla.smla_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+    ms = elapsed_ms / args.steps
+    per_call = float(np.mean([byts[i % R] for i in range(args.steps)]))
+    value = per_call / (ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        host = [(d["ql"].cpu().pin_memory(), d["qr"].cpu().pin_memory(), d["idx"].cpu().pin_memory(),
+                 d["lens"].cpu().pin_memory()) for d in dsets]
+        h2d = sum(x.numel() * x.element_size() for x in host[0])
+
+        def e2e_run(inp, outp):
+            smla.smla_decode_ds_mla(inp[0], inp[1], [pool], inp[2], inp[3], None, w0["bmm1_scale"],
+                                    w0["bmm2_scale"], outp[0], outp[1])
+
+        e2e = e2e_entry(torch, per_call, host, (dsets[0]["ql"], dsets[0]["qr"], dsets[0]["idx"], dsets[0]["lens"]),
+                        e2e_run, (dsets[0]["out"], dsets[0]["lse"]), min(args.steps, 500), h2d,
+                        T * H * (512 * 2 + 4))
+    if rank != 0:
+        return
+    cpu = None if args.no_cpu else ds_mla_cpu_rate(w0, args.cpu_seconds)
+    peak, peak_src = measured_hbm_peak()
+    line = {
+        "metric": DS_MLA_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "us_per_call": round(ms * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/bf16", "data": "synthetic",
+        "config": {"workload": f"{w0['name']}: {T} tokens x {H} heads x 2048 top-k keys, 656-byte fp8_ds_mla rows "
+                               "(E4M3 latents, FP32 block scales, BF16 rope), 1,048,576-row pool, ~50% of rows "
+                               "shared via a 20k-row hot set",
+                   "tokens": T, "heads": H, "width": 2048, "row_bytes": 656, "input_sets": R,
+                   "l2": "rotating %d input sets over distinct rows (~%.2f MB per call) between back-to-back calls"
+                         % (R, per_call / 1e6),
+                   "launch": ("one CUDA graph of the %d timed library calls, replayed once" % args.steps)
+                             if graph is not None else "%d library calls from Python" % args.steps,
+                   "kernel": "32-head tiles, one CTA per (token, 32 heads), 128-key chunks in two stages",
+                   "parallelism": "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic("ds_mla"),
+                     "bytes_alg_per_launch": int(per_call)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(args.steps), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ds_mla_reference(args, rank, world):
+    """The FP64 definition over fp8_ds_mla rows as the reference arm (rank 0)."""
+    if rank != 0:
+        return
+    w = ds_mla_sets(0, 1)[0]
+    budget = min(120.0, max(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    cpu = ds_mla_cpu_rate(w, budget)
+    T, H, _ = w["q_latent"].shape
+    line = {
+        "metric": DS_MLA_METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(cpu["us_per_call"] / 1e3, 3), "extrapolated": cpu["extrapolated"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": w["name"], "tokens": T, "heads": H, "width": 2048, "row_bytes": 656},
+        "cpu_baseline": cpu,
+        "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -1224,6 +1408,8 @@ def main():
             run_mxfp4_reference(args, rank, world)
         elif args.config in ("value", "merge_value"):
             run_value_reference(args, rank, world, fused=args.config == "merge_value")
+        elif args.config == "ds_mla":
+            run_ds_mla_reference(args, rank, world)
         else:
             run_reference(args, rank, world)
         return
@@ -1242,6 +1428,8 @@ def main():
         run_mxfp4(args, rank, world, local_rank)
     elif args.config in ("value", "merge_value"):
         run_value(args, rank, world, local_rank, fused=args.config == "merge_value")
+    elif args.config == "ds_mla":
+        run_ds_mla(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
 

@@ -336,3 +336,30 @@ def ds_mla_small(name: str, seed: int, tokens: int, heads: int, width: int, pool
     w["indices"] = idx
     w["lens"] = np.full(tokens, width, np.int32) if lens is None else np.asarray(lens, np.int32).reshape(tokens)
     return w
+
+
+def ds_mla_batch(seed: int = 1007, tokens: int = 64, heads: int = 128, topk: int = 2048, pool_rows: int = 1 << 20,
+                 hot_rows: int = 20000, pool=None) -> dict:
+    """The 64 x 128 x 2048 bandwidth batch over fp8_ds_mla rows: the same
+    index recipe as ``bandwidth_batch`` (half of each token's rows from a
+    common 20k-row hot set), a 1,048,576 x 656-byte pool, no sinks."""
+    rng = np.random.default_rng(seed)
+    W = topk
+    w = {
+        "name": f"ds_mla_batch_t{tokens}_h{heads}_k{topk}_r656",
+        "q_latent": e4m3_normal(rng, (tokens, heads, 512)),
+        "q_rope": bf16_normal(rng, (tokens, heads, 64)),
+        "pools": [ds_mla_rows(rng, pool_rows) if pool is None else pool],
+        "pool_split": 0,
+        "indices": np.full((tokens, W), -1, np.int32),
+        "lens": np.full(tokens, W, np.int32),
+        "sinks": None,
+        "bmm1_scale": 1.0 / math.sqrt(192.0),
+        "bmm2_scale": 1.0,
+    }
+    hot = unique_rows(rng, pool_rows, hot_rows)
+    for t in range(tokens):
+        a = rng.choice(hot, size=W // 2, replace=False)
+        b = unique_rows(rng, pool_rows, W - W // 2, exclude=hot)
+        w["indices"][t] = rng.permutation(np.concatenate([a, b]))
+    return w
