@@ -222,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     uint64_t* p_full = bars + 8;    // P^T written, O^T rescaled (softmax arrivals)
     uint64_t* drain = bars + 9;     // every MMA done (commit)
     uint64_t* q_full = bars + 10;   // the Q tile landed (TMA transaction bytes)
-    uint64_t* kv_first = bars + 11; // chunk 0 landed (480 cp.async arrivals + 1); later chunks use kv_full
+    uint64_t* kv_first = bars + 11; // chunk 0 landed (480 cp.async arrivals + 1, the producers' at once
+                                    // when they do not help); later chunks use kv_full
     // stage_free[st] (paired): PV of the chunk in stage st finished in both
     // CTAs of the pair (one multicast commit from each), so either may refill
     // the stage in both.
@@ -339,13 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         ok &= mbar_wait_bounded(&pv_done[c % NS], static_cast<uint32_t>((c / NS) & 1), abort_flag, kWaitLimitNs);
     };
 
-    if (warp != kMmaWarp && nch > 0 && !paired) {
-        // ======================= chunk 0 by the softmax-range and producer
-        // warps (the softmax is idle until the first QK, the producers until
-        // chunk 1): the first gather is on every CTA's critical path, and
-        // more issuing warps stream it faster.
+    // Unpaired chunk 0 is gathered by the softmax-range warps (idle until the
+    // first QK), and by the producers too when it is the CTA's only chunk (it
+    // is on every CTA's critical path, and more issuing warps stream it
+    // faster); with more chunks the producers start on chunk 1 at once.
+    const bool producers_help = nch == 1;
+    if (warp >= kProducerWarp && nch > 1 && !paired) cp_async_arrive_noinc(kv_first);  // nothing in flight yet
+    if (warp != kMmaWarp && nch > 0 && !paired && (warp < kMmaWarp || producers_help)) {
+        // ============================================= chunk 0
         const int gw = warp < kMmaWarp ? warp : warp - 1;  // 0 .. 14
-        constexpr int kGatherWarps = kFirstGatherThreads / 32;
+        const int gather_warps = producers_help ? kFirstGatherThreads / 32 : kSoftmaxRange / 32;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
         const int col0 = c_first * C;
         if (tid < C) {
@@ -363,11 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             }
             idx_s[tid] = id;
         }
-        named_barrier(5, kFirstGatherThreads);
+        named_barrier(5, producers_help ? kFirstGatherThreads : kSoftmaxRange);
         if (tid == 0) mbar_arrive(kv_first);  // every idx_s entry (release)
         const uint32_t stage = sbase + L::kKv;
         const uint32_t lane_part = stage + (lane >> 3) * C * 128;
-        for (int k = gw; k < C; k += kGatherWarps) {
+        for (int k = gw; k < C; k += gather_warps) {
             const int32_t id = idx_s[k];
             const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
             const uint8_t* src = (second ? p.pool1 : p.pool0) + static_cast<int64_t>(id >= 0 ? id : 0) * D + lane * 16;
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             cp_async_16(dst, src, id >= 0 ? 16u : 0u);
         }
         if constexpr (L::kRope) {
-            for (int j = gw; j < C / 8; j += kGatherWarps) {
+            for (int j = gw; j < C / 8; j += gather_warps) {
                 const int k = j * 8 + (lane >> 2), u = lane & 3;
                 const int32_t id = idx_s[k];
                 const bool second = p.num_pools == 2 && col0 + k >= p.pool_split;
