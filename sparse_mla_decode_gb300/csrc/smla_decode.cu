@@ -12,21 +12,24 @@
 //
 // GB300 design (one CTA per SM, 512 threads, 16 warps = 4 per SM sub-partition):
 //   warps 0-7  softmax: for a 64-head tile two warpgroups of 32 heads each, for
-//              16 or 32 heads one warpgroup; one thread per key of a 128-key
-//              chunk (the TMEM lane of S^T), per-head maxima by warp
-//              reductions + shared memory, P as E4M3 into shared memory,
-//              rescale of O^T in TMEM, epilogue/merge;
+//              16 or 32 heads one warpgroup; one thread per key of a chunk
+//              (the TMEM lane of S^T), per-head maxima by a shuffle butterfly
+//              + shared memory, P as E4M3 into shared memory, rescale of O^T
+//              in TMEM, epilogue/merge; unpaired, they also gather the first
+//              chunk;
 //   warp 8     allocates TMEM and issues the tcgen05 MMAs from one thread,
 //              QK of the next chunk as soon as its rows landed and PV of the
 //              previous one as soon as its P is ready;
-//   warps 9-15 producers: 16-byte cp.async copies of the chunk's KV rows, one
-//              row per warp instruction, straight into the swizzled K-major
-//              tiles the MMAs read (masked columns are zero-filled); each
-//              thread's arrival on the stage barrier fires when its copies
-//              land, so both stages stream while the other is computed. The Q
-//              tile comes by TMA tile loads. (Random 576-byte rows stream
-//              fastest this way: TMA tile::gather4 reaches only about 60% of
-//              the cp.async rate on L2 hits and needs as many issuing warps.)
+//   warps 9-15 producers. Unpaired: 16-byte cp.async copies of the chunk's KV
+//              rows, one row per warp instruction, straight into the swizzled
+//              K-major tiles the MMAs read (masked columns are zero-filled);
+//              each thread's arrival on the stage barrier fires when its
+//              copies land. Paired (two head tiles of a token in one
+//              cluster): tile::gather4 of half of each chunk's rows, one lane
+//              per warp, multicast into the stage of both CTAs. The Q tile
+//              comes by TMA tile loads.
+// Chunks hold 128 keys in two stages, or 96 keys in three where the planner
+// finds the deeper ring pays (unpaired CTAs streaming many chunks).
 // Both products put the long side on the MMA's M = 128 and the heads on N, as
 // the DeepSeek page sketches:
 //   S^T[key, head]   = KV[key, :] . Q[head, :]      (A = KV K-major, B = Q K-major)
