@@ -71,3 +71,39 @@ def test_traffic_is_reported_only_for_the_source_it_was_taken_on(tmp_path, monke
     monkeypatch.setattr(bench, "ROOT", str(fake_root))
     assert bench.ncu_traffic("batch") is None
     assert bench.ncu_traffic("value") is None  # no record at all
+
+
+def test_fp8_peak_is_the_committed_microbenchmark_figure():
+    peak, source = bench.fp8_peak()
+    with open(os.path.join(ROOT, "profiles", "fp8_mma_peak.json")) as f:
+        assert peak == json.load(f)["fp8_dense_peak_tflops"]
+    assert "measured" in source and "tcgen05" in source
+
+
+def test_ds_mla_bytes_counts_656_byte_rows_q_and_out():
+    from sparse_mla_decode_gb300 import workloads
+
+    w = workloads.ds_mla_small("acct", seed=1, tokens=2, heads=32, width=40, pool_rows=100, holes=0.2)
+    rows = workloads.unique_active_rows(w)
+    assert bench.ds_mla_bytes(w) == rows * 656 + 2 * 32 * (512 + 128) + 2 * 32 * 512 * 2
+
+
+def test_cpu_baseline_times_all_cores_and_one_core_as_medians_of_three():
+    from sparse_mla_decode_gb300 import workloads
+
+    cpu = bench.cpu_oracle_rate([workloads.tiny()], 0.3)
+    assert cpu["kind"] == "oracle" and cpu["unit"] == "GB/s" and cpu["value"] > 0
+    assert cpu["one_core"]["cores"] == 1 and cpu["one_core"]["value"] > 0
+    assert "median of 3" in cpu["sample"] and "median of 3" in cpu["one_core"]["sample"]
+
+
+def test_reference_arm_reports_its_measured_step_and_whether_it_extrapolates():
+    import subprocess
+    import sys
+
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--steps", "2", "--warmup", "0"], capture_output=True, text=True, check=True, cwd=ROOT)
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["extrapolated"] is False  # 16 pairs: the whole call per step
+    assert line["ms_per_step"] * 1e3 == pytest.approx(line["us_per_call_extrapolated"], rel=1e-3)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
