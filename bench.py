@@ -301,6 +301,44 @@ def cpu_oracle_rate(sets, seconds: float):
             "one_core": one}
 
 
+def gather_floor(w, plan):
+    """The time the decode's gathers alone need per call, modelled from the
+    measured landing rates of profiles/row_gather_peak.json (per SM, cold and
+    L2-hot rows, for the gather method the plan uses: paired tile::gather4
+    multicast or cp.async, 7 issuing warps): per (token, head tile, split) CTA,
+    its rows that other tokens also read (L2 hits after the first) at the hot
+    rate, the others at the cold rate; the slowest CTA of one wave, times the
+    number of waves. None when the profile is missing."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "row_gather_peak.json")) as f:
+            rows = json.load(f)["rows"]
+    except (OSError, KeyError, ValueError):
+        return None
+    method = 2 if plan["pair"] == 2 else 0
+    rate = {r["pool"]: r["sm_bytes_per_ns"] for r in rows if r["method"] == method and r["issuers"] == 7}
+    T, W = w["indices"].shape
+    D = w["q"].shape[2]
+    seen = {}
+    for t in range(T):
+        n = max(0, min(int(w["lens"][t]), W))
+        for r in set(int(x) for x in w["indices"][t, :n] if x >= 0):
+            seen[r] = seen.get(r, 0) + 1
+    per_split = plan["chunks_per_split"] * plan["chunk"]
+    worst = 0.0
+    for t in range(T):
+        n = max(0, min(int(w["lens"][t]), W))
+        cols = w["indices"][t, :n]
+        for sp in range(plan["splits"]):
+            part = cols[sp * per_split:(sp + 1) * per_split]
+            part = part[part >= 0]
+            hot = sum(1 for r in part if seen.get(int(r), 0) > 1)
+            ns = (hot * D) / rate["hot"] + ((part.size - hot) * D) / rate["cold"]
+            worst = max(worst, ns)
+    waves = math.ceil(plan["ctas"] / max(1, plan["resident_ctas"]))
+    return {"us": round(worst * waves / 1e3, 2), "method": "paired tile::gather4 multicast" if method == 2 else "cp.async",
+            "source": "profiles/row_gather_peak.json"}
+
+
 def fp8_peak():
     """The dense FP8 tensor peak measured by this library's own tcgen05
     microbenchmark (profiles/fp8_mma_peak.json), else twice the measured BF16
@@ -579,6 +617,9 @@ def run_ours(args, rank, world, local_rank):
     traffic = ncu_traffic(args.config)
     cpu = None if args.no_cpu else cpu_oracle_rate(sets, args.cpu_seconds)
     fp8_peak_tflops, fp8_peak_src = fp8_peak()
+    floor = gather_floor(sets[0], plan) if args.config == "batch" else None
+    if floor is not None:
+        floor["frac"] = round(floor["us"] / (ms * 1e3), 4)  # the kernel's time against its gather floor
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -614,6 +655,7 @@ def run_ours(args, rank, world, local_rank):
             "tensor_tflops": round(step_flops / (ms * 1e-3) / 1e12, 2),
             "tensor_frac_of_fp8_peak": round(step_flops / (ms * 1e-3) / 1e12 / fp8_peak_tflops, 4),
             "fp8_peak_tflops": fp8_peak_tflops, "fp8_peak_source": fp8_peak_src,
+            "gather_floor": floor,
         },
         "cpu_baseline": cpu,
         "e2e": e2e,

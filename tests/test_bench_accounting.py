@@ -107,3 +107,19 @@ def test_reference_arm_reports_its_measured_step_and_whether_it_extrapolates():
     assert line["impl"] == "reference" and line["extrapolated"] is False  # 16 pairs: the whole call per step
     assert line["ms_per_step"] * 1e3 == pytest.approx(line["us_per_call_extrapolated"], rel=1e-3)
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_gather_floor_counts_shared_rows_at_the_hot_rate():
+    import numpy as np
+
+    with open(os.path.join(ROOT, "profiles", "row_gather_peak.json")) as f:
+        rates = {(r["method"], r["issuers"], r["pool"]): r["sm_bytes_per_ns"] for r in json.load(f)["rows"]}
+    # two tokens of 8 columns: rows 0-3 shared by both (hot), 4 more each of their own (cold), one hole
+    idx = np.array([[0, 1, 2, 3, 10, 11, 12, 13], [0, 1, 2, 3, 20, 21, 22, -1]], np.int32)
+    w = {"q": np.zeros((2, 16, 576), np.uint8), "indices": idx, "lens": np.array([8, 8], np.int32)}
+    plan = {"pair": 1, "splits": 1, "chunks_per_split": 1, "chunk": 128, "ctas": 2, "resident_ctas": 152}
+    want = (4 * 576 / rates[(0, 7, "hot")] + 4 * 576 / rates[(0, 7, "cold")]) / 1e3  # token 0, the slower
+    got = bench.gather_floor(w, plan)
+    assert got["us"] == pytest.approx(want, abs=0.01) and got["method"] == "cp.async"
+    plan["pair"] = 2
+    assert bench.gather_floor(w, plan)["method"] == "paired tile::gather4 multicast"
