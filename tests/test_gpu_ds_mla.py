@@ -13,7 +13,6 @@ dequantised latents, sigma_b the largest |s_b| of the token's keys). The test
 takes max(0.02 * row max, E_j) plus one BF16 step of the output, and 1e-3 on
 the base-2 LSE."""
 
-import math
 
 import numpy as np
 import pytest
@@ -166,3 +165,12 @@ def test_zero_tokens_and_zero_width():
     smla.decode_ds_mla(ql, qr, [pool], idx, lens)
     torch.cuda.synchronize()
     assert smla.smla_device_error() == 0
+
+
+def test_batch_shape_over_several_waves():
+    """The 64 x 128 x 2048 batch shape (256 CTAs: more than one wave), half
+    of each token's rows from a shared hot set, against the definition."""
+    w = workloads.ds_mla_batch(seed=21, pool_rows=100_000, hot_rows=5000)
+    got, bits, lse, dev_bits = run_gpu(w)
+    assert dev_bits == 0
+    print("worst", compare(w, got, bits, lse))
