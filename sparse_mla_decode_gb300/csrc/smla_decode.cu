@@ -823,20 +823,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             }
         }
         if (has_heads && !split_empty) {
-#pragma unroll 1
-            for (int blk = 0; blk < 4; ++blk) {
+            auto send_block = [&](int blk, const float* v) {
                 const int slice = blk * 4 + (warp & 3);
                 const int owner = slice % splits, slot = slice / splits;
                 const uint32_t dst =
                     map_to_rank(inbox + (((split * slots + slot) * N + hb) * 32 + lane) * 4, half * splits + owner);
-                float v[HW];
-                const uint32_t col = tmem + lane_base + 2 * N + blk * N + hb;
-                if constexpr (HW == 32)
-                    tmem_load32x1(col, v);
-                else
-                    tmem_load16x1(col, v);
 #pragma unroll
                 for (int j = 0; j < HW; ++j) st_cluster_f32(dst + j * 32 * 4, v[j]);
+            };
+            const uint32_t col = tmem + lane_base + 2 * N + hb;
+            if constexpr (HW == 16) {
+                float v[64];  // the four blocks of this warp's 16 heads, one TMEM round trip
+                tmem_load16x4(col, col + N, col + 2 * N, col + 3 * N, v);
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) send_block(blk, v + 16 * blk);
+            } else {
+#pragma unroll 1
+                for (int blk = 0; blk < 4; blk += 2) {  // two blocks of 32 heads a round trip
+                    float v[64];
+                    tmem_load16x4(col + blk * N, col + blk * N + 16, col + (blk + 1) * N, col + (blk + 1) * N + 16, v);
+                    send_block(blk, v);
+                    send_block(blk + 1, v + 32);
+                }
             }
         }
         cluster_sync_all();  // every partial has landed
