@@ -142,6 +142,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 constexpr uint32_t kSwizzle128B = 2;
 constexpr uint32_t kSwizzle64B = 4;
+constexpr uint32_t kSwizzle32B = 6;
 
 __host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n, int a_mn, int b_mn) {
     return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
@@ -204,8 +205,11 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
         uint64_t b_desc;
         uint32_t b_step;
         if constexpr (BMN) {
-            static_assert(NB == 64 || NB == 128, "MN-major B of 64 or 128 bytes per K-row");
-            b_desc = smem_desc(sbase + kB, 8 * NB, 8 * NB, NB == 64 ? kSwizzle64B : kSwizzle128B);
+            // MN-major B of NB bytes per K-row, 8-row atoms of 8 NB bytes, the
+            // swizzle of the row width (none for 16 bytes), as the decode's P^T
+            static_assert(NB == 16 || NB == 32 || NB == 64 || NB == 128, "MN-major B of 16..128 bytes per K-row");
+            constexpr uint32_t kSw = NB == 128 ? kSwizzle128B : NB == 64 ? kSwizzle64B : NB == 32 ? kSwizzle32B : 0u;
+            b_desc = smem_desc(sbase + kB, 8 * NB, 8 * NB, kSw);
             b_step = (32 * NB) >> 4;
         } else {
             b_desc = smem_desc(sbase + kB, 1024, 1024, kSwizzle128B);
@@ -296,6 +300,10 @@ extern "C" int smla_peak_mma(int cta_group, int n, int a_mn, int b_mn, int iters
     if (cycles == nullptr || ms == nullptr || iters <= 0 || ctas <= 0 || ctas % cta_group != 0) return -1;
 #define SMLA_PEAK_CASE(CG, N, AMN, BMN) \
     if (cta_group == CG && n == N && a_mn == AMN && b_mn == BMN) return run<CG, N, AMN, BMN>(iters, ctas, cycles, ms);
+    SMLA_PEAK_CASE(1, 16, 0, 0)
+    SMLA_PEAK_CASE(1, 16, 1, 1)
+    SMLA_PEAK_CASE(1, 32, 0, 0)
+    SMLA_PEAK_CASE(1, 32, 1, 1)
     SMLA_PEAK_CASE(1, 64, 0, 0)
     SMLA_PEAK_CASE(1, 128, 0, 0)
     SMLA_PEAK_CASE(1, 256, 0, 0)

@@ -4,7 +4,7 @@ microbenchmark (``libsmla_peak.so``, built from ``csrc/smla_peak.cu``).
     python -m sparse_mla_decode_gb300.mma_peak [--json PATH]
 
 For each MMA shape the decode uses or could use (cta_group::1 at M = 128 and
-cta_group::2 at M = 256 over a CTA pair; N = 64 / 128 / 256; operands K-major
+cta_group::2 at M = 256 over a CTA pair; N = 16 / 32 / 64 / 128 / 256; operands K-major
 or MN-major as the decode reads them), two numbers:
 
 * ``cycles_per_mma``: one CTA (or pair) issues 4000 K = 32 MMAs into one
@@ -31,6 +31,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 # (cta_group, N, A MN-major, B MN-major, what the decode uses it for)
 SHAPES = [
+    (1, 16, 0, 0, "QK of a 16-head tile"),
+    (1, 16, 1, 1, "PV of a 16-head tile"),
+    (1, 32, 0, 0, "QK of a 32-head tile"),
+    (1, 32, 1, 1, "PV of a 32-head tile"),
     (1, 64, 0, 0, "QK of a 64-head tile (S^T = KV.Q^T)"),
     (1, 64, 1, 1, "PV of a 64-head tile (O^T = V^T.P^T)"),
     (1, 64, 1, 0, "PV with P^T K-major"),
