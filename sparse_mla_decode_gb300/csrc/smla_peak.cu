@@ -160,9 +160,11 @@ constexpr int kBar = 16384 + 32768;
 constexpr int kSmem = 128 * 1024;
 
 // Each CTA of the launch: the elected thread of the issuing CTA runs `iters`
-// groups of four K = 32 MMAs into one TMEM accumulator of N columns and
-// commits; `cycles` (when non-null) gets the clock64 span of CTA 0's run.
-template <int CG, int N, int AMN, int BMN>
+// groups of four K = 32 MMAs into CH TMEM accumulators of N columns (MMA ks
+// of a group into accumulator ks % CH, so that CH independent chains
+// interleave) and commits; `cycles` (when non-null) gets the clock64 span of
+// CTA 0's run.
+template <int CG, int N, int AMN, int BMN, int CH>
 __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* cycles, int* error) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,7 +184,8 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
         mbar_init(done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    constexpr int kCols = N < 32 ? 32 : N;
+    static_assert(CH == 1 || CH == 2 || CH == 4, "one, two or four chains");
+    constexpr int kCols = N * CH < 32 ? 32 : N * CH;
     if (tid < 32) tmem_alloc<CG>(tmem_slot, kCols);
     tc_fence_before_sync();
     if constexpr (CG == 2)
@@ -219,7 +222,8 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
         for (int it = 0; it < iters; ++it) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_f8<CG>(tmem, a_desc + ks * a_step, b_desc + ks * b_step, idesc, (it | ks) != 0 ? 1u : 0u);
+                mma_f8<CG>(tmem + (ks % CH) * N, a_desc + ks * a_step, b_desc + ks * b_step, idesc,
+                           (it != 0 || ks >= CH) ? 1u : 0u);
         }
         mma_commit<CG>(smem_u32(done));
         if constexpr (CG == 2) mma_commit<CG>(map_to_rank(smem_u32(done), 1));
@@ -239,9 +243,9 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
     if (tid < 32) tmem_dealloc<CG>(tmem, kCols);
 }
 
-template <int CG, int N, int AMN, int BMN>
+template <int CG, int N, int AMN, int BMN, int CH>
 int run(int iters, int ctas, long long* cycles_out, float* ms_out) {
-    auto kernel = mma_rate_kernel<CG, N, AMN, BMN>;
+    auto kernel = mma_rate_kernel<CG, N, AMN, BMN, CH>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) return -3;
     long long* d_cycles = nullptr;
     int* d_error = nullptr;
@@ -299,7 +303,7 @@ extern "C" int smla_peak_mma(int cta_group, int n, int a_mn, int b_mn, int iters
     using namespace smla_peak;
     if (cycles == nullptr || ms == nullptr || iters <= 0 || ctas <= 0 || ctas % cta_group != 0) return -1;
 #define SMLA_PEAK_CASE(CG, N, AMN, BMN) \
-    if (cta_group == CG && n == N && a_mn == AMN && b_mn == BMN) return run<CG, N, AMN, BMN>(iters, ctas, cycles, ms);
+    if (cta_group == CG && n == N && a_mn == AMN && b_mn == BMN) return run<CG, N, AMN, BMN, 1>(iters, ctas, cycles, ms);
     SMLA_PEAK_CASE(1, 16, 0, 0)
     SMLA_PEAK_CASE(1, 16, 1, 1)
     SMLA_PEAK_CASE(1, 32, 0, 0)
@@ -316,5 +320,29 @@ extern "C" int smla_peak_mma(int cta_group, int n, int a_mn, int b_mn, int iters
     SMLA_PEAK_CASE(2, 256, 1, 1)
     SMLA_PEAK_CASE(2, 128, 1, 0)
 #undef SMLA_PEAK_CASE
+    return -1;
+}
+
+// The same with `chains` (1, 2 or 4) accumulators of N columns that the
+// MMAs of each group of four take in turn: whether independent accumulators
+// overlap where one chain does not. Returns as smla_peak_mma.
+extern "C" int smla_peak_mma_chains(int cta_group, int n, int a_mn, int b_mn, int chains, int iters, int ctas,
+                                    long long* cycles, float* ms) {
+    using namespace smla_peak;
+    if (cycles == nullptr || ms == nullptr || iters <= 0 || ctas <= 0 || ctas % cta_group != 0) return -1;
+    if (chains == 1) return smla_peak_mma(cta_group, n, a_mn, b_mn, iters, ctas, cycles, ms);
+#define SMLA_PEAK_CHAINS(N, AMN, BMN, CH)                                        \
+    if (cta_group == 1 && n == N && a_mn == AMN && b_mn == BMN && chains == CH) \
+        return run<1, N, AMN, BMN, CH>(iters, ctas, cycles, ms);
+    SMLA_PEAK_CHAINS(16, 0, 0, 2)
+    SMLA_PEAK_CHAINS(16, 0, 0, 4)
+    SMLA_PEAK_CHAINS(32, 0, 0, 2)
+    SMLA_PEAK_CHAINS(32, 0, 0, 4)
+    SMLA_PEAK_CHAINS(64, 0, 0, 2)
+    SMLA_PEAK_CHAINS(64, 0, 0, 4)
+    SMLA_PEAK_CHAINS(64, 1, 1, 2)
+    SMLA_PEAK_CHAINS(64, 1, 1, 4)
+    SMLA_PEAK_CHAINS(128, 0, 0, 2)
+#undef SMLA_PEAK_CHAINS
     return -1;
 }

@@ -13,6 +13,9 @@ or MN-major as the decode reads them), two numbers:
   multiply-adds in M_cta x N x 32 / 8192 cycles (128 x N x 32 / 8192 = N / 2).
 * ``tflops``: every SM does the same; FLOPs of the launch / its CUDA-event time.
 
+A second table takes 2 or 4 accumulators in turn (independent chains) for the
+narrow shapes, to tell a per-instruction cost from a chain's serialisation.
+
 The largest ``tflops`` is the measured dense FP8 peak that ``bench.py`` quotes
 the decode's tensor fraction against. With ``--json`` the table is written as
 JSON (the summary committed under ``profiles/``).
@@ -48,6 +51,13 @@ SHAPES = [
     (2, 256, 1, 1, "MN-major, N = 256, pair"),
 ]
 
+# (N, A MN-major, B MN-major, chains): cta_group::1 MMAs that take 2 or 4
+# accumulators in turn, against one chain of the same shape above
+CHAIN_SHAPES = [
+    (16, 0, 0, 2), (16, 0, 0, 4), (32, 0, 0, 2), (32, 0, 0, 4), (64, 0, 0, 2), (64, 0, 0, 4),
+    (64, 1, 1, 2), (64, 1, 1, 4), (128, 0, 0, 2),
+]
+
 
 def _lib():
     from sparse_mla_decode_gb300 import build
@@ -57,6 +67,9 @@ def _lib():
     lib.smla_peak_mma.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_longlong),
                                                        ctypes.POINTER(ctypes.c_float)]
     lib.smla_peak_mma.restype = ctypes.c_int
+    lib.smla_peak_mma_chains.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong),
+                                                              ctypes.POINTER(ctypes.c_float)]
+    lib.smla_peak_mma_chains.restype = ctypes.c_int
     return lib
 
 
@@ -83,6 +96,26 @@ def measure(sms: int, iters_one: int = 1000, iters_all: int = 4000):
     return rows
 
 
+def measure_chains(sms: int, iters_one: int = 1000, iters_all: int = 4000):
+    lib = _lib()
+    rows = []
+    for n, amn, bmn, ch in CHAIN_SHAPES:
+        cyc = ctypes.c_longlong(0)
+        ms = ctypes.c_float(0.0)
+        rc = lib.smla_peak_mma_chains(1, n, amn, bmn, ch, iters_one, 1, ctypes.byref(cyc), ctypes.byref(ms))
+        if rc != 0:
+            raise RuntimeError(f"smla_peak_mma_chains({n}, {amn}, {bmn}, {ch}) one CTA: {rc}")
+        per_mma = cyc.value / (4 * iters_one)
+        rc = lib.smla_peak_mma_chains(1, n, amn, bmn, ch, iters_all, sms, ctypes.byref(cyc), ctypes.byref(ms))
+        if rc != 0:
+            raise RuntimeError(f"smla_peak_mma_chains({n}, {amn}, {bmn}, {ch}) all SMs: {rc}")
+        flops = sms * 128 * n * 32 * 2 * 4 * iters_all
+        rows.append({"n": n, "a_mn_major": bool(amn), "b_mn_major": bool(bmn), "chains": ch,
+                     "cycles_per_mma": round(per_mma, 2), "ideal_cycles": n / 2,
+                     "tflops": round(flops / (ms.value * 1e-3) / 1e12, 1)})
+    return rows
+
+
 def clocks():
     try:
         out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm", "--format=csv,noheader,nounits"],
@@ -101,17 +134,24 @@ def main():
 
     props = torch.cuda.get_device_properties(0)
     rows = measure(props.multi_processor_count)
+    chains = measure_chains(props.multi_processor_count)
     peak = max(r["tflops"] for r in rows)
     result = {"gpu": props.name, "sms": props.multi_processor_count, "fp8_dense_peak_tflops": peak,
               "how": "libsmla_peak.so: every SM issues 16000 tcgen05.mma kind::f8f6f4 (K = 32) into one TMEM "
                      "accumulator; FLOPs / CUDA-event time of the launch",
-              "clocks": clocks(), "shapes": rows}
+              "clocks": clocks(), "shapes": rows, "chains": chains}
     print("| cta_group | N | A | B | cycles/MMA | ideal | TFLOP/s (all SMs) | use |")
     print("|---|---|---|---|---|---|---|---|")
     for r in rows:
         print(f"| {r['cta_group']} | {r['n']} | {'MN' if r['a_mn_major'] else 'K'} | "
               f"{'MN' if r['b_mn_major'] else 'K'} | {r['cycles_per_mma']} | {r['ideal_cycles']:.0f} | "
               f"{r['tflops']} | {r['use']} |")
+    print()
+    print("| N | A | B | chains | cycles/MMA | ideal | TFLOP/s (all SMs) |")
+    print("|---|---|---|---|---|---|---|")
+    for r in chains:
+        print(f"| {r['n']} | {'MN' if r['a_mn_major'] else 'K'} | {'MN' if r['b_mn_major'] else 'K'} | "
+              f"{r['chains']} | {r['cycles_per_mma']} | {r['ideal_cycles']:.0f} | {r['tflops']} |")
     print(json.dumps({"fp8_dense_peak_tflops": peak}))
     if args.json:
         with open(args.json, "w") as f:

@@ -308,6 +308,10 @@ def test_peak_library_exports_its_benchmarks_and_rejects_bad_arguments_without_a
     cycles = ctypes.c_longlong(0)
     assert peak.smla_peak_mma(1, 64, 0, 0, 0, 1, ctypes.byref(cycles), ctypes.byref(out)) == -1  # no iterations
     assert peak.smla_peak_mma(2, 128, 0, 0, 10, 3, ctypes.byref(cycles), ctypes.byref(out)) == -1  # odd pair count
+    peak.smla_peak_mma_chains.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_void_p]
+    assert peak.smla_peak_mma_chains(1, 64, 0, 0, 3, 10, 1, ctypes.byref(cycles), ctypes.byref(out)) == -1  # 3 chains
+    assert peak.smla_peak_mma_chains(2, 128, 0, 0, 2, 10, 2, ctypes.byref(cycles), ctypes.byref(out)) == -1  # pair
+    assert peak.smla_peak_mma_chains(1, 64, 0, 0, 2, 0, 1, ctypes.byref(cycles), ctypes.byref(out)) == -1  # no work
     p16 = ctypes.c_void_p(16)
     assert peak.smla_peak_gather(0, 7, None, 100, p16, 2, 1, p16, ctypes.byref(out)) == -2  # no pool
     assert peak.smla_peak_gather(2, 7, p16, 100, p16, 3, 1, p16, ctypes.byref(out)) == -2  # pairs need even CTAs
