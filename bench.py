@@ -805,6 +805,7 @@ def run_ds_mla(args, rank, world, local_rank):
               "lse": torch.empty((T, H), dtype=torch.float32, device=dev)} for w in sets]
     byts = [ds_mla_bytes(w) for w in sets]
     w0 = sets[0]
+    tile = smla.smla_ds_mla_head_tile(T, H)
 
     def call(i):
         d = dsets[i % R]
@@ -884,7 +885,8 @@ def run_ds_mla(args, rank, world, local_rank):
                          % (R, per_call / 1e6),
                    "launch": ("one CUDA graph of the %d timed library calls, replayed once" % args.steps)
                              if graph is not None else "%d library calls from Python" % args.steps,
-                   "kernel": "32-head tiles, one CTA per (token, 32 heads), 128-key chunks in two stages",
+                   "kernel": "%d-head tiles, one CTA per (token, %d heads): %d CTAs, 128-key chunks in two stages"
+                             % (tile, tile, T * H // tile),
                    "parallelism": "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(value / peak, 4), "peak_source": peak_src, "traffic": ncu_traffic("ds_mla"),

@@ -320,7 +320,7 @@ typedef struct smla_ds_mla_shape {
     int32_t width;      /* W >= 0 */
     int32_t num_pools;  /* 1 or 2 */
     int32_t pool_split; /* columns < pool_split read pool 0 (num_pools == 2) */
-    int32_t reserved;   /* 0 */
+    int32_t head_tile;  /* heads per CTA: 0 lets the library choose, 32, or 64 (H a multiple of 64) */
     int64_t q_stride_token, q_stride_head;       /* q_latent: bytes, multiples of 16; head stride >= 512 */
     int64_t rope_stride_token, rope_stride_head; /* q_rope: BF16 elements, multiples of 8; head stride >= 64 */
     int64_t idx_stride_token;                    /* int32 elements, >= W */
@@ -337,14 +337,23 @@ typedef struct smla_ds_mla_shape {
  *   bmm1_scale  multiplies the dot products (> 0); bmm2_scale multiplies the
  *             output (the row scales replace k_scale).
  *   out       device, BF16 [T, H, 512].
- * One CTA per (token, 32 heads), no key split; launched with programmatic
- * dependent launch; captureable in a CUDA graph (no allocation, no
- * synchronisation). Errors: SMLA_EINVAL / SMLA_EUNSUPPORTED before anything is
+ * One CTA per (token, 32 or 64 heads: smla_ds_mla_head_tile), no key split;
+ * launched with programmatic dependent launch; captureable in a CUDA graph
+ * (no allocation, no synchronisation). Both head tiles compute the same
+ * arithmetic in the same order. Errors: SMLA_EINVAL / SMLA_EUNSUPPORTED before anything is
  * launched, SMLA_ECUDA when the launch fails; an index beyond its pool and a
  * wait that timed out set bits in the device error word. */
 int smla_decode_ds_mla(const smla_ds_mla_shape* shape, const void* q_latent, const void* q_rope,
                        const smla_pool* kv_pools, const int32_t* indices, const int32_t* lens, const float* sinks,
                        float bmm1_scale, float bmm2_scale, void* out, float* lse, void* stream);
+
+/* The heads per CTA smla_decode_ds_mla takes for `shape` on a device of
+ * `num_sms` SMs (<= 0: the current device's count): shape->head_tile when it
+ * is 32 or 64; with 0, 64 where H is a multiple of 64 and the 64-head grid
+ * (T x H / 64 CTAs) takes fewer waves of the SMs than the 32-head grid, else
+ * 32. Returns 32, 64, SMLA_EINVAL (a shape smla_decode_ds_mla rejects for
+ * its heads or head_tile) or SMLA_ECUDA (no device to query). */
+int smla_ds_mla_head_tile(const smla_ds_mla_shape* shape, int num_sms);
 
 /* Reads and clears the current device's error word (SMLA_DEV_* bits) in
  * stream order, without synchronising the device: a one-thread kernel on

@@ -16,6 +16,7 @@ from .smla import (  # noqa: F401
     mxfp4_q_quant,
     smla_decode,
     smla_decode_ds_mla,
+    smla_ds_mla_head_tile,
     smla_device_error,
     smla_read_device_error,
     smla_selftest_bounded_wait,

@@ -624,7 +624,550 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel(const __grid
     }
 }
 
+// ---------------------------------------------------------------------------
+// 64 heads per CTA. The same arithmetic, step for step and in the same order,
+// as the 32-head kernel above; what changes is where the products live:
+//   * TMEM: the four O^T blocks of 64 heads take 256 columns, so the five
+//     accumulators of a chunk's QK (the rope first, then latent blocks 0..3)
+//     take turns in a ring of four 64-column slots. The softmax reads each
+//     slot into registers as soon as its product lands and frees it at once,
+//     so the next chunk's products start while it works on this one.
+//   * shared memory: two stages of 82 KB and a 40 KB Q leave room for two
+//     P'_b^T buffers of 8 KB, which take P'_0 and P'_1; P'_2 and P'_3 take
+//     the chunk's 16 KB of rope rows, which nothing reads once its QK is done
+//     and nothing writes before its PV is done (the stage is refilled only
+//     then).
+// Two softmax warpgroups (32 heads each), one MMA warp, seven producers.
+namespace wide {
+
+constexpr int kN = 64;
+constexpr int kThreads = 512;
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp = 9;
+constexpr int kFirstThreads = 256 + kProducerThreads;  // chunk 0: every warp but the MMA warp
+constexpr int kQ = 2 * kStage;
+constexpr int kQRope = kQ + 4 * kN * 128;
+constexpr int kPBlock = kC * kN;              // P'_b^T: 128 keys x 64 heads of E4M3
+constexpr int kP = kQRope + kN * 128;         // P'_0, P'_1 (P'_2, P'_3 in the stage's rope rows)
+static_assert(2 * kPBlock == kC * 128 && kRope % 1024 == 0, "two P' blocks fill the rope rows of a stage");
+constexpr int kIdx = kP + 2 * kPBlock;        // int32 [2][128]
+constexpr int kRed = kIdx + 2 * kC * 4;       // float [4 warps][64 heads]
+constexpr int kSig = kRed + 4 * kN * 4;       // per warpgroup: float [4 warps][4 blocks], sigma[4], beta[4]
+constexpr int kSigBytes = 128;
+constexpr int kHead = kSig + 2 * kSigBytes;   // float [4][64]: m_run, bias, alpha, l
+constexpr int kBar = kHead + 4 * kN * 4;      // 32 mbarriers
+constexpr int kMisc = kBar + 32 * 8;
+constexpr int kBytes = kMisc + 64;
+constexpr int kAlloc = kBytes + 1024;
+static_assert(kAlloc <= 227 * 1024, "one CTA's shared memory");
+static_assert(kQ % 1024 == 0 && kQRope % 1024 == 0 && kP % 1024 == 0, "aligned tiles");
+static_assert(kN * 512 * 2 <= kStage, "the epilogue's BF16 tile fits in a stage");
+
+// TMEM columns: O^T block j at 64 j, S slot i at 256 + 64 i.
+constexpr int kSlot0 = 4 * kN;
+constexpr int kTmemCols = 512;
+constexpr int kAccPerChunk = 5;  // the rope, then latent blocks 0..3
+
+// P'^T of one block: 128 keys x 64 heads, MN-major, 64-byte swizzle.
+__device__ __forceinline__ uint32_t p_unit64(int key, int unit) {
+    return static_cast<uint32_t>(key * kN + ((unit ^ ((key >> 1) & 3)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBar);
+    uint64_t* kv_full = bars + 0;      // [2] a stage's rows landed (224 cp.async arrivals + 1)
+    uint64_t* stage_free = bars + 2;   // [2] PV of the stage's chunk finished
+    uint64_t* slot_full = bars + 4;    // [4] a QK product landed in the slot
+    uint64_t* slot_free = bars + 8;    // [4] the softmax read the slot (one arrival per softmax warp)
+    uint64_t* p_full = bars + 12;      // [4] P'_b written, O^T block b rescaled (256 arrivals)
+    uint64_t* drain = bars + 16;       // every MMA finished
+    uint64_t* q_full = bars + 17;      // the Q tiles landed
+    uint64_t* kv_first = bars + 18;    // chunk 0 landed (480 cp.async arrivals + 1)
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kIdx);
+    float* red = reinterpret_cast<float*>(smem + kRed);
+    float* m_run_s = reinterpret_cast<float*>(smem + kHead);
+    float* bias_s = m_run_s + kN;
+    float* alpha_s = m_run_s + 2 * kN;
+    float* l_s = m_run_s + 3 * kN;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int head0 = static_cast<int>(blockIdx.x) * kN;
+    const int token = blockIdx.y;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], kProducerThreads + 1);
+            mbar_init(&stage_free[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&slot_full[i], 1);
+            mbar_init(&slot_free[i], 8);
+            mbar_init(&p_full[i], 256);
+        }
+        mbar_init(drain, 1);
+        mbar_init(q_full, 1);
+        mbar_init(kv_first, kFirstThreads + 1);
+        misc[1] = 0;
+        mbar_init_fence();
+    }
+    if (tid < kN) {
+        m_run_s[tid] = -INFINITY;
+        bias_s[tid] = -INFINITY;
+        alpha_s[tid] = 1.0f;
+        l_s[tid] = 0.0f;
+    }
+    if (tid < 8) {  // each warpgroup's sigma[4] and beta[4]
+        float* sg = reinterpret_cast<float*>(smem + kSig + (tid >> 2) * kSigBytes) + 16;
+        sg[tid & 3] = 0.0f;
+        sg[4 + (tid & 3)] = 1.0f;
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(misc, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensor_map(&p.q_latent);
+        prefetch_tensor_map(&p.q_rope);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    grid_dependency_wait();  // inputs are read only after this point
+    if (warp == kProducerWarp && lane == 0) {
+        mbar_arrive_expect_tx(q_full, kN * 512 + kN * 128);
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+            tma_load_3d(sbase + kQ + kb * kN * 128, &p.q_latent, kb * 128, head0, token, q_full);
+        tma_load_3d(sbase + kQRope, &p.q_rope, 0, head0, token, q_full);
+    }
+    const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
+    int32_t raw_first = -1;
+    if (tid < kC && tid < p.width) raw_first = idx_row[tid];
+    const int count = min(max(p.lens[token], 0), p.width);
+    const float sink_of_head = (tid < kN && p.sinks != nullptr) ? p.sinks[head0 + tid] * kLog2e : -INFINITY;
+    const int nch = (count + kC - 1) / kC;
+    grid_launch_dependents();
+
+    bool ok = true;
+    auto kv_bar = [&](int c) -> uint64_t* { return c == 0 ? kv_first : &kv_full[c & 1]; };
+    auto kv_parity = [&](int c) -> uint32_t {
+        return c == 0 ? 0u : static_cast<uint32_t>(((c >> 1) - ((c & 1) ? 0 : 1)) & 1);
+    };
+
+    if (warp != kMmaWarp && nch > 0) {
+        // ===================== chunk 0 by the softmax and producer warps
+        if (tid < kC) idx_s[tid] = tid < count ? resolve(p, tid, raw_first) : -1;
+        named_barrier(5, kFirstThreads);
+        if (tid == 0) mbar_arrive(kv_first);  // every idx_s entry (release)
+        gather_chunk(p, sbase, idx_s, 0, warp < kMmaWarp ? warp : warp - 1, kFirstThreads / 32, lane);
+        cp_async_arrive_noinc(kv_first);
+    }
+
+    if (warp >= kProducerWarp) {
+        // ================================================== producers
+        const int g = tid - kProducerWarp * 32;
+        for (int c = 1; c < nch; ++c) {
+            const int b = c & 1;
+            const int col = c * kC + g;
+            const int32_t raw = (g < kC && col < count) ? idx_row[col] : -1;
+            if (c >= 2)
+                ok &= mbar_wait_bounded(&stage_free[b], static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_flag,
+                                        kWaitLimitNs);
+            if (g < kC) idx_s[b * kC + g] = col < count ? resolve(p, col, raw) : -1;
+            named_barrier(3, kProducerThreads);
+            if (g == 0) mbar_arrive(&kv_full[b]);
+            gather_chunk(p, sbase + b * kStage, idx_s + b * kC, c * kC, g >> 5, kProducerThreads / 32, lane);
+            cp_async_arrive_noinc(&kv_full[b]);
+        }
+        cp_async_wait_all();
+    } else if (warp == kMmaWarp) {
+        // ================================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_e4m3(kC, kN, 0, 0);
+            constexpr uint32_t kIdescRope = idesc_bf16_kmajor(kC, kN);
+            constexpr uint32_t kIdescPV = idesc_e4m3(kC, kN, 1, 1);
+            const uint64_t d_kv = smem_desc(sbase + kLat, 1024, 1024, kSwizzle128B);
+            const uint64_t d_kv_rope = smem_desc(sbase + kRope, 1024, 1024, kSwizzle128B);
+            const uint64_t d_q = smem_desc(sbase + kQ, 1024, 1024, kSwizzle128B);
+            const uint64_t d_q_rope = smem_desc(sbase + kQRope, 1024, 1024, kSwizzle128B);
+            const uint64_t d_p = smem_desc(sbase + kP, 8 * kN, 8 * kN, kSwizzle64B);
+            const uint64_t d_p_rope = smem_desc(sbase + kRope, 8 * kN, 8 * kN, kSwizzle64B);
+            const int n_acc = kAccPerChunk * nch, n_pv = 4 * nch;
+            int next_acc = 0, next_pv = 0, landed = -1;
+            bool q_ready = false;
+            uint64_t idle_since = 0;
+            while (next_pv < n_pv) {
+                bool progressed = false;
+                if (!q_ready) q_ready = mbar_test_wait(q_full, 0);
+                if (q_ready && next_acc < n_acc) {
+                    const int c = next_acc / kAccPerChunk, a = next_acc % kAccPerChunk;
+                    const int slot = next_acc & 3, use = next_acc >> 2;
+                    if (landed < c && mbar_test_wait(kv_bar(c), kv_parity(c))) {
+                        landed = c;
+                        fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
+                    }
+                    if (landed >= c &&
+                        (use == 0 || mbar_test_wait(&slot_free[slot], static_cast<uint32_t>((use - 1) & 1)))) {
+                        tc_fence_after_sync();
+                        const uint32_t stage16 = static_cast<uint32_t>((c & 1) * kStage) >> 4;
+                        const uint32_t d_s = tmem + kSlot0 + slot * kN;
+                        if (a == 0) {
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)  // the rope: BF16, 16 values (32 bytes) a step
+                                mma_bf16(d_s, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
+                                         kIdescRope, ks != 0 ? 1u : 0u);
+                        } else {
+                            const int lb = a - 1;  // latent block
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                mma_f8(d_s, d_kv + stage16 + ((lb * kC * 128 + ks * 32) >> 4),
+                                       d_q + ((lb * kN * 128 + ks * 32) >> 4), kIdescQK, ks != 0 ? 1u : 0u);
+                        }
+                        mma_commit(&slot_full[slot]);
+                        ++next_acc;
+                        progressed = true;
+                    }
+                }
+                if (next_pv < n_pv) {
+                    const int c = next_pv >> 2, j = next_pv & 3;
+                    if (next_acc >= kAccPerChunk * (c + 1) && mbar_test_wait(&p_full[j], static_cast<uint32_t>(c & 1))) {
+                        tc_fence_after_sync();
+                        const uint32_t stage16 = static_cast<uint32_t>((c & 1) * kStage) >> 4;
+                        // P'_0, P'_1 in their own buffers, P'_2, P'_3 in the chunk's rope rows
+                        const uint64_t d_pj = j < 2 ? d_p + ((j * kPBlock) >> 4)
+                                                    : d_p_rope + stage16 + (((j - 2) * kPBlock) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kC / 32; ++kk)
+                            mma_f8(tmem + j * kN, d_kv + stage16 + ((j * kC * 128 + kk * 32 * 128) >> 4),
+                                   d_pj + ((kk * 32 * kN) >> 4), kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
+                        if (j == 3) mma_commit(&stage_free[c & 1]);
+                        ++next_pv;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = global_timer_ns();
+                    if (idle_since == 0) idle_since = now;
+                    if (*abort_flag || now - idle_since > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!q_ready) ok &= mbar_wait_bounded(q_full, 0, abort_flag, kWaitLimitNs);  // no copy outlives the CTA
+            mma_commit(drain);
+        }
+        __syncwarp();
+    } else {
+        // ===================================================== softmax
+        // Warpgroup wg owns heads 32 wg .. 32 wg + 31; thread t owns key t of
+        // each chunk (TMEM lane t) and latent row t of each O^T block.
+        const int wg = warp >> 2, t = tid & 127, hb = 32 * wg;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float scale_log2 = p.scale_log2;
+        float* sig_red = reinterpret_cast<float*>(smem + kSig + wg * kSigBytes);  // [4 warps][4 blocks]
+        float* sig_run = sig_red + 16;
+        float* sig_beta = sig_red + 20;
+        float lsum[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) lsum[h] = 0.0f;
+
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1;
+            ok &= mbar_wait_bounded(kv_bar(c), kv_parity(c), abort_flag, kWaitLimitNs);
+            const bool active = idx_s[b * kC + t] >= 0;
+            const float4 sc = *reinterpret_cast<const float4*>(smem + b * kStage + kScale + t * 16);
+            const float sb[4] = {sc.x, sc.y, sc.z, sc.w};
+            // logits of this key: S_rope + sum_b s_b S_b (FP32), slot by slot
+            float s[32];
+#pragma unroll 1
+            for (int a = 0; a < kAccPerChunk; ++a) {
+                const int acc = kAccPerChunk * c + a, slot = acc & 3;
+                ok &= mbar_wait_bounded(&slot_full[slot], static_cast<uint32_t>((acc >> 2) & 1), abort_flag,
+                                        kWaitLimitNs);
+                tc_fence_after_sync();
+                const uint32_t col = tmem + lane_base + kSlot0 + slot * kN + hb;
+                float v[32];
+                tmem_load16x2(col, col + 16, v);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&slot_free[slot]);
+                if (a == 0) {
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) s[h] = v[h];
+                } else {
+                    const float f = a == 1 ? sb[0] : a == 2 ? sb[1] : a == 3 ? sb[2] : sb[3];
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) s[h] = fmaf(f, v[h], s[h]);
+                }
+            }
+            // chunk maxima per head (transposing butterfly: lane l ends with
+            // head hb + l) and per block the largest |scale| of the active keys
+            {
+                float m[16];
+                {
+                    const bool up = (lane & 16) != 0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float lo = active ? s[i] : -INFINITY, hi = active ? s[i + 16] : -INFINITY;
+                        m[i] = fmaxf(up ? hi : lo, __shfl_xor_sync(0xFFFFFFFFu, up ? lo : hi, 16));
+                    }
+                }
+#pragma unroll
+                for (int o = 8, n = 16; n > 1; o >>= 1, n >>= 1) {
+                    const bool up = (lane & o) != 0;
+#pragma unroll
+                    for (int i = 0; i < n / 2; ++i) {
+                        const float send = up ? m[i] : m[i + n / 2];
+                        const float keep = up ? m[i + n / 2] : m[i];
+                        m[i] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+                    }
+                }
+                red[(warp & 3) * kN + hb + lane] = m[0];
+                float g4[4] = {active ? fabsf(sc.x) : 0.0f, active ? fabsf(sc.y) : 0.0f, active ? fabsf(sc.z) : 0.0f,
+                               active ? fabsf(sc.w) : 0.0f};
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) g4[a] = fmaxf(g4[a], __shfl_xor_sync(0xFFFFFFFFu, g4[a], o));
+                if (lane < 4) sig_red[(warp & 3) * 4 + lane] = g4[lane];
+            }
+            named_barrier(1 + wg, 128);
+            if (t < 32) {
+                const int h = hb + t;
+                const float cm = fmaxf(fmaxf(red[h], red[kN + h]), fmaxf(red[2 * kN + h], red[3 * kN + h]));
+                const float mo = m_run_s[h];
+                const float mn = fmaxf(mo, cm * scale_log2);
+                alpha_s[h] = (mo == -INFINITY) ? 1.0f : fast_exp2(mo - mn);
+                bias_s[h] = mn - kLog2P;
+                m_run_s[h] = mn;
+            } else if (t >= 64 && t < 68) {
+                const int a = t - 64;
+                const float so = sig_run[a];
+                const float sn = fmaxf(so, fmaxf(fmaxf(sig_red[a], sig_red[4 + a]), fmaxf(sig_red[8 + a], sig_red[12 + a])));
+                sig_beta[a] = (so > 0.0f && sn > so) ? so / sn : 1.0f;
+                sig_run[a] = sn;
+            }
+            named_barrier(1 + wg, 128);
+
+            // P = 2^(s * scale_log2 - m + log2 448) in place of s (FP32 sums of
+            // the unrounded P)
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 bi = reinterpret_cast<const float4*>(bias_s + hb)[j4];
+                const float4 al = reinterpret_cast<const float4*>(alpha_s + hb)[j4];
+                const int j = 4 * j4;
+                float pr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (active) {
+                    pr[0] = fast_exp2(fmaf(s[j + 0], scale_log2, -bi.x));
+                    pr[1] = fast_exp2(fmaf(s[j + 1], scale_log2, -bi.y));
+                    pr[2] = fast_exp2(fmaf(s[j + 2], scale_log2, -bi.z));
+                    pr[3] = fast_exp2(fmaf(s[j + 3], scale_log2, -bi.w));
+                }
+                lsum[j + 0] = fmaf(lsum[j + 0], al.x, pr[0]);
+                lsum[j + 1] = fmaf(lsum[j + 1], al.y, pr[1]);
+                lsum[j + 2] = fmaf(lsum[j + 2], al.z, pr[2]);
+                lsum[j + 3] = fmaf(lsum[j + 3], al.w, pr[3]);
+                s[j + 0] = pr[0];
+                s[j + 1] = pr[1];
+                s[j + 2] = pr[2];
+                s[j + 3] = pr[3];
+            }
+            bool any_alpha = false;
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 v4 = reinterpret_cast<const float4*>(alpha_s + hb)[j4];
+                any_alpha |= (v4.x != 1.0f) | (v4.y != 1.0f) | (v4.z != 1.0f) | (v4.w != 1.0f);
+            }
+
+            // PV of chunk c - 1 has finished: its P'_0 and P'_1 buffers are free
+            // and its O^T blocks final for this step
+            if (c >= 1)
+                ok &= mbar_wait_bounded(&stage_free[(c - 1) & 1], static_cast<uint32_t>(((c - 1) >> 1) & 1),
+                                        abort_flag, kWaitLimitNs);
+            // block by block: P'_a = P * s_a / sigma_a as E4M3 (P'_0 and P'_1
+            // into their buffers, P'_2 and P'_3 into this chunk's rope rows,
+            // which its QK has finished reading), then O^T block a *= alpha(head)
+            // * beta(a) where either moved; PV of the block may start at once
+#pragma unroll 1
+            for (int a = 0; a < 4; ++a) {
+                const float sg = sig_run[a];
+                const float ratio = sg > 0.0f ? (a == 0 ? sb[0] : a == 1 ? sb[1] : a == 2 ? sb[2] : sb[3]) / sg : 0.0f;
+                uint8_t* pbuf = a < 2 ? smem + kP + a * kPBlock : smem + b * kStage + kRope + (a - 2) * kPBlock;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t words[4];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int j = 16 * g + 4 * q4;
+                        words[q4] = e4m3x2(s[j + 0] * ratio, s[j + 1] * ratio) |
+                                    (e4m3x2(s[j + 2] * ratio, s[j + 3] * ratio) << 16);
+                    }
+                    *reinterpret_cast<uint4*>(pbuf + p_unit64(t, 2 * wg + g)) =
+                        make_uint4(words[0], words[1], words[2], words[3]);
+                }
+                const float beta = sig_beta[a];
+                if (c >= 1 && (any_alpha || beta != 1.0f)) {
+                    tc_fence_after_sync();
+                    const uint32_t col = tmem + lane_base + a * kN + hb;
+                    float v[32];
+                    tmem_load16x2(col, col + 16, v);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 al = reinterpret_cast<const float4*>(alpha_s + hb)[j4];
+                        v[4 * j4 + 0] *= al.x * beta;
+                        v[4 * j4 + 1] *= al.y * beta;
+                        v[4 * j4 + 2] *= al.z * beta;
+                        v[4 * j4 + 3] *= al.w * beta;
+                    }
+                    tmem_store16x2(col, col + 16, v);
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&p_full[a]);
+            }
+        }
+        // every PV finished
+        if (nch > 0)
+            ok &= mbar_wait_bounded(&stage_free[(nch - 1) & 1], static_cast<uint32_t>(((nch - 1) >> 1) & 1),
+                                    abort_flag, kWaitLimitNs);
+        tc_fence_after_sync();
+
+        // per-head totals of the per-thread partial sums
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            float v = lsum[j];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+            if (lane == j) red[(warp & 3) * kN + hb + j] = v;
+        }
+        named_barrier(1 + wg, 128);
+        if (t < 32) {
+            const int h = hb + t;
+            l_s[h] = (red[h] + red[kN + h]) + (red[2 * kN + h] + red[3 * kN + h]);
+        }
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.error, SMLA_DEV_TIMEOUT);
+    }
+    cp_async_wait_all();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+
+    // ================================================ epilogue
+    // bias_s becomes each head's output factor; O^T rows -> BF16 [64][512]
+    // in the free KV stage, then 16-byte stores to out.
+    if (tid < kN) {
+        const int h = head0 + tid;
+        const float m = m_run_s[tid];
+        float scale = 0.0f, lse2 = -INFINITY;
+        if (m != -INFINITY) {
+            float top = m, extra = 0.0f;
+            if (p.sinks != nullptr) {
+                top = fmaxf(m, sink_of_head);
+                extra = 448.0f * fast_exp2(sink_of_head - top);
+            }
+            const float w = fast_exp2(m - top);
+            const float total = l_s[tid] * w + extra;
+            scale = p.out_scale * w / total;
+            lse2 = top - kLog2P + log2f(total);
+        }
+        bias_s[tid] = scale;
+        if (p.lse != nullptr) p.lse[static_cast<int64_t>(token) * p.lse_stride_token + h] = lse2;
+    }
+    __syncthreads();
+    __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + kLat);
+    if (warp < 8) {
+        const int wg = warp >> 2, hb = 32 * wg;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float* sig_run = reinterpret_cast<const float*>(smem + kSig) + 16;  // warpgroup 0's copy
+#pragma unroll 1
+        for (int a = 0; a < 4; ++a) {
+            float v[32];
+            const uint32_t col = tmem + lane_base + a * kN + hb;
+            tmem_load16x2(col, col + 16, v);
+            const float sg = sig_run[a];
+            const int lat = a * 128 + (tid & 127);
+            // a head without active keys has factor 0 and gets +0.0 (its
+            // O^T block may never have been written)
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+                const float f = sg * bias_s[hb + h];
+                tile[(hb + h) * 512 + lat] = __float2bfloat16_rn(f == 0.0f ? 0.0f : v[h] * f);
+            }
+        }
+    }
+    __syncthreads();
+    {
+        __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
+                             static_cast<int64_t>(head0) * p.out_stride_head;
+        const bool wide_rows = ((reinterpret_cast<uintptr_t>(p.out) | static_cast<uintptr_t>(p.out_stride_token * 2) |
+                                 static_cast<uintptr_t>(p.out_stride_head * 2)) & 15u) == 0;
+        if (wide_rows) {
+            for (int i = tid; i < kN * 512 / 8; i += kThreads) {
+                const int h = i / 64, e = (i % 64) * 8;
+                *reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
+                    *reinterpret_cast<const uint4*>(tile + h * 512 + e);
+            }
+        } else {
+            for (int i = tid; i < kN * 512 / 2; i += kThreads) {
+                const int h = i / 256, e = (i % 256) * 2;
+                *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
+                    *reinterpret_cast<const uint32_t*>(tile + h * 512 + e);
+            }
+        }
+    }
+
+    // ---- teardown: every MMA and TMEM access has finished -----------------
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        if (!mbar_wait_bounded(drain, 0, abort_flag, kWaitLimitNs)) {
+            if (lane == 0) atomicOr(p.error, SMLA_DEV_TIMEOUT);
+        }
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace wide
+
 bool g_configured[64] = {};
+bool g_configured_wide[64] = {};
+
+// Heads per CTA for the shape: 64 where H allows it and the 64-head grid
+// takes fewer waves of the device's SMs than the 32-head grid (its CTAs land
+// each row in half as many SMs), else 32; `forced` 32 or 64 overrides.
+int head_tile_for(int tokens, int heads, int forced, int num_sms) {
+    if (forced == 32 || forced == 64) return forced;
+    if (heads % 64 != 0 || num_sms <= 0) return 32;
+    const int64_t ctas32 = static_cast<int64_t>(tokens) * (heads / 32), ctas64 = ctas32 / 2;
+    const int64_t waves32 = (ctas32 + num_sms - 1) / num_sms, waves64 = (ctas64 + num_sms - 1) / num_sms;
+    return waves64 < waves32 ? 64 : 32;
+}
+
+int device_sms(int dev) {
+    static std::atomic<int> cached[64];
+    if (dev < 0 || dev >= 64) return 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0 && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 }  // namespace dsmla
 }  // namespace smla
@@ -637,6 +1180,8 @@ extern "C" int smla_decode_ds_mla(const smla_ds_mla_shape* shape, const void* q_
     if (shape == nullptr) return SMLA_EINVAL;
     const smla_ds_mla_shape& s = *shape;
     if (s.tokens < 0 || s.width < 0 || s.heads <= 0 || s.heads % kN != 0) return SMLA_EINVAL;
+    if (s.head_tile != 0 && s.head_tile != 32 && s.head_tile != 64) return SMLA_EINVAL;
+    if (s.head_tile == 64 && s.heads % 64 != 0) return SMLA_EINVAL;
     if (s.heads > 1024 || s.tokens > 65535) return SMLA_EUNSUPPORTED;
     if (s.num_pools != 1 && s.num_pools != 2) return SMLA_EUNSUPPORTED;
     if (s.num_pools == 2 && (s.pool_split < 0 || s.pool_split > s.width)) return SMLA_EINVAL;
@@ -665,12 +1210,20 @@ extern "C" int smla_decode_ds_mla(const smla_ds_mla_shape* shape, const void* q_
     }
     if (!std::isfinite(bmm1_scale) || !std::isfinite(bmm2_scale) || !(bmm1_scale > 0.0f)) return SMLA_EINVAL;
 
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        smla::note_cuda_error(static_cast<int>(e));
+        return SMLA_ECUDA;
+    }
+    const int tile = head_tile_for(s.tokens, s.heads, s.head_tile, device_sms(dev));
+
     Params p;
     std::memset(&p, 0, sizeof(p));
     {
         // Q latent as {512 bytes, H, T} and Q rope as {128 bytes, H, T}: boxes
-        // of one 128-byte row x 32 heads (a one-token call's token stride is
-        // never used; it is given a legal value)
+        // of one 128-byte row x the CTA's heads (a one-token call's token
+        // stride is never used; it is given a legal value)
         const int64_t qt = s.tokens == 1 && s.q_stride_token < s.q_stride_head * s.heads
                                ? s.q_stride_head * s.heads : s.q_stride_token;
         const int64_t rt = s.tokens == 1 && s.rope_stride_token < s.rope_stride_head * s.heads
@@ -681,7 +1234,7 @@ extern "C" int smla_decode_ds_mla(const smla_ds_mla_shape* shape, const void* q_
         const cuuint64_t rdims[3] = {128, static_cast<cuuint64_t>(s.heads), static_cast<cuuint64_t>(s.tokens)};
         const cuuint64_t rstrides[2] = {static_cast<cuuint64_t>(s.heads > 1 ? s.rope_stride_head * 2 : 128),
                                         static_cast<cuuint64_t>(rt > 0 ? rt * 2 : 128)};
-        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(kN), 1};
+        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(tile), 1};
         if (!smla::encode_bytes_map(&p.q_latent, q_latent, 3, qdims, qstrides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
             !smla::encode_bytes_map(&p.q_rope, q_rope, 3, rdims, rstrides, box, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -709,29 +1262,46 @@ extern "C" int smla_decode_ds_mla(const smla_ds_mla_shape* shape, const void* q_
     p.out_scale = bmm2_scale;
     p.error = smla::device_error_word();
 
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess && p.error == nullptr) e = cudaErrorInvalidSymbol;
-    if (e == cudaSuccess && dev < 64 && !g_configured[dev]) {
-        e = cudaFuncSetAttribute(ds_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
-        if (e == cudaSuccess) g_configured[dev] = true;
+    if (p.error == nullptr) e = cudaErrorInvalidSymbol;
+    const bool wide64 = tile == 64;
+    bool* configured = wide64 ? g_configured_wide : g_configured;
+    if (e == cudaSuccess && dev < 64 && !configured[dev]) {
+        e = wide64 ? cudaFuncSetAttribute(wide::ds_mla_decode_kernel64, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          wide::kAlloc)
+                   : cudaFuncSetAttribute(ds_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+        if (e == cudaSuccess) configured[dev] = true;
     }
     if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(s.heads / kN), static_cast<unsigned>(s.tokens), 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kAlloc;
+        cfg.gridDim = dim3(static_cast<unsigned>(s.heads / tile), static_cast<unsigned>(s.tokens), 1);
+        cfg.blockDim = dim3(wide64 ? wide::kThreads : kThreads, 1, 1);
+        cfg.dynamicSmemBytes = wide64 ? wide::kAlloc : kAlloc;
         cfg.stream = static_cast<cudaStream_t>(stream);
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr.val.programmaticStreamSerializationAllowed = smla::dependent_launch() ? 1 : 0;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, ds_mla_decode_kernel, p);
+        e = wide64 ? cudaLaunchKernelEx(&cfg, wide::ds_mla_decode_kernel64, p)
+                   : cudaLaunchKernelEx(&cfg, ds_mla_decode_kernel, p);
     }
     if (e != cudaSuccess) {
         smla::note_cuda_error(static_cast<int>(e));
         return SMLA_ECUDA;
     }
     return SMLA_OK;
+}
+
+extern "C" int smla_ds_mla_head_tile(const smla_ds_mla_shape* shape, int num_sms) {
+    using namespace smla::dsmla;
+    if (shape == nullptr || shape->tokens < 0 || shape->heads <= 0 || shape->heads % kN != 0) return SMLA_EINVAL;
+    if (shape->head_tile != 0 && shape->head_tile != 32 && shape->head_tile != 64) return SMLA_EINVAL;
+    if (shape->head_tile == 64 && shape->heads % 64 != 0) return SMLA_EINVAL;
+    if (num_sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ECUDA;
+        num_sms = device_sms(dev);
+        if (num_sms <= 0) return SMLA_ECUDA;
+    }
+    return head_tile_for(shape->tokens, shape->heads, shape->head_tile, num_sms);
 }

@@ -164,12 +164,13 @@ constexpr int kSmem = 128 * 1024;
 // of a group into accumulator ks % CH, so that CH independent chains
 // interleave) and commits; `cycles` (when non-null) gets the clock64 span of
 // CTA 0's run.
-template <int CG, int N, int AMN, int BMN, int CH>
+template <int CG, int N, int AMN, int BMN, int CH, int COMMIT = 0>
 __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* cycles, int* error) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     uint64_t* done = reinterpret_cast<uint64_t*>(smem + kBar);
+    uint64_t* every = done + 4;  // COMMIT: a commit after each group of four lands here; nothing waits on it
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBar + 16);
     const int tid = threadIdx.x;
     const uint32_t rank = CG == 2 ? cluster_rank() : 0u;
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (tid == 0) {
         mbar_init(done, 1);
+        mbar_init(every, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     static_assert(CH == 1 || CH == 2 || CH == 4, "one, two or four chains");
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
             for (int ks = 0; ks < 4; ++ks)
                 mma_f8<CG>(tmem + (ks % CH) * N, a_desc + ks * a_step, b_desc + ks * b_step, idesc,
                            (it != 0 || ks >= CH) ? 1u : 0u);
+            if constexpr (COMMIT != 0) mma_commit<CG>(smem_u32(every));
         }
         mma_commit<CG>(smem_u32(done));
         if constexpr (CG == 2) mma_commit<CG>(map_to_rank(smem_u32(done), 1));
@@ -243,9 +246,9 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
     if (tid < 32) tmem_dealloc<CG>(tmem, kCols);
 }
 
-template <int CG, int N, int AMN, int BMN, int CH>
+template <int CG, int N, int AMN, int BMN, int CH, int COMMIT = 0>
 int run(int iters, int ctas, long long* cycles_out, float* ms_out) {
-    auto kernel = mma_rate_kernel<CG, N, AMN, BMN, CH>;
+    auto kernel = mma_rate_kernel<CG, N, AMN, BMN, CH, COMMIT>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) return -3;
     long long* d_cycles = nullptr;
     int* d_error = nullptr;
@@ -345,4 +348,15 @@ extern "C" int smla_peak_mma_chains(int cta_group, int n, int a_mn, int b_mn, in
     SMLA_PEAK_CHAINS(128, 0, 0, 2)
 #undef SMLA_PEAK_CHAINS
     return -1;
+}
+
+// One accumulator with a tcgen05.commit (to an mbarrier nothing waits on)
+// after every group of four MMAs, as a pipeline that hands each accumulator
+// to its consumer issues them: whether commits slow the tensor pipe. N = 64,
+// operands K-major (a_mn = b_mn = 0) or MN-major (1, 1). Returns as
+// smla_peak_mma.
+extern "C" int smla_peak_mma_commit4(int n, int a_mn, int b_mn, int iters, int ctas, long long* cycles, float* ms) {
+    using namespace smla_peak;
+    if (cycles == nullptr || ms == nullptr || iters <= 0 || ctas <= 0 || n != 64 || a_mn != b_mn) return -1;
+    return a_mn ? run<1, 64, 1, 1, 1, 1>(iters, ctas, cycles, ms) : run<1, 64, 0, 0, 1, 1>(iters, ctas, cycles, ms);
 }

@@ -70,6 +70,9 @@ def _lib():
     lib.smla_peak_mma_chains.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_longlong),
                                                               ctypes.POINTER(ctypes.c_float)]
     lib.smla_peak_mma_chains.restype = ctypes.c_int
+    lib.smla_peak_mma_commit4.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_longlong),
+                                                               ctypes.POINTER(ctypes.c_float)]
+    lib.smla_peak_mma_commit4.restype = ctypes.c_int
     return lib
 
 
@@ -116,6 +119,26 @@ def measure_chains(sms: int, iters_one: int = 1000, iters_all: int = 4000):
     return rows
 
 
+def measure_commits(sms: int, iters_one: int = 1000, iters_all: int = 4000):
+    """N = 64 with a tcgen05.commit after every four MMAs."""
+    lib = _lib()
+    rows = []
+    for mn in (0, 1):
+        cyc = ctypes.c_longlong(0)
+        ms = ctypes.c_float(0.0)
+        rc = lib.smla_peak_mma_commit4(64, mn, mn, iters_one, 1, ctypes.byref(cyc), ctypes.byref(ms))
+        if rc != 0:
+            raise RuntimeError(f"smla_peak_mma_commit4({mn}) one CTA: {rc}")
+        per_mma = cyc.value / (4 * iters_one)
+        rc = lib.smla_peak_mma_commit4(64, mn, mn, iters_all, sms, ctypes.byref(cyc), ctypes.byref(ms))
+        if rc != 0:
+            raise RuntimeError(f"smla_peak_mma_commit4({mn}) all SMs: {rc}")
+        flops = sms * 128 * 64 * 32 * 2 * 4 * iters_all
+        rows.append({"n": 64, "a_mn_major": bool(mn), "b_mn_major": bool(mn), "commit_every": 4,
+                     "cycles_per_mma": round(per_mma, 2), "tflops": round(flops / (ms.value * 1e-3) / 1e12, 1)})
+    return rows
+
+
 def clocks():
     try:
         out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm", "--format=csv,noheader,nounits"],
@@ -135,11 +158,12 @@ def main():
     props = torch.cuda.get_device_properties(0)
     rows = measure(props.multi_processor_count)
     chains = measure_chains(props.multi_processor_count)
+    commits = measure_commits(props.multi_processor_count)
     peak = max(r["tflops"] for r in rows)
     result = {"gpu": props.name, "sms": props.multi_processor_count, "fp8_dense_peak_tflops": peak,
               "how": "libsmla_peak.so: every SM issues 16000 tcgen05.mma kind::f8f6f4 (K = 32) into one TMEM "
                      "accumulator; FLOPs / CUDA-event time of the launch",
-              "clocks": clocks(), "shapes": rows, "chains": chains}
+              "clocks": clocks(), "shapes": rows, "chains": chains, "commit_every_4": commits}
     print("| cta_group | N | A | B | cycles/MMA | ideal | TFLOP/s (all SMs) | use |")
     print("|---|---|---|---|---|---|---|---|")
     for r in rows:
@@ -152,6 +176,12 @@ def main():
     for r in chains:
         print(f"| {r['n']} | {'MN' if r['a_mn_major'] else 'K'} | {'MN' if r['b_mn_major'] else 'K'} | "
               f"{r['chains']} | {r['cycles_per_mma']} | {r['ideal_cycles']:.0f} | {r['tflops']} |")
+    print()
+    print("| N | A | B | commit every | cycles/MMA | TFLOP/s (all SMs) |")
+    print("|---|---|---|---|---|---|")
+    for r in commits:
+        print(f"| {r['n']} | {'MN' if r['a_mn_major'] else 'K'} | {'MN' if r['b_mn_major'] else 'K'} | 4 | "
+              f"{r['cycles_per_mma']} | {r['tflops']} |")
     print(json.dumps({"fp8_dense_peak_tflops": peak}))
     if args.json:
         with open(args.json, "w") as f:

@@ -31,7 +31,7 @@ class SmlaPool(ctypes.Structure):
 class SmlaDsMlaShape(ctypes.Structure):
     _fields_ = [
         ("tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("width", ctypes.c_int32),
-        ("num_pools", ctypes.c_int32), ("pool_split", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("num_pools", ctypes.c_int32), ("pool_split", ctypes.c_int32), ("head_tile", ctypes.c_int32),
         ("q_stride_token", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
         ("rope_stride_token", ctypes.c_int64), ("rope_stride_head", ctypes.c_int64),
         ("idx_stride_token", ctypes.c_int64),
@@ -151,6 +151,8 @@ def load(path: str | None = None):
         lib.smla_decode_ds_mla.argtypes = [ctypes.POINTER(SmlaDsMlaShape), vp, vp, ctypes.POINTER(SmlaPool), vp, vp,
                                            vp, ctypes.c_float, ctypes.c_float, vp, vp, vp]
         lib.smla_decode_ds_mla.restype = i32
+        lib.smla_ds_mla_head_tile.argtypes = [ctypes.POINTER(SmlaDsMlaShape), i32]
+        lib.smla_ds_mla_head_tile.restype = i32
         lib.smla_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.smla_read_device_error.restype = i32
         lib.smla_selftest_bounded_wait.argtypes = [i32, ctypes.c_int64, vp]
@@ -256,13 +258,15 @@ DS_MLA_ROW_BYTES = 656
 
 def smla_decode_ds_mla(q_latent: torch.Tensor, q_rope: torch.Tensor, kv_pools, indices: torch.Tensor,
                        lens: torch.Tensor, sinks: torch.Tensor | None, bmm1_scale: float, bmm2_scale: float,
-                       out: torch.Tensor, lse: torch.Tensor | None, stream=None, pool_split: int = 0):
+                       out: torch.Tensor, lse: torch.Tensor | None, stream=None, pool_split: int = 0,
+                       head_tile: int = 0):
     """Sparse MLA decode over fp8_ds_mla rows through the C ABI.
 
     q_latent: uint8 (E4M3 bytes) or float8_e4m3fn [T, H, 512]; q_rope: bfloat16
     [T, H, 64]; kv_pools: list of 1 or 2 uint8 [rows, 656] tensors, rows
     contiguous; indices int32 [T, >= W]; lens int32 [T]; sinks float32 [H] or
     None; out bf16 [T, H, 512]; lse float32 [T, H] or None. H a multiple of 32.
+    head_tile: heads per CTA, 0 (the library's choice), 32 or 64.
     """
     lib = _lib if _lib is not None else load()
     T, H, _ = q_latent.shape
@@ -273,11 +277,12 @@ def smla_decode_ds_mla(q_latent: torch.Tensor, q_rope: torch.Tensor, kv_pools, i
     esz = q_latent.element_size()
     lse_stride = None if lse is None else lse.stride(0)
     key = ("ds", T, H, W, len(kv_pools), pool_split, qst[0] * esz, qst[1] * esz, rst[0], rst[1], ist[0], ost[0],
-           ost[1], lse_stride)
+           ost[1], lse_stride, head_tile)
 
     def build():
         sh = SmlaDsMlaShape()
         sh.tokens, sh.heads, sh.width, sh.num_pools, sh.pool_split = T, H, W, len(kv_pools), pool_split
+        sh.head_tile = head_tile
         sh.q_stride_token, sh.q_stride_head = qst[0] * esz, qst[1] * esz
         sh.rope_stride_token, sh.rope_stride_head = rst[0], rst[1]
         sh.idx_stride_token = ist[0]
@@ -299,13 +304,24 @@ def smla_decode_ds_mla(q_latent: torch.Tensor, q_rope: torch.Tensor, kv_pools, i
 
 
 def decode_ds_mla(q_latent, q_rope, kv_pools, indices, lens, sinks=None, bmm1_scale=1.0, bmm2_scale=1.0,
-                  pool_split=0, stream=None, with_lse=True):
+                  pool_split=0, stream=None, with_lse=True, head_tile=0):
     """Allocates out (and lse) on q_latent's device and calls :func:`smla_decode_ds_mla`."""
     T, H, _ = q_latent.shape
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q_latent.device)
     lse = torch.empty((T, H), dtype=torch.float32, device=q_latent.device) if with_lse else None
     return smla_decode_ds_mla(q_latent, q_rope, kv_pools, indices, lens, sinks, bmm1_scale, bmm2_scale, out, lse,
-                              stream=stream, pool_split=pool_split)
+                              stream=stream, pool_split=pool_split, head_tile=head_tile)
+
+
+def smla_ds_mla_head_tile(tokens: int, heads: int, head_tile: int = 0, num_sms: int = 0) -> int:
+    """Heads per CTA that :func:`smla_decode_ds_mla` takes (C ABI; ``num_sms``
+    0 asks the current device)."""
+    sh = SmlaDsMlaShape()
+    sh.tokens, sh.heads, sh.head_tile, sh.num_pools = tokens, heads, head_tile, 1
+    rc = load().smla_ds_mla_head_tile(ctypes.byref(sh), int(num_sms))
+    if rc < 0:
+        raise SmlaError(rc, "smla_ds_mla_head_tile")
+    return int(rc)
 
 
 def smla_device_error() -> int:

@@ -337,6 +337,8 @@ def _ds_shape(**kw):
     (dict(num_pools=2, pool_split=101), 656, 16),
     (dict(), 576, 16),                       # a 576-byte pool
     (dict(), 656, 8),                        # misaligned q
+    (dict(head_tile=48), 656, 16),           # heads per CTA neither 32 nor 64
+    (dict(heads=96, head_tile=64), 656, 16),  # 64-head tiles of 96 heads
 ])
 def test_ds_mla_decode_rejects_bad_arguments_before_any_launch(lib, kw, row_bytes, ptr):
     pools = (smla.SmlaPool * 2)()
@@ -359,3 +361,23 @@ def test_ds_mla_decode_limits_and_empty_calls(lib):
     assert lib.smla_decode_ds_mla(ctypes.byref(_ds_shape(tokens=0)), *args) == smla.OK  # nothing to launch
     bad_scale = (p16, p16, pools, p16, p16, None, -0.1, 1.0, p16, None, None)
     assert lib.smla_decode_ds_mla(ctypes.byref(_ds_shape()), *bad_scale) == smla.EINVAL
+
+
+def test_ds_mla_head_tile_rule_without_a_device(lib):
+    """64 heads per CTA where H allows it and the grid takes fewer waves of the
+    SMs than with 32; a forced tile wins; shapes the decode rejects are
+    rejected the same way."""
+    def tile(**kw):
+        return lib.smla_ds_mla_head_tile(ctypes.byref(_ds_shape(**kw)), 152)
+    assert tile(tokens=64, heads=128) == 64      # 256 CTAs of 32 heads: 2 waves; 128 of 64: 1
+    assert tile(tokens=1, heads=128) == 32       # 4 or 2 CTAs: one wave either way
+    assert tile(tokens=76, heads=128) == 64      # 304 CTAs of 32: 2 waves; 152 of 64: 1
+    assert tile(tokens=38, heads=128) == 32      # 152 CTAs of 32: already one wave
+    assert tile(tokens=256, heads=128) == 64     # 7 waves against 4
+    assert tile(tokens=64, heads=96) == 32       # 96 heads do not split into 64-head tiles
+    assert tile(tokens=64, heads=128, head_tile=32) == 32
+    assert tile(tokens=1, heads=64, head_tile=64) == 64
+    assert tile(tokens=1, heads=96, head_tile=64) == smla.EINVAL
+    assert tile(tokens=1, heads=64, head_tile=16) == smla.EINVAL
+    assert tile(tokens=1, heads=48) == smla.EINVAL
+    assert smla.smla_ds_mla_head_tile(64, 128, num_sms=152) == 64

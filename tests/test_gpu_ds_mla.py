@@ -43,7 +43,7 @@ def one_pool(w):
     return np.concatenate(w["pools"]), idx.astype(np.int32)
 
 
-def run_gpu(w):
+def run_gpu(w, head_tile=0):
     dev = "cuda"
     ql = torch.from_numpy(w["q_latent"]).to(dev)
     qr = torch.from_numpy(w["q_rope"].view(np.int16)).view(torch.bfloat16).to(dev)
@@ -52,7 +52,7 @@ def run_gpu(w):
     lens = torch.from_numpy(w["lens"]).to(dev)
     sinks = None if w["sinks"] is None else torch.from_numpy(w["sinks"]).to(dev)
     out, lse = smla.decode_ds_mla(ql, qr, pools, idx, lens, sinks, w["bmm1_scale"], w["bmm2_scale"],
-                                  pool_split=w["pool_split"])
+                                  pool_split=w["pool_split"], head_tile=head_tile)
     torch.cuda.synchronize()
     bits = smla.smla_device_error()
     assert bits & smla.DEV_TIMEOUT == 0
@@ -108,39 +108,52 @@ CASES = [
     (1, 32, 128, 500, 0.0, True, None, None),              # one full chunk
     (2, 128, 2048, 10000, 0.05, True, [2048, 1500], None),
     (2, 32, 384, 400, 0.05, True, [384, 200], 128),        # two pools: 128 window + top-k
+    (2, 64, 700, 900, 0.1, True, [700, 5], 256),           # two pools, 64 heads, a token inside chunk 0
+    (1, 64, 1, 10, 0.0, True, None, None),                 # one key
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"t{c[0]}_h{c[1]}_w{c[2]}" + ("_2p" if c[7] else "") for c in CASES])
 def test_ds_mla_rows_match_the_definition(case):
+    """Each head tile the shape allows (32, and 64 where H is a multiple of
+    64) against the definition; the two tiles compute the same arithmetic in
+    the same order, so their outputs agree bit for bit."""
     T, H, W, rows, holes, sinks, lens, split = case
     w = workloads.ds_mla_small("ds", seed=T * 1000 + W, tokens=T, heads=H, width=W, pool_rows=rows, holes=holes,
                                lens=lens, sinks=sinks, two_pools=split is not None, pool_split=split or 0)
-    got, bits, lse, dev_bits = run_gpu(w)
-    assert dev_bits == 0
-    print(case, "worst", compare(w, got, bits, lse))
+    results = {}
+    for tile in (32, 64) if H % 64 == 0 else (32,):
+        got, bits, lse, dev_bits = run_gpu(w, head_tile=tile)
+        assert dev_bits == 0
+        print(case, "tile", tile, "worst", compare(w, got, bits, lse))
+        results[tile] = (bits, lse)
+    if 64 in results:
+        assert np.array_equal(results[32][0], results[64][0]), "64-head tiles: the same bits as 32-head tiles"
+        assert np.array_equal(results[32][1], results[64][1])
 
 
-def test_rising_block_scales_rescale_the_accumulated_blocks():
+@pytest.mark.parametrize("heads,tile", [(32, 32), (64, 64)])
+def test_rising_block_scales_rescale_the_accumulated_blocks(heads, tile):
     """Rows whose scales grow with the row number, gathered in increasing
     order: every chunk raises each block's largest scale, so the accumulated
     output blocks are rescaled chunk after chunk (and each block differently)."""
-    w = workloads.ds_mla_small("rising", seed=5, tokens=2, heads=32, width=1024, pool_rows=1024, sinks=True)
+    w = workloads.ds_mla_small("rising", seed=5, tokens=2, heads=heads, width=1024, pool_rows=1024, sinks=True)
     pool = w["pools"][0]
     r = np.arange(pool.shape[0], dtype=np.float64)
     scales = np.stack([2.0 ** (r / 64.0 - 12 + b) for b in range(4)], axis=1).astype("<f4")
     pool[:, 512:528] = scales.view(np.uint8).reshape(-1, 16)
     w["indices"] = np.tile(np.arange(1024, dtype=np.int32), (2, 1))
     w["lens"] = np.array([1024, 700], np.int32)
-    got, bits, lse, _ = run_gpu(w)
+    got, bits, lse, _ = run_gpu(w, head_tile=tile)
     print("worst", compare(w, got, bits, lse))
 
 
-def test_index_beyond_the_pool_is_masked_and_flagged():
-    w = workloads.ds_mla_small("oob", seed=9, tokens=1, heads=32, width=64, pool_rows=100)
+@pytest.mark.parametrize("heads,tile", [(32, 32), (64, 64)])
+def test_index_beyond_the_pool_is_masked_and_flagged(heads, tile):
+    w = workloads.ds_mla_small("oob", seed=9, tokens=1, heads=heads, width=64, pool_rows=100)
     w["indices"][0, 10] = 100
     w["indices"][0, 11] = 1 << 30
-    got, bits, lse, dev_bits = run_gpu(w)
+    got, bits, lse, dev_bits = run_gpu(w, head_tile=tile)
     assert dev_bits == smla.DEV_INDEX_RANGE
     compare(w, got, bits, lse)  # the definition treats them as holes
 
@@ -167,10 +180,16 @@ def test_zero_tokens_and_zero_width():
     assert smla.smla_device_error() == 0
 
 
-def test_batch_shape_over_several_waves():
-    """The 64 x 128 x 2048 batch shape (256 CTAs: more than one wave), half
-    of each token's rows from a shared hot set, against the definition."""
+def test_batch_shape_in_both_head_tiles():
+    """The 64 x 128 x 2048 batch shape, half of each token's rows from a
+    shared hot set, against the definition: 64-head tiles (the library's
+    choice here: 128 CTAs, one wave) and 32-head tiles (256 CTAs, more than
+    one wave), bit for bit the same."""
     w = workloads.ds_mla_batch(seed=21, pool_rows=100_000, hot_rows=5000)
+    assert smla.smla_ds_mla_head_tile(64, 128) == 64
     got, bits, lse, dev_bits = run_gpu(w)
     assert dev_bits == 0
     print("worst", compare(w, got, bits, lse))
+    _, bits32, lse32, dev_bits = run_gpu(w, head_tile=32)
+    assert dev_bits == 0
+    assert np.array_equal(bits, bits32) and np.array_equal(lse, lse32)
