@@ -246,6 +246,134 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
     if (tid < 32) tmem_dealloc<CG>(tmem, kCols);
 }
 
+// N = 64 K-major FP8 MMAs from thread 0 (groups of four into one
+// accumulator at column 0) while the other three warps keep another unit
+// busy, as the decode's softmax and producers do beside its MMA warp:
+//   MODE 1: tcgen05.ld / tcgen05.st of 16 columns at a time on columns
+//           64..127 of their TMEM lanes (the softmax's logit reads and O^T
+//           rescales);
+//   MODE 2: no other warp; each group of four FP8 MMAs follows one BF16
+//           kind::f16 MMA (K = 16) into the same accumulator (the rope);
+//   MODE 3: 16-byte st.shared by every lane into the shared memory past the
+//           operand tiles (the producers' landing rows).
+// The busy warps run until thread 0's MMAs have drained (a flag in shared
+// memory), at most `iters` * 64 rounds. `cycles` gets thread 0's clock64
+// span from its first issue to the drain.
+template <int MODE>
+__global__ void __launch_bounds__(128, 1) mma_contend_kernel(int iters, long long* cycles, int* error) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* done = reinterpret_cast<uint64_t*>(smem + kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBar + 16);
+    volatile int* stop = reinterpret_cast<volatile int*>(smem + kBar + 32);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < (kBar - kA) / 4; i += blockDim.x) {
+        const uint32_t x = static_cast<uint32_t>(i) * 2654435761u;
+        reinterpret_cast<uint32_t*>(smem)[i] = (x ^ (x >> 13)) & 0x36363636u;  // E4M3 and BF16 without NaN or Inf
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (tid == 0) {
+        mbar_init(done, 1);
+        *stop = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < 32) tmem_alloc<1>(tmem_slot, 128);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+    if (tid == 0) {
+        constexpr uint32_t idesc = idesc_e4m3(128, 64, 0, 0);
+        // kind::f16, BF16 A and B, FP32 D, K-major
+        constexpr uint32_t idesc16 = (1u << 4) | (1u << 7) | (1u << 10) | (64u >> 3 << 17) | (128u >> 4 << 24);
+        const uint64_t a_desc = smem_desc(sbase + kA, 1024, 1024, kSwizzle128B);
+        const uint64_t b_desc = smem_desc(sbase + kB, 1024, 1024, kSwizzle128B);
+        const long long t0 = clock64();
+        for (int it = 0; it < iters; ++it) {
+            if constexpr (MODE == 2) {
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+                    "l"(a_desc), "l"(b_desc), "r"(idesc16), "r"(it != 0 ? 1u : 0u)
+                    : "memory");
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f8<1>(tmem, a_desc + ks * 2, b_desc + ks * 2, idesc, (it != 0 || ks != 0 || MODE == 2) ? 1u : 0u);
+        }
+        mma_commit<1>(smem_u32(done));
+        ok = mbar_wait_bounded(done, 0);
+        const long long t1 = clock64();
+        *stop = 1;
+        if (cycles != nullptr && blockIdx.x == 0) *cycles = t1 - t0;
+    } else if (warp >= 1 && MODE == 1) {
+        const uint32_t col = tmem + (static_cast<uint32_t>(warp * 32) << 16) + 64;
+        for (int r = 0; r < iters * 64; ++r) {
+            // the warp leaves together: the .sync.aligned TMEM accesses need every lane
+            if (__shfl_sync(0xFFFFFFFFu, *stop, 0) != 0) break;
+            uint32_t v[16];
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+                "tcgen05.wait::ld.sync.aligned;"
+                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                : "r"(col + 16 * (r & 3))
+                : "memory");
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] ^= 1u;
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+                "tcgen05.wait::st.sync.aligned;" ::"r"(col + 16 * (r & 3)),
+                "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+                "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                : "memory");
+            __syncwarp();
+        }
+    } else if (warp >= 1 && MODE == 3) {
+        const uint32_t base = sbase + 64 * 1024 + static_cast<uint32_t>(tid - 32) * 16;  // 96 lanes x 16 bytes
+        for (int r = 0; r < iters * 64; ++r) {
+            if (__shfl_sync(0xFFFFFFFFu, *stop, 0) != 0) break;
+            const uint32_t a = base + static_cast<uint32_t>((r & 31) * 96 * 16);  // within 64 KB .. 112 KB
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(static_cast<uint32_t>(r)) : "memory");
+        }
+    }
+    if (!ok) atomicExch(error, 1);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (tid < 32) tmem_dealloc<1>(tmem, 128);
+}
+
+template <int MODE>
+int run_contend(int iters, long long* cycles_out) {
+    auto kernel = mma_contend_kernel<MODE>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) return -3;
+    long long* d_cycles = nullptr;
+    int* d_error = nullptr;
+    if (cudaMalloc(&d_cycles, sizeof(long long)) != cudaSuccess) return -3;
+    if (cudaMalloc(&d_error, sizeof(int)) != cudaSuccess) {
+        cudaFree(d_cycles);
+        return -3;
+    }
+    cudaMemset(d_error, 0, sizeof(int));
+    int rc = 0;
+    for (int pass = 0; pass < 2 && rc == 0; ++pass) {
+        kernel<<<1, 128, kSmem>>>(iters, d_cycles, d_error);
+        if (cudaDeviceSynchronize() != cudaSuccess) rc = -3;
+    }
+    int err = 0;
+    if (rc == 0) {
+        cudaMemcpy(cycles_out, d_cycles, sizeof(long long), cudaMemcpyDeviceToHost);
+        cudaMemcpy(&err, d_error, sizeof(int), cudaMemcpyDeviceToHost);
+        if (err != 0) rc = -4;
+    }
+    cudaFree(d_cycles);
+    cudaFree(d_error);
+    return rc;
+}
+
 template <int CG, int N, int AMN, int BMN, int CH, int COMMIT = 0>
 int run(int iters, int ctas, long long* cycles_out, float* ms_out) {
     auto kernel = mma_rate_kernel<CG, N, AMN, BMN, CH, COMMIT>;
@@ -359,4 +487,17 @@ extern "C" int smla_peak_mma_commit4(int n, int a_mn, int b_mn, int iters, int c
     using namespace smla_peak;
     if (cycles == nullptr || ms == nullptr || iters <= 0 || ctas <= 0 || n != 64 || a_mn != b_mn) return -1;
     return a_mn ? run<1, 64, 1, 1, 1, 1>(iters, ctas, cycles, ms) : run<1, 64, 0, 0, 1, 1>(iters, ctas, cycles, ms);
+}
+
+// One CTA: N = 64 K-major FP8 MMAs (4 * iters of them, plus iters BF16 ones in
+// mode 2) beside the other warps' work of `mode` (1: TMEM loads and stores,
+// 2: BF16 MMAs interleaved, 3: shared-memory stores). Writes the clock64
+// span of the MMAs. Returns as smla_peak_mma.
+extern "C" int smla_peak_mma_contend(int mode, int iters, long long* cycles) {
+    using namespace smla_peak;
+    if (cycles == nullptr || iters <= 0) return -1;
+    if (mode == 1) return run_contend<1>(iters, cycles);
+    if (mode == 2) return run_contend<2>(iters, cycles);
+    if (mode == 3) return run_contend<3>(iters, cycles);
+    return -1;
 }

@@ -73,6 +73,8 @@ def _lib():
     lib.smla_peak_mma_commit4.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_longlong),
                                                                ctypes.POINTER(ctypes.c_float)]
     lib.smla_peak_mma_commit4.restype = ctypes.c_int
+    lib.smla_peak_mma_contend.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong)]
+    lib.smla_peak_mma_contend.restype = ctypes.c_int
     return lib
 
 
@@ -139,6 +141,26 @@ def measure_commits(sms: int, iters_one: int = 1000, iters_all: int = 4000):
     return rows
 
 
+CONTEND = [(1, "three warps loading and storing 16 TMEM columns at a time"),
+           (2, "a BF16 kind::f16 MMA (K = 16) before every four FP8 MMAs"),
+           (3, "three warps storing 16 bytes a lane into shared memory")]
+
+
+def measure_contention(iters: int = 1000):
+    """N = 64 K-major FP8 MMAs of one CTA beside other work."""
+    lib = _lib()
+    rows = []
+    for mode, what in CONTEND:
+        cyc = ctypes.c_longlong(0)
+        rc = lib.smla_peak_mma_contend(mode, iters, ctypes.byref(cyc))
+        if rc != 0:
+            raise RuntimeError(f"smla_peak_mma_contend({mode}): {rc}")
+        mmas = iters * (5 if mode == 2 else 4)
+        rows.append({"mode": mode, "beside": what, "cycles_per_mma": round(cyc.value / mmas, 2),
+                     "cycles_per_fp8_mma": round(cyc.value / (4 * iters), 2)})
+    return rows
+
+
 def clocks():
     try:
         out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm", "--format=csv,noheader,nounits"],
@@ -159,11 +181,13 @@ def main():
     rows = measure(props.multi_processor_count)
     chains = measure_chains(props.multi_processor_count)
     commits = measure_commits(props.multi_processor_count)
+    contention = measure_contention()
     peak = max(r["tflops"] for r in rows)
     result = {"gpu": props.name, "sms": props.multi_processor_count, "fp8_dense_peak_tflops": peak,
               "how": "libsmla_peak.so: every SM issues 16000 tcgen05.mma kind::f8f6f4 (K = 32) into one TMEM "
                      "accumulator; FLOPs / CUDA-event time of the launch",
-              "clocks": clocks(), "shapes": rows, "chains": chains, "commit_every_4": commits}
+              "clocks": clocks(), "shapes": rows, "chains": chains, "commit_every_4": commits,
+              "contention": contention}
     print("| cta_group | N | A | B | cycles/MMA | ideal | TFLOP/s (all SMs) | use |")
     print("|---|---|---|---|---|---|---|---|")
     for r in rows:
@@ -182,6 +206,11 @@ def main():
     for r in commits:
         print(f"| {r['n']} | {'MN' if r['a_mn_major'] else 'K'} | {'MN' if r['b_mn_major'] else 'K'} | 4 | "
               f"{r['cycles_per_mma']} | {r['tflops']} |")
+    print()
+    print("| N = 64 K-major FP8 MMAs beside | cycles per MMA | cycles per FP8 MMA |")
+    print("|---|---|---|")
+    for r in contention:
+        print(f"| {r['beside']} | {r['cycles_per_mma']} | {r['cycles_per_fp8_mma']} |")
     print(json.dumps({"fp8_dense_peak_tflops": peak}))
     if args.json:
         with open(args.json, "w") as f:
