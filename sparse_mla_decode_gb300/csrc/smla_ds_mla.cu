@@ -179,6 +179,29 @@ __device__ __forceinline__ int32_t resolve(const Params& p, int col, int32_t raw
     return -1;
 }
 
+// Writes the BF16 tile [heads][512] in shared memory to out[token][head0 + h],
+// 16 bytes per thread and step where the output rows allow it, else 4.
+__device__ __forceinline__ void store_tile(const Params& p, const __nv_bfloat16* tile, int token, int head0, int heads,
+                                           int tid, int threads) {
+    __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
+                         static_cast<int64_t>(head0) * p.out_stride_head;
+    const bool wide_rows = ((reinterpret_cast<uintptr_t>(p.out) | static_cast<uintptr_t>(p.out_stride_token * 2) |
+                             static_cast<uintptr_t>(p.out_stride_head * 2)) & 15u) == 0;
+    if (wide_rows) {
+        for (int i = tid; i < heads * 512 / 8; i += threads) {
+            const int h = i / 64, e = (i % 64) * 8;
+            *reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
+                *reinterpret_cast<const uint4*>(tile + h * 512 + e);
+        }
+    } else {
+        for (int i = tid; i < heads * 512 / 2; i += threads) {
+            const int h = i / 256, e = (i % 256) * 2;
+            *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
+                *reinterpret_cast<const uint32_t*>(tile + h * 512 + e);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -591,25 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel(const __grid
         }
     }
     __syncthreads();
-    {
-        __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
-                             static_cast<int64_t>(head0) * p.out_stride_head;
-        const bool wide = ((reinterpret_cast<uintptr_t>(p.out) | static_cast<uintptr_t>(p.out_stride_token * 2) |
-                            static_cast<uintptr_t>(p.out_stride_head * 2)) & 15u) == 0;
-        if (wide) {
-            for (int i = tid; i < kN * 512 / 8; i += kThreads) {
-                const int h = i / 64, e = (i % 64) * 8;
-                *reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
-                    *reinterpret_cast<const uint4*>(tile + h * 512 + e);
-            }
-        } else {
-            for (int i = tid; i < kN * 512 / 2; i += kThreads) {
-                const int h = i / 256, e = (i % 256) * 2;
-                *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
-                    *reinterpret_cast<const uint32_t*>(tile + h * 512 + e);
-            }
-        }
-    }
+    store_tile(p, tile, token, head0, kN, tid, kThreads);
 
     // ---- teardown: every MMA and TMEM access has finished -----------------
     tc_fence_before_sync();
@@ -897,19 +902,21 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
                                         kWaitLimitNs);
                 tc_fence_after_sync();
                 const uint32_t col = tmem + lane_base + kSlot0 + slot * kN + hb;
-                float v[32];
-                tmem_load16x2(col, col + 16, v);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&slot_free[slot]);
                 if (a == 0) {
-#pragma unroll
-                    for (int h = 0; h < 32; ++h) s[h] = v[h];
+                    tmem_load16x2(col, col + 16, s);
                 } else {
                     const float f = a == 1 ? sb[0] : a == 2 ? sb[1] : a == 3 ? sb[2] : sb[3];
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) s[h] = fmaf(f, v[h], s[h]);
+                    for (int half = 0; half < 2; ++half) {
+                        float v[16];
+                        tmem_load16x1(col + 16 * half, v);
+#pragma unroll
+                        for (int h = 0; h < 16; ++h) s[16 * half + h] = fmaf(f, v[h], s[16 * half + h]);
+                    }
                 }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&slot_free[slot]);
             }
             // chunk maxima per head (transposing butterfly: lane l ends with
             // head hb + l) and per block the largest |scale| of the active keys
@@ -1111,25 +1118,7 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
         }
     }
     __syncthreads();
-    {
-        __nv_bfloat16* out = p.out + static_cast<int64_t>(token) * p.out_stride_token +
-                             static_cast<int64_t>(head0) * p.out_stride_head;
-        const bool wide_rows = ((reinterpret_cast<uintptr_t>(p.out) | static_cast<uintptr_t>(p.out_stride_token * 2) |
-                                 static_cast<uintptr_t>(p.out_stride_head * 2)) & 15u) == 0;
-        if (wide_rows) {
-            for (int i = tid; i < kN * 512 / 8; i += kThreads) {
-                const int h = i / 64, e = (i % 64) * 8;
-                *reinterpret_cast<uint4*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
-                    *reinterpret_cast<const uint4*>(tile + h * 512 + e);
-            }
-        } else {
-            for (int i = tid; i < kN * 512 / 2; i += kThreads) {
-                const int h = i / 256, e = (i % 256) * 2;
-                *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(h) * p.out_stride_head + e) =
-                    *reinterpret_cast<const uint32_t*>(tile + h * 512 + e);
-            }
-        }
-    }
+    store_tile(p, tile, token, head0, kN, tid, kThreads);
 
     // ---- teardown: every MMA and TMEM access has finished -----------------
     tc_fence_before_sync();
