@@ -642,14 +642,19 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel(const __grid
 //     the chunk's 16 KB of rope rows, which nothing reads once its QK is done
 //     and nothing writes before its PV is done (the stage is refilled only
 //     then).
-// Two softmax warpgroups (32 heads each), one MMA warp, seven producers.
+// Two softmax warpgroups (32 heads each), six producer warps and two issuing
+// warps: one for the QK products, one for PV, so that neither waits behind
+// the other's bursts (a burst of four MMAs and its commit takes a few hundred
+// cycles to issue).
 namespace wide {
 
 constexpr int kN = 64;
 constexpr int kThreads = 512;
-constexpr int kMmaWarp = 8;
-constexpr int kProducerWarp = 9;
-constexpr int kFirstThreads = 256 + kProducerThreads;  // chunk 0: every warp but the MMA warp
+constexpr int kMmaWarp = 8;         // issues the QK products (and holds the TMEM allocation)
+constexpr int kProducerWarp = 9;    // first of six
+constexpr int kPvWarp = 15;         // issues the PV products
+constexpr int kGatherThreads = 192;  // warps 9..14
+constexpr int kFirstThreads = 256 + kGatherThreads;  // chunk 0: the softmax and producer warps
 constexpr int kQ = 2 * kStage;
 constexpr int kQRope = kQ + 4 * kN * 128;
 constexpr int kPBlock = kC * kN;              // P'_b^T: 128 keys x 64 heads of E4M3
@@ -684,14 +689,14 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
     const uint32_t sbase = smem_u32(smem);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBar);
-    uint64_t* kv_full = bars + 0;      // [2] a stage's rows landed (224 cp.async arrivals + 1)
+    uint64_t* kv_full = bars + 0;      // [2] a stage's rows landed (192 cp.async arrivals + 1)
     uint64_t* stage_free = bars + 2;   // [2] PV of the stage's chunk finished
     uint64_t* slot_full = bars + 4;    // [4] a QK product landed in the slot
     uint64_t* slot_free = bars + 8;    // [4] the softmax read the slot (one arrival per softmax warp)
     uint64_t* p_full = bars + 12;      // [4] P'_b written, O^T block b rescaled (256 arrivals)
-    uint64_t* drain = bars + 16;       // every MMA finished
+    uint64_t* drain = bars + 16;       // every MMA of both issuing threads finished
     uint64_t* q_full = bars + 17;      // the Q tiles landed
-    uint64_t* kv_first = bars + 18;    // chunk 0 landed (480 cp.async arrivals + 1)
+    uint64_t* kv_first = bars + 18;    // chunk 0 landed (448 cp.async arrivals + 1)
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kIdx);
@@ -707,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], kProducerThreads + 1);
+            mbar_init(&kv_full[i], kGatherThreads + 1);
             mbar_init(&stage_free[i], 1);
         }
         for (int i = 0; i < 4; ++i) {
@@ -715,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
             mbar_init(&slot_free[i], 8);
             mbar_init(&p_full[i], 256);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);  // one commit from each issuing thread
         mbar_init(q_full, 1);
         mbar_init(kv_first, kFirstThreads + 1);
         misc[1] = 0;
@@ -767,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
         return c == 0 ? 0u : static_cast<uint32_t>(((c >> 1) - ((c & 1) ? 0 : 1)) & 1);
     };
 
-    if (warp != kMmaWarp && nch > 0) {
+    if (warp != kMmaWarp && warp != kPvWarp && nch > 0) {
         // ===================== chunk 0 by the softmax and producer warps
         if (tid < kC) idx_s[tid] = tid < count ? resolve(p, tid, raw_first) : -1;
         named_barrier(5, kFirstThreads);
@@ -776,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
         cp_async_arrive_noinc(kv_first);
     }
 
-    if (warp >= kProducerWarp) {
+    if (warp >= kProducerWarp && warp < kPvWarp) {
         // ================================================== producers
         const int g = tid - kProducerWarp * 32;
         for (int c = 1; c < nch; ++c) {
@@ -787,89 +792,78 @@ __global__ void __launch_bounds__(kThreads, 1) ds_mla_decode_kernel64(const __gr
                 ok &= mbar_wait_bounded(&stage_free[b], static_cast<uint32_t>(((c - 2) >> 1) & 1), abort_flag,
                                         kWaitLimitNs);
             if (g < kC) idx_s[b * kC + g] = col < count ? resolve(p, col, raw) : -1;
-            named_barrier(3, kProducerThreads);
+            named_barrier(3, kGatherThreads);
             if (g == 0) mbar_arrive(&kv_full[b]);
-            gather_chunk(p, sbase + b * kStage, idx_s + b * kC, c * kC, g >> 5, kProducerThreads / 32, lane);
+            gather_chunk(p, sbase + b * kStage, idx_s + b * kC, c * kC, g >> 5, kGatherThreads / 32, lane);
             cp_async_arrive_noinc(&kv_full[b]);
         }
         cp_async_wait_all();
     } else if (warp == kMmaWarp) {
-        // ================================================== MMA issuer
+        // ===================================== QK issuer: the five products
+        // of each chunk into the slot ring, in order
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_e4m3(kC, kN, 0, 0);
             constexpr uint32_t kIdescRope = idesc_bf16_kmajor(kC, kN);
-            constexpr uint32_t kIdescPV = idesc_e4m3(kC, kN, 1, 1);
             const uint64_t d_kv = smem_desc(sbase + kLat, 1024, 1024, kSwizzle128B);
             const uint64_t d_kv_rope = smem_desc(sbase + kRope, 1024, 1024, kSwizzle128B);
             const uint64_t d_q = smem_desc(sbase + kQ, 1024, 1024, kSwizzle128B);
             const uint64_t d_q_rope = smem_desc(sbase + kQRope, 1024, 1024, kSwizzle128B);
+            ok &= mbar_wait_bounded(q_full, 0, abort_flag, kWaitLimitNs);  // also: no copy outlives the CTA
+            for (int acc = 0; ok && acc < kAccPerChunk * nch; ++acc) {
+                const int c = acc / kAccPerChunk, a = acc % kAccPerChunk;
+                const int slot = acc & 3, use = acc >> 2;
+                if (a == 0) {
+                    ok &= mbar_wait_bounded(kv_bar(c), kv_parity(c), abort_flag, kWaitLimitNs);
+                    fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
+                }
+                if (use >= 1)
+                    ok &= mbar_wait_bounded(&slot_free[slot], static_cast<uint32_t>((use - 1) & 1), abort_flag,
+                                            kWaitLimitNs);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t stage16 = static_cast<uint32_t>((c & 1) * kStage) >> 4;
+                const uint32_t d_s = tmem + kSlot0 + slot * kN;
+                if (a == 0) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)  // the rope: BF16, 16 values (32 bytes) a step
+                        mma_bf16(d_s, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
+                                 kIdescRope, ks != 0 ? 1u : 0u);
+                } else {
+                    const int lb = a - 1;  // latent block
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f8(d_s, d_kv + stage16 + ((lb * kC * 128 + ks * 32) >> 4),
+                               d_q + ((lb * kN * 128 + ks * 32) >> 4), kIdescQK, ks != 0 ? 1u : 0u);
+                }
+                mma_commit(&slot_full[slot]);
+            }
+            mma_commit(drain);
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ===================================== PV issuer: block by block as
+        // the softmax hands each P' block over
+        if (lane == 0) {
+            constexpr uint32_t kIdescPV = idesc_e4m3(kC, kN, 1, 1);
+            const uint64_t d_kv = smem_desc(sbase + kLat, 1024, 1024, kSwizzle128B);
             const uint64_t d_p = smem_desc(sbase + kP, 8 * kN, 8 * kN, kSwizzle64B);
             const uint64_t d_p_rope = smem_desc(sbase + kRope, 8 * kN, 8 * kN, kSwizzle64B);
-            const int n_acc = kAccPerChunk * nch, n_pv = 4 * nch;
-            int next_acc = 0, next_pv = 0, landed = -1;
-            bool q_ready = false;
-            uint64_t idle_since = 0;
-            while (next_pv < n_pv) {
-                bool progressed = false;
-                if (!q_ready) q_ready = mbar_test_wait(q_full, 0);
-                if (q_ready && next_acc < n_acc) {
-                    const int c = next_acc / kAccPerChunk, a = next_acc % kAccPerChunk;
-                    const int slot = next_acc & 3, use = next_acc >> 2;
-                    if (landed < c && mbar_test_wait(kv_bar(c), kv_parity(c))) {
-                        landed = c;
-                        fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
-                    }
-                    if (landed >= c &&
-                        (use == 0 || mbar_test_wait(&slot_free[slot], static_cast<uint32_t>((use - 1) & 1)))) {
-                        tc_fence_after_sync();
-                        const uint32_t stage16 = static_cast<uint32_t>((c & 1) * kStage) >> 4;
-                        const uint32_t d_s = tmem + kSlot0 + slot * kN;
-                        if (a == 0) {
+            for (int c = 0; ok && c < nch; ++c) {
+                const uint32_t stage16 = static_cast<uint32_t>((c & 1) * kStage) >> 4;
+                for (int j = 0; j < 4; ++j) {
+                    ok &= mbar_wait_bounded(&p_full[j], static_cast<uint32_t>(c & 1), abort_flag, kWaitLimitNs);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    // P'_0, P'_1 in their own buffers, P'_2, P'_3 in the chunk's rope rows
+                    const uint64_t d_pj = j < 2 ? d_p + ((j * kPBlock) >> 4)
+                                                : d_p_rope + stage16 + (((j - 2) * kPBlock) >> 4);
 #pragma unroll
-                            for (int ks = 0; ks < 4; ++ks)  // the rope: BF16, 16 values (32 bytes) a step
-                                mma_bf16(d_s, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
-                                         kIdescRope, ks != 0 ? 1u : 0u);
-                        } else {
-                            const int lb = a - 1;  // latent block
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks)
-                                mma_f8(d_s, d_kv + stage16 + ((lb * kC * 128 + ks * 32) >> 4),
-                                       d_q + ((lb * kN * 128 + ks * 32) >> 4), kIdescQK, ks != 0 ? 1u : 0u);
-                        }
-                        mma_commit(&slot_full[slot]);
-                        ++next_acc;
-                        progressed = true;
-                    }
-                }
-                if (next_pv < n_pv) {
-                    const int c = next_pv >> 2, j = next_pv & 3;
-                    if (next_acc >= kAccPerChunk * (c + 1) && mbar_test_wait(&p_full[j], static_cast<uint32_t>(c & 1))) {
-                        tc_fence_after_sync();
-                        const uint32_t stage16 = static_cast<uint32_t>((c & 1) * kStage) >> 4;
-                        // P'_0, P'_1 in their own buffers, P'_2, P'_3 in the chunk's rope rows
-                        const uint64_t d_pj = j < 2 ? d_p + ((j * kPBlock) >> 4)
-                                                    : d_p_rope + stage16 + (((j - 2) * kPBlock) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < kC / 32; ++kk)
-                            mma_f8(tmem + j * kN, d_kv + stage16 + ((j * kC * 128 + kk * 32 * 128) >> 4),
-                                   d_pj + ((kk * 32 * kN) >> 4), kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
-                        if (j == 3) mma_commit(&stage_free[c & 1]);
-                        ++next_pv;
-                        progressed = true;
-                    }
-                }
-                if (progressed) {
-                    idle_since = 0;
-                } else {
-                    const uint64_t now = global_timer_ns();
-                    if (idle_since == 0) idle_since = now;
-                    if (*abort_flag || now - idle_since > kWaitLimitNs) {
-                        ok = false;
-                        break;
-                    }
+                    for (int kk = 0; kk < kC / 32; ++kk)
+                        mma_f8(tmem + j * kN, d_kv + stage16 + ((j * kC * 128 + kk * 32 * 128) >> 4),
+                               d_pj + ((kk * 32 * kN) >> 4), kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
+                    if (j == 3) mma_commit(&stage_free[c & 1]);
                 }
             }
-            if (!q_ready) ok &= mbar_wait_bounded(q_full, 0, abort_flag, kWaitLimitNs);  // no copy outlives the CTA
             mma_commit(drain);
         }
         __syncwarp();

@@ -255,12 +255,18 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, long long* 
 //   MODE 2: no other warp; each group of four FP8 MMAs follows one BF16
 //           kind::f16 MMA (K = 16) into the same accumulator (the rope);
 //   MODE 3: 16-byte st.shared by every lane into the shared memory past the
-//           operand tiles (the producers' landing rows).
+//           operand tiles (the producers' landing rows);
+//   MODE 4: warps 4 and 8 (on thread 0's SM sub-partition, as the decode's
+//           softmax warps 0 and 4 share one with its MMA warp) run chains of
+//           FMAs;
+//   MODE 5: no other warp, and `cycles` gets the span of thread 0's issue of
+//           the first group of four MMAs and its commit alone (the issue
+//           cost, before any back-pressure of the pipe).
 // The busy warps run until thread 0's MMAs have drained (a flag in shared
 // memory), at most `iters` * 64 rounds. `cycles` gets thread 0's clock64
 // span from its first issue to the drain.
 template <int MODE>
-__global__ void __launch_bounds__(128, 1) mma_contend_kernel(int iters, long long* cycles, int* error) {
+__global__ void __launch_bounds__(384, 1) mma_contend_kernel(int iters, long long* cycles, int* error) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -275,6 +281,7 @@ __global__ void __launch_bounds__(128, 1) mma_contend_kernel(int iters, long lon
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (tid == 0) {
         mbar_init(done, 1);
+        mbar_init(done + 1, 1);
         *stop = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -291,6 +298,7 @@ __global__ void __launch_bounds__(128, 1) mma_contend_kernel(int iters, long lon
         const uint64_t a_desc = smem_desc(sbase + kA, 1024, 1024, kSwizzle128B);
         const uint64_t b_desc = smem_desc(sbase + kB, 1024, 1024, kSwizzle128B);
         const long long t0 = clock64();
+        long long t_first = 0;
         for (int it = 0; it < iters; ++it) {
             if constexpr (MODE == 2) {
                 asm volatile(
@@ -302,13 +310,17 @@ __global__ void __launch_bounds__(128, 1) mma_contend_kernel(int iters, long lon
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_f8<1>(tmem, a_desc + ks * 2, b_desc + ks * 2, idesc, (it != 0 || ks != 0 || MODE == 2) ? 1u : 0u);
+            if (MODE == 5 && it == 0) {
+                mma_commit<1>(smem_u32(done + 1));
+                t_first = clock64();
+            }
         }
         mma_commit<1>(smem_u32(done));
         ok = mbar_wait_bounded(done, 0);
         const long long t1 = clock64();
         *stop = 1;
-        if (cycles != nullptr && blockIdx.x == 0) *cycles = t1 - t0;
-    } else if (warp >= 1 && MODE == 1) {
+        if (cycles != nullptr && blockIdx.x == 0) *cycles = MODE == 5 ? t_first - t0 : t1 - t0;
+    } else if (warp >= 1 && warp < 4 && MODE == 1) {
         const uint32_t col = tmem + (static_cast<uint32_t>(warp * 32) << 16) + 64;
         for (int r = 0; r < iters * 64; ++r) {
             // the warp leaves together: the .sync.aligned TMEM accesses need every lane
@@ -331,7 +343,18 @@ __global__ void __launch_bounds__(128, 1) mma_contend_kernel(int iters, long lon
                 : "memory");
             __syncwarp();
         }
-    } else if (warp >= 1 && MODE == 3) {
+    } else if ((warp == 4 || warp == 8) && MODE == 4) {
+        float x = static_cast<float>(tid), y = 1.0f;
+        for (int r = 0; r < iters * 64; ++r) {
+            if (__shfl_sync(0xFFFFFFFFu, *stop, 0) != 0) break;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                x = fmaf(x, 0.999f, y);
+                y = fmaf(y, 1.001f, x);
+            }
+        }
+        if (x == 12345.0f) *stop = 2;  // keeps the chain live
+    } else if (warp >= 1 && warp < 4 && MODE == 3) {
         const uint32_t base = sbase + 64 * 1024 + static_cast<uint32_t>(tid - 32) * 16;  // 96 lanes x 16 bytes
         for (int r = 0; r < iters * 64; ++r) {
             if (__shfl_sync(0xFFFFFFFFu, *stop, 0) != 0) break;
@@ -360,7 +383,7 @@ int run_contend(int iters, long long* cycles_out) {
     cudaMemset(d_error, 0, sizeof(int));
     int rc = 0;
     for (int pass = 0; pass < 2 && rc == 0; ++pass) {
-        kernel<<<1, 128, kSmem>>>(iters, d_cycles, d_error);
+        kernel<<<1, MODE == 4 ? 384 : 128, kSmem>>>(iters, d_cycles, d_error);
         if (cudaDeviceSynchronize() != cudaSuccess) rc = -3;
     }
     int err = 0;
@@ -491,13 +514,17 @@ extern "C" int smla_peak_mma_commit4(int n, int a_mn, int b_mn, int iters, int c
 
 // One CTA: N = 64 K-major FP8 MMAs (4 * iters of them, plus iters BF16 ones in
 // mode 2) beside the other warps' work of `mode` (1: TMEM loads and stores,
-// 2: BF16 MMAs interleaved, 3: shared-memory stores). Writes the clock64
-// span of the MMAs. Returns as smla_peak_mma.
+// 2: BF16 MMAs interleaved, 3: shared-memory stores, 4: FMA chains on the
+// issuing warp's sub-partition, 5: nothing, timing the first four issues).
+// Writes the clock64 span of the MMAs (mode 5: of the first four issues and
+// their commit). Returns as smla_peak_mma.
 extern "C" int smla_peak_mma_contend(int mode, int iters, long long* cycles) {
     using namespace smla_peak;
     if (cycles == nullptr || iters <= 0) return -1;
     if (mode == 1) return run_contend<1>(iters, cycles);
     if (mode == 2) return run_contend<2>(iters, cycles);
     if (mode == 3) return run_contend<3>(iters, cycles);
+    if (mode == 4) return run_contend<4>(iters, cycles);
+    if (mode == 5) return run_contend<5>(iters, cycles);
     return -1;
 }

@@ -143,7 +143,9 @@ def measure_commits(sms: int, iters_one: int = 1000, iters_all: int = 4000):
 
 CONTEND = [(1, "three warps loading and storing 16 TMEM columns at a time"),
            (2, "a BF16 kind::f16 MMA (K = 16) before every four FP8 MMAs"),
-           (3, "three warps storing 16 bytes a lane into shared memory")]
+           (3, "three warps storing 16 bytes a lane into shared memory"),
+           (4, "two warps running FMA chains on the issuing warp's sub-partition"),
+           (5, "nothing: the issue of the first four MMAs and their commit alone")]
 
 
 def measure_contention(iters: int = 1000):
@@ -155,9 +157,9 @@ def measure_contention(iters: int = 1000):
         rc = lib.smla_peak_mma_contend(mode, iters, ctypes.byref(cyc))
         if rc != 0:
             raise RuntimeError(f"smla_peak_mma_contend({mode}): {rc}")
-        mmas = iters * (5 if mode == 2 else 4)
+        mmas = 4 if mode == 5 else iters * (5 if mode == 2 else 4)
         rows.append({"mode": mode, "beside": what, "cycles_per_mma": round(cyc.value / mmas, 2),
-                     "cycles_per_fp8_mma": round(cyc.value / (4 * iters), 2)})
+                     "cycles_per_fp8_mma": round(cyc.value / (4 if mode == 5 else 4 * iters), 2)})
     return rows
 
 
