@@ -17,10 +17,12 @@
 //              + shared memory, P as E4M3 into shared memory, rescale of O^T
 //              in TMEM, epilogue/merge; unpaired, they also gather the first
 //              chunk;
-//   warp 8     allocates TMEM and issues the tcgen05 MMAs from one thread,
-//              QK of the next chunk as soon as its rows landed and PV of the
-//              previous one as soon as its P is ready;
-//   warps 9-15 producers. Unpaired: 16-byte cp.async copies of the chunk's KV
+//   warp 8     allocates TMEM and issues QK from one thread, each chunk's as
+//              soon as its rows landed and its S^T buffer is free;
+//   warp 15    issues PV from one thread, each chunk's as soon as its P is
+//              ready (two issuing threads: a burst of MMAs takes hundreds of
+//              cycles to issue, and neither product waits behind the other's);
+//   warps 9-14 producers. Unpaired: 16-byte cp.async copies of the chunk's KV
 //              rows, one row per warp instruction, straight into the swizzled
 //              K-major tiles the MMAs read (masked columns are zero-filled);
 //              each thread's arrival on the stage barrier fires when its
@@ -66,9 +68,10 @@ constexpr int kRows = 128;  // the MMA's M: rows of S^T, latents of an O^T block
 constexpr int kLatent = 512;
 constexpr int kThreads = 512;
 constexpr int kSoftmaxRange = 256;  // warps 0-7: one or two softmax warpgroups
-constexpr int kMmaWarp = 8;
-constexpr int kProducerWarp = 9;  // first of seven
-constexpr int kProducerThreads = 224;
+constexpr int kMmaWarp = 8;       // issues QK (and holds the TMEM allocation)
+constexpr int kProducerWarp = 9;  // first of six
+constexpr int kProducerThreads = 192;
+constexpr int kPvWarp = 15;       // issues PV
 // Unpaired chunk 0 is gathered by every warp but the MMA warp: the softmax
 // range and the producers.
 constexpr int kFirstGatherThreads = kSoftmaxRange + kProducerThreads;
@@ -216,16 +219,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     const uint32_t sbase = smem_u32(smem);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-    uint64_t* kv_full = bars + 0;   // [NS] a stage's rows landed (224 cp.async arrivals + 1)
+    uint64_t* kv_full = bars + 0;   // [NS] a stage's rows landed (192 cp.async arrivals + 1)
     // pv_done[st]: PV of the chunk in stage st finished (its KV stage is free,
     // O^T holds it). One barrier per stage, so that no waiter is ever more
     // than one phase behind the barrier it waits on.
     uint64_t* pv_done = bars + 3;   // [NS] commit
     uint64_t* s_full = bars + 6;    // [2] QK of a chunk done (commit)
     uint64_t* p_full = bars + 8;    // P^T written, O^T rescaled (softmax arrivals)
-    uint64_t* drain = bars + 9;     // every MMA done (commit)
+    uint64_t* drain = bars + 9;     // every MMA of both issuing threads done (commits)
     uint64_t* q_full = bars + 10;   // the Q tile landed (TMA transaction bytes)
-    uint64_t* kv_first = bars + 11; // chunk 0 landed (480 cp.async arrivals + 1, the producers' at once
+    uint64_t* kv_first = bars + 11; // chunk 0 landed (448 cp.async arrivals + 1, the producers' at once
                                     // when they do not help); later chunks use kv_full
     // stage_free[st] (paired): PV of the chunk in stage st finished in both
     // CTAs of the pair (one multicast commit from each), so either may refill
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
         mbar_init(p_full, NG * 128);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);  // one commit from each issuing thread
         mbar_init(kv_first, kFirstGatherThreads + 1);
         misc[1] = 0;
         mbar_init_fence();
@@ -348,10 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
     // is on every CTA's critical path, and more issuing warps stream it
     // faster); with more chunks the producers start on chunk 1 at once.
     const bool producers_help = nch == 1;
-    if (warp >= kProducerWarp && nch > 1 && !paired) cp_async_arrive_noinc(kv_first);  // nothing in flight yet
-    if (warp != kMmaWarp && nch > 0 && !paired && (warp < kMmaWarp || producers_help)) {
+    const bool producer = warp >= kProducerWarp && warp < kPvWarp;
+    if (producer && nch > 1 && !paired) cp_async_arrive_noinc(kv_first);  // nothing in flight yet
+    if (warp != kMmaWarp && warp != kPvWarp && nch > 0 && !paired && (warp < kMmaWarp || producers_help)) {
         // ============================================= chunk 0
-        const int gw = warp < kMmaWarp ? warp : warp - 1;  // 0 .. 14
+        const int gw = warp < kMmaWarp ? warp : warp - 1;  // 0 .. 13
         const int gather_warps = producers_help ? kFirstGatherThreads / 32 : kSoftmaxRange / 32;
         const int32_t* idx_row = p.indices + static_cast<int64_t>(token) * p.idx_stride;
         const int col0 = c_first * C;
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         }
         cp_async_arrive_noinc(kv_first);
     }
-    if (warp >= kProducerWarp && paired) {
+    if (producer && paired) {
         // =========================================== paired producers
         // Both CTAs of the pair hold the same token and split, so the same
         // chunks. Each resolves all 128 indices (the softmax masks by them)
@@ -451,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         if (g == 0)
             for (int c = max(0, nch - NS); c < nch; ++c)
                 ok &= mbar_wait_bounded(&stage_free[c % NS], (c / NS) & 1, abort_flag, kWaitLimitNs);
-    } else if (warp >= kProducerWarp) {
+    } else if (producer) {
         // ================================================== producers
         // Thread g < 128 resolves key g's row; warp w then copies keys w,
-        // w + 7, ..., one 512-byte latent row per instruction (lane l: bytes
+        // w + 6, ..., one 512-byte latent row per instruction (lane l: bytes
         // 16 l .. 16 l + 15), and the 64-byte ropes of eight keys per
         // instruction. Masked keys are zero-filled. Thread 0 also arrives
         // after the index barrier, so that the stage barrier releases idx_s.
@@ -508,13 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
         }
         cp_async_wait_all();
     } else if (warp == kMmaWarp) {
-        // ================================================== MMA issuer
-        // QK(c) as soon as chunk c landed and S buffer c % 2 is free (the
-        // softmax of chunk c - 2 is done, i.e. PV(c - 2) was issued); PV(c) as
-        // soon as P(c) is ready. Whichever is due goes first.
+        // ================================================== QK issuer
+        // QK(c) once chunk c landed and S buffer c % 2 is free (the softmax
+        // of chunk c - 2 has handed over its P).
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_e4m3(kRows, N, 0, 0);
-            constexpr uint32_t kIdescPV = idesc_e4m3(kRows, N, 1, 1);
             // Descriptors of every operand tile; moving a descriptor by b
             // bytes adds b >> 4 to its start field (no carry: shared
             // addresses stay below 256 KB).
@@ -522,70 +524,61 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_kernel(const __
             const uint64_t d_q_rope = smem_desc(sbase + L::kQ + 4 * N * 128, 512, 512, kSwizzle64B);
             const uint64_t d_kv = smem_desc(sbase + L::kKv, 1024, 1024, kSwizzle128B);
             const uint64_t d_kv_rope = smem_desc(sbase + L::kKv + 4 * C * 128, 512, 512, kSwizzle64B);
-            const uint64_t d_p = smem_desc(sbase + L::kP, 8 * N, 8 * N, p_swizzle<N>());
-            int next_qk = 0, next_pv = 0;
-            bool q_ready = false;
-            uint64_t idle_since = 0;
-            while (next_pv < nch) {
-                bool progressed = false;
-                if (!q_ready) q_ready = mbar_test_wait(q_full, 0);
-                if (q_ready && next_qk < nch && next_qk <= next_pv + 1 &&
-                    mbar_test_wait(kv_bar(next_qk), kv_parity(next_qk))) {
-                    const int c = next_qk;
-                    fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
-                    tc_fence_after_sync();
-                    const uint32_t stage16 = static_cast<uint32_t>((c % NS) * L::kStage) >> 4;
-                    // one accumulator: the 16 latent K steps, then the rope's two
-                    const uint32_t d_s = tmem + (c & 1) * N;
+            ok &= mbar_wait_bounded(q_full, 0, abort_flag, kWaitLimitNs);  // also: no copy outlives the CTA
+            for (int c = 0; ok && c < nch; ++c) {
+                if (c >= 2) ok &= mbar_wait_bounded(p_full, static_cast<uint32_t>(c & 1), abort_flag, kWaitLimitNs);
+                ok &= mbar_wait_bounded(kv_bar(c), kv_parity(c), abort_flag, kWaitLimitNs);
+                if (!ok) break;
+                fence_proxy_async_smem();  // the producers' cp.async data, for the tensor cores
+                tc_fence_after_sync();
+                const uint32_t stage16 = static_cast<uint32_t>((c % NS) * L::kStage) >> 4;
+                // one accumulator: the 16 latent K steps, then the rope's two
+                const uint32_t d_s = tmem + (c & 1) * N;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int kb = i >> 2, ks = i & 3;
-                        const uint32_t a = stage16 + ((kb * C * 128 + ks * 32) >> 4);
-                        const uint32_t bq = (kb * N * 128 + ks * 32) >> 4;
-                        mma_f8(d_s, d_kv + a, d_q + bq, kIdescQK, i != 0 ? 1u : 0u);
-                    }
-                    if constexpr (L::kRope) {
-#pragma unroll
-                        for (int ks = 0; ks < 2; ++ks)
-                            mma_f8(d_s, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
-                                   kIdescQK, 1u);
-                    }
-                    mma_commit(&s_full[c & 1]);
-                    ++next_qk;
-                    progressed = true;
+                for (int i = 0; i < 16; ++i) {
+                    const int kb = i >> 2, ks = i & 3;
+                    const uint32_t a = stage16 + ((kb * C * 128 + ks * 32) >> 4);
+                    const uint32_t bq = (kb * N * 128 + ks * 32) >> 4;
+                    mma_f8(d_s, d_kv + a, d_q + bq, kIdescQK, i != 0 ? 1u : 0u);
                 }
-                if (next_pv < next_qk && mbar_test_wait(p_full, next_pv & 1)) {
-                    const int c = next_pv;
-                    tc_fence_after_sync();
-                    const uint32_t stage16 = static_cast<uint32_t>((c % NS) * L::kStage) >> 4;
-                    const uint32_t p16 = static_cast<uint32_t>((c & 1) * C * N) >> 4;
+                if constexpr (L::kRope) {
 #pragma unroll
-                    for (int kk = 0; kk < C / 32; ++kk) {  // the four latent blocks are independent chains
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t a_off = stage16 + ((j * C * 128 + kk * 32 * 128) >> 4);
-                            const uint32_t b_off = p16 + ((kk * 32 * N) >> 4);
-                            mma_f8(tmem + 2 * N + j * N, d_kv + a_off, d_p + b_off, kIdescPV,
-                                   (c > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(&pv_done[c % NS]);
-                    if (paired) mma_commit_multicast(&stage_free[c % NS], pair_mask);
-                    ++next_pv;
-                    progressed = true;
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma_f8(d_s, d_kv_rope + stage16 + ((ks * 32) >> 4), d_q_rope + ((ks * 32) >> 4),
+                               kIdescQK, 1u);
                 }
-                if (progressed) {
-                    idle_since = 0;
-                } else {
-                    const uint64_t now = global_timer_ns();
-                    if (idle_since == 0) idle_since = now;
-                    if (*abort_flag || now - idle_since > kWaitLimitNs) {
-                        ok = false;
-                        break;
-                    }
-                }
+                mma_commit(&s_full[c & 1]);
             }
-            if (!q_ready) ok &= mbar_wait_bounded(q_full, 0, abort_flag, kWaitLimitNs);  // no copy outlives the CTA
+            mma_commit(drain);
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ================================================== PV issuer
+        // PV(c) as soon as P(c) is ready (and O^T rescaled); a separate thread
+        // from QK's, so that neither waits behind the other's burst of MMAs.
+        if (lane == 0) {
+            constexpr uint32_t kIdescPV = idesc_e4m3(kRows, N, 1, 1);
+            const uint64_t d_kv = smem_desc(sbase + L::kKv, 1024, 1024, kSwizzle128B);
+            const uint64_t d_p = smem_desc(sbase + L::kP, 8 * N, 8 * N, p_swizzle<N>());
+            for (int c = 0; ok && c < nch; ++c) {
+                // p_full completes once per chunk; chunk c's is phase c
+                ok &= mbar_wait_bounded(p_full, static_cast<uint32_t>(c & 1), abort_flag, kWaitLimitNs);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t stage16 = static_cast<uint32_t>((c % NS) * L::kStage) >> 4;
+                const uint32_t p16 = static_cast<uint32_t>((c & 1) * C * N) >> 4;
+#pragma unroll
+                for (int kk = 0; kk < C / 32; ++kk) {  // the four latent blocks are independent chains
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t a_off = stage16 + ((j * C * 128 + kk * 32 * 128) >> 4);
+                        const uint32_t b_off = p16 + ((kk * 32 * N) >> 4);
+                        mma_f8(tmem + 2 * N + j * N, d_kv + a_off, d_p + b_off, kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&pv_done[c % NS]);
+                if (paired) mma_commit_multicast(&stage_free[c % NS], pair_mask);
+            }
             mma_commit(drain);
         }
         __syncwarp();
