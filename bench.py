@@ -305,7 +305,8 @@ def gather_floor(w, plan):
     """The time the decode's gathers alone need per call, modelled from the
     measured landing rates of profiles/row_gather_peak.json (per SM, cold and
     L2-hot rows, for the gather method the plan uses: paired tile::gather4
-    multicast or cp.async, 7 issuing warps): per (token, head tile, split) CTA,
+    multicast or cp.async; the 7-warp rows, the nearest measured to the
+    kernel's 6 producer warps): per (token, head tile, split) CTA,
     its rows that other tokens also read (L2 hits after the first) at the hot
     rate, the others at the cold rate; the slowest CTA of one wave, times the
     number of waves. None when the profile is missing."""

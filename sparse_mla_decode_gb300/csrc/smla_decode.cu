@@ -1409,9 +1409,11 @@ extern "C" int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* pl
     // An unpaired CTA of a 32- or 64-head tile that streams eight or more
     // chunks of 128 keys (its cp.async gathers bound the two-stage pipeline)
     // takes chunks of 96 keys in three stages instead: 4-7% faster at 128 x
-    // 64 x 2048 and 256 x 64 x 1024 on GB300; paired CTAs and short streams
-    // measured within 4% either way, slower more often than not.
-    if (forced_chunk == 0 && pair == 1 && n >= 32 && per_cta >= 8 && (best == 1 || merge_fits(n, shape->head_dim, 96, best))) {
+    // 64 x 2048 and 256 x 64 x 1024 on GB300. A paired 64-head CTA does so
+    // from sixteen chunks of 128 on (about 1% at 64 x 128 x 2048); shorter
+    // paired streams measured within 4% either way, slower more often than not.
+    const bool deep_ring = pair == 1 ? (n >= 32 && per_cta >= 8) : (n == 64 && per_cta >= 16);
+    if (forced_chunk == 0 && deep_ring && (best == 1 || merge_fits(n, shape->head_dim, 96, best))) {
         chunk = 96;
         chunks = (shape->width + chunk - 1) / chunk;
     }

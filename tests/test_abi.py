@@ -41,8 +41,8 @@ def shape(**kw):
 
 def test_plan_bandwidth_batch(lib):
     p = smla.smla_plan_for(shape(), num_sms=152)
-    assert p["head_tile"] == 64 and p["head_groups"] == 2 and p["chunk"] == 128
-    assert p["chunks"] == 16 and p["splits"] * p["chunks_per_split"] >= 16
+    assert p["head_tile"] == 64 and p["head_groups"] == 2 and p["chunk"] == 96 and p["pair"] == 2
+    assert p["chunks"] == 22 and p["splits"] * p["chunks_per_split"] >= 22
     assert p["ctas"] == 64 * 2 * p["splits"]
     assert p["smem_bytes"] <= 232448 and p["tmem_columns"] == 512
 
@@ -50,7 +50,8 @@ def test_plan_bandwidth_batch(lib):
 @pytest.mark.parametrize("tokens,heads,width,chunk,chunks,pair", [
     (128, 64, 2048, 96, 22, 1),   # unpaired, 16 chunks of 128 per CTA: three stages of 96
     (256, 64, 1024, 96, 11, 1),   # unpaired, 8 chunks of 128 per CTA
-    (64, 128, 2048, 128, 16, 2),  # paired head groups keep chunks of 128
+    (64, 128, 2048, 96, 22, 2),   # paired, 16 chunks of 128 per CTA: three stages of 96
+    (64, 128, 1024, 128, 8, 2),   # paired, 8 chunks of 128 per CTA keep two stages of 128
     (32, 64, 2048, 128, 16, 1),   # split four ways: 4 chunks per CTA
     (12, 16, 2048, 128, 16, 1),   # 16-head tiles have no room for a third stage
 ])
