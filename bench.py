@@ -220,16 +220,43 @@ KERNEL_SOURCES = {"value": ("smla_value.cu", "smla_ptx.cuh", "smla_merge_row.cuh
                   "ds_mla": ("smla_ds_mla.cu", "smla_ptx.cuh")}
 
 
+def code_text(source: str) -> str:
+    """A C++/CUDA source without its comments and with its whitespace runs
+    collapsed: what the compiler sees, so that editing a comment does not
+    count as changing the kernel. String and character literals are kept as
+    they are."""
+    out, i, n = [], 0, len(source)
+    while i < n:
+        ch = source[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and source[j] != ch:
+                j += 2 if source[j] == "\\" else 1
+            out.append(source[i:j + 1])
+            i = j + 1
+        elif source.startswith("//", i):
+            j = source.find("\n", i)
+            i = n if j < 0 else j
+        elif source.startswith("/*", i):
+            j = source.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sha(config: str = "batch") -> str:
-    """Hash of the sources of the kernel a config times (the decode kernel
-    unless listed in KERNEL_SOURCES): the committed DRAM traffic holds only
-    while they are unchanged."""
+    """Hash of the code (comments and whitespace aside) of the sources of the
+    kernel a config times (the decode kernel unless listed in KERNEL_SOURCES):
+    the committed DRAM traffic holds only while that code is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc")
     for name in KERNEL_SOURCES.get(config, ("smla_decode.cu", "smla_ptx.cuh")):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(code_text(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -72,8 +72,8 @@ constexpr int kMmaWarp = 8;       // issues QK (and holds the TMEM allocation)
 constexpr int kProducerWarp = 9;  // first of six
 constexpr int kProducerThreads = 192;
 constexpr int kPvWarp = 15;       // issues PV
-// Unpaired chunk 0 is gathered by every warp but the MMA warp: the softmax
-// range and the producers.
+// Unpaired chunk 0 is gathered by every warp but the two issuing warps: the
+// softmax range and the producers.
 constexpr int kFirstGatherThreads = kSoftmaxRange + kProducerThreads;
 constexpr int kMaxSplits = 16;
 constexpr float kLog2P = 8.80735492205760410744f;  // log2(448): P of the running max

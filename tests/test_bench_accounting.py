@@ -123,3 +123,15 @@ def test_gather_floor_counts_shared_rows_at_the_hot_rate():
     assert got["us"] == pytest.approx(want, abs=0.01) and got["method"] == "cp.async"
     plan["pair"] = 2
     assert bench.gather_floor(w, plan)["method"] == "paired tile::gather4 multicast"
+
+
+def test_kernel_hash_sees_code_not_comments():
+    """The committed DRAM traffic is keyed by the kernel's code: editing a
+    comment or the layout keeps the key, changing an expression or a string
+    literal does not."""
+    base = 'int f(int x) { return x + 1; }  // one\n/* note */ const char* s = "a // b";\n'
+    assert bench.code_text(base) == bench.code_text(
+        'int f(int x)   {\n  return x + 1;\n}  // another note\nconst char* s = "a // b"; /* x */\n')
+    assert bench.code_text(base) != bench.code_text(base.replace("x + 1", "x + 2"))
+    assert bench.code_text(base) != bench.code_text(base.replace('"a // b"', '"a // c"'))
+    assert bench.code_text('char c = \'/\'; // q') == "char c = '/';"
