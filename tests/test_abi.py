@@ -382,3 +382,36 @@ def test_ds_mla_head_tile_rule_without_a_device(lib):
     assert tile(tokens=1, heads=64, head_tile=16) == smla.EINVAL
     assert tile(tokens=1, heads=48) == smla.EINVAL
     assert smla.smla_ds_mla_head_tile(64, 128, num_sms=152) == 64
+
+
+def test_every_plan_over_a_grid_fits_the_hardware_and_covers_the_keys(lib):
+    """Invariants of the planner over a grid of shapes (no device: 152 SMs):
+    a head tile that divides H, a chunk of 96 keys only on 32/64-head tiles,
+    every key covered by exactly the splits that have work, a cluster of at
+    most 16 CTAs, pairing only of an even number of head groups over one pool,
+    and one CTA's shared memory and TMEM within the SM's."""
+    seen_chunks, seen_pairs = set(), set()
+    for tokens in (1, 2, 5, 12, 33, 64, 128, 300):
+        for heads in (16, 32, 48, 64, 96, 128, 256):
+            for width in (1, 95, 96, 128, 129, 640, 1000, 2048, 4096):
+                for dim, pools in ((576, 1), (512, 1), (576, 2)):
+                    split_col = min(width, 128) if pools == 2 else 0
+                    p = smla.smla_plan_for(smla.make_shape(tokens, heads, width, dim, pools, split_col), num_sms=152)
+                    where = (tokens, heads, width, dim, pools, p)
+                    tile = p["head_tile"]
+                    assert tile in (16, 32, 64) and heads % tile == 0 and p["head_groups"] * tile == heads, where
+                    assert p["chunk"] in (96, 128) and (p["chunk"] == 128 or tile >= 32), where
+                    assert p["chunks"] == -(-width // p["chunk"]), where
+                    assert 1 <= p["splits"] <= 16, where
+                    assert p["splits"] * p["chunks_per_split"] >= p["chunks"], where
+                    assert (p["splits"] - 1) * p["chunks_per_split"] < max(p["chunks"], 1), where
+                    assert p["pair"] in (1, 2) and p["pair"] * p["splits"] <= 16, where
+                    if p["pair"] == 2:
+                        assert p["head_groups"] % 2 == 0 and pools == 1, where
+                    assert p["ctas"] == tokens * p["head_groups"] * p["splits"], where
+                    assert p["threads"] == 512 and p["smem_bytes"] <= 227 * 1024, where
+                    cols = p["tmem_columns"]
+                    assert 32 <= cols <= 512 and cols & (cols - 1) == 0, where
+                    seen_chunks.add(p["chunk"])
+                    seen_pairs.add(p["pair"])
+    assert seen_chunks == {96, 128} and seen_pairs == {1, 2}  # the grid reaches every kind of plan
