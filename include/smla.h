@@ -16,7 +16,8 @@
  *   A token without active columns gets out = +0.0 and lse = -inf.
  *
  * Datapath: E4M3 q and KV, FP32 logits, a base-2 online softmax over chunks of
- * 128 columns, P rounded to E4M3 (RN, satfinite) at 448 of the running maximum
+ * the plan's `chunk` columns (128, or 96 where the planner takes three stages),
+ * P rounded to E4M3 (RN, satfinite) at 448 of the running maximum
  * of the split, FP32 sums of the unrounded P, FP32 accumulation, an FP32 merge
  * of the key splits over distributed shared memory, one BF16 rounding.
  *
@@ -87,7 +88,10 @@ typedef struct smla_shape {
 typedef struct smla_plan {
     int32_t head_tile;        /* heads per CTA (16, 32 or 64) */
     int32_t head_groups;      /* heads / head_tile */
-    int32_t chunk;            /* columns per chunk (128) */
+    int32_t chunk;            /* columns per chunk: 128 in two stages, or 96 in
+                                 three for a 32/64-head tile that streams 8 or
+                                 more chunks of 128 unpaired, 16 or more paired
+                                 (64-head tiles) */
     int32_t chunks;           /* ceil(width / chunk) */
     int32_t splits;           /* CTAs per (token, head group) = cluster size */
     int32_t chunks_per_split; /* ceil(chunks / splits); a token of c active-count
@@ -117,10 +121,9 @@ typedef struct smla_plan {
  * widest tile without splits.
  * Environment overrides (for measurement): SMLA_HEAD_TILE=16|32|64 forces the
  * tile when it divides `heads`; SMLA_PAIR=0 / 1 turns pairing off / on wherever
- * the shape allows it; SMLA_SPLITS=n
- * (n > 0) forces the split count,
+ * the shape allows it; SMLA_SPLITS=n (n > 0) forces the split count,
  * clamped to [1, min(chunks, 16 / pair)], with the widest tile unless one is
- * forced.
+ * forced; SMLA_CHUNK=96|128 forces the chunk (96 only on 32/64-head tiles).
  * Returns SMLA_OK, SMLA_EINVAL, SMLA_EUNSUPPORTED or SMLA_ECUDA. */
 int smla_plan_for(const smla_shape* shape, int num_sms, smla_plan* plan);
 
